@@ -1,0 +1,235 @@
+/*
+ * w8a8.h -- C ABI of the GB300 (sm_103a) w8a8 scaled quantiser and scaled
+ * matrix multiply.
+ *
+ * What it computes (sources are web pages, cited by title and section):
+ *
+ *  - Quantiser, "Enable scaled FP8 (e4m3fn) KV cache on ROCm (AMD GPU)",
+ *    section "Scaling semantics": scale = AbsMax(x) / 448 for e4m3fn (the OCP
+ *    MAXNORM), q = fp8(x / scale), x' = dequant(q) * scale.  The int8 variant
+ *    uses 127.  Dynamic (runtime absmax) and static (given scale) modes, and
+ *    per-tensor / per-token granularity, follow "[Kernel] Support Fp8
+ *    Checkpoints (Dynamic + Static)" (PR description) and "[Kernel] Add w8a8
+ *    CUTLASS kernels" (feature list).
+ *  - Scaled matmul, "[Kernel] Add w8a8 CUTLASS kernels", feature list of
+ *    cutlass_scaled_mm_dq: out = scale_a * scale_b * (A_q @ B_q) with
+ *    symmetric fp8-e4m3 or int8 operands, per-tensor or per-token scale_a,
+ *    per-tensor or per-output-channel scale_b, bf16 or fp16 output; B is
+ *    "column-major" (stored [N, K], K contiguous) as the review thread of the
+ *    same page requires.
+ *
+ * Exact rules where the pages are silent:
+ *  - x / scale is a correctly rounded fp32 division;
+ *  - e4m3: round to nearest, ties to the even code, saturate to +-448
+ *    (+-inf included), NaN -> 0x7F, the sign of zero is kept;
+ *  - int8: round half to even, saturate to [-128, 127], NaN -> 0;
+ *  - absmax ignores NaN; an all-zero row or tensor gets scale 1.0;
+ *  - epilogue: y = ((float)acc * scale_a[m|0]) * scale_b[n|0] in fp32, then
+ *    round-to-nearest-even to bf16/fp16.  The fp8 path accumulates in fp32
+ *    on the tensor cores; the int8 path accumulates exactly in int32.
+ *
+ * Conventions for every entry point:
+ *  - All data pointers are DEVICE pointers (cudaMalloc'd or equivalent) on
+ *    the current device, unless noted.  The caller owns every buffer; the
+ *    library keeps no pointer after a call returns.
+ *  - Matrices are row-major with a leading dimension in ELEMENTS (ld >= cols);
+ *    sub-matrix views (ld > cols) are allowed.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream);
+ *    they never synchronise, never allocate device memory and are safe to
+ *    capture in a CUDA graph.  The first call on a device does a one-time
+ *    host-side set-up (driver entry-point lookup, device attributes); make it
+ *    before any stream capture.
+ *  - Errors are reported by the return status; a status other than W8A8_OK
+ *    means nothing was launched (except W8A8_ERR_CUDA, which reports a launch
+ *    failure) and w8a8_last_error() holds a message.  Inputs are validated,
+ *    never asserted on: no input makes the library abort the process.
+ *  - Thread-safety: calls from several host threads are safe; the last-error
+ *    message is per host thread.
+ */
+#ifndef W8A8_GB300_H
+#define W8A8_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define W8A8_API __attribute__((visibility("default")))
+#else
+#define W8A8_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* w8a8_stream_t;
+
+/* Element types. */
+enum {
+  W8A8_E4M3 = 0, /* OCP float8 e4m3fn, 1 byte */
+  W8A8_INT8 = 1, /* signed 8-bit integer */
+  W8A8_BF16 = 2, /* bfloat16, 2 bytes */
+  W8A8_FP16 = 3, /* IEEE binary16, 2 bytes */
+  W8A8_FP32 = 4, /* scaled_mm output for e4m3 only: y = (acc*scale_a)*scale_b, unrounded */
+  W8A8_INT32 = 5 /* scaled_mm output for int8 only: the exact int32 accumulators, unscaled */
+};
+
+/* Scale granularity.  PER_ROW is per-token for activations [M, K] and
+ * per-output-channel for weights stored [N, K]. */
+enum { W8A8_PER_TENSOR = 0, W8A8_PER_ROW = 1 };
+
+/* Quantiser mode: DYNAMIC computes the scales from absmax and writes them;
+ * STATIC reads the given scales. */
+enum { W8A8_DYNAMIC = 0, W8A8_STATIC = 1 };
+
+/* Status codes. */
+typedef int w8a8_status;
+enum {
+  W8A8_OK = 0,
+  W8A8_ERR_INVALID_ARG = 1, /* null pointer, bad enum, size <= 0, ld < cols */
+  W8A8_ERR_UNSUPPORTED = 2, /* dtype combination or size outside the limits */
+  W8A8_ERR_MISALIGNED = 3,  /* base pointer or row stride not 16-byte aligned */
+  W8A8_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required */
+  W8A8_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+  W8A8_ERR_NO_DEVICE = 6    /* current device is not an sm_103 GPU */
+};
+
+/* Device status bits reported by w8a8_device_status(). */
+enum { W8A8_DEVICE_TIMEOUT = 1 };
+
+/* Message for the last failing call on this host thread ("" if none).
+ * The string is owned by the library and valid until the next call. */
+W8A8_API const char* w8a8_last_error(void);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+W8A8_API int w8a8_version(void);
+
+/* ------------------------------------------------------------------------
+ * Quantiser
+ *
+ * q[i, j] = encode(x[i, j] / scale[i or 0])
+ *
+ *  x        device, [rows, cols] of x_dtype (W8A8_BF16 or W8A8_FP16), leading
+ *           dimension ld_x elements.
+ *  q        device, [rows, cols] of q_dtype (W8A8_E4M3 or W8A8_INT8), leading
+ *           dimension ld_q bytes.
+ *  scale    device fp32, length rows (PER_ROW) or 1 (PER_TENSOR).  DYNAMIC
+ *           writes absmax/448 (e4m3) or absmax/127 (int8), or 1.0 for an
+ *           all-zero row/tensor; STATIC reads it.
+ *  workspace, workspace_bytes
+ *           device scratch of at least w8a8_scaled_quant_workspace_size()
+ *           bytes (0 for every mode except DYNAMIC + PER_TENSOR, which uses
+ *           16 bytes and clears them itself).  May be NULL when 0 is required.
+ *  Alignment: the vectorised path is used when x, q, ld_x*2 and ld_q are
+ *  16-byte aligned; other layouts are accepted and run a scalar path.
+ *  Limits: rows, cols >= 1; rows * cols < 2^40.
+ * ---------------------------------------------------------------------- */
+W8A8_API size_t w8a8_scaled_quant_workspace_size(int64_t rows, int64_t cols, int gran,
+                                        int mode);
+
+W8A8_API w8a8_status w8a8_scaled_quant(const void* x, int x_dtype, int64_t rows,
+                              int64_t cols, int64_t ld_x, void* q, int q_dtype,
+                              int64_t ld_q, float* scale, int gran, int mode,
+                              void* workspace, size_t workspace_bytes,
+                              w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Dequantiser (the KV-cache page's "scaled_fr_fp8_dequant")
+ *
+ * y[i, j] = round16(float(decode(q[i, j])) * scale[i or 0])
+ *
+ *  q      device [rows, cols] of q_dtype (E4M3 or INT8), leading dim ld_q.
+ *  scale  device fp32, length rows (PER_ROW) or 1 (PER_TENSOR).
+ *  y      device [rows, cols] of y_dtype (BF16 or FP16), leading dim ld_y.
+ *  NaN codes decode to NaN.
+ * ---------------------------------------------------------------------- */
+W8A8_API w8a8_status w8a8_scaled_dequant(const void* q, int q_dtype, int64_t rows,
+                                int64_t cols, int64_t ld_q, const float* scale,
+                                int gran, void* y, int y_dtype, int64_t ld_y,
+                                w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Scaled matmul with a dequantising epilogue (cutlass_scaled_mm_dq)
+ *
+ * out[m, n] = round16(((float)sum_k A_q[m, k] * B_q[n, k]) * scale_a[m|0]
+ *                     * scale_b[n|0])
+ *
+ *  a_q      device [M, K] codes of q_dtype, row-major, leading dim lda bytes.
+ *  b_q      device weights stored [N, K] (K contiguous; the "column-major
+ *           [K, N]" B of the CUTLASS page), leading dim ldb bytes.
+ *  scale_a  device fp32, length M (a_gran = PER_ROW) or 1 (PER_TENSOR).
+ *  scale_b  device fp32, length N (b_gran = PER_ROW) or 1 (PER_TENSOR); a
+ *           merged QKV / gate-up weight shares one PER_TENSOR scale.
+ *  out      device [M, N] of out_dtype, leading dim ldc (elements).
+ *           out_dtype is BF16 or FP16 (the method's outputs), or for
+ *           inspection FP32 (e4m3 only: y before the 16-bit rounding) or
+ *           INT32 (int8 only: raw accumulators, scales ignored).
+ *  q_dtype  W8A8_E4M3 (fp32 accumulation) or W8A8_INT8 (exact int32).
+ *  workspace, workspace_bytes
+ *           device scratch of at least w8a8_scaled_mm_workspace_size() bytes.
+ *           It must be zero-filled before its first use; every call that
+ *           returns W8A8_OK leaves its synchronisation counters zero again,
+ *           so one workspace can be reused by later calls on the same stream.
+ *           Calls that may overlap on the GPU need separate workspaces.
+ *  Alignment (the CUTLASS page's "misaligned address" crash turned into a
+ *  status): a_q and b_q 16-byte aligned and lda, ldb multiples of 16
+ *  (W8A8_ERR_MISALIGNED otherwise).  out needs element alignment only.
+ *  Limits: M, N, K >= 1 and < 2^31; for int8 also K % 16 == 0 and
+ *  K <= 131071 (the int32 range).
+ * ---------------------------------------------------------------------- */
+W8A8_API size_t w8a8_scaled_mm_workspace_size(int64_t M, int64_t N, int64_t K,
+                                     int q_dtype);
+
+W8A8_API w8a8_status w8a8_scaled_mm(const void* a_q, int64_t lda, const void* b_q,
+                           int64_t ldb, const float* scale_a, int a_gran,
+                           const float* scale_b, int b_gran, void* out,
+                           int64_t ldc, int64_t M, int64_t N, int64_t K,
+                           int q_dtype, int out_dtype, void* workspace,
+                           size_t workspace_bytes, w8a8_stream_t stream);
+
+/* Kernel configuration of one scaled_mm call (tests and tuning).
+ *  swap_ab   1: the weight rows N are the 128-row MMA side and the tokens M
+ *            the narrow side (small-M / decode regime); 0: tokens M on the
+ *            128-row side (large-M regime).
+ *  block_n   width of the narrow MMA side: 16..256, multiple of 16.
+ *  split_k   number of K slices reduced in a fixed order (>= 1).
+ *  stages    depth of the shared-memory ring (2..8); 0 = automatic.
+ * Fields set to 0 (except swap_ab) mean "choose automatically". */
+typedef struct {
+  int swap_ab;
+  int block_n;
+  int split_k;
+  int stages;
+} w8a8_mm_config;
+
+/* The configuration w8a8_scaled_mm() picks for this problem (host only). */
+W8A8_API w8a8_status w8a8_scaled_mm_pick_config(int64_t M, int64_t N, int64_t K,
+                                       int q_dtype, w8a8_mm_config* cfg);
+
+/* Workspace bytes needed by an explicit configuration. */
+W8A8_API size_t w8a8_scaled_mm_config_workspace_size(int64_t M, int64_t N, int64_t K,
+                                            int q_dtype,
+                                            const w8a8_mm_config* cfg);
+
+/* w8a8_scaled_mm with an explicit configuration (validated: W8A8_ERR_
+ * UNSUPPORTED for a block_n / split_k / stages value outside the limits). */
+W8A8_API w8a8_status w8a8_scaled_mm_with_config(
+    const void* a_q, int64_t lda, const void* b_q, int64_t ldb,
+    const float* scale_a, int a_gran, const float* scale_b, int b_gran,
+    void* out, int64_t ldc, int64_t M, int64_t N, int64_t K, int q_dtype,
+    int out_dtype, void* workspace, size_t workspace_bytes,
+    const w8a8_mm_config* cfg, w8a8_stream_t stream);
+
+/* Reads and clears the library's device-side status word on the current
+ * device (W8A8_DEVICE_* bits; a kernel sets W8A8_DEVICE_TIMEOUT when one of
+ * its bounded pipeline waits gave up instead of hanging).  This call
+ * synchronises the device; use it in tests and diagnostics, not on a hot
+ * path. */
+W8A8_API w8a8_status w8a8_device_status(int* flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W8A8_GB300_H */

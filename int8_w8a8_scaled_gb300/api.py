@@ -1,0 +1,237 @@
+"""Python binding of the C ABI: torch tensors in, library calls out.
+
+This layer only marshals arguments (pointers, sizes, strides, dtypes, the
+current CUDA stream); every step of the computation runs in the CUDA
+library.  Tensors must already live on the current CUDA device.
+
+    scaled_quant(x, q, scale, per_token=True, dynamic=True)
+    scaled_dequant(q, scale, y, per_token=False)
+    scaled_mm(a_q, b_q, scale_a, scale_b, out)
+
+Naming follows the pages: ``cutlass_scaled_mm_dq(a, b, scale_a, scale_b,
+out_dtype)`` of "[Kernel] Add w8a8 CUTLASS kernels" (here the output tensor is
+passed in, as in that page's C++ op) with B given as a [K, N] column-major
+view, i.e. a [N, K] row-major tensor; the quantiser follows the "Scaling
+semantics" section of "Enable scaled FP8 (e4m3fn) KV cache on ROCm".
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import _lib
+from ._lib import (BF16, DYNAMIC, E4M3, FP16, FP32, INT8, INT32, PER_ROW, PER_TENSOR, STATIC,
+                   MmConfig, W8A8Error, check)
+
+__all__ = [
+    "scaled_quant", "scaled_dequant", "scaled_mm", "mm_workspace_size",
+    "quant_workspace_size", "pick_config", "device_status", "Workspace",
+    "W8A8Error", "MmConfig",
+]
+
+
+def _qkind(t: torch.Tensor, q_dtype=None) -> int:
+    if q_dtype is not None:
+        return q_dtype
+    if t.dtype == torch.float8_e4m3fn:
+        return E4M3
+    if t.dtype == torch.int8:
+        return INT8
+    raise TypeError(f"quantised tensors must be float8_e4m3fn or int8 (got {t.dtype}); "
+                    "pass q_dtype= for a uint8 view")
+
+
+def _fkind(t: torch.Tensor, wide: bool = False) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float16:
+        return FP16
+    if wide and t.dtype == torch.float32:
+        return FP32
+    if wide and t.dtype == torch.int32:
+        return INT32
+    raise TypeError(f"expected bfloat16 or float16 (got {t.dtype})")
+
+
+def _ld(t: torch.Tensor) -> int:
+    if t.dim() != 2:
+        raise ValueError("expected a 2-D tensor")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError("rows must be contiguous (stride(1) == 1)")
+    return t.stride(0) if t.shape[0] > 1 else max(t.stride(0), t.shape[1])
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Workspace:
+    """A zero-filled device scratch buffer reused across calls on one stream.
+
+    The matmul's split-K counters must start at zero; the library leaves them
+    at zero after each successful call, so the buffer only needs zeroing once.
+    """
+
+    def __init__(self, nbytes: int = 0, device=None):
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+
+    def ensure(self, nbytes: int) -> "Workspace":
+        if nbytes > self.buf.numel():
+            self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+        return self
+
+    @property
+    def nbytes(self) -> int:
+        return self.buf.numel()
+
+
+_ws_lock = threading.Lock()
+_default_ws: dict = {}
+
+
+def _default_workspace(device: torch.device, nbytes: int) -> Workspace:
+    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+    with _ws_lock:
+        ws = _default_ws.get(key)
+        if ws is None:
+            ws = _default_ws[key] = Workspace(nbytes, device)
+        return ws.ensure(nbytes)
+
+
+def quant_workspace_size(rows: int, cols: int, per_token: bool, dynamic: bool) -> int:
+    return _lib.load().w8a8_scaled_quant_workspace_size(
+        rows, cols, PER_ROW if per_token else PER_TENSOR, DYNAMIC if dynamic else STATIC)
+
+
+def scaled_quant(x: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, per_token: bool = True,
+                 dynamic: bool = True, workspace: torch.Tensor | None = None, q_dtype=None,
+                 stream=None) -> None:
+    """q = sat_round(x / scale); dynamic mode writes scale = absmax / 448
+    (e4m3) or absmax / 127 (int8), per token (row) or per tensor."""
+    _cuda(x, q, scale, workspace)
+    lib = _lib.load()
+    rows, cols = x.shape
+    if tuple(q.shape) != (rows, cols):
+        raise ValueError("q must have the shape of x")
+    if scale.dtype != torch.float32 or not scale.is_contiguous():
+        raise ValueError("scale must be a contiguous float32 tensor")
+    need_scale = rows if per_token else 1
+    if scale.numel() != need_scale:
+        raise ValueError(f"scale must have {need_scale} elements")
+    gran = PER_ROW if per_token else PER_TENSOR
+    mode = DYNAMIC if dynamic else STATIC
+    need = lib.w8a8_scaled_quant_workspace_size(rows, cols, gran, mode)
+    if need and workspace is None:
+        workspace = _default_workspace(x.device, need).buf
+    check(lib.w8a8_scaled_quant(
+        _ptr(x), _fkind(x), rows, cols, _ld(x), _ptr(q), _qkind(q, q_dtype), _ld(q),
+        _ptr(scale), gran, mode, _ptr(workspace) if need else None,
+        workspace.numel() if (need and workspace is not None) else 0, _stream(stream)))
+
+
+def scaled_dequant(q: torch.Tensor, scale: torch.Tensor, y: torch.Tensor, per_token: bool = False,
+                   q_dtype=None, stream=None) -> None:
+    """y = round16(decode(q) * scale)."""
+    _cuda(q, scale, y)
+    lib = _lib.load()
+    rows, cols = q.shape
+    if tuple(y.shape) != (rows, cols):
+        raise ValueError("y must have the shape of q")
+    if scale.dtype != torch.float32 or not scale.is_contiguous():
+        raise ValueError("scale must be a contiguous float32 tensor")
+    check(lib.w8a8_scaled_dequant(
+        _ptr(q), _qkind(q, q_dtype), rows, cols, _ld(q), _ptr(scale),
+        PER_ROW if per_token else PER_TENSOR, _ptr(y), _fkind(y), _ld(y), _stream(stream)))
+
+
+def _cfg(config) -> MmConfig | None:
+    if config is None:
+        return None
+    if isinstance(config, MmConfig):
+        return config
+    return MmConfig(int(config.get("swap_ab", 0)), int(config.get("block_n", 0)),
+                    int(config.get("split_k", 0)), int(config.get("stages", 0)))
+
+
+def pick_config(M: int, N: int, K: int, q_dtype: int = E4M3) -> dict:
+    c = MmConfig()
+    check(_lib.load().w8a8_scaled_mm_pick_config(M, N, K, q_dtype, ctypes.byref(c)))
+    return c.as_dict()
+
+
+def mm_workspace_size(M: int, N: int, K: int, q_dtype: int = E4M3, config=None) -> int:
+    lib = _lib.load()
+    c = _cfg(config)
+    if c is None:
+        return lib.w8a8_scaled_mm_workspace_size(M, N, K, q_dtype)
+    return lib.w8a8_scaled_mm_config_workspace_size(M, N, K, q_dtype, ctypes.byref(c))
+
+
+def scaled_mm(a_q: torch.Tensor, b_q: torch.Tensor, scale_a: torch.Tensor, scale_b: torch.Tensor,
+              out: torch.Tensor, workspace: torch.Tensor | Workspace | None = None, config=None,
+              q_dtype=None, stream=None) -> torch.Tensor:
+    """out[m, n] = round16(sum_k a_q[m, k] b_q[n, k] * scale_a[m|0] * scale_b[n|0]).
+
+    a_q: [M, K] e4m3 / int8, rows contiguous.  b_q: [N, K] (the [K, N]
+    column-major weight), rows contiguous.  scale_a: [M] or [1] fp32,
+    scale_b: [N] or [1] fp32.  out: [M, N] bf16 / fp16 (or float32 for the
+    unrounded e4m3 result, int32 for the raw int8 accumulators).
+    """
+    _cuda(a_q, b_q, scale_a, scale_b, out)
+    lib = _lib.load()
+    M, K = a_q.shape
+    N, K2 = b_q.shape
+    if K != K2:
+        raise ValueError("a_q is [M, K] and b_q is [N, K]: K must match")
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out must be [M, N]")
+    for s in (scale_a, scale_b):
+        if s.dtype != torch.float32 or not s.is_contiguous():
+            raise ValueError("scales must be contiguous float32 tensors")
+    a_gran = PER_ROW if scale_a.numel() == M and M > 1 else PER_TENSOR
+    b_gran = PER_ROW if scale_b.numel() == N and N > 1 else PER_TENSOR
+    if a_gran == PER_TENSOR and scale_a.numel() != 1:
+        raise ValueError("scale_a must have 1 or M elements")
+    if b_gran == PER_TENSOR and scale_b.numel() != 1:
+        raise ValueError("scale_b must have 1 or N elements")
+    qk = _qkind(a_q, q_dtype)
+    if _qkind(b_q, q_dtype) != qk:
+        raise TypeError("a_q and b_q must have the same element type")
+    c = _cfg(config)
+    need = (lib.w8a8_scaled_mm_config_workspace_size(M, N, K, qk, ctypes.byref(c)) if c is not None
+            else lib.w8a8_scaled_mm_workspace_size(M, N, K, qk))
+    if isinstance(workspace, Workspace):
+        workspace = workspace.ensure(need).buf
+    elif workspace is None and need:
+        workspace = _default_workspace(a_q.device, need).buf
+    ws_ptr = _ptr(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    args = (_ptr(a_q), _ld(a_q), _ptr(b_q), _ld(b_q), _ptr(scale_a), a_gran, _ptr(scale_b), b_gran,
+            _ptr(out), _ld(out), M, N, K, qk, _fkind(out, wide=True), ws_ptr, ws_bytes)
+    if c is None:
+        check(lib.w8a8_scaled_mm(*args, _stream(stream)))
+    else:
+        check(lib.w8a8_scaled_mm_with_config(*args, ctypes.byref(c), _stream(stream)))
+    return out
+
+
+def device_status() -> int:
+    """Synchronise and read/clear the device status word (1 = a bounded
+    pipeline wait timed out)."""
+    v = ctypes.c_int(0)
+    check(_lib.load().w8a8_device_status(ctypes.byref(v)))
+    return v.value

@@ -1,0 +1,477 @@
+// api.cu -- the C ABI (include/w8a8.h): argument validation, kernel
+// configuration, TMA tensor maps and launches.  No call allocates device
+// memory or synchronises the stream; every call returns a status and leaves a
+// message for w8a8_last_error() on failure.
+//
+// Input validation instead of assertions follows the review of "[Kernel] Add
+// w8a8 CUTLASS kernels" (no input may crash the caller; a B that is not
+// column-major used to end in "misaligned address" -- here it is a status).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/w8a8.h"
+#include "internal.h"
+
+using namespace w8a8;
+
+namespace {
+
+thread_local std::string t_last_error;
+
+w8a8_status fail(w8a8_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+w8a8_status ok() {
+  t_last_error.clear();
+  return W8A8_OK;
+}
+
+w8a8_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(W8A8_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ------------------------------------------------------------------ device info
+
+struct DeviceInfo {
+  bool ready = false;
+  int major = 0, minor = 0, sms = 0, smem_optin = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+w8a8_status device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(W8A8_ERR_NO_DEVICE, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.ready = true;
+  }
+  if (d.major != 10 || d.minor != 3)
+    return fail(W8A8_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
+                d.major, d.minor);
+  *out = d;
+  return W8A8_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D K-major operand [rows, K] (row stride ld_bytes), box of box_rows rows x
+// 128 bytes, 128-byte swizzle, zero fill outside the tensor.
+w8a8_status make_operand_map(CUtensorMap* map, const void* base, bool f16, long long rows, long long K,
+                             long long ld_bytes, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(W8A8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_bytes)};
+  const cuuint32_t box[2] = {f16 ? 64u : 128u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(W8A8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return W8A8_OK;
+}
+
+// ------------------------------------------------------------------ GEMM configuration
+
+constexpr int kSmemTwoPerSm = 113 * 1024;   // budget that lets two CTAs share an SM
+constexpr int kInt8ChunkK = 1024;           // exact fp32 accumulation bound: 1024 * 128 * 128 = 2^24
+
+bool valid_block_n(int bn, int q_dtype) {
+  if (q_dtype == W8A8_INT8) return bn == 16 || bn == 32 || bn == 64 || bn == 128;
+  return bn == 16 || bn == 32 || bn == 64 || bn == 128 || bn == 256;
+}
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+int num_kb(long long K, int q_dtype) { return static_cast<int>(ceil_div(K, q_dtype == W8A8_INT8 ? 64 : 128)); }
+
+void auto_config(long long M, long long N, long long K, int q_dtype, int sms, w8a8_mm_config* c) {
+  const int kb = num_kb(K, q_dtype);
+  if (M <= 256) {
+    // decode regime: weights on the 128-row side, tokens padded to block_n
+    c->swap_ab = 1;
+    int bn = 16;
+    while (bn < M && bn < 64) bn *= 2;
+    c->block_n = bn;
+    const long long tiles = ceil_div(N, 128) * ceil_div(M, bn);
+    // two CTAs per SM fit at these widths: aim for about 2 * sms CTAs while
+    // keeping >= 4 K blocks per slice
+    long long sp = (2LL * sms + tiles / 2) / std::max<long long>(tiles, 1);
+    sp = std::max<long long>(1, std::min<long long>(sp, kb / 4));
+    sp = std::min<long long>(sp, 16);
+    c->split_k = static_cast<int>(sp);
+  } else {
+    c->swap_ab = 0;
+    c->block_n = (q_dtype == W8A8_INT8) ? 128 : 256;
+    const long long tiles = ceil_div(M, 128) * ceil_div(N, c->block_n);
+    long long sp = 1;
+    if (tiles < sms / 2) sp = std::min<long long>(std::max<long long>(1, sms / tiles), kb / 4);
+    c->split_k = static_cast<int>(std::max<long long>(1, sp));
+  }
+  c->stages = 0;
+}
+
+int auto_stages(int block_n, int smem_optin) {
+  const int budget = (block_n <= 64) ? kSmemTwoPerSm : smem_optin;
+  return std::max(2, std::min(8, max_stages_for(block_n, budget)));
+}
+
+struct Plan {
+  w8a8_mm_config cfg;
+  int kb, kb_per_split, splits, tiles_p, tiles_q, stages;
+  size_t off_counters, off_partial, off_a16, off_b16, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+Plan make_plan(long long M, long long N, long long K, int q_dtype, const w8a8_mm_config& cfg, int smem_optin) {
+  Plan p{};
+  p.cfg = cfg;
+  p.kb = num_kb(K, q_dtype);
+  const long long P = cfg.swap_ab ? N : M;
+  const long long Q = cfg.swap_ab ? M : N;
+  p.tiles_p = static_cast<int>(ceil_div(P, 128));
+  p.tiles_q = static_cast<int>(ceil_div(Q, cfg.block_n));
+  int sp = std::max(1, std::min(cfg.split_k, p.kb));
+  p.kb_per_split = static_cast<int>(ceil_div(p.kb, sp));
+  p.splits = static_cast<int>(ceil_div(p.kb, p.kb_per_split));  // every slice non-empty
+  p.stages = cfg.stages > 0 ? cfg.stages : auto_stages(cfg.block_n, smem_optin);
+  size_t off = 0;
+  const size_t tiles = static_cast<size_t>(p.tiles_p) * p.tiles_q;
+  if (p.splits > 1) {
+    p.off_counters = off;
+    off = align256(off + tiles * sizeof(unsigned));
+    p.off_partial = off;
+    off = align256(off + tiles * p.splits * 128 * cfg.block_n * sizeof(float));
+  }
+  if (q_dtype == W8A8_INT8) {
+    p.off_a16 = off;
+    off = align256(off + static_cast<size_t>(M) * K * 2);
+    p.off_b16 = off;
+    off = align256(off + static_cast<size_t>(N) * K * 2);
+  }
+  p.total = off;
+  return p;
+}
+
+w8a8_status validate_config(const w8a8_mm_config& c, int q_dtype, int smem_optin) {
+  if (c.swap_ab != 0 && c.swap_ab != 1) return fail(W8A8_ERR_UNSUPPORTED, "swap_ab must be 0 or 1");
+  if (!valid_block_n(c.block_n, q_dtype))
+    return fail(W8A8_ERR_UNSUPPORTED, "block_n %d not supported (16..256 powers of two; <= 128 for int8)",
+                c.block_n);
+  if (c.split_k < 1 || c.split_k > 64) return fail(W8A8_ERR_UNSUPPORTED, "split_k must be in [1, 64]");
+  if (c.stages != 0 && (c.stages < 2 || c.stages > 8))
+    return fail(W8A8_ERR_UNSUPPORTED, "stages must be 0 (auto) or in [2, 8]");
+  const int st = c.stages > 0 ? c.stages : auto_stages(c.block_n, smem_optin);
+  if (gemm_smem_bytes(c.block_n, st) > smem_optin)
+    return fail(W8A8_ERR_UNSUPPORTED, "stages=%d with block_n=%d needs %d bytes of shared memory (> %d)", st,
+                c.block_n, gemm_smem_bytes(c.block_n, st), smem_optin);
+  return W8A8_OK;
+}
+
+w8a8_status validate_mm(const void* a_q, long long lda, const void* b_q, long long ldb, const float* sa,
+                        int a_gran, const float* sb, int b_gran, void* out, long long ldc, long long M,
+                        long long N, long long K, int q_dtype, int out_dtype) {
+  if (!a_q || !b_q || !sa || !sb || !out) return fail(W8A8_ERR_INVALID_ARG, "null pointer argument");
+  if (q_dtype != W8A8_E4M3 && q_dtype != W8A8_INT8)
+    return fail(W8A8_ERR_INVALID_ARG, "q_dtype must be W8A8_E4M3 or W8A8_INT8");
+  if (out_dtype != W8A8_BF16 && out_dtype != W8A8_FP16 && out_dtype != W8A8_FP32 && out_dtype != W8A8_INT32)
+    return fail(W8A8_ERR_INVALID_ARG, "out_dtype must be BF16, FP16, FP32 or INT32");
+  if ((out_dtype == W8A8_FP32 && q_dtype != W8A8_E4M3) || (out_dtype == W8A8_INT32 && q_dtype != W8A8_INT8))
+    return fail(W8A8_ERR_UNSUPPORTED, "FP32 output is for e4m3 operands and INT32 output for int8 operands");
+  if ((a_gran != W8A8_PER_TENSOR && a_gran != W8A8_PER_ROW) || (b_gran != W8A8_PER_TENSOR && b_gran != W8A8_PER_ROW))
+    return fail(W8A8_ERR_INVALID_ARG, "granularity must be W8A8_PER_TENSOR or W8A8_PER_ROW");
+  if (M < 1 || N < 1 || K < 1) return fail(W8A8_ERR_INVALID_ARG, "M, N, K must be >= 1 (got %lld, %lld, %lld)", M, N, K);
+  if (M >= (1LL << 31) || N >= (1LL << 31) || K >= (1LL << 31))
+    return fail(W8A8_ERR_UNSUPPORTED, "M, N, K must be < 2^31");
+  if (lda < K || ldb < K) return fail(W8A8_ERR_INVALID_ARG, "lda and ldb must be >= K (%lld)", K);
+  if (ldc < N) return fail(W8A8_ERR_INVALID_ARG, "ldc must be >= N (%lld)", N);
+  if (q_dtype == W8A8_INT8 && K > 131071)
+    return fail(W8A8_ERR_UNSUPPORTED, "int8 needs K <= 131071 so that int32 cannot overflow");
+  if (q_dtype == W8A8_INT8 && K % 16 != 0) return fail(W8A8_ERR_UNSUPPORTED, "int8 needs K to be a multiple of 16");
+  if (!aligned(a_q, 16) || !aligned(b_q, 16))
+    return fail(W8A8_ERR_MISALIGNED, "A and B must be 16-byte aligned (B must be stored [N, K], K contiguous)");
+  if (lda % 16 != 0 || ldb % 16 != 0)
+    return fail(W8A8_ERR_MISALIGNED, "lda and ldb must be multiples of 16 bytes (got %lld, %lld)", lda, ldb);
+  if (!aligned(out, out_dtype >= W8A8_FP32 ? 4 : 2)) return fail(W8A8_ERR_MISALIGNED, "out is not element-aligned");
+  if (!aligned(sa, 4) || !aligned(sb, 4)) return fail(W8A8_ERR_MISALIGNED, "scales must be 4-byte aligned");
+  return W8A8_OK;
+}
+
+w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ldb, const float* sa, int a_gran,
+                   const float* sb, int b_gran, void* out, long long ldc, long long M, long long N, long long K,
+                   int q_dtype, int out_dtype, void* ws, size_t ws_bytes, const w8a8_mm_config* user_cfg,
+                   cudaStream_t stream) {
+  w8a8_status st = validate_mm(a_q, lda, b_q, ldb, sa, a_gran, sb, b_gran, out, ldc, M, N, K, q_dtype, out_dtype);
+  if (st != W8A8_OK) return st;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != W8A8_OK) return st;
+  w8a8_mm_config cfg;
+  if (user_cfg) {
+    cfg = *user_cfg;
+    w8a8_mm_config a;
+    auto_config(M, N, K, q_dtype, dev.sms, &a);
+    if (cfg.block_n == 0) cfg.block_n = a.block_n;
+    if (cfg.split_k == 0) cfg.split_k = a.split_k;
+  } else {
+    auto_config(M, N, K, q_dtype, dev.sms, &cfg);
+  }
+  if ((st = validate_config(cfg, q_dtype, dev.smem_optin)) != W8A8_OK) return st;
+  const Plan plan = make_plan(M, N, K, q_dtype, cfg, dev.smem_optin);
+  if (plan.total > 0) {
+    if (!ws) return fail(W8A8_ERR_WORKSPACE, "this problem needs %zu bytes of workspace", plan.total);
+    if (ws_bytes < plan.total)
+      return fail(W8A8_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes, plan.total);
+    if (!aligned(ws, 256)) return fail(W8A8_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+  }
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const bool i8 = (q_dtype == W8A8_INT8);
+  const void* a_op = a_q;
+  const void* b_op = b_q;
+  long long lda_b = lda, ldb_b = ldb;
+  cudaError_t e;
+  if (i8) {
+    // exact int8 -> f16 widening of both operands into the workspace
+    if ((e = launch_int8_widen(a_q, lda, static_cast<int>(M), static_cast<int>(K), wsb + plan.off_a16, stream)) !=
+        cudaSuccess)
+      return cuda_fail(e, "int8 widen (A) launch");
+    if ((e = launch_int8_widen(b_q, ldb, static_cast<int>(N), static_cast<int>(K), wsb + plan.off_b16, stream)) !=
+        cudaSuccess)
+      return cuda_fail(e, "int8 widen (B) launch");
+    a_op = wsb + plan.off_a16;
+    b_op = wsb + plan.off_b16;
+    lda_b = K * 2;
+    ldb_b = K * 2;
+  }
+  CUtensorMap tp, tq;
+  const void* p_base = cfg.swap_ab ? b_op : a_op;
+  const void* q_base = cfg.swap_ab ? a_op : b_op;
+  const long long p_rows = cfg.swap_ab ? N : M;
+  const long long q_rows = cfg.swap_ab ? M : N;
+  const long long p_ld = cfg.swap_ab ? ldb_b : lda_b;
+  const long long q_ld = cfg.swap_ab ? lda_b : ldb_b;
+  if ((st = make_operand_map(&tp, p_base, i8, p_rows, K, p_ld, 128)) != W8A8_OK) return st;
+  if ((st = make_operand_map(&tq, q_base, i8, q_rows, K, q_ld, cfg.block_n)) != W8A8_OK) return st;
+
+  MmParams prm{};
+  prm.M = static_cast<int>(M);
+  prm.N = static_cast<int>(N);
+  prm.K = static_cast<int>(K);
+  prm.tiles_p = plan.tiles_p;
+  prm.tiles_q = plan.tiles_q;
+  prm.num_kb = plan.kb;
+  prm.kb_per_split = plan.kb_per_split;
+  prm.splits = plan.splits;
+  prm.scale_a = sa;
+  prm.a_per_row = (a_gran == W8A8_PER_ROW);
+  prm.scale_b = sb;
+  prm.b_per_row = (b_gran == W8A8_PER_ROW);
+  prm.out = out;
+  prm.ldc = ldc;
+  const long long out_elem = out_dtype >= W8A8_FP32 ? 4 : 2;
+  prm.out_vec_ok = aligned(out, 16) && ((ldc * out_elem) % 16 == 0);
+  prm.partial = plan.splits > 1 ? reinterpret_cast<float*>(wsb + plan.off_partial) : nullptr;
+  prm.counters = plan.splits > 1 ? reinterpret_cast<unsigned*>(wsb + plan.off_counters) : nullptr;
+  prm.kchunk_kb = kInt8ChunkK / 64;
+  const int out_kind = out_dtype == W8A8_BF16 ? OUT_BF16 : out_dtype == W8A8_FP16 ? OUT_FP16 : OUT_RAW;
+  e = i8 ? launch_int8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream)
+         : launch_fp8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "scaled_mm kernel launch");
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* w8a8_last_error(void) { return t_last_error.c_str(); }
+
+int w8a8_version(void) { return 100; }
+
+size_t w8a8_scaled_quant_workspace_size(int64_t rows, int64_t cols, int gran, int mode) {
+  (void)rows;
+  (void)cols;
+  return (gran == W8A8_PER_TENSOR && mode == W8A8_DYNAMIC) ? 16 : 0;
+}
+
+w8a8_status w8a8_scaled_quant(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld_x, void* q,
+                              int q_dtype, int64_t ld_q, float* scale, int gran, int mode, void* workspace,
+                              size_t workspace_bytes, w8a8_stream_t stream) {
+  if (!x || !q || !scale) return fail(W8A8_ERR_INVALID_ARG, "null pointer argument");
+  if (x_dtype != W8A8_BF16 && x_dtype != W8A8_FP16) return fail(W8A8_ERR_INVALID_ARG, "x_dtype must be BF16 or FP16");
+  if (q_dtype != W8A8_E4M3 && q_dtype != W8A8_INT8) return fail(W8A8_ERR_INVALID_ARG, "q_dtype must be E4M3 or INT8");
+  if (gran != W8A8_PER_TENSOR && gran != W8A8_PER_ROW) return fail(W8A8_ERR_INVALID_ARG, "bad granularity");
+  if (mode != W8A8_DYNAMIC && mode != W8A8_STATIC) return fail(W8A8_ERR_INVALID_ARG, "bad mode");
+  if (rows < 1 || cols < 1) return fail(W8A8_ERR_INVALID_ARG, "rows and cols must be >= 1");
+  if (rows >= (1LL << 31) || rows * cols >= (1LL << 40)) return fail(W8A8_ERR_UNSUPPORTED, "tensor too large");
+  if (ld_x < cols || ld_q < cols) return fail(W8A8_ERR_INVALID_ARG, "leading dimensions must be >= cols");
+  if (!aligned(x, 2)) return fail(W8A8_ERR_MISALIGNED, "x must be 2-byte aligned");
+  if (!aligned(scale, 4)) return fail(W8A8_ERR_MISALIGNED, "scale must be 4-byte aligned");
+  const size_t need = w8a8_scaled_quant_workspace_size(rows, cols, gran, mode);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need)
+      return fail(W8A8_ERR_WORKSPACE, "dynamic per-tensor quantisation needs %zu bytes of workspace", need);
+    if (!aligned(workspace, 4)) return fail(W8A8_ERR_MISALIGNED, "workspace must be 4-byte aligned");
+  }
+  DeviceInfo dev;
+  w8a8_status st = device_info(&dev);
+  if (st != W8A8_OK) return st;
+  QuantArgs a{};
+  a.x = x;
+  a.x_kind = (x_dtype == W8A8_BF16) ? 0 : 1;
+  a.rows = rows;
+  a.cols = cols;
+  a.ld_x = ld_x;
+  a.q = q;
+  a.q_kind = (q_dtype == W8A8_E4M3) ? 0 : 1;
+  a.ld_q = ld_q;
+  a.scale = scale;
+  a.per_row = (gran == W8A8_PER_ROW);
+  a.dynamic = (mode == W8A8_DYNAMIC);
+  a.amax_word = static_cast<unsigned*>(workspace);
+  a.vec = aligned(x, 16) && (ld_x % 8 == 0) && aligned(q, 16) && (ld_q % 8 == 0);
+  cudaError_t e = launch_quant(a, dev.sms, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "scaled_quant launch");
+  return ok();
+}
+
+w8a8_status w8a8_scaled_dequant(const void* q, int q_dtype, int64_t rows, int64_t cols, int64_t ld_q,
+                                const float* scale, int gran, void* y, int y_dtype, int64_t ld_y,
+                                w8a8_stream_t stream) {
+  if (!q || !scale || !y) return fail(W8A8_ERR_INVALID_ARG, "null pointer argument");
+  if (q_dtype != W8A8_E4M3 && q_dtype != W8A8_INT8) return fail(W8A8_ERR_INVALID_ARG, "q_dtype must be E4M3 or INT8");
+  if (y_dtype != W8A8_BF16 && y_dtype != W8A8_FP16) return fail(W8A8_ERR_INVALID_ARG, "y_dtype must be BF16 or FP16");
+  if (gran != W8A8_PER_TENSOR && gran != W8A8_PER_ROW) return fail(W8A8_ERR_INVALID_ARG, "bad granularity");
+  if (rows < 1 || cols < 1) return fail(W8A8_ERR_INVALID_ARG, "rows and cols must be >= 1");
+  if (rows >= (1LL << 31) || rows * cols >= (1LL << 40)) return fail(W8A8_ERR_UNSUPPORTED, "tensor too large");
+  if (ld_q < cols || ld_y < cols) return fail(W8A8_ERR_INVALID_ARG, "leading dimensions must be >= cols");
+  if (!aligned(y, 2)) return fail(W8A8_ERR_MISALIGNED, "y must be 2-byte aligned");
+  if (!aligned(scale, 4)) return fail(W8A8_ERR_MISALIGNED, "scale must be 4-byte aligned");
+  DeviceInfo dev;
+  w8a8_status st = device_info(&dev);
+  if (st != W8A8_OK) return st;
+  DequantArgs a{};
+  a.q = q;
+  a.q_kind = (q_dtype == W8A8_E4M3) ? 0 : 1;
+  a.rows = rows;
+  a.cols = cols;
+  a.ld_q = ld_q;
+  a.scale = scale;
+  a.per_row = (gran == W8A8_PER_ROW);
+  a.y = y;
+  a.y_kind = (y_dtype == W8A8_BF16) ? 0 : 1;
+  a.ld_y = ld_y;
+  a.vec = aligned(q, 16) && aligned(y, 16);
+  cudaError_t e = launch_dequant(a, dev.sms, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "scaled_dequant launch");
+  return ok();
+}
+
+w8a8_status w8a8_scaled_mm_pick_config(int64_t M, int64_t N, int64_t K, int q_dtype, w8a8_mm_config* cfg) {
+  if (!cfg) return fail(W8A8_ERR_INVALID_ARG, "cfg is null");
+  if (M < 1 || N < 1 || K < 1) return fail(W8A8_ERR_INVALID_ARG, "M, N, K must be >= 1");
+  if (q_dtype != W8A8_E4M3 && q_dtype != W8A8_INT8) return fail(W8A8_ERR_INVALID_ARG, "bad q_dtype");
+  int sms = 148;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
+  } else {
+    cudaGetLastError();
+  }
+  auto_config(M, N, K, q_dtype, sms, cfg);
+  return ok();
+}
+
+size_t w8a8_scaled_mm_config_workspace_size(int64_t M, int64_t N, int64_t K, int q_dtype,
+                                            const w8a8_mm_config* cfg) {
+  if (!cfg || M < 1 || N < 1 || K < 1) return 0;
+  w8a8_mm_config c = *cfg;
+  if (c.block_n == 0 || c.split_k == 0) {
+    w8a8_mm_config a;
+    w8a8_scaled_mm_pick_config(M, N, K, q_dtype, &a);
+    if (c.block_n == 0) c.block_n = a.block_n;
+    if (c.split_k == 0) c.split_k = a.split_k;
+  }
+  if (c.split_k < 1) c.split_k = 1;
+  return make_plan(M, N, K, q_dtype, c, 227 * 1024).total;
+}
+
+size_t w8a8_scaled_mm_workspace_size(int64_t M, int64_t N, int64_t K, int q_dtype) {
+  w8a8_mm_config c;
+  if (w8a8_scaled_mm_pick_config(M, N, K, q_dtype, &c) != W8A8_OK) return 0;
+  return w8a8_scaled_mm_config_workspace_size(M, N, K, q_dtype, &c);
+}
+
+w8a8_status w8a8_scaled_mm(const void* a_q, int64_t lda, const void* b_q, int64_t ldb, const float* scale_a,
+                           int a_gran, const float* scale_b, int b_gran, void* out, int64_t ldc, int64_t M,
+                           int64_t N, int64_t K, int q_dtype, int out_dtype, void* workspace,
+                           size_t workspace_bytes, w8a8_stream_t stream) {
+  return run_mm(a_q, lda, b_q, ldb, scale_a, a_gran, scale_b, b_gran, out, ldc, M, N, K, q_dtype, out_dtype,
+                workspace, workspace_bytes, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+w8a8_status w8a8_scaled_mm_with_config(const void* a_q, int64_t lda, const void* b_q, int64_t ldb,
+                                       const float* scale_a, int a_gran, const float* scale_b, int b_gran,
+                                       void* out, int64_t ldc, int64_t M, int64_t N, int64_t K, int q_dtype,
+                                       int out_dtype, void* workspace, size_t workspace_bytes,
+                                       const w8a8_mm_config* cfg, w8a8_stream_t stream) {
+  if (!cfg) return fail(W8A8_ERR_INVALID_ARG, "cfg is null");
+  return run_mm(a_q, lda, b_q, ldb, scale_a, a_gran, scale_b, b_gran, out, ldc, M, N, K, q_dtype, out_dtype,
+                workspace, workspace_bytes, cfg, reinterpret_cast<cudaStream_t>(stream));
+}
+
+w8a8_status w8a8_device_status(int* flags) {
+  if (!flags) return fail(W8A8_ERR_INVALID_ARG, "flags is null");
+  cudaError_t e = read_clear_device_status(flags);
+  if (e != cudaSuccess) return cuda_fail(e, "device status read");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,523 @@
+// gemm.cu -- the scaled matmul kernels (sm_103a).
+//
+// out[m, n] = round16(((float)sum_k A[m, k] B[n, k]) * scale_a[m|0] * scale_b[n|0])
+// ("[Kernel] Add w8a8 CUTLASS kernels", feature list of cutlass_scaled_mm_dq:
+// per-tensor / per-token activation scales, per-tensor / per-channel weight
+// scales, bf16 / fp16 output, dequantisation fused into the GEMM epilogue so
+// the output is written once.)
+//
+// One CTA of 128 threads computes one 128 x BN output tile (or one K slice of
+// it):
+//   warp 0, one lane : TMA producer -- loads 128-byte-wide K blocks of both
+//                      operands into a ring of shared-memory stages
+//                      (128-byte swizzle), signalling a "full" mbarrier;
+//   warp 1           : allocates TMEM; one lane issues tcgen05.mma for each
+//                      K block and commits to the stage's "empty" mbarrier so
+//                      the producer can refill it;
+//   all four warps   : epilogue -- tcgen05.ld of the accumulator lanes (warp
+//                      w owns TMEM lanes 32w..32w+31), scale, round, store.
+//
+// fp8 e4m3 operands go straight to tcgen05 kind::f8f6f4 with an fp32
+// accumulator.  int8 operands (tcgen05 kind::i8 is not available on sm_103a)
+// arrive as f16 planes (int8 -> f16 is exact) and use kind::f16.  Products
+// are at most 2^14, so an fp32 accumulator holds the exact integer sum for up
+// to 1024 K; the MMA issuer therefore alternates two TMEM accumulators per
+// K chunk of <= 1024 and the epilogue warps drain each finished chunk into an
+// exact int32 total kept in a third TMEM region.
+//
+// Split-K (used when there are too few output tiles to fill the GPU, i.e.
+// small-M decode): every slice writes its partial tile to the workspace; the
+// last slice to arrive (atomic counter per tile) sums the partials in slice
+// order 0..S-1 -- a fixed order, so results do not depend on scheduling --
+// applies the epilogue and resets the counter to zero.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "sm103_ptx.cuh"
+
+namespace w8a8 {
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kTileP = 128;       // rows of the P operand per tile (MMA M)
+constexpr int kRowBytes = 128;    // bytes of K per stage row (one swizzle row)
+constexpr int kPBytes = kTileP * kRowBytes;
+
+__host__ __device__ constexpr int tmem_cols_for(int bn, bool int8) {
+  // fp8: one fp32 accumulator of bn columns.  int8: two fp32 chunk
+  // accumulators + one int32 total.
+  int need = int8 ? 3 * bn : bn;
+  int c = 32;
+  while (c < need) c *= 2;
+  return c;
+}
+
+// Output element conversion.  16-bit outputs round to nearest even; FP32
+// stores y = (acc * s_a) * s_b unrounded; INT32 stores the raw accumulator
+// (scales not applied).
+template <typename OutT>
+struct OutConv;
+template <>
+struct OutConv<__nv_bfloat16> {
+  template <typename V>
+  __device__ __forceinline__ static __nv_bfloat16 conv(V v, float sa, float sb) {
+    return __float2bfloat16_rn((static_cast<float>(v) * sa) * sb);
+  }
+};
+template <>
+struct OutConv<__half> {
+  template <typename V>
+  __device__ __forceinline__ static __half conv(V v, float sa, float sb) {
+    return __float2half_rn((static_cast<float>(v) * sa) * sb);
+  }
+};
+template <>
+struct OutConv<float> {
+  template <typename V>
+  __device__ __forceinline__ static float conv(V v, float sa, float sb) {
+    return (static_cast<float>(v) * sa) * sb;
+  }
+};
+template <>
+struct OutConv<int> {
+  template <typename V>
+  __device__ __forceinline__ static int conv(V v, float, float) {
+    return static_cast<int>(v);
+  }
+};
+
+// Map a linear tile id to (tile_p, tile_q): tiles are walked in groups of
+// `group` P-tiles, Q fastest inside a group, so concurrently running CTAs
+// share operand tiles in L2.
+__device__ __forceinline__ void tile_coords(int t, int tiles_p, int tiles_q, int group, int& tp,
+                                            int& tq) {
+  const int per_group = group * tiles_q;
+  const int g = t / per_group;
+  const int first = g * group;
+  const int gsz = min(group, tiles_p - first);
+  const int local = t - g * per_group;
+  tp = first + local % gsz;
+  tq = local / gsz;
+}
+
+// Epilogue store of 16 consecutive accumulator columns of one TMEM lane.
+// Without swap the lane is an output row m and the columns are n; with swap
+// the lane is an output column n and the columns are rows m.  The scale
+// order is always (acc * scale_a) * scale_b.
+template <bool SWAP, typename OutT, typename V>
+__device__ __forceinline__ void store16(const MmParams& prm, int lane_idx, int col0, const V (&v)[16],
+                                        float s_lane) {
+  OutT* out = reinterpret_cast<OutT*>(prm.out);
+  if (!SWAP) {
+    const int m = lane_idx;
+    if (m >= prm.M) return;
+    OutT* row = out + static_cast<long long>(m) * prm.ldc;
+    if (prm.out_vec_ok && col0 + 16 <= prm.N) {
+      alignas(16) OutT o[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float sb = prm.b_per_row ? __ldg(prm.scale_b + col0 + j) : __ldg(prm.scale_b);
+        o[j] = OutConv<OutT>::conv(v[j], s_lane, sb);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(row + col0);
+      const uint4* src = reinterpret_cast<const uint4*>(o);
+#pragma unroll
+      for (int j = 0; j < static_cast<int>(sizeof(o) / 16); ++j) dst[j] = src[j];
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int n = col0 + j;
+        if (n < prm.N) {
+          const float sb = prm.b_per_row ? __ldg(prm.scale_b + n) : __ldg(prm.scale_b);
+          row[n] = OutConv<OutT>::conv(v[j], s_lane, sb);
+        }
+      }
+    }
+  } else {
+    const int n = lane_idx;
+    if (n >= prm.N) return;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int m = col0 + j;
+      if (m < prm.M) {
+        const float sa = prm.a_per_row ? __ldg(prm.scale_a + m) : __ldg(prm.scale_a);
+        out[static_cast<long long>(m) * prm.ldc + n] = OutConv<OutT>::conv(v[j], sa, s_lane);
+      }
+    }
+  }
+}
+
+template <int BN, bool SWAP, bool INT8, typename OutT>
+__global__ void __launch_bounds__(kThreads, 1)
+    w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_p,
+                     const __grid_constant__ CUtensorMap tmap_q, const MmParams prm, int stages,
+                     int group) {
+  constexpr int kQBytes = BN * kRowBytes;
+  constexpr int kStageBytes = kPBytes + kQBytes;
+  constexpr int kKbElems = INT8 ? 64 : 128;  // elements per 128-byte K block
+  constexpr uint32_t kIdesc = make_idesc(kTileP, BN, 0);
+  constexpr int kTmemCols = tmem_cols_for(BN, INT8);
+  constexpr int kGroups = BN / 16;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sp = smem;
+  uint8_t* sq = smem + stages * kPBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sq + stages * kQBytes);
+  // bars: full[stages], empty[stages], chunk_full[2], chunk_empty[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 4);
+  __shared__ int s_is_last;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  const int tiles = prm.tiles_p * prm.tiles_q;
+  const int split = blockIdx.x / tiles;
+  const int tile_lin_sched = blockIdx.x - split * tiles;
+  int tp, tq;
+  tile_coords(tile_lin_sched, prm.tiles_p, prm.tiles_q, group, tp, tq);
+  const int tile_lin = tp * prm.tiles_q + tq;
+  const int p0 = tp * kTileP;
+  const int q0 = tq * BN;
+  const int kb_begin = split * prm.kb_per_split;
+  const int kb_end = min(prm.num_kb, kb_begin + prm.kb_per_split);
+  const int nkb = kb_end - kb_begin;
+  const int chunk_kb = INT8 ? prm.kchunk_kb : (nkb > 0 ? nkb : 1);
+  const int nchunks = (nkb + chunk_kb - 1) / chunk_kb;
+
+  auto full_bar = [&](int s) { return smem_addr(bars + s); };
+  auto empty_bar = [&](int s) { return smem_addr(bars + stages + s); };
+  auto cfull_bar = [&](int b) { return smem_addr(bars + 2 * stages + b); };
+  auto cempty_bar = [&](int b) { return smem_addr(bars + 2 * stages + 2 + b); };
+
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tmap_p);
+    prefetch_tensormap(&tmap_q);
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(cfull_bar(0), 1);
+    mbar_init(cfull_bar(1), 1);
+    mbar_init(cempty_bar(0), kThreads);
+    mbar_init(cempty_bar(1), kThreads);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % stages;
+        const uint32_t ph = (i / stages) & 1;
+        if (!mbar_wait(empty_bar(s), ph ^ 1)) break;
+        mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+        const int kx = (kb_begin + i) * kKbElems;
+        tma_load_2d(smem_addr(sp + s * kPBytes), &tmap_p, full_bar(s), kx, p0);
+        tma_load_2d(smem_addr(sq + s * kQBytes), &tmap_q, full_bar(s), kx, q0);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = true;
+      int i = 0;
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int buf = c & 1;
+        if (c >= 2) {
+          // the epilogue must have drained this accumulator (chunk c - 2)
+          if (!mbar_wait(cempty_bar(buf), ((c - 2) >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+        }
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        const int i_end = min(nkb, i + chunk_kb);
+        for (int first = 1; i < i_end; ++i, first = 0) {
+          const int s = i % stages;
+          const uint32_t ph = (i / stages) & 1;
+          if (!mbar_wait(full_bar(s), ph)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t da = smem_desc_sw128(smem_addr(sp + s * kPBytes));
+          const uint64_t db = smem_desc_sw128(smem_addr(sq + s * kQBytes));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+            if (INT8)
+              mma_f16(d_tmem, da + 2 * kk, db + 2 * kk, kIdesc, acc);
+            else
+              mma_f8f6f4(d_tmem, da + 2 * kk, db + 2 * kk, kIdesc, acc);
+          }
+          mma_commit(empty_bar(s));
+        }
+        mma_commit(cfull_bar(buf));
+      }
+      if (!ok) {
+        // let the epilogue through; its result is discarded (status flagged)
+        mma_commit(cfull_bar(0));
+        mma_commit(cfull_bar(1));
+      }
+    }
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------ epilogue
+  const int row = warp * 32 + lane;  // TMEM lane == tile row on the P side
+  const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+  const int lane_idx = p0 + row;     // global P row of this thread
+  float s_lane;
+  if (!SWAP)
+    s_lane = (lane_idx < prm.M) ? (prm.a_per_row ? __ldg(prm.scale_a + lane_idx) : __ldg(prm.scale_a)) : 0.f;
+  else
+    s_lane = (lane_idx < prm.N) ? (prm.b_per_row ? __ldg(prm.scale_b + lane_idx) : __ldg(prm.scale_b)) : 0.f;
+
+  bool ok = true;
+  const size_t tile_elems = static_cast<size_t>(kTileP) * BN;
+  uint32_t* part = nullptr;
+  if (prm.splits > 1)
+    part = reinterpret_cast<uint32_t*>(prm.partial) + (static_cast<size_t>(tile_lin) * prm.splits + split) * tile_elems;
+
+  for (int c = 0; c < nchunks; ++c) {
+    const int buf = c & 1;
+    if (!mbar_wait(cfull_bar(buf), (c >> 1) & 1)) { ok = false; }
+    tc_fence_after();
+    const bool last = (c == nchunks - 1);
+    const uint32_t acc_addr = lane_base + static_cast<uint32_t>(buf * BN);
+    const uint32_t tot_addr = lane_base + static_cast<uint32_t>(2 * BN);
+#pragma unroll 1
+    for (int g = 0; g < kGroups; ++g) {
+      uint32_t r[16];
+      tmem_ld16(acc_addr + g * 16, r);
+      if (INT8) {
+        uint32_t t[16];
+        if (c > 0) {
+          tmem_ld16(tot_addr + g * 16, t);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            t[j] = static_cast<uint32_t>(static_cast<int>(t[j]) + __float2int_rn(__uint_as_float(r[j])));
+        } else {
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) t[j] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[j])));
+        }
+        if (!last) {
+          tmem_st16(tot_addr + g * 16, t);
+        } else if (prm.splits > 1) {
+          uint4* dst = reinterpret_cast<uint4*>(part + (static_cast<size_t>(g) * kTileP + row) * 16);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(t[4 * j], t[4 * j + 1], t[4 * j + 2], t[4 * j + 3]);
+        } else if (ok) {
+          int v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = static_cast<int>(t[j]);
+          store16<SWAP, OutT>(prm, lane_idx, q0 + g * 16, v, s_lane);
+        }
+      } else {
+        tmem_ld_wait();
+        if (prm.splits > 1) {
+          uint4* dst = reinterpret_cast<uint4*>(part + (static_cast<size_t>(g) * kTileP + row) * 16);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        } else if (ok) {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+          store16<SWAP, OutT>(prm, lane_idx, q0 + g * 16, v, s_lane);
+        }
+      }
+    }
+    if (INT8 && !last) {
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(cempty_bar(buf));
+    }
+  }
+
+  if (prm.splits > 1) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const unsigned old = atomicAdd(prm.counters + tile_lin, 1u);
+      s_is_last = (old == static_cast<unsigned>(prm.splits - 1));
+    }
+    __syncthreads();
+    if (s_is_last) {
+      __threadfence();
+      const uint32_t* base = reinterpret_cast<const uint32_t*>(prm.partial) +
+                             static_cast<size_t>(tile_lin) * prm.splits * tile_elems;
+#pragma unroll 1
+      for (int g = 0; g < kGroups; ++g) {
+        if (INT8) {
+          int v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = 0;
+          for (int s = 0; s < prm.splits; ++s) {
+            const uint4* src = reinterpret_cast<const uint4*>(base + s * tile_elems + (static_cast<size_t>(g) * kTileP + row) * 16);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint4 u = __ldcg(src + j);
+              v[4 * j] += static_cast<int>(u.x);
+              v[4 * j + 1] += static_cast<int>(u.y);
+              v[4 * j + 2] += static_cast<int>(u.z);
+              v[4 * j + 3] += static_cast<int>(u.w);
+            }
+          }
+          if (ok) store16<SWAP, OutT>(prm, lane_idx, q0 + g * 16, v, s_lane);
+        } else {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = 0.f;
+          for (int s = 0; s < prm.splits; ++s) {
+            const float4* src = reinterpret_cast<const float4*>(base + s * tile_elems + (static_cast<size_t>(g) * kTileP + row) * 16);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              float4 u = __ldcg(src + j);
+              v[4 * j] += u.x;
+              v[4 * j + 1] += u.y;
+              v[4 * j + 2] += u.z;
+              v[4 * j + 3] += u.w;
+            }
+          }
+          if (ok) store16<SWAP, OutT>(prm, lane_idx, q0 + g * 16, v, s_lane);
+        }
+      }
+      if (threadIdx.x == 0) prm.counters[tile_lin] = 0u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int BN, bool SWAP, bool INT8, typename OutT>
+cudaError_t launch_one(const CUtensorMap& tp, const CUtensorMap& tq, const MmParams& p, int stages,
+                       cudaStream_t stream) {
+  auto kern = w8a8_gemm_kernel<BN, SWAP, INT8, OutT>;
+  const int smem = gemm_smem_bytes(BN, stages);
+  // the attribute is per function and device; setting it again is harmless
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int group = SWAP ? 1 : 8;
+  const int grid = p.tiles_p * p.tiles_q * p.splits;
+  kern<<<grid, kThreads, smem, stream>>>(tp, tq, p, stages, group);
+  return cudaGetLastError();
+}
+
+template <int BN, bool SWAP, bool INT8>
+cudaError_t launch_out(const CUtensorMap& tp, const CUtensorMap& tq, const MmParams& p, int out_kind,
+                       int stages, cudaStream_t stream) {
+  switch (out_kind) {
+    case OUT_BF16: return launch_one<BN, SWAP, INT8, __nv_bfloat16>(tp, tq, p, stages, stream);
+    case OUT_FP16: return launch_one<BN, SWAP, INT8, __half>(tp, tq, p, stages, stream);
+    case OUT_RAW:
+      if (INT8) return launch_one<BN, SWAP, INT8, int>(tp, tq, p, stages, stream);
+      return launch_one<BN, SWAP, INT8, float>(tp, tq, p, stages, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int BN, bool INT8>
+cudaError_t launch_swap(const CUtensorMap& tp, const CUtensorMap& tq, const MmParams& p, bool swap,
+                        int out_kind, int stages, cudaStream_t stream) {
+  return swap ? launch_out<BN, true, INT8>(tp, tq, p, out_kind, stages, stream)
+              : launch_out<BN, false, INT8>(tp, tq, p, out_kind, stages, stream);
+}
+
+template <bool INT8>
+cudaError_t dispatch(const CUtensorMap& tp, const CUtensorMap& tq, const MmParams& p, int block_n,
+                     bool swap, int out_kind, int stages, cudaStream_t stream) {
+  switch (block_n) {
+    case 16: return launch_swap<16, INT8>(tp, tq, p, swap, out_kind, stages, stream);
+    case 32: return launch_swap<32, INT8>(tp, tq, p, swap, out_kind, stages, stream);
+    case 64: return launch_swap<64, INT8>(tp, tq, p, swap, out_kind, stages, stream);
+    case 128: return launch_swap<128, INT8>(tp, tq, p, swap, out_kind, stages, stream);
+    case 256:
+      // int8 keeps 3 x block_n TMEM columns; 3 x 256 does not fit in 512
+      if (INT8) return cudaErrorInvalidValue;
+      return launch_swap<256, false>(tp, tq, p, swap, out_kind, stages, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// int8 [rows, K] (leading dim ld) -> f16 [rows, K] contiguous, exact.
+__global__ void widen_int8_kernel(const int8_t* __restrict__ src, long long ld, int rows, int K,
+                                  __half* __restrict__ dst) {
+  const int vpr = K / 16;  // K is a multiple of 16
+  const long long total = static_cast<long long>(rows) * vpr;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = i / vpr;
+    const int v = static_cast<int>(i - r * vpr);
+    const int4 w = __ldcs(reinterpret_cast<const int4*>(src + r * ld) + v);
+    const int8_t* b = reinterpret_cast<const int8_t*>(&w);
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      __half lo = __int2half_rn(b[2 * j]);
+      __half hi = __int2half_rn(b[2 * j + 1]);
+      o[j] = static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+    }
+    uint4* d = reinterpret_cast<uint4*>(dst + r * K) + 2 * v;
+    d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+}  // namespace
+
+int gemm_smem_bytes(int block_n, int stages) {
+  return stages * (kPBytes + block_n * kRowBytes) + 1024 /*alignment slack*/ + 256 /*barriers*/;
+}
+
+int max_stages_for(int block_n, int smem_budget) {
+  int s = (smem_budget - 1024 - 256) / (kPBytes + block_n * kRowBytes);
+  return s;
+}
+
+cudaError_t launch_fp8_gemm(const CUtensorMap& tmap_p, const CUtensorMap& tmap_q, const MmParams& p,
+                            int block_n, bool swap, int out_kind, int stages, cudaStream_t stream) {
+  return dispatch<false>(tmap_p, tmap_q, p, block_n, swap, out_kind, stages, stream);
+}
+
+cudaError_t launch_int8_gemm(const CUtensorMap& tmap_p, const CUtensorMap& tmap_q, const MmParams& p,
+                             int block_n, bool swap, int out_kind, int stages, cudaStream_t stream) {
+  return dispatch<true>(tmap_p, tmap_q, p, block_n, swap, out_kind, stages, stream);
+}
+
+cudaError_t read_clear_device_status(int* flags) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int));
+  if (e != cudaSuccess) return e;
+  const int zero = 0;
+  e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+  *flags = v;
+  return e;
+}
+
+cudaError_t launch_int8_widen(const void* src, long long ld_src, int rows, int K, void* dst_f16,
+                              cudaStream_t stream) {
+  const long long total = static_cast<long long>(rows) * (K / 16);
+  long long blocks = (total + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  widen_int8_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+      static_cast<const int8_t*>(src), ld_src, rows, K, static_cast<__half*>(dst_f16));
+  return cudaGetLastError();
+}
+
+}  // namespace w8a8

@@ -1,0 +1,89 @@
+// internal.h -- declarations shared by the library's translation units (not
+// part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace w8a8 {
+
+// Parameters of one scaled-matmul launch.  "P" is the operand on the
+// 128-row MMA side, "Q" the operand on the narrow (block_n) side.  Without
+// swap P = activations [M, K] and Q = weights [N, K]; with swap the roles
+// are exchanged, which keeps small-M (decode) problems on the tensor cores
+// with M padded only up to block_n.
+struct MmParams {
+  int M, N, K;
+  int tiles_p, tiles_q;  // tiles along the P rows (128 each) and Q rows (block_n each)
+  int num_kb;            // K blocks of 128 bytes
+  int kb_per_split;      // K blocks per split
+  int splits;            // >= 1; > 1 reduces fp32 partials in split order
+  const float* scale_a;
+  int a_per_row;
+  const float* scale_b;
+  int b_per_row;
+  void* out;
+  long long ldc;
+  int out_vec_ok;        // 16-byte vector stores allowed along n
+  float* partial;        // [tiles][splits][128 * block_n] fp32 (splits > 1)
+  unsigned* counters;    // [tiles] arrival counters (splits > 1), left zero
+  int kchunk_kb;         // int8 path: K blocks per exact fp32 chunk
+};
+
+// OUT_RAW: fp32 y = (acc * s_a) * s_b for the fp8 path, raw int32
+// accumulators for the int8 path.
+enum OutKind { OUT_BF16 = 0, OUT_FP16 = 1, OUT_RAW = 2 };
+
+// fp8 e4m3 GEMM (tcgen05 kind::f8f6f4).  Tensor maps are uint8 [rows, K]
+// with a 128x128 box for P and a block_n x 128 box for Q, 128-byte swizzle.
+cudaError_t launch_fp8_gemm(const CUtensorMap& tmap_p, const CUtensorMap& tmap_q,
+                            const MmParams& p, int block_n, bool swap, int out_kind,
+                            int stages, cudaStream_t stream);
+
+// int8 GEMM.  Operands are first widened to f16 planes (exact), then
+// multiplied with tcgen05 kind::f16 in K chunks small enough that the fp32
+// accumulator is exact; each chunk is drained into an int32 total.
+cudaError_t launch_int8_widen(const void* src, long long ld_src, int rows, int K,
+                              void* dst_f16, cudaStream_t stream);
+cudaError_t launch_int8_gemm(const CUtensorMap& tmap_p, const CUtensorMap& tmap_q,
+                             const MmParams& p, int block_n, bool swap, int out_kind,
+                             int stages, cudaStream_t stream);
+
+// Synchronises the device, then reads and clears the device status word.
+cudaError_t read_clear_device_status(int* flags);
+
+// Shared-memory bytes a GEMM launch needs (ring + barriers + alignment).
+int gemm_smem_bytes(int block_n, int stages);
+int max_stages_for(int block_n, int smem_budget);
+
+// Quantiser / dequantiser launchers.
+struct QuantArgs {
+  const void* x;
+  int x_kind;  // 0 bf16, 1 fp16
+  long long rows, cols, ld_x;
+  void* q;
+  int q_kind;  // 0 e4m3, 1 int8
+  long long ld_q;
+  float* scale;
+  int per_row;
+  int dynamic;
+  unsigned* amax_word;  // dynamic per-tensor only
+  int vec;              // 16-byte vector path allowed
+};
+cudaError_t launch_quant(const QuantArgs& a, int num_sms, cudaStream_t stream);
+
+struct DequantArgs {
+  const void* q;
+  int q_kind;
+  long long rows, cols, ld_q;
+  const float* scale;
+  int per_row;
+  void* y;
+  int y_kind;
+  long long ld_y;
+  int vec;
+};
+cudaError_t launch_dequant(const DequantArgs& a, int num_sms, cudaStream_t stream);
+
+}  // namespace w8a8

@@ -1,0 +1,475 @@
+// quant.cu -- the scaled quantiser and dequantiser kernels (sm_103a).
+//
+// Semantics ("Enable scaled FP8 (e4m3fn) KV cache on ROCm (AMD GPU)", section
+// "Scaling semantics"; "[Kernel] Support Fp8 Checkpoints (Dynamic + Static)",
+// PR description): scale = absmax / 448 for e4m3 (absmax / 127 for int8),
+// computed at run time (dynamic) or given (static), per tensor or per row
+// (token); q = sat_round(x / scale); dequant = decode(q) * scale.
+//
+// Exactness rules (the codes must match a correctly rounded reference bit
+// for bit): x / scale is an IEEE fp32 division (__fdiv_rn, never a reciprocal
+// multiply); e4m3 uses the hardware round-to-nearest-even satfinite
+// conversion with NaN canonicalised to 0x7F; int8 rounds half to even and
+// saturates; absmax uses fmaxf from 0 so NaN never wins.
+//
+// Kernels:
+//  - quant_rows: one 256-thread CTA per row; the row is read once into
+//    registers with 128-bit loads (up to 8 * 256 * VPT elements), reduced
+//    to absmax with warp shuffles (dynamic per-row), then converted from the
+//    registers and written with 64-bit stores.  Rows longer than the
+//    register budget are re-read (they are still in L2).
+//  - absmax_flat + quant_flat: dynamic per-tensor needs the absmax of the
+//    whole tensor before any code is written, so it is two grid-stride
+//    passes over a contiguous tensor (the absmax word is reduced with
+//    atomicMax on the float's bit pattern, valid for non-negative floats).
+//  - quant_flat alone: static per-tensor on a contiguous tensor.
+//  - dequant_flat / dequant_rows: decode(q) * scale rounded to bf16/fp16.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "internal.h"
+
+namespace w8a8 {
+
+namespace {
+
+constexpr int kRowThreads = 256;
+
+__device__ __forceinline__ float load_f(const uint16_t* p, int kind) {
+  const uint16_t b = *p;
+  return kind == 0 ? __bfloat162float(__ushort_as_bfloat16(b)) : __half2float(__ushort_as_half(b));
+}
+
+template <int KIND>
+__device__ __forceinline__ float cvt_in(uint16_t b) {
+  if (KIND == 0) return __bfloat162float(__ushort_as_bfloat16(b));
+  return __half2float(__ushort_as_half(b));
+}
+
+// 8 consecutive 16-bit inputs from a 128-bit word.
+template <int KIND>
+__device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[2 * j] = cvt_in<KIND>(static_cast<uint16_t>(u[j] & 0xFFFFu));
+    f[2 * j + 1] = cvt_in<KIND>(static_cast<uint16_t>(u[j] >> 16));
+  }
+}
+
+// Two fp32 -> two e4m3 codes (low byte = first), RNE, saturating; NaN -> 0x7F.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+  uint32_t out = r;
+  if (a != a) out = (out & 0xFF00u) | 0x7Fu;
+  if (b != b) out = (out & 0x00FFu) | 0x7F00u;
+  return out;
+}
+
+__device__ __forceinline__ uint32_t int8x1(float a) {
+  int i;
+  asm("cvt.rni.s32.f32 %0, %1;" : "=r"(i) : "f"(a));  // RNE; NaN -> 0; saturates to int32
+  i = max(-128, min(127, i));
+  return static_cast<uint32_t>(i) & 0xFFu;
+}
+
+template <int QK>
+__device__ __forceinline__ uint32_t enc4(float a, float b, float c, float d) {
+  if (QK == 0) return e4m3x2(a, b) | (e4m3x2(c, d) << 16);
+  return int8x1(a) | (int8x1(b) << 8) | (int8x1(c) << 16) | (int8x1(d) << 24);
+}
+
+template <int QK>
+__device__ __forceinline__ uint8_t enc1(float a) {
+  if (QK == 0) return static_cast<uint8_t>(e4m3x2(a, 0.f) & 0xFFu);
+  return static_cast<uint8_t>(int8x1(a));
+}
+
+template <int QK>
+__device__ __forceinline__ float scale_from_amax(float amax) {
+  return amax > 0.f ? __fdiv_rn(amax, QK == 0 ? 448.f : 127.f) : 1.f;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Block-wide max over kRowThreads threads; result broadcast to all.
+__device__ __forceinline__ float block_max(float v, float* red) {
+  v = warp_max(v);
+  const int w = threadIdx.x / 32, l = threadIdx.x % 32;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float r = (l < kRowThreads / 32) ? red[l] : 0.f;
+  r = warp_max(r);
+  __syncthreads();
+  return r;
+}
+
+// ---------------------------------------------------------------- per-row quantiser
+
+// VPT = 128-bit vectors cached per thread (0: vector path disabled, scalar).
+template <int XK, int QK, int VPT>
+__global__ void __launch_bounds__(kRowThreads)
+    quant_rows_kernel(const uint16_t* __restrict__ x, long long ld_x, long long cols,
+                      uint8_t* __restrict__ q, long long ld_q, float* __restrict__ scale,
+                      int per_row, int dynamic) {
+  __shared__ float red[kRowThreads / 32];
+  const long long row = blockIdx.x;
+  const uint16_t* xr = x + row * ld_x;
+  uint8_t* qr = q + row * ld_q;
+
+  if (VPT > 0) {
+    const long long nvec = cols / 8;
+    uint4 cache[VPT > 0 ? VPT : 1];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const long long v = threadIdx.x + static_cast<long long>(i) * kRowThreads;
+      if (v < nvec) {
+        cache[i] = __ldcs(reinterpret_cast<const uint4*>(xr) + v);
+        if (dynamic) {
+          float f[8];
+          unpack8<XK>(cache[i], f);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        }
+      }
+    }
+    // vectors beyond the register cache, and the scalar tail
+    for (long long v = threadIdx.x + static_cast<long long>(VPT) * kRowThreads; dynamic && v < nvec;
+         v += kRowThreads) {
+      float f[8];
+      unpack8<XK>(__ldg(reinterpret_cast<const uint4*>(xr) + v), f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    }
+    for (long long j = nvec * 8 + threadIdx.x; dynamic && j < cols; j += kRowThreads)
+      amax = fmaxf(amax, fabsf(cvt_in<XK>(xr[j])));
+
+    float s;
+    if (dynamic) {
+      amax = block_max(amax, red);
+      s = scale_from_amax<QK>(amax);
+      if (threadIdx.x == 0) scale[row] = s;
+    } else {
+      s = scale[per_row ? row : 0];
+    }
+
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const long long v = threadIdx.x + static_cast<long long>(i) * kRowThreads;
+      if (v < nvec) {
+        float f[8];
+        unpack8<XK>(cache[i], f);
+        uint2 o;
+        o.x = enc4<QK>(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
+        o.y = enc4<QK>(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
+        reinterpret_cast<uint2*>(qr)[v] = o;
+      }
+    }
+    for (long long v = threadIdx.x + static_cast<long long>(VPT) * kRowThreads; v < nvec;
+         v += kRowThreads) {
+      float f[8];
+      unpack8<XK>(__ldg(reinterpret_cast<const uint4*>(xr) + v), f);
+      uint2 o;
+      o.x = enc4<QK>(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
+      o.y = enc4<QK>(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
+      reinterpret_cast<uint2*>(qr)[v] = o;
+    }
+    for (long long j = nvec * 8 + threadIdx.x; j < cols; j += kRowThreads)
+      qr[j] = enc1<QK>(__fdiv_rn(cvt_in<XK>(xr[j]), s));
+  } else {
+    // scalar path for unaligned layouts
+    float s;
+    if (dynamic) {
+      float amax = 0.f;
+      for (long long j = threadIdx.x; j < cols; j += kRowThreads)
+        amax = fmaxf(amax, fabsf(cvt_in<XK>(xr[j])));
+      amax = block_max(amax, red);
+      s = scale_from_amax<QK>(amax);
+      if (threadIdx.x == 0) scale[row] = s;
+    } else {
+      s = scale[per_row ? row : 0];
+    }
+    for (long long j = threadIdx.x; j < cols; j += kRowThreads)
+      qr[j] = enc1<QK>(__fdiv_rn(cvt_in<XK>(xr[j]), s));
+  }
+}
+
+// ---------------------------------------------------------------- per-tensor (flat)
+
+template <int XK>
+__global__ void __launch_bounds__(256)
+    absmax_flat_kernel(const uint16_t* __restrict__ x, long long n, unsigned* __restrict__ word) {
+  __shared__ float red[8];
+  float amax = 0.f;
+  const long long nvec = n / 8;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  // 4 independent 128-bit loads in flight per thread
+  for (; v + 3 * stride < nvec; v += 4 * stride) {
+    uint4 w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) w[u] = __ldg(reinterpret_cast<const uint4*>(x) + v + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float f[8];
+      unpack8<XK>(w[u], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    }
+  }
+  for (; v < nvec; v += stride) {
+    float f[8];
+    unpack8<XK>(__ldg(reinterpret_cast<const uint4*>(x) + v), f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+  }
+  for (long long j = nvec * 8 + blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; j < n;
+       j += stride)
+    amax = fmaxf(amax, fabsf(cvt_in<XK>(x[j])));
+  amax = warp_max(amax);
+  const int w = threadIdx.x / 32, l = threadIdx.x % 32;
+  if (l == 0) red[w] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float r = (l < 8) ? red[l] : 0.f;
+    r = warp_max(r);
+    // non-negative, non-NaN floats order like their bit patterns
+    if (l == 0 && r > 0.f) atomicMax(word, __float_as_uint(r));
+  }
+}
+
+// Per-row absmax of a strided tensor, reduced into one word (per-tensor
+// dynamic on a non-contiguous view).
+template <int XK>
+__global__ void __launch_bounds__(kRowThreads)
+    absmax_rows_kernel(const uint16_t* __restrict__ x, long long ld_x, long long cols,
+                       unsigned* __restrict__ word) {
+  __shared__ float red[kRowThreads / 32];
+  const uint16_t* xr = x + static_cast<long long>(blockIdx.x) * ld_x;
+  float amax = 0.f;
+  for (long long j = threadIdx.x; j < cols; j += kRowThreads) amax = fmaxf(amax, fabsf(cvt_in<XK>(xr[j])));
+  amax = block_max(amax, red);
+  if (threadIdx.x == 0 && amax > 0.f) atomicMax(word, __float_as_uint(amax));
+}
+
+// q = enc(x / s) over a contiguous tensor, s from the absmax word (dynamic)
+// or from scale[0] (static).  16 elements per thread per step.
+template <int XK, int QK>
+__global__ void __launch_bounds__(256)
+    quant_flat_kernel(const uint16_t* __restrict__ x, long long n, uint8_t* __restrict__ q,
+                      float* __restrict__ scale, const unsigned* __restrict__ word, int dynamic) {
+  float s;
+  if (dynamic) {
+    s = scale_from_amax<QK>(__uint_as_float(*word));
+    if (blockIdx.x == 0 && threadIdx.x == 0) scale[0] = s;
+  } else {
+    s = __ldg(scale);
+  }
+  const long long n16 = n / 16;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  for (; v + stride < n16; v += 2 * stride) {
+    uint4 w[4];
+    w[0] = __ldcs(reinterpret_cast<const uint4*>(x) + 2 * v);
+    w[1] = __ldcs(reinterpret_cast<const uint4*>(x) + 2 * v + 1);
+    w[2] = __ldcs(reinterpret_cast<const uint4*>(x) + 2 * (v + stride));
+    w[3] = __ldcs(reinterpret_cast<const uint4*>(x) + 2 * (v + stride) + 1);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float f[16];
+      unpack8<XK>(w[2 * u], *reinterpret_cast<float(*)[8]>(f));
+      unpack8<XK>(w[2 * u + 1], *reinterpret_cast<float(*)[8]>(f + 8));
+      uint4 o;
+      o.x = enc4<QK>(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
+      o.y = enc4<QK>(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
+      o.z = enc4<QK>(__fdiv_rn(f[8], s), __fdiv_rn(f[9], s), __fdiv_rn(f[10], s), __fdiv_rn(f[11], s));
+      o.w = enc4<QK>(__fdiv_rn(f[12], s), __fdiv_rn(f[13], s), __fdiv_rn(f[14], s), __fdiv_rn(f[15], s));
+      __stcs(reinterpret_cast<uint4*>(q) + (u == 0 ? v : v + stride), o);
+    }
+  }
+  for (; v < n16; v += stride) {
+    float f[16];
+    unpack8<XK>(__ldcs(reinterpret_cast<const uint4*>(x) + 2 * v), *reinterpret_cast<float(*)[8]>(f));
+    unpack8<XK>(__ldcs(reinterpret_cast<const uint4*>(x) + 2 * v + 1), *reinterpret_cast<float(*)[8]>(f + 8));
+    uint4 o;
+    o.x = enc4<QK>(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
+    o.y = enc4<QK>(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
+    o.z = enc4<QK>(__fdiv_rn(f[8], s), __fdiv_rn(f[9], s), __fdiv_rn(f[10], s), __fdiv_rn(f[11], s));
+    o.w = enc4<QK>(__fdiv_rn(f[12], s), __fdiv_rn(f[13], s), __fdiv_rn(f[14], s), __fdiv_rn(f[15], s));
+    __stcs(reinterpret_cast<uint4*>(q) + v, o);
+  }
+  for (long long j = n16 * 16 + blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; j < n;
+       j += stride)
+    q[j] = enc1<QK>(__fdiv_rn(cvt_in<XK>(x[j]), s));
+}
+
+// Per-row quantiser driven by a per-tensor scale from the absmax word (the
+// second pass of dynamic per-tensor on a strided view).
+template <int XK, int QK>
+__global__ void __launch_bounds__(kRowThreads)
+    quant_rows_from_word_kernel(const uint16_t* __restrict__ x, long long ld_x, long long cols,
+                                uint8_t* __restrict__ q, long long ld_q, float* __restrict__ scale,
+                                const unsigned* __restrict__ word) {
+  const float s = scale_from_amax<QK>(__uint_as_float(*word));
+  if (blockIdx.x == 0 && threadIdx.x == 0) scale[0] = s;
+  const uint16_t* xr = x + static_cast<long long>(blockIdx.x) * ld_x;
+  uint8_t* qr = q + static_cast<long long>(blockIdx.x) * ld_q;
+  for (long long j = threadIdx.x; j < cols; j += kRowThreads) qr[j] = enc1<QK>(__fdiv_rn(cvt_in<XK>(xr[j]), s));
+}
+
+// ---------------------------------------------------------------- dequantiser
+
+template <int QK>
+__device__ __forceinline__ float dec1(uint8_t c) {
+  if (QK == 0) {
+    __nv_fp8_e4m3 v;
+    v.__x = c;
+    return static_cast<float>(v);  // exact
+  }
+  return static_cast<float>(static_cast<int8_t>(c));
+}
+
+template <int YK>
+__device__ __forceinline__ uint16_t out16(float y) {
+  if (YK == 0) return __bfloat16_as_ushort(__float2bfloat16_rn(y));
+  return __half_as_ushort(__float2half_rn(y));
+}
+
+template <int QK, int YK>
+__global__ void __launch_bounds__(256)
+    dequant_flat_kernel(const uint8_t* __restrict__ q, long long n, const float* __restrict__ scale,
+                        uint16_t* __restrict__ y) {
+  const float s = __ldg(scale);
+  const long long n16 = n / 16;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; v < n16; v += stride) {
+    const uint4 w = __ldcs(reinterpret_cast<const uint4*>(q) + v);
+    const uint8_t* b = reinterpret_cast<const uint8_t*>(&w);
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      o[j] = static_cast<uint32_t>(out16<YK>(dec1<QK>(b[2 * j]) * s)) |
+             (static_cast<uint32_t>(out16<YK>(dec1<QK>(b[2 * j + 1]) * s)) << 16);
+    uint4* d = reinterpret_cast<uint4*>(y) + 2 * v;
+    __stcs(d, make_uint4(o[0], o[1], o[2], o[3]));
+    __stcs(d + 1, make_uint4(o[4], o[5], o[6], o[7]));
+  }
+  for (long long j = n16 * 16 + blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; j < n;
+       j += stride)
+    y[j] = out16<YK>(dec1<QK>(q[j]) * s);
+}
+
+template <int QK, int YK>
+__global__ void __launch_bounds__(kRowThreads)
+    dequant_rows_kernel(const uint8_t* __restrict__ q, long long ld_q, long long cols,
+                        const float* __restrict__ scale, int per_row, uint16_t* __restrict__ y,
+                        long long ld_y) {
+  const long long row = blockIdx.x;
+  const float s = __ldg(scale + (per_row ? row : 0));
+  const uint8_t* qr = q + row * ld_q;
+  uint16_t* yr = y + row * ld_y;
+  for (long long j = threadIdx.x; j < cols; j += kRowThreads) yr[j] = out16<YK>(dec1<QK>(qr[j]) * s);
+}
+
+// ---------------------------------------------------------------- launch helpers
+
+template <int XK, int QK>
+cudaError_t launch_rows(const QuantArgs& a, cudaStream_t st) {
+  const uint16_t* x = static_cast<const uint16_t*>(a.x);
+  uint8_t* q = static_cast<uint8_t*>(a.q);
+  const long long nvec = a.cols / 8;
+  const long long per_thread = (nvec + kRowThreads - 1) / kRowThreads;
+  const dim3 grid(static_cast<unsigned>(a.rows));
+  if (!a.vec) {
+    quant_rows_kernel<XK, QK, 0><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.per_row, a.dynamic);
+  } else if (per_thread <= 1) {
+    quant_rows_kernel<XK, QK, 1><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.per_row, a.dynamic);
+  } else if (per_thread <= 2) {
+    quant_rows_kernel<XK, QK, 2><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.per_row, a.dynamic);
+  } else if (per_thread <= 4) {
+    quant_rows_kernel<XK, QK, 4><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.per_row, a.dynamic);
+  } else if (per_thread <= 8) {
+    quant_rows_kernel<XK, QK, 8><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.per_row, a.dynamic);
+  } else {
+    quant_rows_kernel<XK, QK, 16><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.per_row, a.dynamic);
+  }
+  return cudaGetLastError();
+}
+
+int flat_blocks(long long work_items, int num_sms) {
+  long long b = (work_items + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms) * 8;
+  if (b > cap) b = cap;
+  if (b < 1) b = 1;
+  return static_cast<int>(b);
+}
+
+template <int XK, int QK>
+cudaError_t launch_quant_t(const QuantArgs& a, int num_sms, cudaStream_t st) {
+  const uint16_t* x = static_cast<const uint16_t*>(a.x);
+  uint8_t* q = static_cast<uint8_t*>(a.q);
+  const bool contiguous = (a.ld_x == a.cols && a.ld_q == a.cols) || a.rows == 1;
+  if (a.per_row) return launch_rows<XK, QK>(a, st);
+  if (!a.dynamic) {
+    if (contiguous && a.vec) {
+      const long long n = a.rows * a.cols;
+      quant_flat_kernel<XK, QK><<<flat_blocks(n / 16, num_sms), 256, 0, st>>>(x, n, q, a.scale, nullptr, 0);
+      return cudaGetLastError();
+    }
+    return launch_rows<XK, QK>(a, st);
+  }
+  // dynamic per-tensor: absmax pass, then quantise pass
+  cudaError_t e = cudaMemsetAsync(a.amax_word, 0, sizeof(unsigned), st);
+  if (e != cudaSuccess) return e;
+  if (contiguous && a.vec) {
+    const long long n = a.rows * a.cols;
+    absmax_flat_kernel<XK><<<flat_blocks(n / 8, num_sms), 256, 0, st>>>(x, n, a.amax_word);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    quant_flat_kernel<XK, QK><<<flat_blocks(n / 16, num_sms), 256, 0, st>>>(x, n, q, a.scale, a.amax_word, 1);
+    return cudaGetLastError();
+  }
+  const dim3 grid(static_cast<unsigned>(a.rows));
+  absmax_rows_kernel<XK><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, a.amax_word);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  quant_rows_from_word_kernel<XK, QK><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.amax_word);
+  return cudaGetLastError();
+}
+
+template <int QK, int YK>
+cudaError_t launch_dequant_t(const DequantArgs& a, int num_sms, cudaStream_t st) {
+  const uint8_t* q = static_cast<const uint8_t*>(a.q);
+  uint16_t* y = static_cast<uint16_t*>(a.y);
+  const bool contiguous = (a.ld_q == a.cols && a.ld_y == a.cols) || a.rows == 1;
+  if (!a.per_row && contiguous && a.vec) {
+    const long long n = a.rows * a.cols;
+    dequant_flat_kernel<QK, YK><<<flat_blocks(n / 16, num_sms), 256, 0, st>>>(q, n, a.scale, y);
+    return cudaGetLastError();
+  }
+  dequant_rows_kernel<QK, YK><<<static_cast<unsigned>(a.rows), kRowThreads, 0, st>>>(q, a.ld_q, a.cols, a.scale, a.per_row, y, a.ld_y);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quant(const QuantArgs& a, int num_sms, cudaStream_t st) {
+  if (a.x_kind == 0)
+    return a.q_kind == 0 ? launch_quant_t<0, 0>(a, num_sms, st) : launch_quant_t<0, 1>(a, num_sms, st);
+  return a.q_kind == 0 ? launch_quant_t<1, 0>(a, num_sms, st) : launch_quant_t<1, 1>(a, num_sms, st);
+}
+
+cudaError_t launch_dequant(const DequantArgs& a, int num_sms, cudaStream_t st) {
+  if (a.q_kind == 0)
+    return a.y_kind == 0 ? launch_dequant_t<0, 0>(a, num_sms, st) : launch_dequant_t<0, 1>(a, num_sms, st);
+  return a.y_kind == 0 ? launch_dequant_t<1, 0>(a, num_sms, st) : launch_dequant_t<1, 1>(a, num_sms, st);
+}
+
+}  // namespace w8a8

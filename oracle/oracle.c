@@ -170,12 +170,14 @@ double orc_e4m3_value(int code) {
   return s ? -v : v;
 }
 
-static double g_e4m3_table[127]; /* ascending values of codes 0x00..0x7E */
+static double g_e4m3_table[127];  /* ascending values of codes 0x00..0x7E */
+static double g_e4m3_decode[256]; /* value of every code, NaN for 0x7F/0xFF */
 static int g_table_ready = 0;
 
 static void build_table(void) {
   if (g_table_ready) return;
   for (int c = 0; c < 127; ++c) g_e4m3_table[c] = orc_e4m3_value(c);
+  for (int c = 0; c < 256; ++c) g_e4m3_decode[c] = orc_e4m3_value(c);
   g_table_ready = 1;
 }
 
@@ -217,7 +219,7 @@ int8_t orc_encode_int8(float v) {
 }
 
 static double decode_q(uint8_t c, int qdtype) {
-  return qdtype == ORC_E4M3 ? orc_e4m3_value(c) : (double)(int8_t)c;
+  return qdtype == ORC_E4M3 ? g_e4m3_decode[c] : (double)(int8_t)c;
 }
 
 /* ------------------------------------------------------------------ */
@@ -281,6 +283,7 @@ void orc_quant(const uint16_t* x, int x_dtype, int64_t rows, int64_t cols,
 void orc_dequant(const uint8_t* q, int q_dtype, int64_t rows, int64_t cols,
                  int64_t ld_q, const float* scale, int gran, uint16_t* y,
                  int y_dtype, int64_t ld_y) {
+  build_table();
 #pragma omp parallel for schedule(static)
   for (int64_t i = 0; i < rows; ++i) {
     float s = scale[gran == ORC_PER_ROW ? i : 0];
@@ -312,7 +315,7 @@ static void one_element(const uint8_t* A, int64_t lda, const uint8_t* B,
   float accf;
   if (q_dtype == ORC_E4M3) {
     double acc = 0.0;
-    for (int64_t k = 0; k < K; ++k) acc += orc_e4m3_value(a[k]) * orc_e4m3_value(b[k]);
+    for (int64_t k = 0; k < K; ++k) acc += g_e4m3_decode[a[k]] * g_e4m3_decode[b[k]];
     if (acc_out) *acc_out = acc;
     if (iacc_out) *iacc_out = 0;
     accf = (float)acc;

@@ -1,0 +1,111 @@
+"""Host-only checks of the C ABI: the library builds, loads and exports every
+symbol include/w8a8.h declares; invalid arguments come back as status codes
+(validated before any CUDA call, so nothing here touches a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import int8_w8a8_scaled_gb300 as w8
+from int8_w8a8_scaled_gb300 import _lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "w8a8.h")
+
+
+def header_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"W8A8_API\s+[\w\s\*]+?\b(w8a8_\w+)\s*\(", text)))
+
+
+def test_header_declares_expected_symbols():
+    assert header_symbols() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = _lib.load()
+    for name in header_symbols():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version_and_last_error():
+    lib = _lib.load()
+    assert lib.w8a8_version() >= 100
+    assert isinstance(lib.w8a8_last_error(), bytes)
+
+
+FAKE = ctypes.c_void_p(0x7F0000000000)      # never dereferenced: validation fails first
+FAKE_ODD = ctypes.c_void_p(0x7F0000000001)
+
+
+def mm(lib, a=FAKE, lda=64, b=FAKE, ldb=64, sa=FAKE, ag=0, sb=FAKE, bg=0, out=FAKE, ldc=64,
+       M=4, N=64, K=64, qd=w8.E4M3, od=w8.BF16, ws=None, wsb=0):
+    return lib.w8a8_scaled_mm(a, lda, b, ldb, sa, ag, sb, bg, out, ldc, M, N, K, qd, od, ws, wsb, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(a=None), 1), (dict(b=None), 1), (dict(sa=None), 1), (dict(sb=None), 1), (dict(out=None), 1),
+    (dict(qd=7), 1), (dict(od=9), 1), (dict(ag=3), 1), (dict(M=0), 1), (dict(N=-1), 1), (dict(K=0), 1),
+    (dict(lda=32), 1), (dict(ldc=10), 1),
+    (dict(od=w8.INT32), 2), (dict(qd=w8.INT8, od=w8.FP32), 2),
+    (dict(qd=w8.INT8, K=131072, lda=131072, ldb=131072), 2), (dict(qd=w8.INT8, K=40, lda=48, ldb=48), 2),
+    (dict(a=FAKE_ODD), 3), (dict(lda=72), 3), (dict(ldb=88), 3),
+])
+def test_scaled_mm_rejects_bad_arguments(kw, status):
+    lib = _lib.load()
+    assert mm(lib, **kw) == status
+    assert lib.w8a8_last_error()
+
+
+def test_b_not_k_major_is_a_status_not_a_crash():
+    """The CUTLASS review thread: passing B with the wrong layout used to end
+    in "misaligned address".  Here a row stride that is not a 16-byte
+    multiple is rejected with W8A8_ERR_MISALIGNED."""
+    lib = _lib.load()
+    assert mm(lib, M=8, N=8192, K=4096, lda=4096, ldb=4097, ldc=8192) == 3
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), 1), (dict(xd=w8.E4M3), 1), (dict(qd=w8.BF16), 1), (dict(rows=0), 1),
+    (dict(ldx=3), 1), (dict(gran=5), 1), (dict(mode=4), 1), (dict(x=FAKE_ODD), 3),
+    (dict(gran=0, mode=0), 4),
+])
+def test_scaled_quant_rejects_bad_arguments(kw, status):
+    lib = _lib.load()
+    a = dict(x=FAKE, xd=w8.BF16, rows=4, cols=64, ldx=64, q=FAKE, qd=w8.E4M3, ldq=64, scale=FAKE,
+             gran=1, mode=0, ws=None, wsb=0)
+    a.update(kw)
+    st = lib.w8a8_scaled_quant(a["x"], a["xd"], a["rows"], a["cols"], a["ldx"], a["q"], a["qd"], a["ldq"],
+                               a["scale"], a["gran"], a["mode"], a["ws"], a["wsb"], None)
+    assert st == status
+
+
+def test_scaled_dequant_rejects_bad_arguments():
+    lib = _lib.load()
+    assert lib.w8a8_scaled_dequant(None, 0, 4, 4, 4, FAKE, 0, FAKE, w8.BF16, 4, None) == 1
+    assert lib.w8a8_scaled_dequant(FAKE, 0, 4, 4, 4, FAKE, 0, FAKE, w8.E4M3, 4, None) == 1
+    assert lib.w8a8_scaled_dequant(FAKE, 0, 4, 4, 4, FAKE, 0, FAKE_ODD, w8.BF16, 4, None) == 3
+
+
+def test_workspace_sizes():
+    assert w8.quant_workspace_size(10, 10, per_token=False, dynamic=True) == 16
+    assert w8.quant_workspace_size(10, 10, per_token=True, dynamic=True) == 0
+    assert w8.quant_workspace_size(10, 10, per_token=False, dynamic=False) == 0
+    # no split, fp8: no workspace
+    assert w8.mm_workspace_size(4096, 4096, 4096, w8.E4M3) == 0
+    # int8 widens both operands to f16 planes
+    assert w8.mm_workspace_size(512, 256, 1024, w8.INT8) >= (512 + 256) * 1024 * 2
+    # split-K partials + counters
+    cfg = {"swap_ab": 1, "block_n": 16, "split_k": 4}
+    assert w8.mm_workspace_size(1, 4096, 4096, w8.E4M3, cfg) >= 32 * 4 * 128 * 16 * 4
+
+
+@pytest.mark.parametrize("M", [1, 16, 64, 256, 4096])
+def test_pick_config_regimes(M):
+    c = w8.pick_config(M, 4096, 4096, w8.E4M3)
+    assert c["swap_ab"] == (1 if M <= 256 else 0)
+    assert c["block_n"] in (16, 32, 64, 128, 256)
+    assert c["split_k"] >= 1
+    c8 = w8.pick_config(M, 4096, 4096, w8.INT8)
+    assert c8["block_n"] <= 128
