@@ -103,8 +103,10 @@ _ws_lock = threading.Lock()
 _default_ws: dict = {}
 
 
-def _default_workspace(device: torch.device, nbytes: int) -> Workspace:
-    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+def _default_workspace(device: torch.device, nbytes: int, kind: str) -> Workspace:
+    """Per (device, stream, kind) scratch; the matmul's buffer is never shared
+    with the quantiser (whose absmax word would land on a counter)."""
+    key = (kind, device.index, torch.cuda.current_stream(device).cuda_stream)
     with _ws_lock:
         ws = _default_ws.get(key)
         if ws is None:
@@ -136,7 +138,7 @@ def scaled_quant(x: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, per_toke
     mode = DYNAMIC if dynamic else STATIC
     need = lib.w8a8_scaled_quant_workspace_size(rows, cols, gran, mode)
     if need and workspace is None:
-        workspace = _default_workspace(x.device, need).buf
+        workspace = _default_workspace(x.device, need, "quant").buf
     check(lib.w8a8_scaled_quant(
         _ptr(x), _fkind(x), rows, cols, _ld(x), _ptr(q), _qkind(q, q_dtype), _ld(q),
         _ptr(scale), gran, mode, _ptr(workspace) if need else None,
@@ -217,7 +219,7 @@ def scaled_mm(a_q: torch.Tensor, b_q: torch.Tensor, scale_a: torch.Tensor, scale
     if isinstance(workspace, Workspace):
         workspace = workspace.ensure(need).buf
     elif workspace is None and need:
-        workspace = _default_workspace(a_q.device, need).buf
+        workspace = _default_workspace(a_q.device, need, "mm").buf
     ws_ptr = _ptr(workspace) if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     args = (_ptr(a_q), _ld(a_q), _ptr(b_q), _ld(b_q), _ptr(scale_a), a_gran, _ptr(scale_b), b_gran,

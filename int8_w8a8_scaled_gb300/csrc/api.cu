@@ -170,6 +170,14 @@ struct Plan {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Workspace layout.  The split-K arrival counters live in a fixed region at
+// the head of every workspace and nothing else is ever written there: each
+// call that uses them leaves them zero, so a zero-filled workspace stays valid
+// across calls of any shape and configuration (scratch data -- split-K
+// partials, int8 f16 planes -- always lives after the region).
+constexpr size_t kCounterSlots = 16384;
+constexpr size_t kCounterRegion = kCounterSlots * sizeof(unsigned);
+
 Plan make_plan(long long M, long long N, long long K, int q_dtype, const w8a8_mm_config& cfg, int smem_optin) {
   Plan p{};
   p.cfg = cfg;
@@ -182,11 +190,11 @@ Plan make_plan(long long M, long long N, long long K, int q_dtype, const w8a8_mm
   p.kb_per_split = static_cast<int>(ceil_div(p.kb, sp));
   p.splits = static_cast<int>(ceil_div(p.kb, p.kb_per_split));  // every slice non-empty
   p.stages = cfg.stages > 0 ? cfg.stages : auto_stages(cfg.block_n, smem_optin);
-  size_t off = 0;
   const size_t tiles = static_cast<size_t>(p.tiles_p) * p.tiles_q;
+  const bool need_ws = p.splits > 1 || q_dtype == W8A8_INT8;
+  size_t off = need_ws ? kCounterRegion : 0;
+  p.off_counters = 0;
   if (p.splits > 1) {
-    p.off_counters = off;
-    off = align256(off + tiles * sizeof(unsigned));
     p.off_partial = off;
     off = align256(off + tiles * p.splits * 128 * cfg.block_n * sizeof(float));
   }
@@ -264,6 +272,9 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
   }
   if ((st = validate_config(cfg, q_dtype, dev.smem_optin)) != W8A8_OK) return st;
   const Plan plan = make_plan(M, N, K, q_dtype, cfg, dev.smem_optin);
+  if (plan.splits > 1 && static_cast<size_t>(plan.tiles_p) * plan.tiles_q > kCounterSlots)
+    return fail(W8A8_ERR_UNSUPPORTED, "split_k > 1 supports at most %zu output tiles (got %d)", kCounterSlots,
+                plan.tiles_p * plan.tiles_q);
   if (plan.total > 0) {
     if (!ws) return fail(W8A8_ERR_WORKSPACE, "this problem needs %zu bytes of workspace", plan.total);
     if (ws_bytes < plan.total)

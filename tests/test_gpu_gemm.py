@@ -277,3 +277,33 @@ def test_split_k_workspace_is_left_zeroed():
 
 def test_no_device_timeouts_recorded():
     assert w8.device_status() == 0
+
+
+def test_shared_workspace_across_shapes_and_dtypes():
+    """One zero-filled workspace serves any sequence of calls: an int8 call
+    (f16 planes in the scratch area) followed by split-K calls must still
+    find zero arrival counters."""
+    ws = w8.Workspace(1 << 20)
+    seqs = [((130, 260, 2112), w8.INT8, None), ((5, 100, 1040), w8.INT8, {"swap_ab": 1, "block_n": 16, "split_k": 4}),
+            ((3, 300, 1024), w8.E4M3, {"swap_ab": 1, "block_n": 16, "split_k": 3}),
+            ((64, 512, 4096), w8.INT8, None), ((1, 1024, 4096), w8.E4M3, None)]
+    for (M, N, K), qd, cfg in seqs * 2:
+        if qd == w8.INT8:
+            A, B, sa, sb = int8_problem(M, N, K, seed=M + N)
+            ref = oracle.scaled_mm(A, B, sa, sb, oracle.INT8, oracle.FP16)
+            a_g, b_g = to_gpu_codes(A, oracle.INT8), to_gpu_codes(B, oracle.INT8)
+            acc = torch.empty(M, N, dtype=torch.int32, device="cuda")
+            w8.scaled_mm(a_g, b_g, torch.from_numpy(sa).cuda(), torch.from_numpy(sb).cuda(), acc,
+                         workspace=ws, config=cfg)
+            torch.cuda.synchronize()
+            assert np.array_equal(acc.cpu().numpy().astype(np.int64), ref["iacc"]), (M, N, K, cfg)
+        else:
+            A, B, sa, sb = fp8_problem(M, N, K, seed=M + N)
+            ref = oracle.scaled_mm(A, B, sa, sb, oracle.E4M3, oracle.BF16)
+            a_g, b_g = to_gpu_codes(A, oracle.E4M3), to_gpu_codes(B, oracle.E4M3)
+            out = torch.empty(M, N, dtype=torch.float32, device="cuda")
+            w8.scaled_mm(a_g, b_g, torch.from_numpy(sa).cuda(), torch.from_numpy(sb).cuda(), out,
+                         workspace=ws, config=cfg)
+            torch.cuda.synchronize()
+            assert_fp8_close(out.cpu().numpy(), ref["y"], f"{(M, N, K, cfg)}")
+    assert not ws.buf[:65536].any().item()
