@@ -87,6 +87,8 @@ def _load():
         lib.orc_scaled_mm_sample.restype = None
         lib.orc_scaled_mm_sample.argtypes = [P, I64, P, I64, P, I, P, I, I64, I,
                                              I, P, P, I64, P, P, P, P]
+        lib.orc_requant_shards.restype = None
+        lib.orc_requant_shards.argtypes = [P, I, I64, I64, P, P, I, P, I64, P]
         lib.orc_num_threads.restype = I
         lib.orc_set_num_threads.argtypes = [I]
         lib.orc_init()
@@ -276,3 +278,22 @@ def scaled_mm_sample(A, B, sa, sb, q_dtype: int, out_dtype: int, idx_m, idx_n):
                                  _ptr(idx_m), _ptr(idx_n), cnt, _ptr(acc),
                                  _ptr(iacc), _ptr(y), _ptr(out))
     return {"acc": acc, "iacc": iacc, "y": y, "out": out}
+
+
+def requant_shards(q, q_dtype: int, shard_scales, shard_rows):
+    """Rewrite a row-sharded merged weight to one shared scale
+    s_max = max(shard_scales): q' = encode(decode(q) * (s_i / s_max)).
+    Returns (codes [rows, cols] uint8, scale [1] float32)."""
+    q = np.asarray(q)
+    if q.dtype == np.int8:
+        q = q.view(np.uint8)
+    rows, cols, ld = _rows_view(q)
+    ss = np.ascontiguousarray(np.asarray(shard_scales, dtype=np.float32).reshape(-1))
+    sr = np.ascontiguousarray(np.asarray(shard_rows, dtype=np.int64).reshape(-1))
+    if ss.size != sr.size or ss.size < 1 or int(sr.sum()) != rows or (sr < 0).any():
+        raise ValueError("shard_rows must be non-negative and sum to the number of rows")
+    out = np.empty((rows, cols), dtype=np.uint8)
+    smax = np.zeros(1, dtype=np.float32)
+    _load().orc_requant_shards(_ptr(q), q_dtype, cols, ld, _ptr(ss), _ptr(sr), ss.size, _ptr(out), cols,
+                               _ptr(smax))
+    return out, smax

@@ -383,3 +383,42 @@ void orc_set_num_threads(int n) {
   (void)n;
 #endif
 }
+
+/* ------------------------------------------------------------------ */
+/* merged-layer shards: requantise to one shared scale                 */
+/* ------------------------------------------------------------------ */
+
+/* A merged weight (QKV or gate-up) stored [rows, cols] whose consecutive row
+ * shards i = 0..nshards-1 (shard_rows[i] rows each) were quantised with their
+ * own scales shard_scales[i] is rewritten to one shared scale
+ * s_max = max_i shard_scales[i] ("[Kernel] Support Fp8 Checkpoints (Dynamic
+ * + Static)", review discussion: w_scale = max(wq_scale, wk_scale,
+ * wv_scale); wq' = (wq_scale / w_scale) * wq):
+ *   r_i = s_i / s_max                      (one fp32 division)
+ *   q'[row, j] = encode(decode(q) * r_i)    (one fp32 multiplication, then
+ *                                            the same encoder as quantise)
+ * scale_out[0] = s_max. */
+void orc_requant_shards(const uint8_t* q, int q_dtype, int64_t cols, int64_t ld,
+                        const float* shard_scales, const int64_t* shard_rows,
+                        int nshards, uint8_t* out, int64_t ld_out,
+                        float* scale_out) {
+  build_table();
+  float smax = shard_scales[0];
+  for (int i = 1; i < nshards; ++i)
+    if (shard_scales[i] > smax) smax = shard_scales[i];
+  scale_out[0] = smax;
+  int64_t row0 = 0;
+  for (int i = 0; i < nshards; ++i) {
+    float r = shard_scales[i] / smax;
+#pragma omp parallel for schedule(static)
+    for (int64_t rr = 0; rr < shard_rows[i]; ++rr) {
+      int64_t row = row0 + rr;
+      for (int64_t j = 0; j < cols; ++j) {
+        float v = (float)decode_q(q[row * ld + j], q_dtype) * r;
+        out[row * ld_out + j] = q_dtype == ORC_E4M3 ? orc_encode_e4m3(v)
+                                                    : (uint8_t)orc_encode_int8(v);
+      }
+    }
+    row0 += shard_rows[i];
+  }
+}

@@ -498,3 +498,82 @@ def test_fp16_input_quant():
     xf = x.float()
     ref = torch_e4m3_encode((xf / torch.from_numpy(s)[:, None]).numpy())
     assert np.array_equal(q, ref)
+
+
+# ---------------------------------------------------------------- merged-layer shards
+
+def _shards(seed, qd=oracle.E4M3):
+    rows = (48, 16, 16)                      # e.g. q / k / v row blocks
+    parts, scales = [], []
+    for i, r in enumerate(rows):
+        x = si.normal((r, 64), seed=seed + i, std=0.02 * (1 + i))
+        q, s = oracle.quant(si.bits16(x), oracle.BF16, qd, oracle.PER_TENSOR)
+        parts.append(q)
+        scales.append(s[0])
+    return np.concatenate(parts), np.array(scales, np.float32), np.array(rows)
+
+
+def test_requant_shards_matches_page_expression():
+    """w_scale = max(shard scales); w_i' = (s_i / w_scale) * w_i, cast back
+    to e4m3 (torch's clamp-then-cast as the library reference)."""
+    q, ss, rows = _shards(31)
+    out, smax = oracle.requant_shards(q, oracle.E4M3, ss, rows)
+    assert smax[0] == ss.max()
+    row0 = 0
+    for i, r in enumerate(rows):
+        ratio = torch.tensor(np.float32(ss[i]) / np.float32(smax[0]))
+        v = torch.from_numpy(torch_e4m3_values(q[row0:row0 + r]).astype(np.float32)) * ratio
+        want = v.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(out[row0:row0 + r], want)
+        row0 += r
+
+
+def test_requant_shards_max_shard_unchanged_and_error_bound():
+    q, ss, rows = _shards(37)
+    out, smax = oracle.requant_shards(q, oracle.E4M3, ss, rows)
+    imax = int(np.argmax(ss))
+    starts = np.concatenate([[0], np.cumsum(rows)])
+    sl = slice(starts[imax], starts[imax + 1])
+    assert np.array_equal(out[sl], q[sl])          # ratio 1: codes unchanged
+    before = torch_e4m3_values(q) * np.repeat(ss, rows)[:, None]
+    after = torch_e4m3_values(out) * float(smax[0])
+    v = np.abs(before / float(smax[0]))
+    e = np.floor(np.log2(np.maximum(v, 2.0 ** -6)))
+    half_ulp = 0.5 * np.where(v < 2.0 ** -6, 2.0 ** -9, 2.0 ** (e - 3)) * float(smax[0])
+    assert np.all(np.abs(after - before) <= half_ulp * (1 + 2.0 ** -20) + 2.0 ** -22 * np.abs(before))
+
+
+def test_requant_shards_power_of_two_ratio_is_exact():
+    q = np.array([[0x38, 0x40, 0xB0, 0x50, 0x01, 0x7E]], np.uint8)   # 1, 2, -0.5, 8, 2^-9, 448
+    out, smax = oracle.requant_shards(np.concatenate([q, q]), oracle.E4M3,
+                                      np.array([0.5, 1.0], np.float32), [1, 1])
+    assert smax[0] == 1.0
+    assert list(torch_e4m3_values(out[0])) == [0.5, 1.0, -0.25, 4.0, 0.0, 224.0]  # 2^-10 ties to 0
+    assert np.array_equal(out[1], q[0])
+
+
+def test_requant_shards_int8():
+    q, ss, rows = _shards(41, qd=oracle.INT8)
+    out, smax = oracle.requant_shards(q, oracle.INT8, ss, rows)
+    row0 = 0
+    for i, r in enumerate(rows):
+        ratio = np.float32(ss[i]) / np.float32(smax[0])
+        v = q[row0:row0 + r].view(np.int8).astype(np.float32) * ratio
+        want = np.clip(np.rint(v.astype(np.float64)), -128, 127).astype(np.int8).view(np.uint8)
+        assert np.array_equal(out[row0:row0 + r], want)
+        row0 += r
+
+
+def test_per_shard_scales_equal_expanded_per_channel():
+    """A per-shard weight scale is a per-output-channel scale that is constant
+    over each shard: the fused-epilogue reading of the merged layer."""
+    rng = np.random.default_rng(3)
+    A = _finite_e4m3_codes(rng, (5, 64))
+    B, ss, rows = _shards(43)
+    sa = (rng.random(5) * 0.01).astype(np.float32)
+    per_channel = np.repeat(ss, rows).astype(np.float32)
+    full = oracle.scaled_mm(A, B, sa, per_channel, oracle.E4M3, oracle.BF16)
+    starts = np.concatenate([[0], np.cumsum(rows)])
+    for i in range(len(rows)):
+        part = oracle.scaled_mm(A, B[starts[i]:starts[i + 1]], sa, [ss[i]], oracle.E4M3, oracle.BF16)
+        assert np.array_equal(full["out"][:, starts[i]:starts[i + 1]], part["out"])
