@@ -147,6 +147,24 @@ def traffic_for(kernel_key: str):
     return ent.get("dram_bytes_per_launch_scaled")
 
 
+def max_over_ranks(t_local: float, device=None) -> float:
+    """Max of a per-rank time over all ranks (identity without a process
+    group).  The replicas share no data; this is the timing reduction only."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return t_local
+    tt = torch.tensor([t_local], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def aggregate_tflops(flops_per_step_per_rank: float, steps: int, t_max: float, world: int) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time (weak scaling: per-rank work is fixed)."""
+    return world * flops_per_step_per_rank * steps / t_max / 1e12
+
+
 # ---------------------------------------------------------------- workloads (GPU)
 
 class DecodeWorkload:
@@ -408,6 +426,72 @@ def oracle_decode_sample(budget_s: float, seed=5000):
     return flops, elapsed, rows, oracle.num_threads()
 
 
+# ---------------------------------------------------------------- ncu cases
+
+PROFILE_CASES = {
+    # name: (description, builder) -- small enough for an ncu capture, inputs
+    # larger than L2 where DRAM figures matter
+    "decode_gemm": "fp8 decode GEMM, M=16 x gate-up [28672 x 4096] (117 MB of weights)",
+    "prefill_gemm": "fp8 prefill GEMM, M=4096 x gate-up [28672 x 4096]",
+    "int8_gemm": "int8 GEMM, M=8192 x QKV-70B [10240 x 8192]",
+    "quant_tokens": "per-token dynamic e4m3 quantiser, [4096 x 14336] bf16",
+    "quant_kv": "per-tensor dynamic e4m3 quantiser (absmax + convert), KV [524288 x 128] bf16",
+    "dequant_kv": "e4m3 -> bf16 dequantiser, KV [524288 x 128]",
+}
+
+
+def run_profile_case(name: str, launches: int):
+    """Run `launches` calls of one kernel family on a fixed small case (for
+    ncu: capture with -k/-s/-c).  Prints the kernel configuration."""
+    import torch
+    import int8_w8a8_scaled_gb300 as w8
+    import synthetic_inputs as si
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+
+    def quantised(shape, seed, qdtype, per_row, weight):
+        x = (si.normal(shape, seed=seed, std=0.02, device=dev) if weight
+             else si.normal_with_outliers(shape, seed=seed, device=dev))
+        q = torch.empty(*shape, dtype=qdtype, device=dev)
+        s = torch.empty(shape[0] if per_row else 1, dtype=torch.float32, device=dev)
+        w8.scaled_quant(x, q, s, per_token=per_row, dynamic=True)
+        return q, s
+
+    if name.endswith("_gemm"):
+        M, N, K, qd = {"decode_gemm": (16, 28672, 4096, w8.E4M3), "prefill_gemm": (4096, 28672, 4096, w8.E4M3),
+                       "int8_gemm": (8192, 10240, 8192, w8.INT8)}[name]
+        qt = torch.float8_e4m3fn if qd == w8.E4M3 else torch.int8
+        a, sa = quantised((M, K), 1, qt, True, False)
+        b, sb = quantised((N, K), 2, qt, True, True)
+        out = torch.empty(M, N, dtype=torch.bfloat16 if qd == w8.E4M3 else torch.float16, device=dev)
+        ws = w8.Workspace(w8.mm_workspace_size(M, N, K, qd), dev)
+        print(json.dumps({"case": name, "config": w8.pick_config(M, N, K, qd)}), flush=True)
+        for _ in range(launches):
+            w8.scaled_mm(a, b, sa, sb, out, workspace=ws)
+    elif name == "quant_tokens":
+        x = si.normal_with_outliers((4096, 14336), seed=3, device=dev)
+        q = torch.empty(4096, 14336, dtype=torch.float8_e4m3fn, device=dev)
+        s = torch.empty(4096, dtype=torch.float32, device=dev)
+        for _ in range(launches):
+            w8.scaled_quant(x, q, s, per_token=True, dynamic=True)
+    elif name in ("quant_kv", "dequant_kv"):
+        x = si.kv_with_spikes(65536, 8, 128, seed=4, device=dev).reshape(-1, 128)
+        q = torch.empty(x.shape, dtype=torch.float8_e4m3fn, device=dev)
+        s = torch.empty(1, dtype=torch.float32, device=dev)
+        w8.scaled_quant(x, q, s, per_token=False, dynamic=True)
+        y = torch.empty_like(x)
+        for _ in range(launches):
+            if name == "quant_kv":
+                w8.scaled_quant(x, q, s, per_token=False, dynamic=True)
+            else:
+                w8.scaled_dequant(q, s, y)
+    else:
+        raise SystemExit(f"unknown profile case {name}; known: {sorted(PROFILE_CASES)}")
+    torch.cuda.synchronize()
+    if w8.device_status() != 0:
+        raise SystemExit("a kernel reported a pipeline timeout")
+
+
 # ---------------------------------------------------------------- main paths
 
 def run_reference(args):
@@ -471,13 +555,9 @@ def run_ours(args):
     sampler.start()
     t = time_graph(g_step, stream, args.steps, args.warmup, barrier)
     clocks = sampler.stop()
-    if ws_n > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([t], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
+    t = max_over_ranks(t, dev)
     flops_step = wl.flops()
-    value = ws_n * flops_step * args.steps / t / 1e12
+    value = aggregate_tflops(flops_step, args.steps, t, ws_n)
     ms_per_step = t / args.steps * 1e3
 
     # per-kernel-class timing over their own timed regions
@@ -516,8 +596,8 @@ def run_ours(args):
             e2e_step()
         e_ev.record(stream)
     torch.cuda.synchronize()
-    t_e2e = s_ev.elapsed_time(e_ev) / 1e3
-    e2e_val = ws_n * flops_step * e2e_steps / t_e2e / 1e12
+    t_e2e = max_over_ranks(s_ev.elapsed_time(e_ev) / 1e3, dev)
+    e2e_val = aggregate_tflops(flops_step, e2e_steps, t_e2e, ws_n)
 
     workloads = {}
     if not args.main_only:
@@ -578,7 +658,13 @@ def main():
     ap.add_argument("--main-only", action="store_true", help="skip the extra workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
+                    help="run a few launches of one kernel on a small case (for ncu) and exit")
+    ap.add_argument("--launches", type=int, default=5)
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case, args.launches)
+        return 0
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

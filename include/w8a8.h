@@ -225,6 +225,37 @@ W8A8_API w8a8_status w8a8_scaled_mm_with_config(
     int out_dtype, void* workspace, size_t workspace_bytes,
     const w8a8_mm_config* cfg, w8a8_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Merged-layer (QKV / gate-up) helpers
+ *
+ * A merged weight stored [N, K] consists of nshards consecutive row shards
+ * (shard_rows[i] rows each, HOST array, 1 <= nshards <= 16, sum = N) that may
+ * have been quantised with their own per-tensor scales shard_scales[i]
+ * (DEVICE fp32 array).  "[Kernel] Support Fp8 Checkpoints (Dynamic +
+ * Static)" runs such a layer as one GEMM either with the shard scales fused
+ * into the epilogue or after rewriting every shard to one shared scale.
+ * ---------------------------------------------------------------------- */
+
+/* scale_b[n] = shard_scales[shard of row n]  (device fp32 [N]).  Passing the
+ * result as a PER_ROW scale_b to w8a8_scaled_mm applies each shard's scale in
+ * the fused epilogue. */
+W8A8_API w8a8_status w8a8_expand_shard_scales(const float* shard_scales,
+                                              const int64_t* shard_rows,
+                                              int nshards, float* scale_b,
+                                              w8a8_stream_t stream);
+
+/* q_out[r, j] = encode(decode(q[r, j]) * (s_i / s_max)) with s_max the
+ * largest shard scale (written to scale_out[0], device fp32 [1]); the ratio
+ * is one IEEE fp32 division, the product one fp32 multiplication, the encode
+ * the quantiser's rounding and saturation.  q and q_out are [N, cols] codes
+ * of q_dtype with leading dimensions ld_q / ld_out bytes; q_out may equal q
+ * (in place, same leading dimension). */
+W8A8_API w8a8_status w8a8_requant_shards(const void* q, int q_dtype, int64_t cols,
+                                         int64_t ld_q, const float* shard_scales,
+                                         const int64_t* shard_rows, int nshards,
+                                         void* q_out, int64_t ld_out,
+                                         float* scale_out, w8a8_stream_t stream);
+
 /* Reads and clears the library's device-side status word on the current
  * device (W8A8_DEVICE_* bits; a kernel sets W8A8_DEVICE_TIMEOUT when one of
  * its bounded pipeline waits gave up instead of hanging).  This call

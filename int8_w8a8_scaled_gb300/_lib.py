@@ -39,6 +39,8 @@ EXPORTS = (
     "w8a8_scaled_mm_config_workspace_size",
     "w8a8_scaled_mm_with_config",
     "w8a8_device_status",
+    "w8a8_expand_shard_scales",
+    "w8a8_requant_shards",
 )
 
 
@@ -96,6 +98,10 @@ def load(build_if_needed: bool = True):
         lib.w8a8_scaled_mm_with_config.restype = I
         lib.w8a8_scaled_mm_with_config.argtypes = [P, I64, P, I64, P, I, P, I, P, I64, I64, I64, I64, I, I,
                                                    P, SZ, ctypes.POINTER(MmConfig), P]
+        lib.w8a8_expand_shard_scales.restype = I
+        lib.w8a8_expand_shard_scales.argtypes = [P, P, I, P, P]
+        lib.w8a8_requant_shards.restype = I
+        lib.w8a8_requant_shards.argtypes = [P, I, I64, I64, P, P, I, P, I64, P, P]
         lib.w8a8_device_status.restype = I
         lib.w8a8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
         _lib = lib

@@ -28,6 +28,7 @@ from ._lib import (BF16, DYNAMIC, E4M3, FP16, FP32, INT8, INT32, PER_ROW, PER_TE
 __all__ = [
     "scaled_quant", "scaled_dequant", "scaled_mm", "mm_workspace_size",
     "quant_workspace_size", "pick_config", "device_status", "Workspace",
+    "expand_shard_scales", "requant_shards",
     "W8A8Error", "MmConfig",
 ]
 
@@ -229,6 +230,33 @@ def scaled_mm(a_q: torch.Tensor, b_q: torch.Tensor, scale_a: torch.Tensor, scale
     else:
         check(lib.w8a8_scaled_mm_with_config(*args, ctypes.byref(c), _stream(stream)))
     return out
+
+
+def _shard_rows(shard_rows):
+    arr = (ctypes.c_int64 * len(shard_rows))(*[int(r) for r in shard_rows])
+    return arr, len(shard_rows)
+
+
+def expand_shard_scales(shard_scales: torch.Tensor, shard_rows, scale_b: torch.Tensor, stream=None) -> torch.Tensor:
+    """scale_b[n] = shard_scales[shard of row n]: per-shard weight scales of a
+    merged layer as a per-channel vector for the fused epilogue."""
+    _cuda(shard_scales, scale_b)
+    arr, n = _shard_rows(shard_rows)
+    check(_lib.load().w8a8_expand_shard_scales(_ptr(shard_scales), arr, n, _ptr(scale_b), _stream(stream)))
+    return scale_b
+
+
+def requant_shards(q: torch.Tensor, shard_scales: torch.Tensor, shard_rows, q_out: torch.Tensor,
+                   scale_out: torch.Tensor, q_dtype=None, stream=None) -> None:
+    """Rewrite a row-sharded merged weight to one shared scale (the largest
+    shard scale, written to scale_out): q' = encode(decode(q) * s_i / s_max)."""
+    _cuda(q, shard_scales, q_out, scale_out)
+    arr, n = _shard_rows(shard_rows)
+    rows, cols = q.shape
+    if tuple(q_out.shape) != (rows, cols):
+        raise ValueError("q_out must have the shape of q")
+    check(_lib.load().w8a8_requant_shards(_ptr(q), _qkind(q, q_dtype), cols, _ld(q), _ptr(shard_scales), arr, n,
+                                          _ptr(q_out), _ld(q_out), _ptr(scale_out), _stream(stream)))
 
 
 def device_status() -> int:

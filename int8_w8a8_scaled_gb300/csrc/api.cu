@@ -330,6 +330,8 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
   prm.partial = plan.splits > 1 ? reinterpret_cast<float*>(wsb + plan.off_partial) : nullptr;
   prm.counters = plan.splits > 1 ? reinterpret_cast<unsigned*>(wsb + plan.off_counters) : nullptr;
   prm.kchunk_kb = kInt8ChunkK / 64;
+  prm.num_sms = dev.sms;
+  prm.pdl = 1;
   const int out_kind = out_dtype == W8A8_BF16 ? OUT_BF16 : out_dtype == W8A8_FP16 ? OUT_FP16 : OUT_RAW;
   e = i8 ? launch_int8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream)
          : launch_fp8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream);
@@ -476,6 +478,58 @@ w8a8_status w8a8_scaled_mm_with_config(const void* a_q, int64_t lda, const void*
   if (!cfg) return fail(W8A8_ERR_INVALID_ARG, "cfg is null");
   return run_mm(a_q, lda, b_q, ldb, scale_a, a_gran, scale_b, b_gran, out, ldc, M, N, K, q_dtype, out_dtype,
                 workspace, workspace_bytes, cfg, reinterpret_cast<cudaStream_t>(stream));
+}
+
+namespace {
+w8a8_status shard_table(const int64_t* shard_rows, int nshards, ShardTable* t) {
+  if (!shard_rows) return fail(W8A8_ERR_INVALID_ARG, "shard_rows is null");
+  if (nshards < 1 || nshards > kMaxShards)
+    return fail(W8A8_ERR_UNSUPPORTED, "nshards must be in [1, %d]", kMaxShards);
+  t->n = nshards;
+  long long acc = 0;
+  for (int i = 0; i < nshards; ++i) {
+    if (shard_rows[i] < 0) return fail(W8A8_ERR_INVALID_ARG, "shard_rows must be >= 0");
+    acc += shard_rows[i];
+    if (acc >= (1LL << 31)) return fail(W8A8_ERR_UNSUPPORTED, "too many rows");
+    t->end[i] = acc;
+  }
+  if (acc < 1) return fail(W8A8_ERR_INVALID_ARG, "the shards hold no rows");
+  return W8A8_OK;
+}
+}  // namespace
+
+w8a8_status w8a8_expand_shard_scales(const float* shard_scales, const int64_t* shard_rows, int nshards,
+                                     float* scale_b, w8a8_stream_t stream) {
+  if (!shard_scales || !scale_b) return fail(W8A8_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(shard_scales, 4) || !aligned(scale_b, 4)) return fail(W8A8_ERR_MISALIGNED, "scales must be 4-byte aligned");
+  ShardTable t;
+  w8a8_status st = shard_table(shard_rows, nshards, &t);
+  if (st != W8A8_OK) return st;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != W8A8_OK) return st;
+  cudaError_t e = launch_expand_shard_scales(shard_scales, t, scale_b, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "expand_shard_scales launch");
+  return ok();
+}
+
+w8a8_status w8a8_requant_shards(const void* q, int q_dtype, int64_t cols, int64_t ld_q, const float* shard_scales,
+                                const int64_t* shard_rows, int nshards, void* q_out, int64_t ld_out,
+                                float* scale_out, w8a8_stream_t stream) {
+  if (!q || !shard_scales || !q_out || !scale_out) return fail(W8A8_ERR_INVALID_ARG, "null pointer argument");
+  if (q_dtype != W8A8_E4M3 && q_dtype != W8A8_INT8) return fail(W8A8_ERR_INVALID_ARG, "q_dtype must be E4M3 or INT8");
+  if (cols < 1) return fail(W8A8_ERR_INVALID_ARG, "cols must be >= 1");
+  if (ld_q < cols || ld_out < cols) return fail(W8A8_ERR_INVALID_ARG, "leading dimensions must be >= cols");
+  if (q == q_out && ld_q != ld_out) return fail(W8A8_ERR_INVALID_ARG, "in-place requantisation needs ld_out == ld_q");
+  if (!aligned(shard_scales, 4) || !aligned(scale_out, 4)) return fail(W8A8_ERR_MISALIGNED, "scales must be 4-byte aligned");
+  ShardTable t;
+  w8a8_status st = shard_table(shard_rows, nshards, &t);
+  if (st != W8A8_OK) return st;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != W8A8_OK) return st;
+  cudaError_t e = launch_requant_shards(q, q_dtype == W8A8_E4M3 ? 0 : 1, cols, ld_q, shard_scales, t, q_out, ld_out,
+                                        scale_out, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "requant_shards launch");
+  return ok();
 }
 
 w8a8_status w8a8_device_status(int* flags) {

@@ -40,7 +40,8 @@ namespace w8a8 {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kEpiThreads = 128;
 constexpr int kTileP = 128;       // rows of the P operand per tile (MMA M)
 constexpr int kRowBytes = 128;    // bytes of K per stage row (one swizzle row)
 constexpr int kPBytes = kTileP * kRowBytes;
@@ -149,6 +150,44 @@ __device__ __forceinline__ void store16(const MmParams& prm, int lane_idx, int c
   }
 }
 
+// One work unit is a (K slice, output tile) pair; the persistent CTAs walk
+// the units round-robin.  Units are numbered slice-major so that the slices
+// of a tile are spread over different CTAs.
+struct Unit {
+  int p0, q0, tile_lin, split, kb_begin, nkb;
+};
+
+__device__ __forceinline__ Unit unit_of(int w, const MmParams& prm, int group, int bn) {
+  const int tiles = prm.tiles_p * prm.tiles_q;
+  Unit u;
+  u.split = w / tiles;
+  int tp, tq;
+  tile_coords(w - u.split * tiles, prm.tiles_p, prm.tiles_q, group, tp, tq);
+  u.tile_lin = tp * prm.tiles_q + tq;
+  u.p0 = tp * kTileP;
+  u.q0 = tq * bn;
+  u.kb_begin = u.split * prm.kb_per_split;
+  u.nkb = min(prm.num_kb, u.kb_begin + prm.kb_per_split) - u.kb_begin;
+  return u;
+}
+
+__device__ __forceinline__ void epi_bar_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding kernel in the stream
+// (and its memory) before touching global memory; allow the next kernel to
+// start its prologue.  Both are no-ops without the launch attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Persistent, warp-specialised scaled matmul.
+//   warp 0 (one lane)  TMA producer over all units of this CTA;
+//   warp 1             TMEM owner; one lane issues the MMAs;
+//   warps 2..5         epilogue; warp w reads TMEM lanes 32*(w%4)...
+// Accumulation units (one per work unit for e4m3, one per <= 1024-K chunk
+// for int8) alternate between two TMEM accumulators, so the epilogue of one
+// unit overlaps the MMAs of the next.
 template <int BN, bool SWAP, bool INT8, typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
     w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_p,
@@ -167,31 +206,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sp = smem;
   uint8_t* sq = smem + stages * kPBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sq + stages * kQBytes);
-  // bars: full[stages], empty[stages], chunk_full[2], chunk_empty[2]
+  // bars: full[stages], empty[stages], unit_full[2], unit_empty[2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 4);
   __shared__ int s_is_last;
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-
-  const int tiles = prm.tiles_p * prm.tiles_q;
-  const int split = blockIdx.x / tiles;
-  const int tile_lin_sched = blockIdx.x - split * tiles;
-  int tp, tq;
-  tile_coords(tile_lin_sched, prm.tiles_p, prm.tiles_q, group, tp, tq);
-  const int tile_lin = tp * prm.tiles_q + tq;
-  const int p0 = tp * kTileP;
-  const int q0 = tq * BN;
-  const int kb_begin = split * prm.kb_per_split;
-  const int kb_end = min(prm.num_kb, kb_begin + prm.kb_per_split);
-  const int nkb = kb_end - kb_begin;
-  const int chunk_kb = INT8 ? prm.kchunk_kb : (nkb > 0 ? nkb : 1);
-  const int nchunks = (nkb + chunk_kb - 1) / chunk_kb;
+  const int units = prm.tiles_p * prm.tiles_q * prm.splits;
 
   auto full_bar = [&](int s) { return smem_addr(bars + s); };
   auto empty_bar = [&](int s) { return smem_addr(bars + stages + s); };
-  auto cfull_bar = [&](int b) { return smem_addr(bars + 2 * stages + b); };
-  auto cempty_bar = [&](int b) { return smem_addr(bars + 2 * stages + 2 + b); };
+  auto ufull_bar = [&](int b) { return smem_addr(bars + 2 * stages + b); };
+  auto uempty_bar = [&](int b) { return smem_addr(bars + 2 * stages + 2 + b); };
 
   if (threadIdx.x == 0) {
     prefetch_tensormap(&tmap_p);
@@ -200,10 +226,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    mbar_init(cfull_bar(0), 1);
-    mbar_init(cfull_bar(1), 1);
-    mbar_init(cempty_bar(0), kThreads);
-    mbar_init(cempty_bar(1), kThreads);
+    mbar_init(ufull_bar(0), 1);
+    mbar_init(ufull_bar(1), 1);
+    mbar_init(uempty_bar(0), kEpiThreads);
+    mbar_init(uempty_bar(1), kEpiThreads);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -214,183 +240,191 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();
+  griddep_launch();
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % stages;
-        const uint32_t ph = (i / stages) & 1;
-        if (!mbar_wait(empty_bar(s), ph ^ 1)) break;
-        mbar_arrive_expect_tx(full_bar(s), kStageBytes);
-        const int kx = (kb_begin + i) * kKbElems;
-        tma_load_2d(smem_addr(sp + s * kPBytes), &tmap_p, full_bar(s), kx, p0);
-        tma_load_2d(smem_addr(sq + s * kQBytes), &tmap_q, full_bar(s), kx, q0);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < units && ok; w += gridDim.x) {
+        const Unit un = unit_of(w, prm, group, BN);
+        for (int i = 0; i < un.nkb; ++i, ++it) {
+          const int s = it % stages;
+          const uint32_t ph = (it / stages) & 1;
+          if (!mbar_wait(empty_bar(s), ph ^ 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+          const int kx = (un.kb_begin + i) * kKbElems;
+          tma_load_2d(smem_addr(sp + s * kPBytes), &tmap_p, full_bar(s), kx, un.p0);
+          tma_load_2d(smem_addr(sq + s * kQBytes), &tmap_q, full_bar(s), kx, un.q0);
+        }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
+      uint32_t it = 0, u = 0;
       bool ok = true;
-      int i = 0;
-      for (int c = 0; c < nchunks && ok; ++c) {
-        const int buf = c & 1;
-        if (c >= 2) {
-          // the epilogue must have drained this accumulator (chunk c - 2)
-          if (!mbar_wait(cempty_bar(buf), ((c - 2) >> 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-        }
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-        const int i_end = min(nkb, i + chunk_kb);
-        for (int first = 1; i < i_end; ++i, first = 0) {
-          const int s = i % stages;
-          const uint32_t ph = (i / stages) & 1;
-          if (!mbar_wait(full_bar(s), ph)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t da = smem_desc_sw128(smem_addr(sp + s * kPBytes));
-          const uint64_t db = smem_desc_sw128(smem_addr(sq + s * kQBytes));
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-            if (INT8)
-              mma_f16(d_tmem, da + 2 * kk, db + 2 * kk, kIdesc, acc);
-            else
-              mma_f8f6f4(d_tmem, da + 2 * kk, db + 2 * kk, kIdesc, acc);
+      for (int w = blockIdx.x; w < units && ok; w += gridDim.x) {
+        const Unit un = unit_of(w, prm, group, BN);
+        const int chunk = INT8 ? prm.kchunk_kb : un.nkb;
+        const int nch = (un.nkb + chunk - 1) / chunk;
+        for (int c = 0; c < nch && ok; ++c, ++u) {
+          const int b = u & 1;
+          if (u >= 2) {
+            if (!mbar_wait(uempty_bar(b), ((u - 2) >> 1) & 1)) { ok = false; break; }
+            tc_fence_after();
           }
-          mma_commit(empty_bar(s));
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+          const int i_end = min(un.nkb, (c + 1) * chunk);
+          for (int i = c * chunk; i < i_end; ++i, ++it) {
+            const int s = it % stages;
+            const uint32_t ph = (it / stages) & 1;
+            if (!mbar_wait(full_bar(s), ph)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t da = smem_desc_sw128(smem_addr(sp + s * kPBytes));
+            const uint64_t db = smem_desc_sw128(smem_addr(sq + s * kQBytes));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t acc = (i == c * chunk && kk == 0) ? 0u : 1u;
+              if (INT8)
+                mma_f16(d_tmem, da + 2 * kk, db + 2 * kk, kIdesc, acc);
+              else
+                mma_f8f6f4(d_tmem, da + 2 * kk, db + 2 * kk, kIdesc, acc);
+            }
+            mma_commit(empty_bar(s));
+          }
+          mma_commit(ufull_bar(b));
         }
-        mma_commit(cfull_bar(buf));
-      }
-      if (!ok) {
-        // let the epilogue through; its result is discarded (status flagged)
-        mma_commit(cfull_bar(0));
-        mma_commit(cfull_bar(1));
       }
     }
     __syncwarp();
-  }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // TMEM lane == tile row on the P side
+    const int et = threadIdx.x - 2 * 32;  // 0..127
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    const size_t tile_elems = static_cast<size_t>(kTileP) * BN;
+    uint32_t u = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < units && ok; w += gridDim.x) {
+      const Unit un = unit_of(w, prm, group, BN);
+      const int chunk = INT8 ? prm.kchunk_kb : un.nkb;
+      const int nch = (un.nkb + chunk - 1) / chunk;
+      const int lane_idx = un.p0 + row;  // global P row of this thread
+      // columns of this tile inside the problem (the Q side is M with swap)
+      const int qvalid = min(BN, (SWAP ? prm.M : prm.N) - un.q0);
+      float s_lane;
+      if (!SWAP)
+        s_lane = (lane_idx < prm.M) ? (prm.a_per_row ? __ldg(prm.scale_a + lane_idx) : __ldg(prm.scale_a)) : 0.f;
+      else
+        s_lane = (lane_idx < prm.N) ? (prm.b_per_row ? __ldg(prm.scale_b + lane_idx) : __ldg(prm.scale_b)) : 0.f;
+      uint32_t* part = nullptr;
+      if (prm.splits > 1)
+        part = reinterpret_cast<uint32_t*>(prm.partial) +
+               (static_cast<size_t>(un.tile_lin) * prm.splits + un.split) * tile_elems;
 
-  // ------------------------------------------------------------ epilogue
-  const int row = warp * 32 + lane;  // TMEM lane == tile row on the P side
-  const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
-  const int lane_idx = p0 + row;     // global P row of this thread
-  float s_lane;
-  if (!SWAP)
-    s_lane = (lane_idx < prm.M) ? (prm.a_per_row ? __ldg(prm.scale_a + lane_idx) : __ldg(prm.scale_a)) : 0.f;
-  else
-    s_lane = (lane_idx < prm.N) ? (prm.b_per_row ? __ldg(prm.scale_b + lane_idx) : __ldg(prm.scale_b)) : 0.f;
-
-  bool ok = true;
-  const size_t tile_elems = static_cast<size_t>(kTileP) * BN;
-  uint32_t* part = nullptr;
-  if (prm.splits > 1)
-    part = reinterpret_cast<uint32_t*>(prm.partial) + (static_cast<size_t>(tile_lin) * prm.splits + split) * tile_elems;
-
-  for (int c = 0; c < nchunks; ++c) {
-    const int buf = c & 1;
-    if (!mbar_wait(cfull_bar(buf), (c >> 1) & 1)) { ok = false; }
-    tc_fence_after();
-    const bool last = (c == nchunks - 1);
-    const uint32_t acc_addr = lane_base + static_cast<uint32_t>(buf * BN);
-    const uint32_t tot_addr = lane_base + static_cast<uint32_t>(2 * BN);
+      for (int c = 0; c < nch; ++c, ++u) {
+        const int b = u & 1;
+        if (!mbar_wait(ufull_bar(b), (u >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const bool last = (c == nch - 1);
+        const uint32_t acc_addr = lane_base + static_cast<uint32_t>(b * BN);
+        const uint32_t tot_addr = lane_base + static_cast<uint32_t>(2 * BN);
 #pragma unroll 1
-    for (int g = 0; g < kGroups; ++g) {
-      uint32_t r[16];
-      tmem_ld16(acc_addr + g * 16, r);
-      if (INT8) {
-        uint32_t t[16];
-        if (c > 0) {
-          tmem_ld16(tot_addr + g * 16, t);
-          tmem_ld_wait();
+        for (int g = 0; g < kGroups; ++g) {
+          uint32_t r[16];
+          tmem_ld16(acc_addr + g * 16, r);
+          if (INT8) {
+            uint32_t t[16];
+            if (c > 0) {
+              tmem_ld16(tot_addr + g * 16, t);
+              tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            t[j] = static_cast<uint32_t>(static_cast<int>(t[j]) + __float2int_rn(__uint_as_float(r[j])));
-        } else {
-          tmem_ld_wait();
+              for (int j = 0; j < 16; ++j)
+                t[j] = static_cast<uint32_t>(static_cast<int>(t[j]) + __float2int_rn(__uint_as_float(r[j])));
+            } else {
+              tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) t[j] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[j])));
-        }
-        if (!last) {
-          tmem_st16(tot_addr + g * 16, t);
-        } else if (prm.splits > 1) {
-          uint4* dst = reinterpret_cast<uint4*>(part + (static_cast<size_t>(g) * kTileP + row) * 16);
+              for (int j = 0; j < 16; ++j) t[j] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[j])));
+            }
+            if (!last) {
+              tmem_st16(tot_addr + g * 16, t);
+            } else if (prm.splits > 1) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(t[4 * j], t[4 * j + 1], t[4 * j + 2], t[4 * j + 3]);
-        } else if (ok) {
-          int v[16];
+              for (int j = 0; j < 16; ++j)
+                if (g * 16 + j < qvalid) part[static_cast<size_t>(g * 16 + j) * kTileP + row] = t[j];
+            } else {
+              int v[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = static_cast<int>(t[j]);
-          store16<SWAP, OutT>(prm, lane_idx, q0 + g * 16, v, s_lane);
-        }
-      } else {
-        tmem_ld_wait();
-        if (prm.splits > 1) {
-          uint4* dst = reinterpret_cast<uint4*>(part + (static_cast<size_t>(g) * kTileP + row) * 16);
+              for (int j = 0; j < 16; ++j) v[j] = static_cast<int>(t[j]);
+              store16<SWAP, OutT>(prm, lane_idx, un.q0 + g * 16, v, s_lane);
+            }
+          } else {
+            tmem_ld_wait();
+            if (prm.splits > 1) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-        } else if (ok) {
-          float v[16];
+              for (int j = 0; j < 16; ++j)
+                if (g * 16 + j < qvalid) part[static_cast<size_t>(g * 16 + j) * kTileP + row] = r[j];
+            } else {
+              float v[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-          store16<SWAP, OutT>(prm, lane_idx, q0 + g * 16, v, s_lane);
-        }
-      }
-    }
-    if (INT8 && !last) {
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(cempty_bar(buf));
-    }
-  }
-
-  if (prm.splits > 1) {
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const unsigned old = atomicAdd(prm.counters + tile_lin, 1u);
-      s_is_last = (old == static_cast<unsigned>(prm.splits - 1));
-    }
-    __syncthreads();
-    if (s_is_last) {
-      __threadfence();
-      const uint32_t* base = reinterpret_cast<const uint32_t*>(prm.partial) +
-                             static_cast<size_t>(tile_lin) * prm.splits * tile_elems;
-#pragma unroll 1
-      for (int g = 0; g < kGroups; ++g) {
-        if (INT8) {
-          int v[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = 0;
-          for (int s = 0; s < prm.splits; ++s) {
-            const uint4* src = reinterpret_cast<const uint4*>(base + s * tile_elems + (static_cast<size_t>(g) * kTileP + row) * 16);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint4 u = __ldcg(src + j);
-              v[4 * j] += static_cast<int>(u.x);
-              v[4 * j + 1] += static_cast<int>(u.y);
-              v[4 * j + 2] += static_cast<int>(u.z);
-              v[4 * j + 3] += static_cast<int>(u.w);
+              for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+              store16<SWAP, OutT>(prm, lane_idx, un.q0 + g * 16, v, s_lane);
             }
           }
-          if (ok) store16<SWAP, OutT>(prm, lane_idx, q0 + g * 16, v, s_lane);
-        } else {
-          float v[16];
+        }
+        if (INT8 && !last) tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(uempty_bar(b));
+      }
+      if (!ok) break;
+
+      if (prm.splits > 1) {
+        // the last slice to arrive sums all partials in slice order
+        __threadfence();
+        epi_bar_sync();
+        if (et == 0) {
+          const unsigned old = atomicAdd(prm.counters + un.tile_lin, 1u);
+          s_is_last = (old == static_cast<unsigned>(prm.splits - 1));
+        }
+        epi_bar_sync();
+        if (s_is_last) {
+          __threadfence();
+          const uint32_t* base = reinterpret_cast<const uint32_t*>(prm.partial) +
+                                 static_cast<size_t>(un.tile_lin) * prm.splits * tile_elems;
+#pragma unroll 1
+          for (int g = 0; g < kGroups; ++g) {
+            if (g * 16 >= qvalid) break;
+            if (INT8) {
+              int v[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = 0.f;
-          for (int s = 0; s < prm.splits; ++s) {
-            const float4* src = reinterpret_cast<const float4*>(base + s * tile_elems + (static_cast<size_t>(g) * kTileP + row) * 16);
+              for (int j = 0; j < 16; ++j) v[j] = 0;
+              for (int sl = 0; sl < prm.splits; ++sl) {
+                const uint32_t* src = base + sl * tile_elems + static_cast<size_t>(g * 16) * kTileP + row;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              float4 u = __ldcg(src + j);
-              v[4 * j] += u.x;
-              v[4 * j + 1] += u.y;
-              v[4 * j + 2] += u.z;
-              v[4 * j + 3] += u.w;
+                for (int j = 0; j < 16; ++j)
+                  if (g * 16 + j < qvalid) v[j] += static_cast<int>(__ldcg(src + j * kTileP));
+              }
+              store16<SWAP, OutT>(prm, lane_idx, un.q0 + g * 16, v, s_lane);
+            } else {
+              float v[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] = 0.f;
+              for (int sl = 0; sl < prm.splits; ++sl) {
+                const float* src = reinterpret_cast<const float*>(base + sl * tile_elems) +
+                                   static_cast<size_t>(g * 16) * kTileP + row;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (g * 16 + j < qvalid) v[j] += __ldcg(src + j * kTileP);
+              }
+              store16<SWAP, OutT>(prm, lane_idx, un.q0 + g * 16, v, s_lane);
             }
           }
-          if (ok) store16<SWAP, OutT>(prm, lane_idx, q0 + g * 16, v, s_lane);
+          if (et == 0) prm.counters[un.tile_lin] = 0u;
         }
       }
-      if (threadIdx.x == 0) prm.counters[tile_lin] = 0u;
     }
   }
 
@@ -410,9 +444,25 @@ cudaError_t launch_one(const CUtensorMap& tp, const CUtensorMap& tq, const MmPar
   // the attribute is per function and device; setting it again is harmless
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
+  if (e != cudaSuccess) return e;
+  occ = max(1, min(occ, 512 / tmem_cols_for(BN, INT8)));
+  const int units = p.tiles_p * p.tiles_q * p.splits;
+  const int grid = max(1, min(units, p.num_sms * occ));
   const int group = SWAP ? 1 : 8;
-  const int grid = p.tiles_p * p.tiles_q * p.splits;
-  kern<<<grid, kThreads, smem, stream>>>(tp, tq, p, stages, group);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, tp, tq, p, stages, group);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -455,6 +505,7 @@ cudaError_t dispatch(const CUtensorMap& tp, const CUtensorMap& tq, const MmParam
 // int8 [rows, K] (leading dim ld) -> f16 [rows, K] contiguous, exact.
 __global__ void widen_int8_kernel(const int8_t* __restrict__ src, long long ld, int rows, int K,
                                   __half* __restrict__ dst) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int vpr = K / 16;  // K is a multiple of 16
   const long long total = static_cast<long long>(rows) * vpr;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;

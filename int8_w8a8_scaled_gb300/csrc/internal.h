@@ -29,6 +29,8 @@ struct MmParams {
   float* partial;        // [tiles][splits][128 * block_n] fp32 (splits > 1)
   unsigned* counters;    // [tiles] arrival counters (splits > 1), left zero
   int kchunk_kb;         // int8 path: K blocks per exact fp32 chunk
+  int num_sms;           // persistent grid = min(units, num_sms * resident CTAs per SM)
+  int pdl;               // launch with programmatic stream serialisation
 };
 
 // OUT_RAW: fp32 y = (acc * s_a) * s_b for the fp8 path, raw int32
@@ -85,5 +87,17 @@ struct DequantArgs {
   int vec;
 };
 cudaError_t launch_dequant(const DequantArgs& a, int num_sms, cudaStream_t stream);
+
+// Row shards of a merged weight: cumulative row ends.
+constexpr int kMaxShards = 16;
+struct ShardTable {
+  int n;
+  long long end[kMaxShards];
+};
+cudaError_t launch_expand_shard_scales(const float* shard_scales, const ShardTable& t, float* out,
+                                       cudaStream_t stream);
+cudaError_t launch_requant_shards(const void* q, int q_kind, long long cols, long long ld,
+                                  const float* shard_scales, const ShardTable& t, void* out, long long ld_out,
+                                  float* scale_out, cudaStream_t stream);
 
 }  // namespace w8a8

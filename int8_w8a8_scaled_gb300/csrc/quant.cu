@@ -36,6 +36,12 @@ namespace {
 
 constexpr int kRowThreads = 256;
 
+// Let the next kernel in the stream start its prologue now; it still waits
+// (griddepcontrol.wait) for this grid to finish before touching memory.
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float load_f(const uint16_t* p, int kind) {
   const uint16_t b = *p;
   return kind == 0 ? __bfloat162float(__ushort_as_bfloat16(b)) : __half2float(__ushort_as_half(b));
@@ -118,6 +124,7 @@ __global__ void __launch_bounds__(kRowThreads)
     quant_rows_kernel(const uint16_t* __restrict__ x, long long ld_x, long long cols,
                       uint8_t* __restrict__ q, long long ld_q, float* __restrict__ scale,
                       int per_row, int dynamic) {
+  allow_dependents();
   __shared__ float red[kRowThreads / 32];
   const long long row = blockIdx.x;
   const uint16_t* xr = x + row * ld_x;
@@ -206,6 +213,7 @@ __global__ void __launch_bounds__(kRowThreads)
 template <int XK>
 __global__ void __launch_bounds__(256)
     absmax_flat_kernel(const uint16_t* __restrict__ x, long long n, unsigned* __restrict__ word) {
+  allow_dependents();
   __shared__ float red[8];
   float amax = 0.f;
   const long long nvec = n / 8;
@@ -251,6 +259,7 @@ template <int XK>
 __global__ void __launch_bounds__(kRowThreads)
     absmax_rows_kernel(const uint16_t* __restrict__ x, long long ld_x, long long cols,
                        unsigned* __restrict__ word) {
+  allow_dependents();
   __shared__ float red[kRowThreads / 32];
   const uint16_t* xr = x + static_cast<long long>(blockIdx.x) * ld_x;
   float amax = 0.f;
@@ -265,6 +274,7 @@ template <int XK, int QK>
 __global__ void __launch_bounds__(256)
     quant_flat_kernel(const uint16_t* __restrict__ x, long long n, uint8_t* __restrict__ q,
                       float* __restrict__ scale, const unsigned* __restrict__ word, int dynamic) {
+  allow_dependents();
   float s;
   if (dynamic) {
     s = scale_from_amax<QK>(__uint_as_float(*word));
@@ -317,6 +327,7 @@ __global__ void __launch_bounds__(kRowThreads)
     quant_rows_from_word_kernel(const uint16_t* __restrict__ x, long long ld_x, long long cols,
                                 uint8_t* __restrict__ q, long long ld_q, float* __restrict__ scale,
                                 const unsigned* __restrict__ word) {
+  allow_dependents();
   const float s = scale_from_amax<QK>(__uint_as_float(*word));
   if (blockIdx.x == 0 && threadIdx.x == 0) scale[0] = s;
   const uint16_t* xr = x + static_cast<long long>(blockIdx.x) * ld_x;
@@ -346,6 +357,7 @@ template <int QK, int YK>
 __global__ void __launch_bounds__(256)
     dequant_flat_kernel(const uint8_t* __restrict__ q, long long n, const float* __restrict__ scale,
                         uint16_t* __restrict__ y) {
+  allow_dependents();
   const float s = __ldg(scale);
   const long long n16 = n / 16;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -371,6 +383,7 @@ __global__ void __launch_bounds__(kRowThreads)
     dequant_rows_kernel(const uint8_t* __restrict__ q, long long ld_q, long long cols,
                         const float* __restrict__ scale, int per_row, uint16_t* __restrict__ y,
                         long long ld_y) {
+  allow_dependents();
   const long long row = blockIdx.x;
   const float s = __ldg(scale + (per_row ? row : 0));
   const uint8_t* qr = q + row * ld_q;

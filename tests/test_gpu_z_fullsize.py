@@ -32,8 +32,11 @@ def sample_points(M, N, seed, tile_p=128):
         pts.update((r, n) for n in range(N))
     for c in cols:
         pts.update((m, c) for m in range(M))
-    for m0 in range(0, M, tile_p):       # tile corners on a 128 x 16 grid
-        for n0 in range(0, N, 16):
+    # tile corners on a 128 x 16 grid (every few tiles on the largest shapes)
+    n_tiles = ((M + tile_p - 1) // tile_p) * ((N + 15) // 16)
+    step = max(1, int(np.sqrt(n_tiles / 4096.0)) + (1 if n_tiles > 4096 else 0))
+    for m0 in range(0, M, tile_p * step):
+        for n0 in range(0, N, 16 * step):
             for dm, dn in ((0, 0), (min(tile_p, M - m0) - 1, 0), (0, min(16, N - n0) - 1),
                            (min(tile_p, M - m0) - 1, min(16, N - n0) - 1)):
                 pts.add((m0 + dm, n0 + dn))
