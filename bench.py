@@ -437,6 +437,7 @@ PROFILE_CASES = {
     "quant_tokens": "per-token dynamic e4m3 quantiser, [4096 x 14336] bf16",
     "quant_kv": "per-tensor dynamic e4m3 quantiser (absmax + convert), KV [524288 x 128] bf16",
     "dequant_kv": "e4m3 -> bf16 dequantiser, KV [524288 x 128]",
+    "decode_step": "the decode step (16 quantisers + 16 GEMMs), eager launches",
 }
 
 
@@ -457,6 +458,14 @@ def run_profile_case(name: str, launches: int):
         w8.scaled_quant(x, q, s, per_token=per_row, dynamic=True)
         return q, s
 
+    if name == "decode_step":
+        wl = DecodeWorkload(dev)
+        for _ in range(launches):
+            wl.run_step()
+        torch.cuda.synchronize()
+        print(json.dumps({"case": name, "configs": {f"M{it['M']}_{it['name']}": w8.pick_config(
+            it["M"], wl.weights[it["name"]][2], wl.weights[it["name"]][3], w8.E4M3) for it in wl.items}}))
+        return
     if name.endswith("_gemm"):
         M, N, K, qd = {"decode_gemm": (16, 28672, 4096, w8.E4M3), "prefill_gemm": (4096, 28672, 4096, w8.E4M3),
                        "int8_gemm": (8192, 10240, 8192, w8.INT8)}[name]
@@ -490,6 +499,64 @@ def run_profile_case(name: str, launches: int):
     torch.cuda.synchronize()
     if w8.device_status() != 0:
         raise SystemExit("a kernel reported a pipeline timeout")
+
+
+# ---------------------------------------------------------------- config sweep
+
+def sweep_decode(out_path: str, reps: int = 20):
+    """Time every decode GEMM shape under a grid of kernel configurations
+    (CUDA graph of 8 launches cycling over 4 weight copies, so weights come
+    from HBM).  Writes one JSON line per (shape, config)."""
+    import torch
+    import int8_w8a8_scaled_gb300 as w8
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    lines = []
+    for M in DECODE_MS:
+        for name, N, K, shared in LLAMA8B:
+            g = torch.Generator(device=dev)
+            g.manual_seed(M * 7 + N)
+            copies = [torch.randint(0, 126, (N, K), generator=g, device=dev, dtype=torch.uint8).view(torch.float8_e4m3fn)
+                      for _ in range(4)]
+            a = torch.randint(0, 126, (M, K), generator=g, device=dev, dtype=torch.uint8).view(torch.float8_e4m3fn)
+            sa = torch.rand(M, device=dev) * 0.01
+            sb = torch.rand(1 if shared else N, device=dev) * 0.01
+            out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            cfgs = []
+            bns = [b for b in (16, 32, 64, 128, 256) if b <= max(16, 2 * M) or b <= 64]
+            for bn in bns:
+                for sp in (1, 2, 3, 4, 6, 8, 12, 16):
+                    cfgs.append({"swap_ab": 1, "block_n": bn, "split_k": sp})
+            if M >= 64:
+                for bn in (64, 128, 256):
+                    for sp in (1, 2, 4):
+                        cfgs.append({"swap_ab": 0, "block_n": bn, "split_k": sp})
+            auto = w8.pick_config(M, N, K, w8.E4M3)
+            bytes_ = N * K + M * K + 2 * M * N
+            for cfg in [None] + cfgs:
+                ws = w8.Workspace(w8.mm_workspace_size(M, N, K, w8.E4M3, cfg), dev)
+
+                def fn():
+                    for i in range(8):
+                        w8.scaled_mm(a, copies[i % 4], sa, sb, out, workspace=ws, config=cfg)
+                try:
+                    gr = graph_of(fn, stream)
+                    t = time_graph(gr, stream, reps, 3) / (8 * reps)
+                except Exception as e:  # unsupported configuration
+                    lines.append({"M": M, "proj": name, "config": cfg, "error": str(e)[:200]})
+                    continue
+                lines.append({"M": M, "proj": name, "N": N, "K": K, "config": cfg or {"auto": auto},
+                              "us": t * 1e6, "gbs": bytes_ / t / 1e9})
+                del gr
+            del copies
+            torch.cuda.empty_cache()
+    if w8.device_status() != 0:
+        raise SystemExit("a kernel reported a pipeline timeout")
+    with open(out_path, "w") as f:
+        for ln in lines:
+            f.write(json.dumps(ln) + "\n")
+    print(f"wrote {len(lines)} lines to {out_path}")
 
 
 # ---------------------------------------------------------------- main paths
@@ -661,7 +728,12 @@ def main():
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
                     help="run a few launches of one kernel on a small case (for ncu) and exit")
     ap.add_argument("--launches", type=int, default=5)
+    ap.add_argument("--sweep-decode", metavar="OUT", default=None,
+                    help="time the decode GEMM shapes under a grid of configurations, write JSON lines to OUT")
     args = ap.parse_args()
+    if args.sweep_decode:
+        sweep_decode(args.sweep_decode)
+        return 0
     if args.profile_case:
         run_profile_case(args.profile_case, args.launches)
         return 0

@@ -131,28 +131,41 @@ long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 int num_kb(long long K, int q_dtype) { return static_cast<int>(ceil_div(K, q_dtype == W8A8_INT8 ? 64 : 128)); }
 
+// Split count that balances work units over the resident persistent CTAs:
+// the smallest split whose wave efficiency units / (waves * slots) is within
+// 3 % of the best, keeping at least `min_kb` K blocks per slice.
+int balanced_split(long long tiles, int kb, int slots, int min_kb, int max_split) {
+  double best_eff = 0.0;
+  int best = 1;
+  const int cap = std::max(1, std::min(max_split, kb / std::max(1, min_kb)));
+  double effs[65];
+  for (int s = 1; s <= cap; ++s) {
+    const long long units = tiles * s;
+    const long long waves = (units + slots - 1) / slots;
+    effs[s] = static_cast<double>(units) / static_cast<double>(waves * slots);
+    if (effs[s] > best_eff + 1e-9) best_eff = effs[s];
+  }
+  for (int s = 1; s <= cap; ++s)
+    if (effs[s] >= best_eff - 0.03) { best = s; break; }
+  return best;
+}
+
 void auto_config(long long M, long long N, long long K, int q_dtype, int sms, w8a8_mm_config* c) {
   const int kb = num_kb(K, q_dtype);
   if (M <= 256) {
-    // decode regime: weights on the 128-row side, tokens padded to block_n
+    // decode regime: weights on the 128-row side, tokens padded to block_n;
+    // narrow tiles keep two CTAs resident per SM
     c->swap_ab = 1;
     int bn = 16;
     while (bn < M && bn < 64) bn *= 2;
     c->block_n = bn;
     const long long tiles = ceil_div(N, 128) * ceil_div(M, bn);
-    // two CTAs per SM fit at these widths: aim for about 2 * sms CTAs while
-    // keeping >= 4 K blocks per slice
-    long long sp = (2LL * sms + tiles / 2) / std::max<long long>(tiles, 1);
-    sp = std::max<long long>(1, std::min<long long>(sp, kb / 4));
-    sp = std::min<long long>(sp, 16);
-    c->split_k = static_cast<int>(sp);
+    c->split_k = balanced_split(tiles, kb, 2 * sms, 4, 16);
   } else {
     c->swap_ab = 0;
     c->block_n = (q_dtype == W8A8_INT8) ? 128 : 256;
     const long long tiles = ceil_div(M, 128) * ceil_div(N, c->block_n);
-    long long sp = 1;
-    if (tiles < sms / 2) sp = std::min<long long>(std::max<long long>(1, sms / tiles), kb / 4);
-    c->split_k = static_cast<int>(std::max<long long>(1, sp));
+    c->split_k = tiles < sms / 2 ? balanced_split(tiles, kb, sms, 8, 16) : 1;
   }
   c->stages = 0;
 }

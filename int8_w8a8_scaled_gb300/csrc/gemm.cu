@@ -444,6 +444,10 @@ cudaError_t launch_one(const CUtensorMap& tp, const CUtensorMap& tq, const MmPar
   // the attribute is per function and device; setting it again is harmless
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  // all of the unified L1/shared storage as shared memory, so that two
+  // CTAs of the narrow (decode) configurations fit on one SM
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return e;
   int occ = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
   if (e != cudaSuccess) return e;
@@ -505,6 +509,7 @@ cudaError_t dispatch(const CUtensorMap& tp, const CUtensorMap& tq, const MmParam
 // int8 [rows, K] (leading dim ld) -> f16 [rows, K] contiguous, exact.
 __global__ void widen_int8_kernel(const int8_t* __restrict__ src, long long ld, int rows, int K,
                                   __half* __restrict__ dst) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int vpr = K / 16;  // K is a multiple of 16
   const long long total = static_cast<long long>(rows) * vpr;
@@ -566,8 +571,18 @@ cudaError_t launch_int8_widen(const void* src, long long ld_src, int rows, int K
   long long blocks = (total + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
-  widen_int8_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-      static_cast<const int8_t*>(src), ld_src, rows, K, static_cast<__half*>(dst_f16));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, widen_int8_kernel, static_cast<const int8_t*>(src), ld_src, rows, K,
+                                     static_cast<__half*>(dst_f16));
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

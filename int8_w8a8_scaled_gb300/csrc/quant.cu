@@ -36,10 +36,31 @@ namespace {
 
 constexpr int kRowThreads = 256;
 
-// Let the next kernel in the stream start its prologue now; it still waits
-// (griddepcontrol.wait) for this grid to finish before touching memory.
+// Programmatic dependent launch.  Every kernel here is launched with the
+// programmatic-serialisation attribute: it first waits for the preceding
+// kernel in the stream (and its memory) to finish, then lets the next kernel
+// start its own prologue.  Both instructions are no-ops without the
+// attribute.
 __device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, cudaStream_t st, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Params>(args)...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 __device__ __forceinline__ float load_f(const uint16_t* p, int kind) {
@@ -399,21 +420,16 @@ cudaError_t launch_rows(const QuantArgs& a, cudaStream_t st) {
   uint8_t* q = static_cast<uint8_t*>(a.q);
   const long long nvec = a.cols / 8;
   const long long per_thread = (nvec + kRowThreads - 1) / kRowThreads;
-  const dim3 grid(static_cast<unsigned>(a.rows));
-  if (!a.vec) {
-    quant_rows_kernel<XK, QK, 0><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.per_row, a.dynamic);
-  } else if (per_thread <= 1) {
-    quant_rows_kernel<XK, QK, 1><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.per_row, a.dynamic);
-  } else if (per_thread <= 2) {
-    quant_rows_kernel<XK, QK, 2><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.per_row, a.dynamic);
-  } else if (per_thread <= 4) {
-    quant_rows_kernel<XK, QK, 4><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.per_row, a.dynamic);
-  } else if (per_thread <= 8) {
-    quant_rows_kernel<XK, QK, 8><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.per_row, a.dynamic);
-  } else {
-    quant_rows_kernel<XK, QK, 16><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.per_row, a.dynamic);
-  }
-  return cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(a.rows)), block(kRowThreads);
+#define W8A8_ROWS(V) \
+  launch_pdl(quant_rows_kernel<XK, QK, V>, grid, block, st, x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.per_row, a.dynamic)
+  if (!a.vec) return W8A8_ROWS(0);
+  if (per_thread <= 1) return W8A8_ROWS(1);
+  if (per_thread <= 2) return W8A8_ROWS(2);
+  if (per_thread <= 4) return W8A8_ROWS(4);
+  if (per_thread <= 8) return W8A8_ROWS(8);
+  return W8A8_ROWS(16);
+#undef W8A8_ROWS
 }
 
 int flat_blocks(long long work_items, int num_sms) {
@@ -429,12 +445,13 @@ cudaError_t launch_quant_t(const QuantArgs& a, int num_sms, cudaStream_t st) {
   const uint16_t* x = static_cast<const uint16_t*>(a.x);
   uint8_t* q = static_cast<uint8_t*>(a.q);
   const bool contiguous = (a.ld_x == a.cols && a.ld_q == a.cols) || a.rows == 1;
+  const dim3 b256(256);
   if (a.per_row) return launch_rows<XK, QK>(a, st);
   if (!a.dynamic) {
     if (contiguous && a.vec) {
       const long long n = a.rows * a.cols;
-      quant_flat_kernel<XK, QK><<<flat_blocks(n / 16, num_sms), 256, 0, st>>>(x, n, q, a.scale, nullptr, 0);
-      return cudaGetLastError();
+      return launch_pdl(quant_flat_kernel<XK, QK>, dim3(flat_blocks(n / 16, num_sms)), b256, st, x, n, q, a.scale,
+                        static_cast<const unsigned*>(nullptr), 0);
     }
     return launch_rows<XK, QK>(a, st);
   }
@@ -443,18 +460,16 @@ cudaError_t launch_quant_t(const QuantArgs& a, int num_sms, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (contiguous && a.vec) {
     const long long n = a.rows * a.cols;
-    absmax_flat_kernel<XK><<<flat_blocks(n / 8, num_sms), 256, 0, st>>>(x, n, a.amax_word);
-    e = cudaGetLastError();
+    e = launch_pdl(absmax_flat_kernel<XK>, dim3(flat_blocks(n / 8, num_sms)), b256, st, x, n, a.amax_word);
     if (e != cudaSuccess) return e;
-    quant_flat_kernel<XK, QK><<<flat_blocks(n / 16, num_sms), 256, 0, st>>>(x, n, q, a.scale, a.amax_word, 1);
-    return cudaGetLastError();
+    return launch_pdl(quant_flat_kernel<XK, QK>, dim3(flat_blocks(n / 16, num_sms)), b256, st, x, n, q, a.scale,
+                      static_cast<const unsigned*>(a.amax_word), 1);
   }
-  const dim3 grid(static_cast<unsigned>(a.rows));
-  absmax_rows_kernel<XK><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, a.amax_word);
-  e = cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(a.rows)), block(kRowThreads);
+  e = launch_pdl(absmax_rows_kernel<XK>, grid, block, st, x, a.ld_x, a.cols, a.amax_word);
   if (e != cudaSuccess) return e;
-  quant_rows_from_word_kernel<XK, QK><<<grid, kRowThreads, 0, st>>>(x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.amax_word);
-  return cudaGetLastError();
+  return launch_pdl(quant_rows_from_word_kernel<XK, QK>, grid, block, st, x, a.ld_x, a.cols, q, a.ld_q, a.scale,
+                    static_cast<const unsigned*>(a.amax_word));
 }
 
 template <int QK, int YK>
@@ -464,11 +479,10 @@ cudaError_t launch_dequant_t(const DequantArgs& a, int num_sms, cudaStream_t st)
   const bool contiguous = (a.ld_q == a.cols && a.ld_y == a.cols) || a.rows == 1;
   if (!a.per_row && contiguous && a.vec) {
     const long long n = a.rows * a.cols;
-    dequant_flat_kernel<QK, YK><<<flat_blocks(n / 16, num_sms), 256, 0, st>>>(q, n, a.scale, y);
-    return cudaGetLastError();
+    return launch_pdl(dequant_flat_kernel<QK, YK>, dim3(flat_blocks(n / 16, num_sms)), dim3(256), st, q, n, a.scale, y);
   }
-  dequant_rows_kernel<QK, YK><<<static_cast<unsigned>(a.rows), kRowThreads, 0, st>>>(q, a.ld_q, a.cols, a.scale, a.per_row, y, a.ld_y);
-  return cudaGetLastError();
+  return launch_pdl(dequant_rows_kernel<QK, YK>, dim3(static_cast<unsigned>(a.rows)), dim3(kRowThreads), st, q, a.ld_q,
+                    a.cols, a.scale, a.per_row, y, a.ld_y);
 }
 
 }  // namespace
