@@ -170,7 +170,7 @@ def aggregate_tflops(flops_per_step_per_rank: float, steps: int, t_max: float, w
 class DecodeWorkload:
     """Llama-3-8B decode fp8: 4 token counts x 4 projections."""
 
-    def __init__(self, dev, seed=1000):
+    def __init__(self, dev, seed=1000, override=None):
         import torch
         import int8_w8a8_scaled_gb300 as w8
         import synthetic_inputs as si
@@ -192,8 +192,11 @@ class DecodeWorkload:
                 aq = torch.empty(M, K, dtype=torch.float8_e4m3fn, device=dev)
                 sa = torch.empty(M, dtype=torch.float32, device=dev)
                 out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-                self.items.append({"M": M, "name": name, "x": x, "aq": aq, "sa": sa, "out": out})
-                ws_need = max(ws_need, w8.mm_workspace_size(M, N, K, w8.E4M3))
+                cfg = None
+                if override:
+                    cfg = dict(w8.pick_config(M, N, K, w8.E4M3), **override)
+                self.items.append({"M": M, "name": name, "x": x, "aq": aq, "sa": sa, "out": out, "cfg": cfg})
+                ws_need = max(ws_need, w8.mm_workspace_size(M, N, K, w8.E4M3, cfg))
         self.ws = w8.Workspace(ws_need, dev)
         torch.cuda.synchronize()
 
@@ -220,13 +223,13 @@ class DecodeWorkload:
     def run_gemm(self):
         for it in self.items:
             wq, sw, _, _ = self.weights[it["name"]]
-            self.w8.scaled_mm(it["aq"], wq, it["sa"], sw, it["out"], workspace=self.ws)
+            self.w8.scaled_mm(it["aq"], wq, it["sa"], sw, it["out"], workspace=self.ws, config=it["cfg"])
 
     def run_step(self):
         for it in self.items:
             wq, sw, _, _ = self.weights[it["name"]]
             self.w8.scaled_quant(it["x"], it["aq"], it["sa"], per_token=True, dynamic=True)
-            self.w8.scaled_mm(it["aq"], wq, it["sa"], sw, it["out"], workspace=self.ws)
+            self.w8.scaled_mm(it["aq"], wq, it["sa"], sw, it["out"], workspace=self.ws, config=it["cfg"])
 
     def launches_per_step(self):
         return 2 * len(self.items)
@@ -503,6 +506,55 @@ def run_profile_case(name: str, launches: int):
 
 # ---------------------------------------------------------------- config sweep
 
+def sweep_large(out_path: str, reps: int = 5):
+    """Time the prefill (M=4096) fp8 shapes and the int8 70B shapes (M=8192)
+    under a grid of large-M kernel configurations."""
+    import torch
+    import int8_w8a8_scaled_gb300 as w8
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    lines = []
+    cases = [(4096, N, K, w8.E4M3) for _, N, K, _ in LLAMA8B] + [(8192, N, K, w8.INT8) for _, N, K in LLAMA70B]
+    for M, N, K, qd in cases:
+        qt = torch.float8_e4m3fn if qd == w8.E4M3 else torch.int8
+        g = torch.Generator(device=dev)
+        g.manual_seed(M + N + K)
+        lo, hi = (0, 126) if qd == w8.E4M3 else (0, 256)
+        a = torch.randint(lo, hi, (M, K), generator=g, device=dev, dtype=torch.uint8).view(qt)
+        b = torch.randint(lo, hi, (N, K), generator=g, device=dev, dtype=torch.uint8).view(qt)
+        sa = torch.rand(M, device=dev) * 0.01
+        sb = torch.rand(N, device=dev) * 0.01
+        out = torch.empty(M, N, dtype=torch.bfloat16 if qd == w8.E4M3 else torch.float16, device=dev)
+        bns = (64, 128, 256) if qd == w8.E4M3 else (64, 128)
+        cfgs = [None] + [{"swap_ab": 0, "block_n": bn, "split_k": sp, "stages": st}
+                         for bn in bns for sp in (1, 2) for st in (0, 3)]
+        flops = 2.0 * M * N * K
+        for cfg in cfgs:
+            ws = w8.Workspace(w8.mm_workspace_size(M, N, K, qd, cfg), dev)
+
+            def fn():
+                w8.scaled_mm(a, b, sa, sb, out, workspace=ws, config=cfg)
+            try:
+                gr = graph_of(fn, stream)
+                t = time_graph(gr, stream, reps, 2) / reps
+            except Exception as e:
+                lines.append({"M": M, "N": N, "K": K, "config": cfg, "error": str(e)[:200]})
+                continue
+            lines.append({"M": M, "N": N, "K": K, "q": "e4m3" if qd == w8.E4M3 else "int8",
+                          "config": cfg or {"auto": w8.pick_config(M, N, K, qd)}, "us": t * 1e6,
+                          "tflops": flops / t / 1e12})
+            del gr, ws
+        del a, b, out
+        torch.cuda.empty_cache()
+    if w8.device_status() != 0:
+        raise SystemExit("a kernel reported a pipeline timeout")
+    with open(out_path, "w") as f:
+        for ln in lines:
+            f.write(json.dumps(ln) + "\n")
+    print(f"wrote {len(lines)} lines to {out_path}")
+
+
 def sweep_decode(out_path: str, reps: int = 20):
     """Time every decode GEMM shape under a grid of kernel configurations
     (CUDA graph of 8 launches cycling over 4 weight copies, so weights come
@@ -613,7 +665,7 @@ def run_ours(args):
     pk, pk_kind = peaks()
     stream = torch.cuda.Stream(device=dev)
 
-    wl = DecodeWorkload(dev)
+    wl = DecodeWorkload(dev, override=json.loads(args.override) if args.override else None)
     g_step = graph_of(wl.run_step, stream)
     g_gemm = graph_of(wl.run_gemm, stream)
     g_quant = graph_of(wl.run_quant, stream)
@@ -728,9 +780,17 @@ def main():
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
                     help="run a few launches of one kernel on a small case (for ncu) and exit")
     ap.add_argument("--launches", type=int, default=5)
+    ap.add_argument("--override", default=None,
+                    help="JSON dict merged into the automatic matmul configuration of every decode GEMM "
+                         "(experiments; the default run uses the library's choice)")
     ap.add_argument("--sweep-decode", metavar="OUT", default=None,
                     help="time the decode GEMM shapes under a grid of configurations, write JSON lines to OUT")
+    ap.add_argument("--sweep-large", metavar="OUT", default=None,
+                    help="time the prefill / int8 70B shapes under large-M configurations")
     args = ap.parse_args()
+    if args.sweep_large:
+        sweep_large(args.sweep_large)
+        return 0
     if args.sweep_decode:
         sweep_decode(args.sweep_decode)
         return 0

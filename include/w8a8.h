@@ -199,12 +199,15 @@ W8A8_API w8a8_status w8a8_scaled_mm(const void* a_q, int64_t lda, const void* b_
  *  block_n   width of the narrow MMA side: 16..256, multiple of 16.
  *  split_k   number of K slices reduced in a fixed order (>= 1).
  *  stages    depth of the shared-memory ring (2..8); 0 = automatic.
+ *  ctas_per_sm  cap on the persistent CTAs per SM (1..4); 0 = as many as
+ *            the kernel's shared memory, registers and TMEM allow.
  * Fields set to 0 (except swap_ab) mean "choose automatically". */
 typedef struct {
   int swap_ab;
   int block_n;
   int split_k;
   int stages;
+  int ctas_per_sm;
 } w8a8_mm_config;
 
 /* The configuration w8a8_scaled_mm() picks for this problem (host only). */

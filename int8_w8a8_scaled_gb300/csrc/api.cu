@@ -131,43 +131,46 @@ long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 int num_kb(long long K, int q_dtype) { return static_cast<int>(ceil_div(K, q_dtype == W8A8_INT8 ? 64 : 128)); }
 
-// Split count that balances work units over the resident persistent CTAs:
-// the smallest split whose wave efficiency units / (waves * slots) is within
-// 3 % of the best, keeping at least `min_kb` K blocks per slice.
-int balanced_split(long long tiles, int kb, int slots, int min_kb, int max_split) {
-  double best_eff = 0.0;
-  int best = 1;
-  const int cap = std::max(1, std::min(max_split, kb / std::max(1, min_kb)));
-  double effs[65];
-  for (int s = 1; s <= cap; ++s) {
-    const long long units = tiles * s;
-    const long long waves = (units + slots - 1) / slots;
-    effs[s] = static_cast<double>(units) / static_cast<double>(waves * slots);
-    if (effs[s] > best_eff + 1e-9) best_eff = effs[s];
-  }
-  for (int s = 1; s <= cap; ++s)
-    if (effs[s] >= best_eff - 0.03) { best = s; break; }
-  return best;
+// Automatic configuration, fitted to the decode and prefill sweeps of
+// `bench.py --sweep-decode / --sweep-large` on GB300:
+//  - M <= 64: weights on the 128-row MMA side (swap), block_n 16 (M <= 8) or
+//    32 -- narrow tiles keep two CTAs resident per SM;
+//  - M > 64: tokens on the 128-row side, the widest block_n in {256, 128, 64}
+//    that still gives >= 0.6 tiles per SM;
+//  - split-K: as many K slices as fit in one wave of resident CTAs
+//    (floor(slots / tiles)), at least 4 K blocks per slice, at most 16.
+//    More waves or wider splits lose to the fixed cost of each unit and of
+//    the partial reduction.
+int one_wave_split(long long tiles, int kb, long long slots) {
+  long long sp = slots / std::max<long long>(1, tiles);
+  sp = std::min<long long>(sp, std::max(1, kb / 4));
+  sp = std::min<long long>(sp, 16);
+  return static_cast<int>(std::max<long long>(1, sp));
 }
+
+int resident_per_sm(int block_n) { return block_n <= 64 ? 2 : 1; }
 
 void auto_config(long long M, long long N, long long K, int q_dtype, int sms, w8a8_mm_config* c) {
   const int kb = num_kb(K, q_dtype);
-  if (M <= 256) {
-    // decode regime: weights on the 128-row side, tokens padded to block_n;
-    // narrow tiles keep two CTAs resident per SM
+  if (M <= 64) {
     c->swap_ab = 1;
-    int bn = 16;
-    while (bn < M && bn < 64) bn *= 2;
-    c->block_n = bn;
-    const long long tiles = ceil_div(N, 128) * ceil_div(M, bn);
-    c->split_k = balanced_split(tiles, kb, 2 * sms, 4, 16);
+    c->block_n = M <= 8 ? 16 : 32;
   } else {
     c->swap_ab = 0;
-    c->block_n = (q_dtype == W8A8_INT8) ? 128 : 256;
-    const long long tiles = ceil_div(M, 128) * ceil_div(N, c->block_n);
-    c->split_k = tiles < sms / 2 ? balanced_split(tiles, kb, sms, 8, 16) : 1;
+    const int widest = (q_dtype == W8A8_INT8) ? 128 : 256;
+    c->block_n = 64;
+    for (int bn = widest; bn >= 64; bn /= 2) {
+      if (ceil_div(M, 128) * ceil_div(N, bn) * 10 >= 6LL * sms) {
+        c->block_n = bn;
+        break;
+      }
+    }
   }
+  const long long tiles = c->swap_ab ? ceil_div(N, 128) * ceil_div(M, c->block_n)
+                                     : ceil_div(M, 128) * ceil_div(N, c->block_n);
+  c->split_k = one_wave_split(tiles, kb, static_cast<long long>(sms) * resident_per_sm(c->block_n));
   c->stages = 0;
+  c->ctas_per_sm = 0;
 }
 
 int auto_stages(int block_n, int smem_optin) {
@@ -229,6 +232,8 @@ w8a8_status validate_config(const w8a8_mm_config& c, int q_dtype, int smem_optin
   if (c.split_k < 1 || c.split_k > 64) return fail(W8A8_ERR_UNSUPPORTED, "split_k must be in [1, 64]");
   if (c.stages != 0 && (c.stages < 2 || c.stages > 8))
     return fail(W8A8_ERR_UNSUPPORTED, "stages must be 0 (auto) or in [2, 8]");
+  if (c.ctas_per_sm < 0 || c.ctas_per_sm > 4)
+    return fail(W8A8_ERR_UNSUPPORTED, "ctas_per_sm must be 0 (auto) or in [1, 4]");
   const int st = c.stages > 0 ? c.stages : auto_stages(c.block_n, smem_optin);
   if (gemm_smem_bytes(c.block_n, st) > smem_optin)
     return fail(W8A8_ERR_UNSUPPORTED, "stages=%d with block_n=%d needs %d bytes of shared memory (> %d)", st,
@@ -345,6 +350,10 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
   prm.kchunk_kb = kInt8ChunkK / 64;
   prm.num_sms = dev.sms;
   prm.pdl = 1;
+  // up to 256 KB of each CTA's first weight slice (16 KB per K block of 128
+  // weight rows)
+  prm.prefetch_kb = 16;
+  prm.max_ctas_per_sm = cfg.ctas_per_sm;
   const int out_kind = out_dtype == W8A8_BF16 ? OUT_BF16 : out_dtype == W8A8_FP16 ? OUT_FP16 : OUT_RAW;
   e = i8 ? launch_int8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream)
          : launch_fp8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream);

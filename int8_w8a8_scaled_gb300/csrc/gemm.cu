@@ -150,6 +150,44 @@ __device__ __forceinline__ void store16(const MmParams& prm, int lane_idx, int c
   }
 }
 
+// Split-K partial of one TMEM lane: 16 consecutive accumulator columns
+// starting at col0, written as float4s into the lane's row of the partial
+// tile (row stride = valid columns rounded up to 4).
+__device__ __forceinline__ void write_partial16(uint32_t* prow, int col0, int qvalid, const uint32_t (&v)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (col0 + 4 * j < qvalid)
+      *reinterpret_cast<uint4*>(prow + col0 + 4 * j) = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+}
+
+// Epilogue store of four reduced accumulators at P row p and Q columns
+// q..q+3 (only the first `nvalid` are inside the problem).
+template <bool SWAP, typename OutT, typename V>
+__device__ __forceinline__ void store4(const MmParams& prm, int p, int q, int nvalid, const V (&v)[4]) {
+  OutT* out = reinterpret_cast<OutT*>(prm.out);
+  if (!SWAP) {
+    if (p >= prm.M) return;
+    const float sa = prm.a_per_row ? __ldg(prm.scale_a + p) : __ldg(prm.scale_a);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j < nvalid) {
+        const float sb = prm.b_per_row ? __ldg(prm.scale_b + q + j) : __ldg(prm.scale_b);
+        out[static_cast<long long>(p) * prm.ldc + q + j] = OutConv<OutT>::conv(v[j], sa, sb);
+      }
+    }
+  } else {
+    if (p >= prm.N) return;
+    const float sb = prm.b_per_row ? __ldg(prm.scale_b + p) : __ldg(prm.scale_b);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j < nvalid) {
+        const float sa = prm.a_per_row ? __ldg(prm.scale_a + q + j) : __ldg(prm.scale_a);
+        out[static_cast<long long>(q + j) * prm.ldc + p] = OutConv<OutT>::conv(v[j], sa, sb);
+      }
+    }
+  }
+}
+
 // One work unit is a (K slice, output tile) pair; the persistent CTAs walk
 // the units round-robin.  Units are numbered slice-major so that the slices
 // of a tile are spread over different CTAs.
@@ -213,6 +251,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int units = prm.tiles_p * prm.tiles_q * prm.splits;
+
+  // Warm L2 with the weight tiles of this CTA's first work unit before
+  // waiting on the preceding kernel: a prefetch only reads (coherent) global
+  // memory into L2, so it is safe whatever that kernel writes, and the
+  // weight stream starts while the preceding kernel is still running.
+  if (threadIdx.x == 0 && blockIdx.x < units) {
+    const Unit un = unit_of(blockIdx.x, prm, group, BN);
+    const CUtensorMap* wmap = SWAP ? &tmap_p : &tmap_q;
+    const int w_row = SWAP ? un.p0 : un.q0;
+    const int n_pf = min(un.nkb, prm.prefetch_kb);
+    for (int i = 0; i < n_pf; ++i) tma_prefetch_l2_2d(wmap, (un.kb_begin + i) * kKbElems, w_row);
+  }
 
   auto full_bar = [&](int s) { return smem_addr(bars + s); };
   auto empty_bar = [&](int s) { return smem_addr(bars + stages + s); };
@@ -315,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lane_idx = un.p0 + row;  // global P row of this thread
       // columns of this tile inside the problem (the Q side is M with swap)
       const int qvalid = min(BN, (SWAP ? prm.M : prm.N) - un.q0);
+      const int qv4 = (qvalid + 3) & ~3;  // row stride of a partial tile (floats)
       float s_lane;
       if (!SWAP)
         s_lane = (lane_idx < prm.M) ? (prm.a_per_row ? __ldg(prm.scale_a + lane_idx) : __ldg(prm.scale_a)) : 0.f;
@@ -352,9 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!last) {
               tmem_st16(tot_addr + g * 16, t);
             } else if (prm.splits > 1) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (g * 16 + j < qvalid) part[static_cast<size_t>(g * 16 + j) * kTileP + row] = t[j];
+              write_partial16(part + static_cast<size_t>(row) * qv4, g * 16, qvalid, t);
             } else {
               int v[16];
 #pragma unroll
@@ -364,9 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             tmem_ld_wait();
             if (prm.splits > 1) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (g * 16 + j < qvalid) part[static_cast<size_t>(g * 16 + j) * kTileP + row] = r[j];
+              write_partial16(part + static_cast<size_t>(row) * qv4, g * 16, qvalid, r);
             } else {
               float v[16];
 #pragma unroll
@@ -392,34 +439,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         epi_bar_sync();
         if (s_is_last) {
           __threadfence();
+          // the 128 epilogue threads sweep the tile's partials with
+          // independent float4 loads (slice order 0..S-1 per element) and
+          // each finishes four outputs
           const uint32_t* base = reinterpret_cast<const uint32_t*>(prm.partial) +
                                  static_cast<size_t>(un.tile_lin) * prm.splits * tile_elems;
-#pragma unroll 1
-          for (int g = 0; g < kGroups; ++g) {
-            if (g * 16 >= qvalid) break;
+          const int nvec = kTileP * qv4 / 4;
+#pragma unroll 2
+          for (int v = et; v < nvec; v += kEpiThreads) {
+            const int row_r = (v * 4) / qv4;
+            const int col = (v * 4) - row_r * qv4;
             if (INT8) {
-              int v[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] = 0;
+              int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
               for (int sl = 0; sl < prm.splits; ++sl) {
-                const uint32_t* src = base + sl * tile_elems + static_cast<size_t>(g * 16) * kTileP + row;
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  if (g * 16 + j < qvalid) v[j] += static_cast<int>(__ldcg(src + j * kTileP));
+                const uint4 x = __ldcg(reinterpret_cast<const uint4*>(base + sl * tile_elems) + v);
+                a0 += static_cast<int>(x.x);
+                a1 += static_cast<int>(x.y);
+                a2 += static_cast<int>(x.z);
+                a3 += static_cast<int>(x.w);
               }
-              store16<SWAP, OutT>(prm, lane_idx, un.q0 + g * 16, v, s_lane);
+              const int vals[4] = {a0, a1, a2, a3};
+              store4<SWAP, OutT>(prm, un.p0 + row_r, un.q0 + col, qvalid - col, vals);
             } else {
-              float v[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] = 0.f;
+              float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
               for (int sl = 0; sl < prm.splits; ++sl) {
-                const float* src = reinterpret_cast<const float*>(base + sl * tile_elems) +
-                                   static_cast<size_t>(g * 16) * kTileP + row;
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  if (g * 16 + j < qvalid) v[j] += __ldcg(src + j * kTileP);
+                const float4 x = __ldcg(reinterpret_cast<const float4*>(base + sl * tile_elems) + v);
+                a0 += x.x;
+                a1 += x.y;
+                a2 += x.z;
+                a3 += x.w;
               }
-              store16<SWAP, OutT>(prm, lane_idx, un.q0 + g * 16, v, s_lane);
+              const float vals[4] = {a0, a1, a2, a3};
+              store4<SWAP, OutT>(prm, un.p0 + row_r, un.q0 + col, qvalid - col, vals);
             }
           }
           if (et == 0) prm.counters[un.tile_lin] = 0u;
@@ -448,10 +499,22 @@ cudaError_t launch_one(const CUtensorMap& tp, const CUtensorMap& tq, const MmPar
   // CTAs of the narrow (decode) configurations fit on one SM
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
-  int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
+  // resident CTAs per SM from the kernel's own resources (shared memory,
+  // registers, threads, TMEM columns)
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
+  int dev = 0, smem_sm = 0, reserved = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
+  const int per_cta_smem = smem + static_cast<int>(fa.sharedSizeBytes) + reserved;
+  const int regs_per_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+  int occ = smem_sm / per_cta_smem;
+  occ = min(occ, 65536 / (regs_per_warp * (kThreads / 32)));
+  occ = min(occ, 2048 / kThreads);
   occ = max(1, min(occ, 512 / tmem_cols_for(BN, INT8)));
+  if (p.max_ctas_per_sm > 0) occ = min(occ, p.max_ctas_per_sm);
   const int units = p.tiles_p * p.tiles_q * p.splits;
   const int grid = max(1, min(units, p.num_sms * occ));
   const int group = SWAP ? 1 : 8;

@@ -31,6 +31,8 @@ struct MmParams {
   int kchunk_kb;         // int8 path: K blocks per exact fp32 chunk
   int num_sms;           // persistent grid = min(units, num_sms * resident CTAs per SM)
   int pdl;               // launch with programmatic stream serialisation
+  int prefetch_kb;       // weight K blocks of the first unit prefetched into L2 early
+  int max_ctas_per_sm;   // 0: as many as fit; else cap the persistent grid per SM
 };
 
 // OUT_RAW: fp32 y = (acc * s_a) * s_b for the fp8 path, raw int32
