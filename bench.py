@@ -526,7 +526,7 @@ def sweep_large(out_path: str, reps: int = 5):
         sa = torch.rand(M, device=dev) * 0.01
         sb = torch.rand(N, device=dev) * 0.01
         out = torch.empty(M, N, dtype=torch.bfloat16 if qd == w8.E4M3 else torch.float16, device=dev)
-        bns = (64, 128, 256) if qd == w8.E4M3 else (64, 128)
+        bns = (128, 160, 192, 224, 256) if qd == w8.E4M3 else (64, 128)
         cfgs = [None] + [{"swap_ab": 0, "block_n": bn, "split_k": sp, "stages": st}
                          for bn in bns for sp in (1, 2) for st in (0, 3)]
         flops = 2.0 * M * N * K
@@ -581,7 +581,7 @@ def sweep_decode(out_path: str, reps: int = 20):
                 for sp in (1, 2, 3, 4, 6, 8, 12, 16):
                     cfgs.append({"swap_ab": 1, "block_n": bn, "split_k": sp})
             if M >= 64:
-                for bn in (64, 128, 256):
+                for bn in (64, 128, 160, 192, 224, 256):
                     for sp in (1, 2, 4):
                         cfgs.append({"swap_ab": 0, "block_n": bn, "split_k": sp})
             auto = w8.pick_config(M, N, K, w8.E4M3)

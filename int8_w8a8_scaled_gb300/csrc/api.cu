@@ -122,9 +122,11 @@ w8a8_status make_operand_map(CUtensorMap* map, const void* base, bool f16, long 
 constexpr int kSmemTwoPerSm = 113 * 1024;   // budget that lets two CTAs share an SM
 constexpr int kInt8ChunkK = 1024;           // exact fp32 accumulation bound: 1024 * 128 * 128 = 2^24
 
-bool valid_block_n(int bn, int q_dtype) {
-  if (q_dtype == W8A8_INT8) return bn == 16 || bn == 32 || bn == 64 || bn == 128;
-  return bn == 16 || bn == 32 || bn == 64 || bn == 128 || bn == 256;
+bool valid_block_n(int bn, int q_dtype, int swap_ab) {
+  if (bn == 16 || bn == 32 || bn == 64 || bn == 128) return true;
+  if (q_dtype == W8A8_INT8) return false;
+  if (bn == 256) return true;
+  return !swap_ab && (bn == 160 || bn == 192 || bn == 224);
 }
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
@@ -157,12 +159,33 @@ void auto_config(long long M, long long N, long long K, int q_dtype, int sms, w8
     c->block_n = M <= 8 ? 16 : 32;
   } else {
     c->swap_ab = 0;
-    const int widest = (q_dtype == W8A8_INT8) ? 128 : 256;
-    c->block_n = 64;
-    for (int bn = widest; bn >= 64; bn /= 2) {
-      if (ceil_div(M, 128) * ceil_div(N, bn) * 10 >= 6LL * sms) {
-        c->block_n = bn;
-        break;
+    if (q_dtype == W8A8_INT8) {
+      c->block_n = 64;
+      for (int bn = 128; bn >= 64; bn /= 2) {
+        if (ceil_div(M, 128) * ceil_div(N, bn) * 10 >= 6LL * sms) {
+          c->block_n = bn;
+          break;
+        }
+      }
+    } else {
+      // widest tile first; prefer a narrower one only when it balances the
+      // persistent waves clearly better (a wave of width-w tiles costs ~w)
+      const int cands[5] = {256, 224, 192, 160, 128};
+      double best = 1e30;
+      c->block_n = 64;
+      for (int i = 0; i < 5; ++i) {
+        const int bn = cands[i];
+        const long long tiles = ceil_div(M, 128) * ceil_div(N, bn);
+        if (tiles * 10 < 6LL * sms) continue;
+        const long long waves = (tiles + sms - 1) / sms;
+        // time ~ waves * bn / efficiency(bn); narrower tiles lose a little
+        // per-flop efficiency (operand re-reads), modelled as 3 % per step
+        const double t = static_cast<double>(waves) * bn * (1.0 + 0.03 * i) /
+                         static_cast<double>(std::min<long long>(N, ceil_div(N, bn) * bn));
+        if (t < best - 1e-12) {
+          best = t;
+          c->block_n = bn;
+        }
       }
     }
   }
@@ -226,8 +249,9 @@ Plan make_plan(long long M, long long N, long long K, int q_dtype, const w8a8_mm
 
 w8a8_status validate_config(const w8a8_mm_config& c, int q_dtype, int smem_optin) {
   if (c.swap_ab != 0 && c.swap_ab != 1) return fail(W8A8_ERR_UNSUPPORTED, "swap_ab must be 0 or 1");
-  if (!valid_block_n(c.block_n, q_dtype))
-    return fail(W8A8_ERR_UNSUPPORTED, "block_n %d not supported (16..256 powers of two; <= 128 for int8)",
+  if (!valid_block_n(c.block_n, q_dtype, c.swap_ab))
+    return fail(W8A8_ERR_UNSUPPORTED,
+                "block_n %d not supported (16, 32, 64, 128, 256; 160/192/224 for e4m3 without swap; <= 128 for int8)",
                 c.block_n);
   if (c.split_k < 1 || c.split_k > 64) return fail(W8A8_ERR_UNSUPPORTED, "split_k must be in [1, 64]");
   if (c.stages != 0 && (c.stages < 2 || c.stages > 8))

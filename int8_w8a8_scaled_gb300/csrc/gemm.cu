@@ -47,9 +47,9 @@ constexpr int kRowBytes = 128;    // bytes of K per stage row (one swizzle row)
 constexpr int kPBytes = kTileP * kRowBytes;
 
 __host__ __device__ constexpr int tmem_cols_for(int bn, bool int8) {
-  // fp8: one fp32 accumulator of bn columns.  int8: two fp32 chunk
-  // accumulators + one int32 total.
-  int need = int8 ? 3 * bn : bn;
+  // Accumulation units alternate between two fp32 accumulators of bn
+  // columns at columns 0 and bn; int8 adds an int32 total at 2 * bn.
+  int need = int8 ? 3 * bn : 2 * bn;
   int c = 32;
   while (c < need) c *= 2;
   return c;
@@ -237,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kIdesc = make_idesc(kTileP, BN, 0);
   constexpr int kTmemCols = tmem_cols_for(BN, INT8);
   constexpr int kGroups = BN / 16;
+  static_assert((INT8 ? 3 : 2) * BN <= kTmemCols && kTmemCols <= 512, "accumulators must fit the TMEM allocation");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -565,6 +566,17 @@ cudaError_t dispatch(const CUtensorMap& tp, const CUtensorMap& tq, const MmParam
       // int8 keeps 3 x block_n TMEM columns; 3 x 256 does not fit in 512
       if (INT8) return cudaErrorInvalidValue;
       return launch_swap<256, false>(tp, tq, p, swap, out_kind, stages, stream);
+    // wave-balancing widths for the large-M e4m3 regime (tokens on the
+    // 128-row side only)
+    case 160:
+      if (INT8 || swap) return cudaErrorInvalidValue;
+      return launch_out<160, false, false>(tp, tq, p, out_kind, stages, stream);
+    case 192:
+      if (INT8 || swap) return cudaErrorInvalidValue;
+      return launch_out<192, false, false>(tp, tq, p, out_kind, stages, stream);
+    case 224:
+      if (INT8 || swap) return cudaErrorInvalidValue;
+      return launch_out<224, false, false>(tp, tq, p, out_kind, stages, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -69,6 +69,9 @@ FP8_CONFIGS = [
     {"swap_ab": 1, "block_n": 128, "split_k": 3},
     {"swap_ab": 1, "block_n": 256, "split_k": 1},
     {"swap_ab": 0, "block_n": 256, "split_k": 2, "stages": 2},
+    {"swap_ab": 0, "block_n": 160, "split_k": 1},
+    {"swap_ab": 0, "block_n": 192, "split_k": 2},
+    {"swap_ab": 0, "block_n": 224, "split_k": 1},
 ]
 
 FP8_SHAPES = [(1, 256, 512), (32, 256, 512), (3, 100, 272), (129, 300, 1040), (300, 384, 640),
@@ -307,3 +310,54 @@ def test_shared_workspace_across_shapes_and_dtypes():
             torch.cuda.synchronize()
             assert_fp8_close(out.cpu().numpy(), ref["y"], f"{(M, N, K, cfg)}")
     assert not ws.buf[:65536].any().item()
+
+
+@pytest.mark.parametrize("cfg", [{"swap_ab": 1, "block_n": 32, "split_k": 2},
+                                 {"swap_ab": 1, "block_n": 64, "split_k": 1},
+                                 {"swap_ab": 1, "block_n": 16, "split_k": 3},
+                                 {"swap_ab": 0, "block_n": 64, "split_k": 1, "stages": 3},
+                                 {"swap_ab": 0, "block_n": 128, "split_k": 1, "stages": 3},
+                                 {"swap_ab": 0, "block_n": 224, "split_k": 1, "stages": 3}],
+                         ids=lambda c: "_".join(f"{k}{v}" for k, v in c.items()))
+def test_fp8_many_resident_ctas(cfg):
+    """Enough work units that several persistent CTAs share each SM (each
+    with its own TMEM allocation), checked element-wise."""
+    M, N, K = (32, 16384, 1024) if cfg["swap_ab"] else (1024, 7168, 512)
+    A, B, sa, sb = fp8_problem(M, N, K, seed=61)
+    out = run_gpu(A, B, sa, sb, oracle.E4M3, torch.float32, config=cfg)
+    im = np.random.default_rng(0).integers(0, M, 4000)
+    inn = np.random.default_rng(1).integers(0, N, 4000)
+    ref = oracle.scaled_mm_sample(A, B, sa, sb, oracle.E4M3, oracle.BF16, im, inn)
+    assert_fp8_close(out.cpu().numpy()[im, inn], ref["y"], str(cfg))
+
+
+def test_back_to_back_graph_of_gemms_with_overlap():
+    """Several different GEMMs replayed back to back in one CUDA graph
+    (programmatic dependent launch lets the next kernel's CTAs start while
+    the previous one finishes); every output checked against the oracle."""
+    shapes = [(16, 4096, 1024), (16, 8192, 1024), (300, 3072, 512), (1, 6144, 2048)]
+    probs = [fp8_problem(M, N, K, seed=70 + i) for i, (M, N, K) in enumerate(shapes)]
+    dev = [(to_gpu_codes(A, oracle.E4M3), to_gpu_codes(B, oracle.E4M3), torch.from_numpy(sa).cuda(),
+            torch.from_numpy(sb).cuda(), torch.empty(A.shape[0], B.shape[0], dtype=torch.float32, device="cuda"))
+           for A, B, sa, sb in probs]
+    ws = w8.Workspace(max(w8.mm_workspace_size(M, N, K, w8.E4M3) for M, N, K in shapes))
+    s = torch.cuda.Stream()
+
+    def run():
+        for a, b, sa, sb, out in dev:
+            w8.scaled_mm(a, b, sa, sb, out, workspace=ws)
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            run()
+    for _, _, _, _, out in dev:
+        out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for (A, B, sa, sb), (_, _, _, _, out) in zip(probs, dev):
+        ref = oracle.scaled_mm(A, B, sa, sb, oracle.E4M3, oracle.BF16)
+        assert_fp8_close(out.cpu().numpy(), ref["y"])
+    assert w8.device_status() == 0
