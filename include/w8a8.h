@@ -259,6 +259,43 @@ W8A8_API w8a8_status w8a8_requant_shards(const void* q, int q_dtype, int64_t col
                                          void* q_out, int64_t ld_out,
                                          float* scale_out, w8a8_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Scaled matmul without a caller-provided workspace
+ *
+ * No counterpart on the source pages: this entry point exists for callers
+ * that cannot allocate device memory where they run the matmul -- code
+ * running inside an allocator hook or a CUDA-graph-capturing runtime that
+ * forbids new allocations, plug-ins handed only their operand and output
+ * buffers, or processes whose memory is fully reserved by another runtime.
+ *
+ * Same arguments and results as w8a8_scaled_mm, minus the workspace.  The
+ * scratch the matmul needs (split-K arrival counters and partial tiles)
+ * lives in one fixed array of w8a8_scaled_mm_noalloc_max_scratch() bytes
+ * (8 MiB + 64 KiB) that the library defines in device memory: every GPU that
+ * loads the library holds it until the process exits.  Nothing is allocated
+ * or freed by the call, not even through a library routine.
+ *
+ *  - Problems whose scratch need (w8a8_scaled_mm_workspace_size) exceeds the
+ *    array are rejected with W8A8_ERR_WORKSPACE and a message; in practice
+ *    this covers e4m3 at every size (large M needs no scratch) and int8 only
+ *    where its widened operand planes fit.
+ *  - The array is shared by every call on a device and keeps the previous
+ *    call's contents; each call clears the counters it relies on (an
+ *    asynchronous memset on `stream`).  Calls that may overlap on the GPU
+ *    (different streams without ordering) race on the array: serialise them.
+ *  - The first call on a device looks up the array's device address (a host
+ *    query, once per device, with that device current); make that first call
+ *    before any stream capture.
+ */
+W8A8_API size_t w8a8_scaled_mm_noalloc_max_scratch(void);
+
+W8A8_API w8a8_status w8a8_scaled_mm_noalloc(const void* a_q, int64_t lda, const void* b_q,
+                                            int64_t ldb, const float* scale_a, int a_gran,
+                                            const float* scale_b, int b_gran, void* out,
+                                            int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                            int q_dtype, int out_dtype,
+                                            w8a8_stream_t stream);
+
 /* Reads and clears the library's device-side status word on the current
  * device (W8A8_DEVICE_* bits; a kernel sets W8A8_DEVICE_TIMEOUT when one of
  * its bounded pipeline waits gave up instead of hanging).  This call

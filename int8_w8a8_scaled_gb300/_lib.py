@@ -41,6 +41,8 @@ EXPORTS = (
     "w8a8_device_status",
     "w8a8_expand_shard_scales",
     "w8a8_requant_shards",
+    "w8a8_scaled_mm_noalloc_max_scratch",
+    "w8a8_scaled_mm_noalloc",
 )
 
 
@@ -102,6 +104,10 @@ def load(build_if_needed: bool = True):
         lib.w8a8_expand_shard_scales.argtypes = [P, P, I, P, P]
         lib.w8a8_requant_shards.restype = I
         lib.w8a8_requant_shards.argtypes = [P, I, I64, I64, P, P, I, P, I64, P, P]
+        lib.w8a8_scaled_mm_noalloc_max_scratch.restype = SZ
+        lib.w8a8_scaled_mm_noalloc_max_scratch.argtypes = []
+        lib.w8a8_scaled_mm_noalloc.restype = I
+        lib.w8a8_scaled_mm_noalloc.argtypes = [P, I64, P, I64, P, I, P, I, P, I64, I64, I64, I64, I, I, P]
         lib.w8a8_device_status.restype = I
         lib.w8a8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
         _lib = lib

@@ -387,6 +387,8 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
 
 }  // namespace
 
+void w8a8::set_last_error(const char* msg) { t_last_error = msg ? msg : ""; }
+
 extern "C" {
 
 const char* w8a8_last_error(void) { return t_last_error.c_str(); }

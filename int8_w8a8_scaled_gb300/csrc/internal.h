@@ -90,6 +90,9 @@ struct DequantArgs {
 };
 cudaError_t launch_dequant(const DequantArgs& a, int num_sms, cudaStream_t stream);
 
+// Sets the message returned by w8a8_last_error() on this host thread.
+void set_last_error(const char* msg);
+
 // Row shards of a merged weight: cumulative row ends.
 constexpr int kMaxShards = 16;
 struct ShardTable {

@@ -1,0 +1,91 @@
+// noalloc.cu -- a scaled_mm entry point that needs no caller-provided
+// workspace and allocates nothing.
+//
+// Some callers cannot allocate device memory at the point where they run a
+// matmul: code that executes inside a framework's own allocator hook, a
+// plug-in that is handed only the operand and output buffers, or a runtime
+// that has already reserved all device memory for itself.  For them this
+// file keeps the matmul's scratch (the split-K arrival counters and the
+// split-K partial tiles) in one file-scope device array of fixed size, which
+// the CUDA runtime creates when the library is loaded on a device and keeps
+// until the process exits.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/w8a8.h"
+
+#include "internal.h"
+
+// 8 MiB of split-K partials plus the 64 KiB counter region at the head.
+static constexpr size_t kScratchBytes = (8u << 20) + (64u << 10);
+
+// The scratch itself: one per device that loads the library, zero at load.
+static __device__ __align__(256) unsigned char g_w8a8_static_scratch[kScratchBytes];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_ptr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+// Device address of the scratch array on the current device.  The array's
+// name in host code is only a host-side handle, so the address is looked up
+// once per device, with that device current, and cached.
+w8a8_status scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return W8A8_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_w8a8_static_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      w8a8::set_last_error("scaled_mm_noalloc: cudaGetSymbolAddress of the scratch array failed");
+      return W8A8_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return W8A8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t w8a8_scaled_mm_noalloc_max_scratch(void) { return kScratchBytes; }
+
+w8a8_status w8a8_scaled_mm_noalloc(const void* a_q, int64_t lda, const void* b_q, int64_t ldb,
+                                   const float* scale_a, int a_gran, const float* scale_b, int b_gran,
+                                   void* out, int64_t ldc, int64_t M, int64_t N, int64_t K, int q_dtype,
+                                   int out_dtype, w8a8_stream_t stream) {
+  if (M < 1 || N < 1 || K < 1) {
+    // let the regular entry point produce the message
+    return w8a8_scaled_mm(a_q, lda, b_q, ldb, scale_a, a_gran, scale_b, b_gran, out, ldc, M, N, K, q_dtype,
+                          out_dtype, nullptr, 0, stream);
+  }
+  const size_t need = w8a8_scaled_mm_workspace_size(M, N, K, q_dtype);
+  if (need > kScratchBytes) {
+    w8a8::set_last_error("scaled_mm_noalloc: this problem needs more scratch than the library's fixed array");
+    return W8A8_ERR_WORKSPACE;
+  }
+  void* scratch = nullptr;
+  w8a8_status st = scratch_address(&scratch);
+  if (st != W8A8_OK) return st;
+  if (need > 0) {
+    // The array keeps whatever the previous call left; the split-K arrival
+    // counters at its head must start at zero.
+    if (cudaMemsetAsync(scratch, 0, 64u << 10, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+      cudaGetLastError();
+      w8a8::set_last_error("scaled_mm_noalloc: clearing the split-K counters failed");
+      return W8A8_ERR_CUDA;
+    }
+  }
+  return w8a8_scaled_mm(a_q, lda, b_q, ldb, scale_a, a_gran, scale_b, b_gran, out, ldc, M, N, K, q_dtype, out_dtype,
+                        need > 0 ? scratch : nullptr, need > 0 ? kScratchBytes : 0, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+"""The allocation-free scaled matmul entry point.
+
+w8a8_scaled_mm_noalloc serves callers that cannot allocate device memory
+where they run the matmul (allocator hooks, plug-ins given only operand and
+output buffers, processes whose memory another runtime has reserved): it
+keeps its split-K scratch in a fixed array the library defines in device
+memory.  Checked here through the C ABI against w8a8_scaled_mm with a
+caller workspace, on two calls in a row, within the fp8 tolerance used by
+the other matmul tests.  This file is collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from int8_w8a8_scaled_gb300 import _lib
+
+pytestmark = pytest.mark.gpu
+
+E4M3, BF16, PER_ROW, PER_TENSOR = 0, 2, 1, 0
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _problem(M, N, K, seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    a = torch.randint(0, 126, (M, K), generator=g, device="cuda", dtype=torch.uint8)
+    b = torch.randint(0, 126, (N, K), generator=g, device="cuda", dtype=torch.uint8)
+    a[:, ::3] |= 0x80  # mixed signs
+    sa = torch.rand(M, generator=g, device="cuda") * 1e-3
+    sb = torch.rand(N, generator=g, device="cuda") * 1e-3
+    return a, b, sa, sb
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (16, 6144, 4096), (64, 4096, 14336), (3, 300, 1040)])
+def test_noalloc_matches_workspace_entry_point_twice(M, N, K):
+    lib = _lib.load()
+    a, b, sa, sb = _problem(M, N, K, seed=M + N)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    need = lib.w8a8_scaled_mm_workspace_size(M, N, K, E4M3)
+    assert 0 < need <= lib.w8a8_scaled_mm_noalloc_max_scratch()  # split-K scratch is in use
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    ref = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    st = lib.w8a8_scaled_mm(_p(a), K, _p(b), K, _p(sa), PER_ROW, _p(sb), PER_ROW, _p(ref), N, M, N, K, E4M3, BF16,
+                            _p(ws), need, stream)
+    assert st == 0, lib.w8a8_last_error()
+    for _ in range(2):
+        out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        st = lib.w8a8_scaled_mm_noalloc(_p(a), K, _p(b), K, _p(sa), PER_ROW, _p(sb), PER_ROW, _p(out), N, M, N, K,
+                                        E4M3, BF16, stream)
+        assert st == 0, lib.w8a8_last_error()
+        torch.cuda.synchronize()
+        r = ref.float().cpu().numpy().astype(np.float64)
+        o = out.float().cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(o - r) <= 2.0 ** -7 * np.abs(r) + 1e-3)
+
+
+def test_noalloc_rejects_problems_beyond_its_array():
+    lib = _lib.load()
+    a, b, sa, sb = _problem(16, 64, 64, seed=1)
+    out = torch.empty(16, 64, dtype=torch.float16, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    # int8 widens both operands into f16 planes: 2 * (8192 + 8192) * 8192
+    # bytes, far beyond the fixed array; rejected before any launch
+    M = N = K = 8192
+    assert lib.w8a8_scaled_mm_workspace_size(M, N, K, 1) > lib.w8a8_scaled_mm_noalloc_max_scratch()
+    st = lib.w8a8_scaled_mm_noalloc(_p(a), K, _p(b), K, _p(sa), PER_ROW, _p(sb), PER_ROW, _p(out), N, M, N, K,
+                                    1, 3, stream)
+    assert st == 4  # W8A8_ERR_WORKSPACE
+    assert b"fixed array" in lib.w8a8_last_error()
