@@ -441,6 +441,7 @@ PROFILE_CASES = {
     "quant_kv": "per-tensor dynamic e4m3 quantiser (absmax + convert), KV [524288 x 128] bf16",
     "dequant_kv": "e4m3 -> bf16 dequantiser, KV [524288 x 128]",
     "decode_step": "the decode step (16 quantisers + 16 GEMMs), eager launches",
+    "quant_decode": "per-token dynamic e4m3 quantiser of one decode token, [1 x 4096] bf16",
 }
 
 
@@ -480,6 +481,12 @@ def run_profile_case(name: str, launches: int):
         print(json.dumps({"case": name, "config": w8.pick_config(M, N, K, qd)}), flush=True)
         for _ in range(launches):
             w8.scaled_mm(a, b, sa, sb, out, workspace=ws)
+    elif name == "quant_decode":
+        x = si.normal_with_outliers((1, 4096), seed=3, device=dev)
+        q = torch.empty(1, 4096, dtype=torch.float8_e4m3fn, device=dev)
+        s = torch.empty(1, dtype=torch.float32, device=dev)
+        for _ in range(launches):
+            w8.scaled_quant(x, q, s, per_token=True, dynamic=True)
     elif name == "quant_tokens":
         x = si.normal_with_outliers((4096, 14336), seed=3, device=dev)
         q = torch.empty(4096, 14336, dtype=torch.float8_e4m3fn, device=dev)

@@ -178,3 +178,52 @@ def test_quant_dequant_round_trip_kv_shape():
 
 def test_no_device_timeouts_recorded():
     assert w8.device_status() == 0
+
+
+@pytest.mark.parametrize("qd", QDS)
+def test_all_bf16_patterns_under_many_scales(qd):
+    """The quantiser takes the code from a reciprocal multiply where that
+    provably equals the code of the IEEE quotient: every bf16 pattern under
+    64 random static scales, bit-exact against the oracle."""
+    rng = np.random.default_rng(17)
+    scales = np.exp(rng.uniform(np.log(1e-4), np.log(30.0), 64)).astype(np.float32)
+    x = all_patterns(torch.bfloat16).reshape(1, -1).repeat(64, 1)   # [64, 65536]
+    g, _ = gpu_quant(x.cuda(), qd, per_token=True, dynamic=False, scale=scales)
+    o, _ = oracle_quant(x, qd, per_token=True, scale=scales)
+    assert np.array_equal(g, o)
+
+
+def _near_decision_points(qd, dtype, seed):
+    """Inputs whose quotient by a random scale lands within a few 16-bit ulps
+    of every decision point of the encoder (e4m3 midpoints, int8 halves)."""
+    rng = np.random.default_rng(seed)
+    if qd == oracle.E4M3:
+        vals = np.array([oracle.e4m3_value(c) for c in range(0x7F)])
+        mids = (vals[:-1] + vals[1:]) / 2
+    else:
+        mids = np.arange(-128, 128) + 0.5
+    rows, scales = [], []
+    for _ in range(32):
+        s = np.float32(np.exp(rng.uniform(np.log(1e-3), np.log(10.0))))
+        t = torch.tensor(np.concatenate([mids, -mids]) * float(s), dtype=torch.float32).to(dtype)
+        bits = t.view(torch.int16).to(torch.int32)
+        nb = torch.cat([bits + d for d in (-3, -2, -1, 0, 1, 2, 3)])
+        rows.append(nb.to(torch.int16).view(dtype))
+        scales.append(s)
+    n = min(r.numel() for r in rows)
+    return torch.stack([r[:n] for r in rows]), np.array(scales, np.float32)
+
+
+@pytest.mark.parametrize("qd", QDS)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_inputs_at_decision_points(qd, dtype):
+    x, scales = _near_decision_points(qd, dtype, seed=5)
+    g, _ = gpu_quant(x.cuda(), qd, per_token=True, dynamic=False, scale=scales)
+    o, _ = oracle_quant(x, qd, per_token=True, scale=scales)
+    assert np.array_equal(g, o)
+    # the same rows through the flat per-tensor kernel, one scale at a time
+    for i in range(0, 32, 8):
+        xi = x[i:i + 1].repeat(64, 1)
+        g1, _ = gpu_quant(xi.cuda(), qd, per_token=False, dynamic=False, scale=[scales[i]])
+        o1, _ = oracle_quant(xi, qd, per_token=False, scale=np.array([scales[i]], np.float32))
+        assert np.array_equal(g1, o1)
