@@ -384,34 +384,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool last = (c == nch - 1);
         const uint32_t acc_addr = lane_base + static_cast<uint32_t>(b * BN);
         const uint32_t tot_addr = lane_base + static_cast<uint32_t>(2 * BN);
+        if (INT8) {
+          // drain in batches of up to four 16-column groups: all TMEM loads
+          // of a batch are in flight together (one wait per batch), so the
+          // drain of a 1024-K chunk stays shorter than the next chunk's MMAs
+          constexpr int kBatch = kGroups < 4 ? kGroups : 4;
 #pragma unroll 1
-        for (int g = 0; g < kGroups; ++g) {
-          uint32_t r[16];
-          tmem_ld16(acc_addr + g * 16, r);
-          if (INT8) {
-            uint32_t t[16];
-            if (c > 0) {
-              tmem_ld16(tot_addr + g * 16, t);
-              tmem_ld_wait();
+          for (int g0 = 0; g0 < kGroups; g0 += kBatch) {
+            uint32_t r[kBatch][16], t[kBatch][16];
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                t[j] = static_cast<uint32_t>(static_cast<int>(t[j]) + __float2int_rn(__uint_as_float(r[j])));
-            } else {
-              tmem_ld_wait();
-#pragma unroll
-              for (int j = 0; j < 16; ++j) t[j] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[j])));
+            for (int bb = 0; bb < kBatch; ++bb) {
+              tmem_ld16(acc_addr + (g0 + bb) * 16, r[bb]);
+              if (c > 0) tmem_ld16(tot_addr + (g0 + bb) * 16, t[bb]);
             }
-            if (!last) {
-              tmem_st16(tot_addr + g * 16, t);
-            } else if (prm.splits > 1) {
-              write_partial16(part + static_cast<size_t>(row) * qv4, g * 16, qvalid, t);
-            } else {
-              int v[16];
+            tmem_ld_wait();
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] = static_cast<int>(t[j]);
-              store16<SWAP, OutT>(prm, lane_idx, un.q0 + g * 16, v, s_lane);
+            for (int bb = 0; bb < kBatch; ++bb) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int prev = (c > 0) ? static_cast<int>(t[bb][j]) : 0;
+                t[bb][j] = static_cast<uint32_t>(prev + __float2int_rn(__uint_as_float(r[bb][j])));
+              }
+              const int g = g0 + bb;
+              if (!last) {
+                tmem_st16(tot_addr + g * 16, t[bb]);
+              } else if (prm.splits > 1) {
+                write_partial16(part + static_cast<size_t>(row) * qv4, g * 16, qvalid, t[bb]);
+              } else {
+                int v[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = static_cast<int>(t[bb][j]);
+                store16<SWAP, OutT>(prm, lane_idx, un.q0 + g * 16, v, s_lane);
+              }
             }
-          } else {
+          }
+        } else {
+#pragma unroll 1
+          for (int g = 0; g < kGroups; ++g) {
+            uint32_t r[16];
+            tmem_ld16(acc_addr + g * 16, r);
             tmem_ld_wait();
             if (prm.splits > 1) {
               write_partial16(part + static_cast<size_t>(row) * qv4, g * 16, qvalid, r);

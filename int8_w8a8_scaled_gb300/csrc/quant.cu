@@ -7,8 +7,9 @@
 // (token); q = sat_round(x / scale); dequant = decode(q) * scale.
 //
 // Exactness rules (the codes must match a correctly rounded reference bit
-// for bit): x / scale is an IEEE fp32 division (__fdiv_rn, never a reciprocal
-// multiply); e4m3 uses the hardware round-to-nearest-even satfinite
+// for bit): x / scale is the correctly rounded fp32 quotient -- computed with
+// a reciprocal and an exact-remainder correction step (div_by), or __fdiv_rn
+// where its preconditions fail; never a bare reciprocal multiply; e4m3 uses the hardware round-to-nearest-even satfinite
 // conversion with NaN canonicalised to 0x7F; int8 rounds half to even and
 // saturates; absmax uses fmaxf from 0 so NaN never wins.
 //
@@ -114,6 +115,36 @@ __device__ __forceinline__ uint8_t enc1(float a) {
   return static_cast<uint8_t>(int8x1(a));
 }
 
+// Correctly rounded x / s without a per-element division.
+//
+// With y = RN(1/s) (one IEEE division per thread), q0 = RN(x*y) lies within
+// one ulp of x/s, so the remainder x - s*q0 is exact in one FMA and
+// RN(q0 + remainder*y) is the correctly rounded quotient RN(x/s)
+// (Markstein's correction step for IEEE division with a correctly rounded
+// reciprocal).  Preconditions: s and y are normal finite floats (checked per
+// thread; otherwise the plain IEEE division is used) and no intermediate
+// overflows -- when x*y overflows, q0 = +-inf already gives the code of the
+// exact quotient (saturation), and the NaN the correction step would make is
+// replaced by q0.  A zero remainder means q0 is exact; it is returned as is
+// (q0 + 0 would turn -0 into +0).  Quotients in the fp32 subnormal range all
+// encode to a signed zero, whatever their last bits.
+__device__ __forceinline__ bool recip_ok(float s, float* y) {
+  const float r = __fdiv_rn(1.0f, s);
+  *y = r;
+  const uint32_t es = (__float_as_uint(s) >> 23) & 0xFFu, er = (__float_as_uint(r) >> 23) & 0xFFu;
+  return es != 0u && es != 0xFFu && er != 0u && er != 0xFFu;
+}
+
+__device__ __forceinline__ float div_by(float x, float s, float y, bool ok) {
+  if (!ok) return __fdiv_rn(x, s);
+  const float q0 = __fmul_rn(x, y);
+  const float rem = __fmaf_rn(-q0, s, x);
+  const float q1 = __fmaf_rn(rem, y, q0);
+  // rem == 0: q0 is the exact quotient (and keeps the sign of a zero, which
+  // q0 + 0 would lose for x = -0)
+  return (rem == 0.0f || q1 != q1) ? q0 : q1;
+}
+
 template <int QK>
 __device__ __forceinline__ float scale_from_amax(float amax) {
   return amax > 0.f ? __fdiv_rn(amax, QK == 0 ? 448.f : 127.f) : 1.f;
@@ -187,6 +218,8 @@ __global__ void __launch_bounds__(kRowThreads)
     } else {
       s = scale[per_row ? row : 0];
     }
+    float y;
+    const bool ok = recip_ok(s, &y);
 
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
@@ -195,8 +228,8 @@ __global__ void __launch_bounds__(kRowThreads)
         float f[8];
         unpack8<XK>(cache[i], f);
         uint2 o;
-        o.x = enc4<QK>(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
-        o.y = enc4<QK>(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
+        o.x = enc4<QK>(div_by(f[0], s, y, ok), div_by(f[1], s, y, ok), div_by(f[2], s, y, ok), div_by(f[3], s, y, ok));
+        o.y = enc4<QK>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
         reinterpret_cast<uint2*>(qr)[v] = o;
       }
     }
@@ -205,12 +238,12 @@ __global__ void __launch_bounds__(kRowThreads)
       float f[8];
       unpack8<XK>(__ldg(reinterpret_cast<const uint4*>(xr) + v), f);
       uint2 o;
-      o.x = enc4<QK>(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
-      o.y = enc4<QK>(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
+      o.x = enc4<QK>(div_by(f[0], s, y, ok), div_by(f[1], s, y, ok), div_by(f[2], s, y, ok), div_by(f[3], s, y, ok));
+      o.y = enc4<QK>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
       reinterpret_cast<uint2*>(qr)[v] = o;
     }
     for (long long j = nvec * 8 + threadIdx.x; j < cols; j += kRowThreads)
-      qr[j] = enc1<QK>(__fdiv_rn(cvt_in<XK>(xr[j]), s));
+      qr[j] = enc1<QK>(div_by(cvt_in<XK>(xr[j]), s, y, ok));
   } else {
     // scalar path for unaligned layouts
     float s;
@@ -224,8 +257,10 @@ __global__ void __launch_bounds__(kRowThreads)
     } else {
       s = scale[per_row ? row : 0];
     }
+    float y;
+    const bool ok = recip_ok(s, &y);
     for (long long j = threadIdx.x; j < cols; j += kRowThreads)
-      qr[j] = enc1<QK>(__fdiv_rn(cvt_in<XK>(xr[j]), s));
+      qr[j] = enc1<QK>(div_by(cvt_in<XK>(xr[j]), s, y, ok));
   }
 }
 
@@ -303,6 +338,8 @@ __global__ void __launch_bounds__(256)
   } else {
     s = __ldg(scale);
   }
+  float y;
+  const bool ok = recip_ok(s, &y);
   const long long n16 = n / 16;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
@@ -318,10 +355,10 @@ __global__ void __launch_bounds__(256)
       unpack8<XK>(w[2 * u], *reinterpret_cast<float(*)[8]>(f));
       unpack8<XK>(w[2 * u + 1], *reinterpret_cast<float(*)[8]>(f + 8));
       uint4 o;
-      o.x = enc4<QK>(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
-      o.y = enc4<QK>(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
-      o.z = enc4<QK>(__fdiv_rn(f[8], s), __fdiv_rn(f[9], s), __fdiv_rn(f[10], s), __fdiv_rn(f[11], s));
-      o.w = enc4<QK>(__fdiv_rn(f[12], s), __fdiv_rn(f[13], s), __fdiv_rn(f[14], s), __fdiv_rn(f[15], s));
+      o.x = enc4<QK>(div_by(f[0], s, y, ok), div_by(f[1], s, y, ok), div_by(f[2], s, y, ok), div_by(f[3], s, y, ok));
+      o.y = enc4<QK>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
+      o.z = enc4<QK>(div_by(f[8], s, y, ok), div_by(f[9], s, y, ok), div_by(f[10], s, y, ok), div_by(f[11], s, y, ok));
+      o.w = enc4<QK>(div_by(f[12], s, y, ok), div_by(f[13], s, y, ok), div_by(f[14], s, y, ok), div_by(f[15], s, y, ok));
       __stcs(reinterpret_cast<uint4*>(q) + (u == 0 ? v : v + stride), o);
     }
   }
@@ -330,15 +367,15 @@ __global__ void __launch_bounds__(256)
     unpack8<XK>(__ldcs(reinterpret_cast<const uint4*>(x) + 2 * v), *reinterpret_cast<float(*)[8]>(f));
     unpack8<XK>(__ldcs(reinterpret_cast<const uint4*>(x) + 2 * v + 1), *reinterpret_cast<float(*)[8]>(f + 8));
     uint4 o;
-    o.x = enc4<QK>(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
-    o.y = enc4<QK>(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
-    o.z = enc4<QK>(__fdiv_rn(f[8], s), __fdiv_rn(f[9], s), __fdiv_rn(f[10], s), __fdiv_rn(f[11], s));
-    o.w = enc4<QK>(__fdiv_rn(f[12], s), __fdiv_rn(f[13], s), __fdiv_rn(f[14], s), __fdiv_rn(f[15], s));
+    o.x = enc4<QK>(div_by(f[0], s, y, ok), div_by(f[1], s, y, ok), div_by(f[2], s, y, ok), div_by(f[3], s, y, ok));
+    o.y = enc4<QK>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
+    o.z = enc4<QK>(div_by(f[8], s, y, ok), div_by(f[9], s, y, ok), div_by(f[10], s, y, ok), div_by(f[11], s, y, ok));
+    o.w = enc4<QK>(div_by(f[12], s, y, ok), div_by(f[13], s, y, ok), div_by(f[14], s, y, ok), div_by(f[15], s, y, ok));
     __stcs(reinterpret_cast<uint4*>(q) + v, o);
   }
   for (long long j = n16 * 16 + blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; j < n;
        j += stride)
-    q[j] = enc1<QK>(__fdiv_rn(cvt_in<XK>(x[j]), s));
+    q[j] = enc1<QK>(div_by(cvt_in<XK>(x[j]), s, y, ok));
 }
 
 // Per-row quantiser driven by a per-tensor scale from the absmax word (the
@@ -351,9 +388,11 @@ __global__ void __launch_bounds__(kRowThreads)
   allow_dependents();
   const float s = scale_from_amax<QK>(__uint_as_float(*word));
   if (blockIdx.x == 0 && threadIdx.x == 0) scale[0] = s;
+  float y;
+  const bool ok = recip_ok(s, &y);
   const uint16_t* xr = x + static_cast<long long>(blockIdx.x) * ld_x;
   uint8_t* qr = q + static_cast<long long>(blockIdx.x) * ld_q;
-  for (long long j = threadIdx.x; j < cols; j += kRowThreads) qr[j] = enc1<QK>(__fdiv_rn(cvt_in<XK>(xr[j]), s));
+  for (long long j = threadIdx.x; j < cols; j += kRowThreads) qr[j] = enc1<QK>(div_by(cvt_in<XK>(xr[j]), s, y, ok));
 }
 
 // ---------------------------------------------------------------- dequantiser
