@@ -533,7 +533,7 @@ def sweep_large(out_path: str, reps: int = 5):
         sa = torch.rand(M, device=dev) * 0.01
         sb = torch.rand(N, device=dev) * 0.01
         out = torch.empty(M, N, dtype=torch.bfloat16 if qd == w8.E4M3 else torch.float16, device=dev)
-        bns = (128, 160, 192, 224, 256) if qd == w8.E4M3 else (64, 128)
+        bns = (128, 160, 192, 224, 256) if qd == w8.E4M3 else (64, 128, 256)
         cfgs = [None] + [{"swap_ab": 0, "block_n": bn, "split_k": sp, "stages": st}
                          for bn in bns for sp in (1, 2) for st in (0, 3)]
         flops = 2.0 * M * N * K

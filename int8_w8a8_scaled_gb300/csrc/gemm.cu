@@ -21,9 +21,9 @@
 // accumulator.  int8 operands (tcgen05 kind::i8 is not available on sm_103a)
 // arrive as f16 planes (int8 -> f16 is exact) and use kind::f16.  Products
 // are at most 2^14, so an fp32 accumulator holds the exact integer sum for up
-// to 1024 K; the MMA issuer therefore alternates two TMEM accumulators per
-// K chunk of <= 1024 and the epilogue warps drain each finished chunk into an
-// exact int32 total kept in a third TMEM region.
+// to 1024 K; the MMA issuer accumulates one K chunk of <= 1024 at a time and
+// the epilogue warps drain each finished chunk into an exact int32 total kept
+// in a second TMEM region (2 * block_n columns, so two CTAs share an SM).
 //
 // Split-K (used when there are too few output tiles to fill the GPU, i.e.
 // small-M decode): every slice writes its partial tile to the workspace; the
@@ -46,10 +46,15 @@ constexpr int kTileP = 128;       // rows of the P operand per tile (MMA M)
 constexpr int kRowBytes = 128;    // bytes of K per stage row (one swizzle row)
 constexpr int kPBytes = kTileP * kRowBytes;
 
+// e4m3: accumulation units alternate between two fp32 accumulators (columns
+// 0 and bn) so the epilogue of one unit overlaps the next unit's MMAs.
+// int8: one fp32 chunk accumulator (column 0) and the int32 total (column
+// bn) -- 2 * bn columns, so two CTAs share an SM and one CTA's MMAs fill the
+// tensor pipe while the other drains a chunk.
+__host__ __device__ constexpr int acc_bufs(bool int8) { return int8 ? 1 : 2; }
+
 __host__ __device__ constexpr int tmem_cols_for(int bn, bool int8) {
-  // Accumulation units alternate between two fp32 accumulators of bn
-  // columns at columns 0 and bn; int8 adds an int32 total at 2 * bn.
-  int need = int8 ? 3 * bn : 2 * bn;
+  int need = int8 ? 2 * bn : 2 * bn;
   int c = 32;
   while (c < need) c *= 2;
   return c;
@@ -237,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kIdesc = make_idesc(kTileP, BN, 0);
   constexpr int kTmemCols = tmem_cols_for(BN, INT8);
   constexpr int kGroups = BN / 16;
-  static_assert((INT8 ? 3 : 2) * BN <= kTmemCols && kTmemCols <= 512, "accumulators must fit the TMEM allocation");
+  static_assert((INT8 ? acc_bufs(INT8) + 1 : acc_bufs(INT8)) * BN <= kTmemCols && kTmemCols <= 512,
+                "accumulators must fit the TMEM allocation");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -321,9 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int chunk = INT8 ? prm.kchunk_kb : un.nkb;
         const int nch = (un.nkb + chunk - 1) / chunk;
         for (int c = 0; c < nch && ok; ++c, ++u) {
-          const int b = u & 1;
-          if (u >= 2) {
-            if (!mbar_wait(uempty_bar(b), ((u - 2) >> 1) & 1)) { ok = false; break; }
+          constexpr int kBufs = acc_bufs(INT8);
+          const int b = static_cast<int>(u % kBufs);
+          if (u >= static_cast<uint32_t>(kBufs)) {
+            if (!mbar_wait(uempty_bar(b), ((u - kBufs) / kBufs) & 1)) { ok = false; break; }
             tc_fence_after();
           }
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
@@ -378,12 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                (static_cast<size_t>(un.tile_lin) * prm.splits + un.split) * tile_elems;
 
       for (int c = 0; c < nch; ++c, ++u) {
-        const int b = u & 1;
-        if (!mbar_wait(ufull_bar(b), (u >> 1) & 1)) { ok = false; break; }
+        constexpr int kBufs = acc_bufs(INT8);
+        const int b = static_cast<int>(u % kBufs);
+        if (!mbar_wait(ufull_bar(b), (u / kBufs) & 1)) { ok = false; break; }
         tc_fence_after();
         const bool last = (c == nch - 1);
         const uint32_t acc_addr = lane_base + static_cast<uint32_t>(b * BN);
-        const uint32_t tot_addr = lane_base + static_cast<uint32_t>(2 * BN);
+        const uint32_t tot_addr = lane_base + static_cast<uint32_t>(kBufs * BN);
         if (INT8) {
           // drain in batches of up to four 16-column groups: all TMEM loads
           // of a batch are in flight together (one wait per batch), so the
@@ -574,8 +582,8 @@ cudaError_t dispatch(const CUtensorMap& tp, const CUtensorMap& tq, const MmParam
     case 64: return launch_swap<64, INT8>(tp, tq, p, swap, out_kind, stages, stream);
     case 128: return launch_swap<128, INT8>(tp, tq, p, swap, out_kind, stages, stream);
     case 256:
-      // int8 keeps 3 x block_n TMEM columns; 3 x 256 does not fit in 512
-      if (INT8) return cudaErrorInvalidValue;
+      // int8 at 256 columns: tokens on the 128-row side only
+      if (INT8) return swap ? cudaErrorInvalidValue : launch_out<256, false, true>(tp, tq, p, out_kind, stages, stream);
       return launch_swap<256, false>(tp, tq, p, swap, out_kind, stages, stream);
     // wave-balancing widths for the large-M e4m3 regime (tokens on the
     // 128-row side only)

@@ -174,6 +174,8 @@ INT8_CONFIGS = [
     {"swap_ab": 1, "block_n": 16, "split_k": 3},
     {"swap_ab": 1, "block_n": 32, "split_k": 1},
     {"swap_ab": 1, "block_n": 128, "split_k": 2},
+    {"swap_ab": 0, "block_n": 256, "split_k": 1},
+    {"swap_ab": 0, "block_n": 256, "split_k": 2},
 ]
 
 INT8_SHAPES = [(1, 128, 64), (5, 100, 1040), (130, 260, 2112), (300, 128, 3072)]
@@ -193,6 +195,7 @@ def test_int8_variants_bit_exact(cfg, shape):
 
 
 @pytest.mark.parametrize("cfg", [None, {"swap_ab": 0, "block_n": 128, "split_k": 1},
+                                 {"swap_ab": 0, "block_n": 256, "split_k": 1},
                                  {"swap_ab": 1, "block_n": 16, "split_k": 4}])
 def test_int8_worst_case_magnitudes_exact(cfg):
     """+-127 / -128 everywhere at a long K: every 1024-long chunk reaches
