@@ -197,7 +197,7 @@ W8A8_API w8a8_status w8a8_scaled_mm(const void* a_q, int64_t lda, const void* b_
  *            the narrow side (small-M / decode regime); 0: tokens M on the
  *            128-row side (large-M regime).
  *  block_n   width of the narrow MMA side: 16..256, multiple of 16.
- *  split_k   number of K slices reduced in a fixed order (>= 1).
+ *  split_k   number of K slices reduced in a fixed order (1..16).
  *  stages    depth of the shared-memory ring (2..8); 0 = automatic.
  *  ctas_per_sm  cap on the persistent CTAs per SM (1..4); 0 = as many as
  *            the kernel's shared memory, registers and TMEM allow.
@@ -295,6 +295,16 @@ W8A8_API w8a8_status w8a8_scaled_mm_noalloc(const void* a_q, int64_t lda, const 
                                             int64_t ldc, int64_t M, int64_t N, int64_t K,
                                             int q_dtype, int out_dtype,
                                             w8a8_stream_t stream);
+
+/* Debug: per-CTA phase trace of subsequent scaled_mm launches (process
+ * wide).  buf is a device buffer of `bytes` bytes; each persistent CTA c <
+ * bytes / 64 writes eight 64-bit words at buf[8c..8c+7]: %globaltimer (ns)
+ * at kernel entry, after its prologue (barriers, TMEM), when the preceding
+ * kernel's dependency was released, when its first operand stage landed,
+ * when its last MMA was issued, when its epilogue finished, at exit, and its
+ * SM id.  Each launch overwrites the buffer.  NULL turns tracing off (the
+ * default).  Not for production use: concurrent launches share the buffer. */
+W8A8_API w8a8_status w8a8_debug_mm_trace(void* buf, size_t bytes);
 
 /* Reads and clears the library's device-side status word on the current
  * device (W8A8_DEVICE_* bits; a kernel sets W8A8_DEVICE_TIMEOUT when one of

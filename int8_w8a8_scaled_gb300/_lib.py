@@ -43,6 +43,7 @@ EXPORTS = (
     "w8a8_requant_shards",
     "w8a8_scaled_mm_noalloc_max_scratch",
     "w8a8_scaled_mm_noalloc",
+    "w8a8_debug_mm_trace",
 )
 
 
@@ -108,6 +109,8 @@ def load(build_if_needed: bool = True):
         lib.w8a8_scaled_mm_noalloc_max_scratch.argtypes = []
         lib.w8a8_scaled_mm_noalloc.restype = I
         lib.w8a8_scaled_mm_noalloc.argtypes = [P, I64, P, I64, P, I, P, I, P, I64, I64, I64, I64, I, I, P]
+        lib.w8a8_debug_mm_trace.restype = I
+        lib.w8a8_debug_mm_trace.argtypes = [P, SZ]
         lib.w8a8_device_status.restype = I
         lib.w8a8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
         _lib = lib

@@ -12,6 +12,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -23,6 +24,10 @@ using namespace w8a8;
 namespace {
 
 thread_local std::string t_last_error;
+
+// debug trace target (process-wide; set and read on the host only)
+std::atomic<unsigned long long*> g_trace_buf{nullptr};
+std::atomic<int> g_trace_ctas{0};
 
 w8a8_status fail(w8a8_status st, const char* fmt, ...) {
   char buf[512];
@@ -257,7 +262,7 @@ w8a8_status validate_config(const w8a8_mm_config& c, int q_dtype, int smem_optin
     return fail(W8A8_ERR_UNSUPPORTED,
                 "block_n %d not supported (16, 32, 64, 128, 256; 160/192/224 for e4m3 without swap; 256 for int8 without swap)",
                 c.block_n);
-  if (c.split_k < 1 || c.split_k > 64) return fail(W8A8_ERR_UNSUPPORTED, "split_k must be in [1, 64]");
+  if (c.split_k < 1 || c.split_k > 16) return fail(W8A8_ERR_UNSUPPORTED, "split_k must be in [1, 16]");
   if (c.stages != 0 && (c.stages < 2 || c.stages > 8))
     return fail(W8A8_ERR_UNSUPPORTED, "stages must be 0 (auto) or in [2, 8]");
   if (c.ctas_per_sm < 0 || c.ctas_per_sm > 4)
@@ -382,6 +387,8 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
   // weight rows)
   prm.prefetch_kb = 16;
   prm.max_ctas_per_sm = cfg.ctas_per_sm;
+  prm.trace = g_trace_buf.load();
+  prm.trace_ctas = g_trace_ctas.load();
   const int out_kind = out_dtype == W8A8_BF16 ? OUT_BF16 : out_dtype == W8A8_FP16 ? OUT_FP16 : OUT_RAW;
   e = i8 ? launch_int8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream)
          : launch_fp8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream);
@@ -584,10 +591,22 @@ w8a8_status w8a8_requant_shards(const void* q, int q_dtype, int64_t cols, int64_
   return ok();
 }
 
+w8a8_status w8a8_debug_mm_trace(void* buf, size_t bytes) {
+  if (buf && !aligned(buf, 8)) return fail(W8A8_ERR_MISALIGNED, "trace buffer must be 8-byte aligned");
+  const size_t per_cta = 8 * sizeof(unsigned long long);
+  g_trace_ctas.store(buf ? static_cast<int>(std::min<size_t>(bytes / per_cta, 1u << 20)) : 0);
+  g_trace_buf.store(buf ? static_cast<unsigned long long*>(buf) : nullptr);
+  return ok();
+}
+
 w8a8_status w8a8_device_status(int* flags) {
   if (!flags) return fail(W8A8_ERR_INVALID_ARG, "flags is null");
   cudaError_t e = read_clear_device_status(flags);
   if (e != cudaSuccess) return cuda_fail(e, "device status read");
+  int qf = 0;
+  e = read_clear_quant_status(&qf);
+  if (e != cudaSuccess) return cuda_fail(e, "device status read");
+  *flags |= qf;
   return ok();
 }
 

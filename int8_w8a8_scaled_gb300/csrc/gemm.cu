@@ -6,16 +6,20 @@
 // scales, bf16 / fp16 output, dequantisation fused into the GEMM epilogue so
 // the output is written once.)
 //
-// One CTA of 128 threads computes one 128 x BN output tile (or one K slice of
-// it):
+// A persistent kernel: each CTA of 192 threads walks a list of work units
+// (one 128 x BN output tile, or one K slice of it):
 //   warp 0, one lane : TMA producer -- loads 128-byte-wide K blocks of both
 //                      operands into a ring of shared-memory stages
 //                      (128-byte swizzle), signalling a "full" mbarrier;
 //   warp 1           : allocates TMEM; one lane issues tcgen05.mma for each
 //                      K block and commits to the stage's "empty" mbarrier so
-//                      the producer can refill it;
-//   all four warps   : epilogue -- tcgen05.ld of the accumulator lanes (warp
-//                      w owns TMEM lanes 32w..32w+31), scale, round, store.
+//                      the producer can refill it, and to a per-accumulator
+//                      "full" mbarrier at the end of a unit;
+//   warps 2..5       : epilogue -- tcgen05.ld of the accumulator lanes (warp
+//                      w owns TMEM lanes 32(w%4)..32(w%4)+31), scale, round,
+//                      store; then release the accumulator to the MMA warp.
+// With small M the operands swap roles (weights on the 128-row MMA side, the
+// few tokens on the BN side) so the narrow dimension costs no padding.
 //
 // fp8 e4m3 operands go straight to tcgen05 kind::f8f6f4 with an fp32
 // accumulator.  int8 operands (tcgen05 kind::i8 is not available on sm_103a)
@@ -42,6 +46,7 @@ namespace {
 
 constexpr int kThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kEpiThreads = 128;
+constexpr int kMaxSplits = 16;   // split_k limit of the reduction (host enforces)
 constexpr int kTileP = 128;       // rows of the P operand per tile (MMA M)
 constexpr int kRowBytes = 128;    // bytes of K per stage row (one swizzle row)
 constexpr int kPBytes = kTileP * kRowBytes;
@@ -54,7 +59,7 @@ constexpr int kPBytes = kTileP * kRowBytes;
 __host__ __device__ constexpr int acc_bufs(bool int8) { return int8 ? 1 : 2; }
 
 __host__ __device__ constexpr int tmem_cols_for(int bn, bool int8) {
-  int need = int8 ? 2 * bn : 2 * bn;
+  const int need = acc_bufs(int8) * bn + (int8 ? bn : 0);
   int c = 32;
   while (c < need) c *= 2;
   return c;
@@ -193,6 +198,24 @@ __device__ __forceinline__ void store4(const MmParams& prm, int p, int q, int nv
   }
 }
 
+// store4 with the scales already in registers: s_p for P row p, s_q[j] for
+// Q column q + j.  The product order stays (acc * scale_a) * scale_b.
+template <bool SWAP, typename OutT, typename V>
+__device__ __forceinline__ void store4s(const MmParams& prm, int p, int q, int nvalid, const V (&v)[4], float s_p,
+                                        const float (&s_q)[4]) {
+  OutT* out = reinterpret_cast<OutT*>(prm.out);
+  if (p >= (SWAP ? prm.N : prm.M)) return;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (j < nvalid) {
+      if (!SWAP)
+        out[static_cast<long long>(p) * prm.ldc + q + j] = OutConv<OutT>::conv(v[j], s_p, s_q[j]);
+      else
+        out[static_cast<long long>(q + j) * prm.ldc + p] = OutConv<OutT>::conv(v[j], s_q[j], s_p);
+    }
+  }
+}
+
 // One work unit is a (K slice, output tile) pair; the persistent CTAs walk
 // the units round-robin.  Units are numbered slice-major so that the slices
 // of a tile are spread over different CTAs.
@@ -214,6 +237,16 @@ __device__ __forceinline__ Unit unit_of(int w, const MmParams& prm, int group, i
   return u;
 }
 
+// Optional per-CTA phase trace (debug): kTraceSlots 64-bit %globaltimer
+// stamps per CTA, written only when a trace buffer is set.
+constexpr int kTraceSlots = 8;
+enum TraceSlot { T_START = 0, T_PROLOGUE, T_DEP_RELEASED, T_FIRST_DATA, T_MMA_ISSUED, T_EPI_DONE, T_END, T_SMID };
+
+__device__ __forceinline__ void trace_stamp(const MmParams& prm, int slot) {
+  if (prm.trace && blockIdx.x < prm.trace_ctas)
+    prm.trace[static_cast<size_t>(blockIdx.x) * kTraceSlots + slot] = global_timer_ns();
+}
+
 __device__ __forceinline__ void epi_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
 }
@@ -231,8 +264,12 @@ __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.
 // Accumulation units (one per work unit for e4m3, one per <= 1024-K chunk
 // for int8) alternate between two TMEM accumulators, so the epilogue of one
 // unit overlaps the MMAs of the next.
+// Narrow tiles run two CTAs per SM (the dispatch sizes their shared memory
+// for that); cap their registers so that two fit (<= 168 per thread).
+__host__ __device__ constexpr int min_ctas_for(int bn, bool int8) { return (bn <= 64 || (int8 && bn <= 128)) ? 2 : 1; }
+
 template <int BN, bool SWAP, bool INT8, typename OutT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
     w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_p,
                      const __grid_constant__ CUtensorMap tmap_q, const MmParams prm, int stages,
                      int group) {
@@ -258,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int units = prm.tiles_p * prm.tiles_q * prm.splits;
+  if (threadIdx.x == 0) trace_stamp(prm, T_START);
 
   // Warm L2 with the weight tiles of this CTA's first work unit before
   // waiting on the preceding kernel: a prefetch only reads (coherent) global
@@ -297,8 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) trace_stamp(prm, T_PROLOGUE);
   griddep_wait();
   griddep_launch();
+  if (threadIdx.x == 0) trace_stamp(prm, T_DEP_RELEASED);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -339,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = it % stages;
             const uint32_t ph = (it / stages) & 1;
             if (!mbar_wait(full_bar(s), ph)) { ok = false; break; }
+            if (it == 0) trace_stamp(prm, T_FIRST_DATA);
             tc_fence_after();
             const uint64_t da = smem_desc_sw128(smem_addr(sp + s * kPBytes));
             const uint64_t db = smem_desc_sw128(smem_addr(sq + s * kQBytes));
@@ -393,10 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t acc_addr = lane_base + static_cast<uint32_t>(b * BN);
         const uint32_t tot_addr = lane_base + static_cast<uint32_t>(kBufs * BN);
         if (INT8) {
-          // drain in batches of up to four 16-column groups: all TMEM loads
+          // drain in batches of up to four (two when two CTAs share the SM)
+          // 16-column groups: all TMEM loads
           // of a batch are in flight together (one wait per batch), so the
           // drain of a 1024-K chunk stays shorter than the next chunk's MMAs
-          constexpr int kBatch = kGroups < 4 ? kGroups : 4;
+          constexpr int kBatchMax = min_ctas_for(BN, INT8) == 2 ? 2 : 4;  // register budget
+          constexpr int kBatch = kGroups < kBatchMax ? kGroups : kBatchMax;
 #pragma unroll 1
           for (int g0 = 0; g0 < kGroups; g0 += kBatch) {
             uint32_t r[kBatch][16], t[kBatch][16];
@@ -465,32 +508,70 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t* base = reinterpret_cast<const uint32_t*>(prm.partial) +
                                  static_cast<size_t>(un.tile_lin) * prm.splits * tile_elems;
           const int nvec = kTileP * qv4 / 4;
-#pragma unroll 2
-          for (int v = et; v < nvec; v += kEpiThreads) {
-            const int row_r = (v * 4) / qv4;
-            const int col = (v * 4) - row_r * qv4;
-            if (INT8) {
-              int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-              for (int sl = 0; sl < prm.splits; ++sl) {
-                const uint4 x = __ldcg(reinterpret_cast<const uint4*>(base + sl * tile_elems) + v);
-                a0 += static_cast<int>(x.x);
-                a1 += static_cast<int>(x.y);
-                a2 += static_cast<int>(x.z);
-                a3 += static_cast<int>(x.w);
-              }
-              const int vals[4] = {a0, a1, a2, a3};
-              store4<SWAP, OutT>(prm, un.p0 + row_r, un.q0 + col, qvalid - col, vals);
-            } else {
-              float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-              for (int sl = 0; sl < prm.splits; ++sl) {
-                const float4 x = __ldcg(reinterpret_cast<const float4*>(base + sl * tile_elems) + v);
-                a0 += x.x;
-                a1 += x.y;
-                a2 += x.z;
-                a3 += x.w;
-              }
-              const float vals[4] = {a0, a1, a2, a3};
-              store4<SWAP, OutT>(prm, un.p0 + row_r, un.q0 + col, qvalid - col, vals);
+          // slices requested per batch: fewer where two CTAs share an SM's
+          // registers
+          constexpr int kRedBatch = min_ctas_for(BN, INT8) == 2 ? 4 : 8;
+          // Each thread finishes two float4s of the tile per pass.  All
+          // loads of a pass -- the slices' partials (in batches of four
+          // or eight slices) and the scales the four outputs need -- are requested
+          // before any is used, so a pass costs about one L2 round trip; the
+          // sum runs in slice order 0..S-1.
+          for (int v0 = et; v0 < nvec; v0 += 2 * kEpiThreads) {
+            int vv[2] = {v0, v0 + kEpiThreads};
+            float sp[2], sq[2][4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int v = vv[h] < nvec ? vv[h] : v0;
+              const int row_r = (v * 4) / qv4;
+              const int col = v * 4 - row_r * qv4;
+              const int p = un.p0 + row_r;
+              const float* ps = SWAP ? prm.scale_b : prm.scale_a;
+              const int pp = SWAP ? prm.b_per_row : prm.a_per_row;
+              const int plim = SWAP ? prm.N : prm.M;
+              sp[h] = pp ? __ldg(ps + min(p, plim - 1)) : __ldg(ps);
+              const float* qs = SWAP ? prm.scale_a : prm.scale_b;
+              const int qp = SWAP ? prm.a_per_row : prm.b_per_row;
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                sq[h][j] = qp ? __ldg(qs + min(un.q0 + col + j, un.q0 + qvalid - 1)) : __ldg(qs);
+            }
+            float fa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            int ia[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+            for (int sl0 = 0; sl0 < prm.splits; sl0 += kRedBatch) {
+              uint4 x[2][kRedBatch];
+#pragma unroll
+              for (int k = 0; k < kRedBatch; ++k)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                  if (sl0 + k < prm.splits && vv[h] < nvec)
+                    x[h][k] = __ldcg(reinterpret_cast<const uint4*>(base + (sl0 + k) * tile_elems) + vv[h]);
+#pragma unroll
+              for (int k = 0; k < kRedBatch; ++k)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                  if (sl0 + k < prm.splits && vv[h] < nvec) {
+                    if (INT8) {
+                      ia[h][0] += static_cast<int>(x[h][k].x);
+                      ia[h][1] += static_cast<int>(x[h][k].y);
+                      ia[h][2] += static_cast<int>(x[h][k].z);
+                      ia[h][3] += static_cast<int>(x[h][k].w);
+                    } else {
+                      fa[h][0] += __uint_as_float(x[h][k].x);
+                      fa[h][1] += __uint_as_float(x[h][k].y);
+                      fa[h][2] += __uint_as_float(x[h][k].z);
+                      fa[h][3] += __uint_as_float(x[h][k].w);
+                    }
+                  }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (vv[h] >= nvec) continue;
+              const int row_r = (vv[h] * 4) / qv4;
+              const int col = vv[h] * 4 - row_r * qv4;
+              if (INT8)
+                store4s<SWAP, OutT>(prm, un.p0 + row_r, un.q0 + col, qvalid - col, ia[h], sp[h], sq[h]);
+              else
+                store4s<SWAP, OutT>(prm, un.p0 + row_r, un.q0 + col, qvalid - col, fa[h], sp[h], sq[h]);
             }
           }
           if (et == 0) prm.counters[un.tile_lin] = 0u;
@@ -499,11 +580,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (warp == 1 && lane == 0) trace_stamp(prm, T_MMA_ISSUED);
+  if (threadIdx.x == 2 * 32) trace_stamp(prm, T_EPI_DONE);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+  if (threadIdx.x == 0 && prm.trace && blockIdx.x < prm.trace_ctas) {
+    trace_stamp(prm, T_END);
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    prm.trace[static_cast<size_t>(blockIdx.x) * kTraceSlots + T_SMID] = smid;
   }
 }
 

@@ -33,7 +33,13 @@ struct MmParams {
   int pdl;               // launch with programmatic stream serialisation
   int prefetch_kb;       // weight K blocks of the first unit prefetched into L2 early
   int max_ctas_per_sm;   // 0: as many as fit; else cap the persistent grid per SM
+  unsigned long long* trace;  // debug: per-CTA phase stamps (null = off)
+  int trace_ctas;             // CTAs the trace buffer has room for
 };
+
+// Debug trace buffer for subsequent scaled_mm launches (null disables).
+void set_mm_trace(unsigned long long* buf, int ctas);
+void get_mm_trace(unsigned long long** buf, int* ctas);
 
 // OUT_RAW: fp32 y = (acc * s_a) * s_b for the fp8 path, raw int32
 // accumulators for the int8 path.
@@ -56,6 +62,8 @@ cudaError_t launch_int8_gemm(const CUtensorMap& tmap_p, const CUtensorMap& tmap_
 
 // Synchronises the device, then reads and clears the device status word.
 cudaError_t read_clear_device_status(int* flags);
+// Reads and clears the quantiser kernels' status word (call after a sync).
+cudaError_t read_clear_quant_status(int* flags);
 
 // Shared-memory bytes a GEMM launch needs (ring + barriers + alignment).
 int gemm_smem_bytes(int block_n, int stages);

@@ -30,12 +30,14 @@
 #include <cuda_fp8.h>
 
 #include "internal.h"
+#include "sm103_ptx.cuh"
 
 namespace w8a8 {
 
 namespace {
 
 constexpr int kRowThreads = 256;
+constexpr long long kBulkRowMaxCols = 65536;  // 128 KB of 16-bit row in shared memory
 
 // Programmatic dependent launch.  Every kernel here is launched with the
 // programmatic-serialisation attribute: it first waits for the preceding
@@ -45,6 +47,24 @@ constexpr int kRowThreads = 256;
 __device__ __forceinline__ void allow_dependents() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl_smem(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Params>(args)...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 template <typename... Params, typename... Args>
@@ -169,6 +189,61 @@ __device__ __forceinline__ float block_max(float v, float* red) {
 }
 
 // ---------------------------------------------------------------- per-row quantiser
+
+// Per-row quantiser for rows whose start and length are 16-byte multiples:
+// one thread pulls the whole row into shared memory with a single bulk async
+// copy (no chain of dependent loads, which matters when a decode step has one
+// row per kernel), then all threads reduce absmax and convert from shared
+// memory in short loops (small code: the kernel runs cold on few SMs).
+template <int XK, int QK>
+__global__ void __launch_bounds__(kRowThreads)
+    quant_row_bulk_kernel(const uint16_t* __restrict__ x, long long ld_x, long long cols,
+                          uint8_t* __restrict__ q, long long ld_q, float* __restrict__ scale, int per_row,
+                          int dynamic) {
+  extern __shared__ __align__(16) uint4 row_s[];
+  __shared__ uint64_t bar;
+  __shared__ float red[kRowThreads / 32];
+  allow_dependents();
+  const long long row = blockIdx.x;
+  const uint32_t bytes = static_cast<uint32_t>(cols * 2);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(smem_addr(&bar), bytes);
+    bulk_load(smem_addr(row_s), x + row * ld_x, bytes, smem_addr(&bar));
+  }
+  __syncthreads();
+  if (!mbar_wait(smem_addr(&bar), 0)) return;  // flagged in the device status
+  const int nvec = static_cast<int>(cols / 8);
+  float s;
+  if (dynamic) {
+    float amax = 0.f;
+#pragma unroll 4
+    for (int v = threadIdx.x; v < nvec; v += kRowThreads) {
+      float f[8];
+      unpack8<XK>(row_s[v], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    }
+    amax = block_max(amax, red);
+    s = scale_from_amax<QK>(amax);
+    if (threadIdx.x == 0) scale[row] = s;
+  } else {
+    s = scale[per_row ? row : 0];
+  }
+  float y;
+  const bool ok = recip_ok(s, &y);
+  uint2* qr = reinterpret_cast<uint2*>(q + row * ld_q);
+#pragma unroll 2
+  for (int v = threadIdx.x; v < nvec; v += kRowThreads) {
+    float f[8];
+    unpack8<XK>(row_s[v], f);
+    uint2 o;
+    o.x = enc4<QK>(div_by(f[0], s, y, ok), div_by(f[1], s, y, ok), div_by(f[2], s, y, ok), div_by(f[3], s, y, ok));
+    o.y = enc4<QK>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
+    qr[v] = o;
+  }
+}
 
 // VPT = 128-bit vectors cached per thread (0: vector path disabled, scalar).
 template <int XK, int QK, int VPT>
@@ -460,6 +535,15 @@ cudaError_t launch_rows(const QuantArgs& a, cudaStream_t st) {
   const long long nvec = a.cols / 8;
   const long long per_thread = (nvec + kRowThreads - 1) / kRowThreads;
   const dim3 grid(static_cast<unsigned>(a.rows)), block(kRowThreads);
+  if (a.vec && a.cols % 8 == 0 && a.ld_x % 8 == 0 && a.cols <= kBulkRowMaxCols) {
+    const size_t smem = static_cast<size_t>(a.cols) * 2;
+    auto kern = quant_row_bulk_kernel<XK, QK>;
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+    }
+    return launch_pdl_smem(kern, grid, block, smem, st, x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.per_row, a.dynamic);
+  }
 #define W8A8_ROWS(V) \
   launch_pdl(quant_rows_kernel<XK, QK, V>, grid, block, st, x, a.ld_x, a.cols, q, a.ld_q, a.scale, a.per_row, a.dynamic)
   if (!a.vec) return W8A8_ROWS(0);
@@ -525,6 +609,16 @@ cudaError_t launch_dequant_t(const DequantArgs& a, int num_sms, cudaStream_t st)
 }
 
 }  // namespace
+
+cudaError_t read_clear_quant_status(int* flags) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int));
+  if (e != cudaSuccess) return e;
+  const int zero = 0;
+  e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+  *flags = v;
+  return e;
+}
 
 cudaError_t launch_quant(const QuantArgs& a, int num_sms, cudaStream_t st) {
   if (a.x_kind == 0)
