@@ -201,13 +201,29 @@ W8A8_API w8a8_status w8a8_scaled_mm(const void* a_q, int64_t lda, const void* b_
  *  stages    depth of the shared-memory ring (2..8); 0 = automatic.
  *  ctas_per_sm  cap on the persistent CTAs per SM (1..4); 0 = as many as
  *            the kernel's shared memory, registers and TMEM allow.
+ *  reduce    how split_k > 1 slices are summed (both in slice order 0..S-1,
+ *            so the result does not depend on scheduling):
+ *            W8A8_REDUCE_GLOBAL  partial tiles in the workspace, the last
+ *                                slice to arrive sums them;
+ *            W8A8_REDUCE_CLUSTER the slices of a tile run as one
+ *                                thread-block cluster and sum each other's
+ *                                partial tiles from shared memory (split_k
+ *                                <= 8; no workspace);
+ *            W8A8_REDUCE_AUTO    the cluster reduction when split_k <= 8
+ *                                and the stage ring holds a fp32 tile,
+ *                                else the global one.
  * Fields set to 0 (except swap_ab) mean "choose automatically". */
+#define W8A8_REDUCE_AUTO 0
+#define W8A8_REDUCE_GLOBAL 1
+#define W8A8_REDUCE_CLUSTER 2
+
 typedef struct {
   int swap_ab;
   int block_n;
   int split_k;
   int stages;
   int ctas_per_sm;
+  int reduce;
 } w8a8_mm_config;
 
 /* The configuration w8a8_scaled_mm() picks for this problem (host only). */

@@ -15,6 +15,7 @@ from . import _build
 E4M3, INT8, BF16, FP16, FP32, INT32 = 0, 1, 2, 3, 4, 5
 PER_TENSOR, PER_ROW = 0, 1
 DYNAMIC, STATIC = 0, 1
+REDUCE_AUTO, REDUCE_GLOBAL, REDUCE_CLUSTER = 0, 1, 2
 
 STATUS_NAMES = {
     0: "W8A8_OK",
@@ -49,7 +50,8 @@ EXPORTS = (
 
 class MmConfig(ctypes.Structure):
     _fields_ = [("swap_ab", ctypes.c_int), ("block_n", ctypes.c_int),
-                ("split_k", ctypes.c_int), ("stages", ctypes.c_int), ("ctas_per_sm", ctypes.c_int)]
+                ("split_k", ctypes.c_int), ("stages", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
+                ("reduce", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -201,8 +201,14 @@ void auto_config(long long M, long long N, long long K, int q_dtype, int sms, w8
   const long long tiles = c->swap_ab ? ceil_div(N, 128) * ceil_div(M, c->block_n)
                                      : ceil_div(M, 128) * ceil_div(N, c->block_n);
   c->split_k = one_wave_split(tiles, kb, static_cast<long long>(sms) * resident_per_sm(c->block_n, q_dtype));
+  // the slices of a tile reduce through distributed shared memory when they
+  // fit one portable cluster (<= 8): a few more idle slots are cheaper than
+  // the global-memory round trip, fence and arrival counter of the
+  // workspace reduction
+  if (c->split_k > 8) c->split_k = 8;
   c->stages = 0;
   c->ctas_per_sm = 0;
+  c->reduce = W8A8_REDUCE_AUTO;
 }
 
 int auto_stages(int block_n, int q_dtype, int smem_optin) {
@@ -213,6 +219,7 @@ int auto_stages(int block_n, int q_dtype, int smem_optin) {
 struct Plan {
   w8a8_mm_config cfg;
   int kb, kb_per_split, splits, tiles_p, tiles_q, stages;
+  bool cluster;  // split slices reduce through distributed shared memory
   size_t off_counters, off_partial, off_a16, off_b16, total;
 };
 
@@ -238,11 +245,14 @@ Plan make_plan(long long M, long long N, long long K, int q_dtype, const w8a8_mm
   p.kb_per_split = static_cast<int>(ceil_div(p.kb, sp));
   p.splits = static_cast<int>(ceil_div(p.kb, p.kb_per_split));  // every slice non-empty
   p.stages = cfg.stages > 0 ? cfg.stages : auto_stages(cfg.block_n, q_dtype, smem_optin);
+  p.cluster = p.splits > 1 && cfg.reduce != W8A8_REDUCE_GLOBAL && p.splits <= kMaxClusterSplit &&
+              cluster_reduce_fits(cfg.block_n, p.stages);
   const size_t tiles = static_cast<size_t>(p.tiles_p) * p.tiles_q;
-  const bool need_ws = p.splits > 1 || q_dtype == W8A8_INT8;
+  const bool global_split = p.splits > 1 && !p.cluster;
+  const bool need_ws = global_split || q_dtype == W8A8_INT8;
   size_t off = need_ws ? kCounterRegion : 0;
   p.off_counters = 0;
-  if (p.splits > 1) {
+  if (global_split) {
     p.off_partial = off;
     off = align256(off + tiles * p.splits * 128 * cfg.block_n * sizeof(float));
   }
@@ -267,10 +277,17 @@ w8a8_status validate_config(const w8a8_mm_config& c, int q_dtype, int smem_optin
     return fail(W8A8_ERR_UNSUPPORTED, "stages must be 0 (auto) or in [2, 8]");
   if (c.ctas_per_sm < 0 || c.ctas_per_sm > 4)
     return fail(W8A8_ERR_UNSUPPORTED, "ctas_per_sm must be 0 (auto) or in [1, 4]");
+  if (c.reduce < W8A8_REDUCE_AUTO || c.reduce > W8A8_REDUCE_CLUSTER)
+    return fail(W8A8_ERR_UNSUPPORTED, "reduce must be W8A8_REDUCE_AUTO, _GLOBAL or _CLUSTER");
   const int st = c.stages > 0 ? c.stages : auto_stages(c.block_n, q_dtype, smem_optin);
   if (gemm_smem_bytes(c.block_n, st) > smem_optin)
     return fail(W8A8_ERR_UNSUPPORTED, "stages=%d with block_n=%d needs %d bytes of shared memory (> %d)", st,
                 c.block_n, gemm_smem_bytes(c.block_n, st), smem_optin);
+  if (c.reduce == W8A8_REDUCE_CLUSTER && c.split_k > kMaxClusterSplit)
+    return fail(W8A8_ERR_UNSUPPORTED, "the cluster reduction takes split_k <= %d", kMaxClusterSplit);
+  if (c.reduce == W8A8_REDUCE_CLUSTER && !cluster_reduce_fits(c.block_n, st))
+    return fail(W8A8_ERR_UNSUPPORTED, "the cluster reduction needs the %d-stage ring to hold a 128 x %d fp32 tile",
+                st, c.block_n);
   return W8A8_OK;
 }
 
@@ -323,7 +340,7 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
   }
   if ((st = validate_config(cfg, q_dtype, dev.smem_optin)) != W8A8_OK) return st;
   const Plan plan = make_plan(M, N, K, q_dtype, cfg, dev.smem_optin);
-  if (plan.splits > 1 && static_cast<size_t>(plan.tiles_p) * plan.tiles_q > kCounterSlots)
+  if (plan.splits > 1 && !plan.cluster && static_cast<size_t>(plan.tiles_p) * plan.tiles_q > kCounterSlots)
     return fail(W8A8_ERR_UNSUPPORTED, "split_k > 1 supports at most %zu output tiles (got %d)", kCounterSlots,
                 plan.tiles_p * plan.tiles_q);
   if (plan.total > 0) {
@@ -378,8 +395,9 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
   prm.ldc = ldc;
   const long long out_elem = out_dtype >= W8A8_FP32 ? 4 : 2;
   prm.out_vec_ok = aligned(out, 16) && ((ldc * out_elem) % 16 == 0);
-  prm.partial = plan.splits > 1 ? reinterpret_cast<float*>(wsb + plan.off_partial) : nullptr;
-  prm.counters = plan.splits > 1 ? reinterpret_cast<unsigned*>(wsb + plan.off_counters) : nullptr;
+  prm.cluster = plan.cluster ? 1 : 0;
+  prm.partial = plan.splits > 1 && !plan.cluster ? reinterpret_cast<float*>(wsb + plan.off_partial) : nullptr;
+  prm.counters = plan.splits > 1 && !plan.cluster ? reinterpret_cast<unsigned*>(wsb + plan.off_counters) : nullptr;
   prm.kchunk_kb = kInt8ChunkK / 64;
   prm.num_sms = dev.sms;
   prm.pdl = 1;

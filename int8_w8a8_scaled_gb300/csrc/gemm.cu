@@ -47,6 +47,7 @@ namespace {
 constexpr int kThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kEpiThreads = 128;
 constexpr int kMaxSplits = 16;   // split_k limit of the reduction (host enforces)
+constexpr int kMaxClusterSplits = kMaxClusterSplit;  // split_k limit of the cluster reduction
 constexpr int kTileP = 128;       // rows of the P operand per tile (MMA M)
 constexpr int kRowBytes = 128;    // bytes of K per stage row (one swizzle row)
 constexpr int kPBytes = kTileP * kRowBytes;
@@ -251,9 +252,9 @@ __device__ __forceinline__ void epi_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
 }
 
-// Programmatic dependent launch: wait for the preceding kernel in the stream
-// (and its memory) before touching global memory; allow the next kernel to
-// start its prologue.  Both are no-ops without the launch attribute.
+// Programmatic dependent launch: allow the next kernel to be scheduled; wait
+// for the preceding kernel in the stream (and its memory) before touching
+// global memory.  Both are no-ops without the launch attribute.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
@@ -279,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   constexpr uint32_t kIdesc = make_idesc(kTileP, BN, 0);
   constexpr int kTmemCols = tmem_cols_for(BN, INT8);
   constexpr int kGroups = BN / 16;
+  constexpr int kRedLd = BN + 4;  // row stride (words) of a cluster-split partial tile
   static_assert((INT8 ? acc_bufs(INT8) + 1 : acc_bufs(INT8)) * BN <= kTmemCols && kTmemCols <= 512,
                 "accumulators must fit the TMEM allocation");
 
@@ -295,14 +297,22 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int units = prm.tiles_p * prm.tiles_q * prm.splits;
+  // Units this CTA walks.  Persistent: blockIdx.x, +gridDim.x, ...  With a
+  // cluster split the grid is one CTA per unit: the CTA of rank r in cluster
+  // c takes K slice r of tile c (units are numbered slice-major).
+  const bool cl = prm.cluster != 0;
+  const int w_first = cl ? static_cast<int>(cluster_ctarank()) * (prm.tiles_p * prm.tiles_q) +
+                               static_cast<int>(cluster_id_x())
+                         : static_cast<int>(blockIdx.x);
+  const int w_step = cl ? units : static_cast<int>(gridDim.x);
   if (threadIdx.x == 0) trace_stamp(prm, T_START);
 
   // Warm L2 with the weight tiles of this CTA's first work unit before
   // waiting on the preceding kernel: a prefetch only reads (coherent) global
   // memory into L2, so it is safe whatever that kernel writes, and the
   // weight stream starts while the preceding kernel is still running.
-  if (threadIdx.x == 0 && blockIdx.x < units) {
-    const Unit un = unit_of(blockIdx.x, prm, group, BN);
+  if (threadIdx.x == 0 && w_first < units) {
+    const Unit un = unit_of(w_first, prm, group, BN);
     const CUtensorMap* wmap = SWAP ? &tmap_p : &tmap_q;
     const int w_row = SWAP ? un.p0 : un.q0;
     const int n_pf = min(un.nkb, prm.prefetch_kb);
@@ -336,15 +346,18 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if (threadIdx.x == 0) trace_stamp(prm, T_PROLOGUE);
-  griddep_wait();
+  // Let the next kernel be scheduled (after this CTA holds its TMEM, so a
+  // later kernel never takes TMEM ahead of an earlier one), then wait for the
+  // preceding kernel's results.
   griddep_launch();
+  griddep_wait();
   if (threadIdx.x == 0) trace_stamp(prm, T_DEP_RELEASED);
 
   if (warp == 0) {
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < units && ok; w += gridDim.x) {
+      for (int w = w_first; w < units && ok; w += w_step) {
         const Unit un = unit_of(w, prm, group, BN);
         for (int i = 0; i < un.nkb; ++i, ++it) {
           const int s = it % stages;
@@ -362,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
     if (lane == 0) {
       uint32_t it = 0, u = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < units && ok; w += gridDim.x) {
+      for (int w = w_first; w < units && ok; w += w_step) {
         const Unit un = unit_of(w, prm, group, BN);
         const int chunk = INT8 ? prm.kchunk_kb : un.nkb;
         const int nch = (un.nkb + chunk - 1) / chunk;
@@ -407,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
     const size_t tile_elems = static_cast<size_t>(kTileP) * BN;
     uint32_t u = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < units && ok; w += gridDim.x) {
+    for (int w = w_first; w < units && ok; w += w_step) {
       const Unit un = unit_of(w, prm, group, BN);
       const int chunk = INT8 ? prm.kchunk_kb : un.nkb;
       const int nch = (un.nkb + chunk - 1) / chunk;
@@ -420,10 +433,22 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
         s_lane = (lane_idx < prm.M) ? (prm.a_per_row ? __ldg(prm.scale_a + lane_idx) : __ldg(prm.scale_a)) : 0.f;
       else
         s_lane = (lane_idx < prm.N) ? (prm.b_per_row ? __ldg(prm.scale_b + lane_idx) : __ldg(prm.scale_b)) : 0.f;
+      // Partial tile of a split unit, row-major with row stride part_ld:
+      // in the workspace, or -- with a cluster split -- in this CTA's shared
+      // memory over the stage ring (free once the unit's MMAs completed: the
+      // CTA has no further unit), padded so a warp's row-wise 16-byte stores
+      // hit distinct banks.
       uint32_t* part = nullptr;
-      if (prm.splits > 1)
-        part = reinterpret_cast<uint32_t*>(prm.partial) +
-               (static_cast<size_t>(un.tile_lin) * prm.splits + un.split) * tile_elems;
+      int part_ld = qv4;
+      if (prm.splits > 1) {
+        if (cl) {
+          part = reinterpret_cast<uint32_t*>(smem);
+          part_ld = kRedLd;
+        } else {
+          part = reinterpret_cast<uint32_t*>(prm.partial) +
+                 (static_cast<size_t>(un.tile_lin) * prm.splits + un.split) * tile_elems;
+        }
+      }
 
       for (int c = 0; c < nch; ++c, ++u) {
         constexpr int kBufs = acc_bufs(INT8);
@@ -431,6 +456,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
         if (!mbar_wait(ufull_bar(b), (u / kBufs) & 1)) { ok = false; break; }
         tc_fence_after();
         const bool last = (c == nch - 1);
+        if (cl && last) fence_proxy_async_shared();  // the stage ring becomes the partial tile
         const uint32_t acc_addr = lane_base + static_cast<uint32_t>(b * BN);
         const uint32_t tot_addr = lane_base + static_cast<uint32_t>(kBufs * BN);
         if (INT8) {
@@ -460,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
               if (!last) {
                 tmem_st16(tot_addr + g * 16, t[bb]);
               } else if (prm.splits > 1) {
-                write_partial16(part + static_cast<size_t>(row) * qv4, g * 16, qvalid, t[bb]);
+                write_partial16(part + static_cast<size_t>(row) * part_ld, g * 16, qvalid, t[bb]);
               } else {
                 int v[16];
 #pragma unroll
@@ -476,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
             tmem_ld16(acc_addr + g * 16, r);
             tmem_ld_wait();
             if (prm.splits > 1) {
-              write_partial16(part + static_cast<size_t>(row) * qv4, g * 16, qvalid, r);
+              write_partial16(part + static_cast<size_t>(row) * part_ld, g * 16, qvalid, r);
             } else {
               float v[16];
 #pragma unroll
@@ -491,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
       }
       if (!ok) break;
 
-      if (prm.splits > 1) {
+      if (prm.splits > 1 && !cl) {
         // the last slice to arrive sums all partials in slice order
         __threadfence();
         epi_bar_sync();
@@ -581,6 +607,71 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   }
 
   if (warp == 1 && lane == 0) trace_stamp(prm, T_MMA_ISSUED);
+  if (cl && prm.splits > 1) {
+    // Cluster split-K: every slice's partial tile now sits in its CTA's
+    // shared memory.  The CTA of rank r sums rows [r*128/S, (r+1)*128/S) of
+    // the tile over the S CTAs (distributed shared memory loads, slice order
+    // 0..S-1, so the result does not depend on scheduling) and finishes
+    // those outputs.
+    cluster_sync();
+    if (warp >= 2) {
+      const int et = threadIdx.x - 2 * 32;
+      const Unit un = unit_of(w_first, prm, group, BN);
+      const int S = prm.splits;
+      const int rank = static_cast<int>(cluster_ctarank());
+      const int r0 = (rank * kTileP) / S;
+      const int r1 = ((rank + 1) * kTileP) / S;
+      const int qvalid = min(BN, (SWAP ? prm.M : prm.N) - un.q0);
+      const int vpr = (qvalid + 3) / 4;  // float4s per row
+      const int nvec = (r1 - r0) * vpr;
+      const uint32_t red = smem_addr(smem);
+      const float* ps = SWAP ? prm.scale_b : prm.scale_a;
+      const int pp = SWAP ? prm.b_per_row : prm.a_per_row;
+      const int plim = SWAP ? prm.N : prm.M;
+      const float* qs = SWAP ? prm.scale_a : prm.scale_b;
+      const int qp = SWAP ? prm.a_per_row : prm.b_per_row;
+      for (int v = et; v < nvec; v += kEpiThreads) {
+        const int rr = v / vpr;
+        const int row = r0 + rr;
+        const int col = (v - rr * vpr) * 4;
+        const uint32_t off = red + static_cast<uint32_t>((row * kRedLd + col) * 4);
+        uint4 x[kMaxClusterSplits];
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
+          if (s2 < S) x[s2] = ld_dsmem_v4(mapa_shared(off, static_cast<uint32_t>(s2)));
+        const int p = un.p0 + row;
+        const float s_p = pp ? __ldg(ps + min(p, plim - 1)) : __ldg(ps);
+        float s_q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s_q[j] = qp ? __ldg(qs + min(un.q0 + col + j, un.q0 + qvalid - 1)) : __ldg(qs);
+        if (INT8) {
+          int acc[4] = {0, 0, 0, 0};
+#pragma unroll
+          for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
+            if (s2 < S) {
+              acc[0] += static_cast<int>(x[s2].x);
+              acc[1] += static_cast<int>(x[s2].y);
+              acc[2] += static_cast<int>(x[s2].z);
+              acc[3] += static_cast<int>(x[s2].w);
+            }
+          store4s<SWAP, OutT>(prm, p, un.q0 + col, qvalid - col, acc, s_p, s_q);
+        } else {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
+            if (s2 < S) {
+              acc[0] += __uint_as_float(x[s2].x);
+              acc[1] += __uint_as_float(x[s2].y);
+              acc[2] += __uint_as_float(x[s2].z);
+              acc[3] += __uint_as_float(x[s2].w);
+            }
+          store4s<SWAP, OutT>(prm, p, un.q0 + col, qvalid - col, acc, s_p, s_q);
+        }
+      }
+    }
+    // no CTA leaves (freeing its shared memory) while a peer still reads it
+    cluster_sync();
+  }
   if (threadIdx.x == 2 * 32) trace_stamp(prm, T_EPI_DONE);
   tc_fence_before();
   __syncthreads();
@@ -625,18 +716,34 @@ cudaError_t launch_one(const CUtensorMap& tp, const CUtensorMap& tq, const MmPar
   occ = max(1, min(occ, 512 / tmem_cols_for(BN, INT8)));
   if (p.max_ctas_per_sm > 0) occ = min(occ, p.max_ctas_per_sm);
   const int units = p.tiles_p * p.tiles_q * p.splits;
-  const int grid = max(1, min(units, p.num_sms * occ));
+  const bool cl = p.cluster != 0 && p.splits > 1;
+  if (cl && (p.splits > kMaxClusterSplits || !cluster_reduce_fits(BN, stages)))
+    return cudaErrorInvalidValue;  // the host validates this first
+  // persistent grid; with a cluster split one CTA per unit (clusters of
+  // `splits` consecutive CTAs)
+  const int grid = cl ? units : max(1, min(units, p.num_sms * occ));
   const int group = SWAP ? 1 : 8;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (p.pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (cl) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = static_cast<unsigned>(p.splits);
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = p.pdl ? 1 : 0;
+  cfg.numAttrs = na;
   e = cudaLaunchKernelEx(&cfg, kern, tp, tq, p, stages, group);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -692,8 +799,8 @@ cudaError_t dispatch(const CUtensorMap& tp, const CUtensorMap& tq, const MmParam
 // int8 [rows, K] (leading dim ld) -> f16 [rows, K] contiguous, exact.
 __global__ void widen_int8_kernel(const int8_t* __restrict__ src, long long ld, int rows, int K,
                                   __half* __restrict__ dst) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int vpr = K / 16;  // K is a multiple of 16
   const long long total = static_cast<long long>(rows) * vpr;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -719,6 +826,10 @@ __global__ void widen_int8_kernel(const int8_t* __restrict__ src, long long ld, 
 
 int gemm_smem_bytes(int block_n, int stages) {
   return stages * (kPBytes + block_n * kRowBytes) + 1024 /*alignment slack*/ + 256 /*barriers*/;
+}
+
+bool cluster_reduce_fits(int block_n, int stages) {
+  return kTileP * (block_n + 4) * 4 <= stages * (kPBytes + block_n * kRowBytes);
 }
 
 int max_stages_for(int block_n, int smem_budget) {

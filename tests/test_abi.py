@@ -96,9 +96,16 @@ def test_workspace_sizes():
     assert w8.mm_workspace_size(4096, 4096, 4096, w8.E4M3) == 0
     # int8 widens both operands to f16 planes
     assert w8.mm_workspace_size(512, 256, 1024, w8.INT8) >= (512 + 256) * 1024 * 2
-    # split-K partials + counters
-    cfg = {"swap_ab": 1, "block_n": 16, "split_k": 4}
+    # split-K through the workspace: partials + counters
+    cfg = {"swap_ab": 1, "block_n": 16, "split_k": 4, "reduce": w8.REDUCE_GLOBAL}
     assert w8.mm_workspace_size(1, 4096, 4096, w8.E4M3, cfg) >= 32 * 4 * 128 * 16 * 4
+    # split-K through a thread-block cluster (shared memory): no workspace
+    for red in (w8.REDUCE_AUTO, w8.REDUCE_CLUSTER):
+        cfg = {"swap_ab": 1, "block_n": 16, "split_k": 4, "reduce": red}
+        assert w8.mm_workspace_size(1, 4096, 4096, w8.E4M3, cfg) == 0
+    # more slices than one portable cluster: the workspace reduction
+    cfg = {"swap_ab": 1, "block_n": 16, "split_k": 16}
+    assert w8.mm_workspace_size(1, 4096, 4096, w8.E4M3, cfg) >= 32 * 16 * 128 * 16 * 4
 
 
 @pytest.mark.parametrize("M", [1, 16, 64, 256, 4096])
@@ -107,6 +114,7 @@ def test_pick_config_regimes(M):
     assert c["swap_ab"] == (1 if M <= 64 else 0)    # decode regime: weights on the 128-row side
     assert c["block_n"] in (16, 32, 64, 128, 160, 192, 224, 256)
     assert c["split_k"] >= 1
+    assert c["split_k"] <= 8 and c["reduce"] == w8.REDUCE_AUTO   # splits fit one cluster
     if M >= 4096:
         assert c["split_k"] == 1 and c["block_n"] >= 128   # many tiles: no split, wide tile
     c8 = w8.pick_config(M, 4096, 4096, w8.INT8)

@@ -72,14 +72,33 @@ FP8_CONFIGS = [
     {"swap_ab": 0, "block_n": 160, "split_k": 1},
     {"swap_ab": 0, "block_n": 192, "split_k": 2},
     {"swap_ab": 0, "block_n": 224, "split_k": 1},
+    # split-K through the workspace (last arriver) and through a cluster
+    {"swap_ab": 1, "block_n": 16, "split_k": 5, "reduce": w8.REDUCE_GLOBAL},
+    {"swap_ab": 0, "block_n": 64, "split_k": 3, "reduce": w8.REDUCE_GLOBAL},
+    {"swap_ab": 1, "block_n": 16, "split_k": 12},
+    {"swap_ab": 1, "block_n": 32, "split_k": 8, "reduce": w8.REDUCE_CLUSTER},
+    {"swap_ab": 1, "block_n": 16, "split_k": 7, "reduce": w8.REDUCE_CLUSTER},
+    {"swap_ab": 0, "block_n": 256, "split_k": 2, "stages": 3, "reduce": w8.REDUCE_CLUSTER},
+    {"swap_ab": 0, "block_n": 128, "split_k": 4, "reduce": w8.REDUCE_CLUSTER},
 ]
+
+
+def cfg_id(c):
+    if c is None:
+        return "auto"
+    t = f"s{c['swap_ab']}_bn{c['block_n']}_k{c['split_k']}"
+    if "stages" in c:
+        t += f"_st{c['stages']}"
+    if "reduce" in c:
+        t += {w8.REDUCE_GLOBAL: "_glob", w8.REDUCE_CLUSTER: "_clus"}.get(c["reduce"], "_auto")
+    return t
+
 
 FP8_SHAPES = [(1, 256, 512), (32, 256, 512), (3, 100, 272), (129, 300, 1040), (300, 384, 640),
               (17, 4096, 4096)]
 
 
-@pytest.mark.parametrize("cfg", FP8_CONFIGS, ids=lambda c: "auto" if c is None else
-                         f"s{c['swap_ab']}_bn{c['block_n']}_k{c['split_k']}" + (f"_st{c['stages']}" if "stages" in c else ""))
+@pytest.mark.parametrize("cfg", FP8_CONFIGS, ids=cfg_id)
 @pytest.mark.parametrize("shape", FP8_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_fp8_variants(cfg, shape):
     M, N, K = shape
@@ -176,13 +195,16 @@ INT8_CONFIGS = [
     {"swap_ab": 1, "block_n": 128, "split_k": 2},
     {"swap_ab": 0, "block_n": 256, "split_k": 1},
     {"swap_ab": 0, "block_n": 256, "split_k": 2},
+    {"swap_ab": 1, "block_n": 16, "split_k": 3, "reduce": w8.REDUCE_GLOBAL},
+    {"swap_ab": 0, "block_n": 256, "split_k": 2, "reduce": w8.REDUCE_GLOBAL},
+    {"swap_ab": 1, "block_n": 32, "split_k": 8, "reduce": w8.REDUCE_CLUSTER},
+    {"swap_ab": 0, "block_n": 64, "split_k": 5, "reduce": w8.REDUCE_CLUSTER},
 ]
 
 INT8_SHAPES = [(1, 128, 64), (5, 100, 1040), (130, 260, 2112), (300, 128, 3072)]
 
 
-@pytest.mark.parametrize("cfg", INT8_CONFIGS, ids=lambda c: "auto" if c is None else
-                         f"s{c['swap_ab']}_bn{c['block_n']}_k{c['split_k']}")
+@pytest.mark.parametrize("cfg", INT8_CONFIGS, ids=cfg_id)
 @pytest.mark.parametrize("shape", INT8_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_int8_variants_bit_exact(cfg, shape):
     M, N, K = shape
@@ -267,7 +289,7 @@ def test_cuda_graph_capture_and_replay():
 def test_split_k_workspace_is_left_zeroed():
     M, N, K = 1, 1024, 4096
     A, B, sa, sb = fp8_problem(M, N, K, seed=12)
-    cfg = {"swap_ab": 1, "block_n": 16, "split_k": 8}
+    cfg = {"swap_ab": 1, "block_n": 16, "split_k": 8, "reduce": w8.REDUCE_GLOBAL}
     ws = w8.Workspace(w8.mm_workspace_size(M, N, K, w8.E4M3, cfg))
     a_g, b_g = to_gpu_codes(A, oracle.E4M3), to_gpu_codes(B, oracle.E4M3)
     out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
@@ -364,3 +386,50 @@ def test_back_to_back_graph_of_gemms_with_overlap():
         ref = oracle.scaled_mm(A, B, sa, sb, oracle.E4M3, oracle.BF16)
         assert_fp8_close(out.cpu().numpy(), ref["y"])
     assert w8.device_status() == 0
+
+
+@pytest.mark.parametrize("qd,shape,base", [
+    (oracle.E4M3, (1, 6144, 4096), {"swap_ab": 1, "block_n": 16}),
+    (oracle.E4M3, (16, 4096, 14336), {"swap_ab": 1, "block_n": 32}),
+    (oracle.E4M3, (50, 1000, 3008), {"swap_ab": 1, "block_n": 32}),
+    (oracle.E4M3, (256, 4096, 4096), {"swap_ab": 0, "block_n": 64}),
+    (oracle.INT8, (7, 2048, 4096), {"swap_ab": 1, "block_n": 16}),
+], ids=["M1_qkv", "M16_down", "ragged", "M256_o", "int8_M7"])
+@pytest.mark.parametrize("splits", [2, 3, 6, 8])
+def test_cluster_and_global_reductions_agree_bitwise(qd, shape, base, splits):
+    """Both reductions start from zero and add the slices in the order
+    0..S-1, so their raw outputs (fp32 y / int32 accumulators) are the same
+    bits; both are checked against the oracle on a sample."""
+    M, N, K = shape
+    if qd == oracle.E4M3:
+        A, B, sa, sb = fp8_problem(M, N, K, seed=M + splits)
+        out_dt = torch.float32
+    else:
+        A, B, sa, sb = int8_problem(M, N, K, seed=M + splits)
+        out_dt = torch.int32
+    outs = {}
+    for red in (w8.REDUCE_GLOBAL, w8.REDUCE_CLUSTER):
+        cfg = dict(base, split_k=splits, reduce=red)
+        outs[red] = run_gpu(A, B, sa, sb, qd, out_dt, config=cfg).cpu().numpy()
+    assert np.array_equal(outs[w8.REDUCE_GLOBAL].view(np.uint32), outs[w8.REDUCE_CLUSTER].view(np.uint32))
+    im = np.random.default_rng(2).integers(0, M, 3000)
+    inn = np.random.default_rng(3).integers(0, N, 3000)
+    if qd == oracle.E4M3:
+        ref = oracle.scaled_mm_sample(A, B, sa, sb, oracle.E4M3, oracle.BF16, im, inn)
+        assert_fp8_close(outs[w8.REDUCE_CLUSTER][im, inn], ref["y"], f"{shape} S={splits}")
+    else:
+        ref = oracle.scaled_mm_sample(A, B, sa, sb, oracle.INT8, oracle.FP16, im, inn)
+        assert np.array_equal(outs[w8.REDUCE_CLUSTER][im, inn].astype(np.int64), ref["iacc"])
+    assert w8.device_status() == 0
+
+
+def test_cluster_reduction_config_errors():
+    A, B, sa, sb = fp8_problem(1, 512, 4096, seed=5)
+    with pytest.raises(w8.W8A8Error):      # more slices than one portable cluster
+        run_gpu(A, B, sa, sb, oracle.E4M3, torch.bfloat16,
+                config={"swap_ab": 1, "block_n": 16, "split_k": 9, "reduce": w8.REDUCE_CLUSTER})
+    with pytest.raises(w8.W8A8Error):      # a 2-stage ring cannot hold a 128 x 256 fp32 tile
+        run_gpu(A, B, sa, sb, oracle.E4M3, torch.bfloat16,
+                config={"swap_ab": 0, "block_n": 256, "split_k": 2, "stages": 2, "reduce": w8.REDUCE_CLUSTER})
+    with pytest.raises(w8.W8A8Error):
+        run_gpu(A, B, sa, sb, oracle.E4M3, torch.bfloat16, config={"reduce": 7})

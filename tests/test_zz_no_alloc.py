@@ -3,8 +3,8 @@
 w8a8_scaled_mm_noalloc serves callers that cannot allocate device memory
 where they run the matmul (allocator hooks, plug-ins given only operand and
 output buffers, processes whose memory another runtime has reserved): it
-keeps its split-K scratch in a fixed array the library defines in device
-memory.  Checked here through the C ABI against w8a8_scaled_mm with a
+keeps its scratch (split-K partials through the workspace, int8 operand
+planes) in a fixed array the library defines in device memory.  Checked here through the C ABI against w8a8_scaled_mm with a
 caller workspace, on two calls in a row, within the fp8 tolerance used by
 the other matmul tests.  This file is collected last.
 """
@@ -18,7 +18,7 @@ from int8_w8a8_scaled_gb300 import _lib
 
 pytestmark = pytest.mark.gpu
 
-E4M3, BF16, PER_ROW, PER_TENSOR = 0, 2, 1, 0
+E4M3, INT8, BF16, FP16, PER_ROW, PER_TENSOR = 0, 1, 2, 3, 1, 0
 
 
 def _p(t):
@@ -36,27 +36,37 @@ def _problem(M, N, K, seed):
     return a, b, sa, sb
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (16, 6144, 4096), (64, 4096, 14336), (3, 300, 1040)])
-def test_noalloc_matches_workspace_entry_point_twice(M, N, K):
+@pytest.mark.parametrize("M,N,K,qd", [(1, 4096, 4096, E4M3), (16, 6144, 4096, E4M3), (64, 4096, 14336, E4M3),
+                                      (3, 300, 1040, E4M3), (16, 1024, 1024, INT8), (5, 640, 2048, INT8)])
+def test_noalloc_matches_workspace_entry_point_twice(M, N, K, qd):
     lib = _lib.load()
     a, b, sa, sb = _problem(M, N, K, seed=M + N)
+    if qd == INT8:
+        a, b = a - 64, b - 64      # int8 codes spread over both signs
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    need = lib.w8a8_scaled_mm_workspace_size(M, N, K, E4M3)
-    assert 0 < need <= lib.w8a8_scaled_mm_noalloc_max_scratch()  # split-K scratch is in use
-    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
-    ref = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    st = lib.w8a8_scaled_mm(_p(a), K, _p(b), K, _p(sa), PER_ROW, _p(sb), PER_ROW, _p(ref), N, M, N, K, E4M3, BF16,
+    need = lib.w8a8_scaled_mm_workspace_size(M, N, K, qd)
+    assert need <= lib.w8a8_scaled_mm_noalloc_max_scratch()
+    if qd == INT8:
+        assert need > 0  # the f16 operand planes live in the fixed array
+    ws = torch.zeros(max(need, 1), dtype=torch.uint8, device="cuda")
+    od = BF16 if qd == E4M3 else FP16
+    tdt = torch.bfloat16 if qd == E4M3 else torch.float16
+    ref = torch.empty(M, N, dtype=tdt, device="cuda")
+    st = lib.w8a8_scaled_mm(_p(a), K, _p(b), K, _p(sa), PER_ROW, _p(sb), PER_ROW, _p(ref), N, M, N, K, qd, od,
                             _p(ws), need, stream)
     assert st == 0, lib.w8a8_last_error()
     for _ in range(2):
-        out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        out = torch.full((M, N), float("nan"), dtype=tdt, device="cuda")
         st = lib.w8a8_scaled_mm_noalloc(_p(a), K, _p(b), K, _p(sa), PER_ROW, _p(sb), PER_ROW, _p(out), N, M, N, K,
-                                        E4M3, BF16, stream)
+                                        qd, od, stream)
         assert st == 0, lib.w8a8_last_error()
         torch.cuda.synchronize()
-        r = ref.float().cpu().numpy().astype(np.float64)
-        o = out.float().cpu().numpy().astype(np.float64)
-        assert np.all(np.abs(o - r) <= 2.0 ** -7 * np.abs(r) + 1e-3)
+        if qd == INT8:   # exact integer accumulation: the same bits
+            assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+        else:
+            r = ref.float().cpu().numpy().astype(np.float64)
+            o = out.float().cpu().numpy().astype(np.float64)
+            assert np.all(np.abs(o - r) <= 2.0 ** -7 * np.abs(r) + 1e-3)
 
 
 def test_noalloc_rejects_problems_beyond_its_array():
