@@ -448,6 +448,7 @@ PROFILE_CASES = {
     # name: (description, builder) -- small enough for an ncu capture, inputs
     # larger than L2 where DRAM figures matter
     "decode_gemm": "fp8 decode GEMM, M=16 x gate-up [28672 x 4096] (117 MB of weights)",
+    "m256_gemm": "fp8 decode GEMM, M=256 x down [4096 x 14336] (59 MB of weights)",
     "prefill_gemm": "fp8 prefill GEMM, M=4096 x gate-up [28672 x 4096]",
     "int8_gemm": "int8 GEMM, M=8192 x QKV-70B [10240 x 8192]",
     "quant_tokens": "per-token dynamic e4m3 quantiser, [4096 x 14336] bf16",
@@ -458,7 +459,7 @@ PROFILE_CASES = {
 }
 
 
-def run_profile_case(name: str, launches: int):
+def run_profile_case(name: str, launches: int, override=None):
     """Run `launches` calls of one kernel family on a fixed small case (for
     ncu: capture with -k/-s/-c).  Prints the kernel configuration."""
     import torch
@@ -485,15 +486,16 @@ def run_profile_case(name: str, launches: int):
         return
     if name.endswith("_gemm"):
         M, N, K, qd = {"decode_gemm": (16, 28672, 4096, w8.E4M3), "prefill_gemm": (4096, 28672, 4096, w8.E4M3),
-                       "int8_gemm": (8192, 10240, 8192, w8.INT8)}[name]
+                       "int8_gemm": (8192, 10240, 8192, w8.INT8), "m256_gemm": (256, 4096, 14336, w8.E4M3)}[name]
         qt = torch.float8_e4m3fn if qd == w8.E4M3 else torch.int8
         a, sa = quantised((M, K), 1, qt, True, False)
         b, sb = quantised((N, K), 2, qt, True, True)
         out = torch.empty(M, N, dtype=torch.bfloat16 if qd == w8.E4M3 else torch.float16, device=dev)
-        ws = w8.Workspace(w8.mm_workspace_size(M, N, K, qd), dev)
-        print(json.dumps({"case": name, "config": w8.pick_config(M, N, K, qd)}), flush=True)
+        cfg = dict(w8.pick_config(M, N, K, qd), **override) if override else None
+        ws = w8.Workspace(w8.mm_workspace_size(M, N, K, qd, cfg), dev)
+        print(json.dumps({"case": name, "config": cfg or w8.pick_config(M, N, K, qd)}), flush=True)
         for _ in range(launches):
-            w8.scaled_mm(a, b, sa, sb, out, workspace=ws)
+            w8.scaled_mm(a, b, sa, sb, out, workspace=ws, config=cfg)
     elif name == "quant_decode":
         x = si.normal_with_outliers((1, 4096), seed=3, device=dev)
         q = torch.empty(1, 4096, dtype=torch.float8_e4m3fn, device=dev)
@@ -602,7 +604,7 @@ def sweep_decode(out_path: str, reps: int = 20):
                     cfgs.append({"swap_ab": 1, "block_n": bn, "split_k": sp})
             if M >= 64:
                 for bn in (64, 128, 160, 192, 224, 256):
-                    for sp in (1, 2, 4):
+                    for sp in (1, 2, 4, 8):
                         cfgs.append({"swap_ab": 0, "block_n": bn, "split_k": sp})
             auto = w8.pick_config(M, N, K, w8.E4M3)
             bytes_ = N * K + M * K + 2 * M * N
@@ -815,7 +817,7 @@ def main():
         sweep_decode(args.sweep_decode)
         return 0
     if args.profile_case:
-        run_profile_case(args.profile_case, args.launches)
+        run_profile_case(args.profile_case, args.launches, json.loads(args.override) if args.override else None)
         return 0
     if args.warmup < 3:
         args.warmup = 3

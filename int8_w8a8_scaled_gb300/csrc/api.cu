@@ -140,19 +140,26 @@ int num_kb(long long K, int q_dtype) { return static_cast<int>(ceil_div(K, q_dty
 
 // Automatic configuration, fitted to the decode and prefill sweeps of
 // `bench.py --sweep-decode / --sweep-large` on GB300:
-//  - M <= 64: weights on the 128-row MMA side (swap), block_n 16 (M <= 8) or
-//    32 -- narrow tiles keep two CTAs resident per SM;
+//  - M <= 64: weights on the 128-row MMA side (swap), block_n the smallest of
+//    16 / 32 / 64 that holds all M tokens -- one token tile, so every weight
+//    byte crosses L2 once, and two CTAs resident per SM;
 //  - M > 64: tokens on the 128-row side, the widest block_n in {256, 128, 64}
 //    that still gives >= 0.6 tiles per SM;
-//  - split-K: as many K slices as fit in one wave of resident CTAs
-//    (floor(slots / tiles)), at least 4 K blocks per slice, at most 16.
-//    More waves or wider splits lose to the fixed cost of each unit and of
-//    the partial reduction.
+//  - split-K: the largest power of two of K slices that fits one wave of
+//    resident CTAs (<= slots / tiles), at least 4 K blocks per slice, at
+//    most 8 (one portable cluster: the slices reduce through distributed
+//    shared memory).  More waves or wider splits lose to the fixed cost of
+//    each unit and of the reduction.
 int one_wave_split(long long tiles, int kb, long long slots) {
   long long sp = slots / std::max<long long>(1, tiles);
   sp = std::min<long long>(sp, std::max(1, kb / 4));
-  sp = std::min<long long>(sp, 16);
-  return static_cast<int>(std::max<long long>(1, sp));
+  sp = std::min<long long>(sp, 8);
+  // a power of two: clusters of 3, 5, 6 or 7 CTAs co-schedule poorly (the
+  // decode sweep measured 6 slices of a 48-tile QKV at 13 us against 8.2 us
+  // for 4)
+  long long p2 = 1;
+  while (p2 * 2 <= sp) p2 *= 2;
+  return static_cast<int>(p2);
 }
 
 int resident_per_sm(int block_n, int q_dtype) {
@@ -162,8 +169,9 @@ int resident_per_sm(int block_n, int q_dtype) {
 void auto_config(long long M, long long N, long long K, int q_dtype, int sms, w8a8_mm_config* c) {
   const int kb = num_kb(K, q_dtype);
   if (M <= 64) {
+    // all tokens in one narrow tile: the weights stream through L2 once
     c->swap_ab = 1;
-    c->block_n = M <= 8 ? 16 : 32;
+    c->block_n = M <= 16 ? 16 : M <= 32 ? 32 : 64;
   } else {
     c->swap_ab = 0;
     if (q_dtype == W8A8_INT8) {
@@ -201,11 +209,6 @@ void auto_config(long long M, long long N, long long K, int q_dtype, int sms, w8
   const long long tiles = c->swap_ab ? ceil_div(N, 128) * ceil_div(M, c->block_n)
                                      : ceil_div(M, 128) * ceil_div(N, c->block_n);
   c->split_k = one_wave_split(tiles, kb, static_cast<long long>(sms) * resident_per_sm(c->block_n, q_dtype));
-  // the slices of a tile reduce through distributed shared memory when they
-  // fit one portable cluster (<= 8): a few more idle slots are cheaper than
-  // the global-memory round trip, fence and arrival counter of the
-  // workspace reduction
-  if (c->split_k > 8) c->split_k = 8;
   c->stages = 0;
   c->ctas_per_sm = 0;
   c->reduce = W8A8_REDUCE_AUTO;
