@@ -313,12 +313,15 @@ W8A8_API w8a8_status w8a8_scaled_mm_noalloc(const void* a_q, int64_t lda, const 
                                             w8a8_stream_t stream);
 
 /* Debug: per-CTA phase trace of subsequent scaled_mm launches (process
- * wide).  buf is a device buffer of `bytes` bytes; each persistent CTA c <
- * bytes / 64 writes eight 64-bit words at buf[8c..8c+7]: %globaltimer (ns)
- * at kernel entry, after its prologue (barriers, TMEM), when the preceding
- * kernel's dependency was released, when its first operand stage landed,
- * when its last MMA was issued, when its epilogue finished, at exit, and its
- * SM id.  Each launch overwrites the buffer.  NULL turns tracing off (the
+ * wide).  buf is a device buffer of `bytes` bytes; each CTA c < bytes / 128
+ * writes sixteen 64-bit words at buf[16c..16c+15]: %globaltimer (ns) at
+ * kernel entry [0], after its prologue (barriers, TMEM) [1], when the
+ * preceding kernel's dependency was released [2], when its first operand
+ * stage landed [3], when its last MMA was issued [4], when its epilogue
+ * finished [5], at exit [6], its SM id [7], and for its last unit: when the
+ * accumulator was complete [8] and drained [9], and with a cluster split,
+ * after the cluster barrier [10] and its share of the reduction [11]; unused
+ * words are left as they were.  Each launch overwrites the buffer.  NULL turns tracing off (the
  * default).  Not for production use: concurrent launches share the buffer. */
 W8A8_API w8a8_status w8a8_debug_mm_trace(void* buf, size_t bytes);
 

@@ -614,7 +614,7 @@ w8a8_status w8a8_requant_shards(const void* q, int q_dtype, int64_t cols, int64_
 
 w8a8_status w8a8_debug_mm_trace(void* buf, size_t bytes) {
   if (buf && !aligned(buf, 8)) return fail(W8A8_ERR_MISALIGNED, "trace buffer must be 8-byte aligned");
-  const size_t per_cta = 8 * sizeof(unsigned long long);
+  const size_t per_cta = 16 * sizeof(unsigned long long);
   g_trace_ctas.store(buf ? static_cast<int>(std::min<size_t>(bytes / per_cta, 1u << 20)) : 0);
   g_trace_buf.store(buf ? static_cast<unsigned long long*>(buf) : nullptr);
   return ok();

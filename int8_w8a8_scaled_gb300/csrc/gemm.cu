@@ -117,10 +117,12 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_p, int tiles_q, int
 // Epilogue store of 16 consecutive accumulator columns of one TMEM lane.
 // Without swap the lane is an output row m and the columns are n; with swap
 // the lane is an output column n and the columns are rows m.  The scale
-// order is always (acc * scale_a) * scale_b.
+// order is always (acc * scale_a) * scale_b.  s_lane is the lane's P-side
+// scale; sq the unit's Q-side scales, staged in shared memory and indexed
+// from the tile's first column (col0 - q0 = local column).
 template <bool SWAP, typename OutT, typename V>
-__device__ __forceinline__ void store16(const MmParams& prm, int lane_idx, int col0, const V (&v)[16],
-                                        float s_lane) {
+__device__ __forceinline__ void store16(const MmParams& prm, int lane_idx, int col0, int lcol0, const V (&v)[16],
+                                        float s_lane, const float* sq) {
   OutT* out = reinterpret_cast<OutT*>(prm.out);
   if (!SWAP) {
     const int m = lane_idx;
@@ -129,10 +131,7 @@ __device__ __forceinline__ void store16(const MmParams& prm, int lane_idx, int c
     if (prm.out_vec_ok && col0 + 16 <= prm.N) {
       alignas(16) OutT o[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float sb = prm.b_per_row ? __ldg(prm.scale_b + col0 + j) : __ldg(prm.scale_b);
-        o[j] = OutConv<OutT>::conv(v[j], s_lane, sb);
-      }
+      for (int j = 0; j < 16; ++j) o[j] = OutConv<OutT>::conv(v[j], s_lane, sq[lcol0 + j]);
       uint4* dst = reinterpret_cast<uint4*>(row + col0);
       const uint4* src = reinterpret_cast<const uint4*>(o);
 #pragma unroll
@@ -141,10 +140,7 @@ __device__ __forceinline__ void store16(const MmParams& prm, int lane_idx, int c
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int n = col0 + j;
-        if (n < prm.N) {
-          const float sb = prm.b_per_row ? __ldg(prm.scale_b + n) : __ldg(prm.scale_b);
-          row[n] = OutConv<OutT>::conv(v[j], s_lane, sb);
-        }
+        if (n < prm.N) row[n] = OutConv<OutT>::conv(v[j], s_lane, sq[lcol0 + j]);
       }
     }
   } else {
@@ -153,10 +149,7 @@ __device__ __forceinline__ void store16(const MmParams& prm, int lane_idx, int c
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int m = col0 + j;
-      if (m < prm.M) {
-        const float sa = prm.a_per_row ? __ldg(prm.scale_a + m) : __ldg(prm.scale_a);
-        out[static_cast<long long>(m) * prm.ldc + n] = OutConv<OutT>::conv(v[j], sa, s_lane);
-      }
+      if (m < prm.M) out[static_cast<long long>(m) * prm.ldc + n] = OutConv<OutT>::conv(v[j], sq[lcol0 + j], s_lane);
     }
   }
 }
@@ -240,8 +233,11 @@ __device__ __forceinline__ Unit unit_of(int w, const MmParams& prm, int group, i
 
 // Optional per-CTA phase trace (debug): kTraceSlots 64-bit %globaltimer
 // stamps per CTA, written only when a trace buffer is set.
-constexpr int kTraceSlots = 8;
-enum TraceSlot { T_START = 0, T_PROLOGUE, T_DEP_RELEASED, T_FIRST_DATA, T_MMA_ISSUED, T_EPI_DONE, T_END, T_SMID };
+constexpr int kTraceSlots = 16;
+enum TraceSlot {
+  T_START = 0, T_PROLOGUE, T_DEP_RELEASED, T_FIRST_DATA, T_MMA_ISSUED, T_EPI_DONE, T_END, T_SMID,
+  T_ACC_READY, T_DRAINED, T_SYNCED, T_REDUCED
+};
 
 __device__ __forceinline__ void trace_stamp(const MmParams& prm, int slot) {
   if (prm.trace && blockIdx.x < prm.trace_ctas)
@@ -265,6 +261,73 @@ __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.
 // Accumulation units (one per work unit for e4m3, one per <= 1024-K chunk
 // for int8) alternate between two TMEM accumulators, so the epilogue of one
 // unit overlaps the MMAs of the next.
+// Cluster split-K, final sum of rows [r0, r0 + nvec / vpr) of a tile: each
+// epilogue thread takes B float4 vectors per pass and requests all B * S
+// partial vectors (distributed shared memory of the S CTAs) before using
+// any, sums each in slice order 0..S-1 from zero (the order of the
+// workspace reduction, so both give the same bits) and stores its four
+// outputs with the staged scales.  S == 0: s_rt slices (any count up to
+// kMaxClusterSplits), one vector per pass.
+template <int S, int B, int BN, bool SWAP, bool INT8, typename OutT>
+__device__ __forceinline__ void cluster_reduce_rows(const MmParams& prm, const Unit& un, uint32_t red, int r0,
+                                                    int vpr, int nvec, int et, int qvalid, const float* s_scale_p,
+                                                    const float* s_scale_q, int s_rt = 0) {
+  constexpr int kLd = BN + 4;  // row stride (words) of the partial tiles
+  constexpr int SS = S > 0 ? S : kMaxClusterSplits;
+  const int nsl = S > 0 ? S : s_rt;
+  for (int v0 = et; v0 < nvec; v0 += B * kEpiThreads) {
+    uint4 x[B][SS];
+    uint32_t off[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int v = v0 + b * kEpiThreads;
+      const int vc = v < nvec ? v : v0;  // past the end: load an in-range vector, store nothing
+      const int rr = vc / vpr;
+      off[b] = red + static_cast<uint32_t>(((r0 + rr) * kLd + (vc - rr * vpr) * 4) * 4);
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b)
+#pragma unroll
+      for (int s2 = 0; s2 < SS; ++s2)
+        if (S > 0 || s2 < nsl) x[b][s2] = ld_dsmem_v4(mapa_shared(off[b], static_cast<uint32_t>(s2)));
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int v = v0 + b * kEpiThreads;
+      if (v >= nvec) break;
+      const int rr = v / vpr;
+      const int row = r0 + rr;
+      const int col = (v - rr * vpr) * 4;
+      const float s_p = s_scale_p[row];
+      float s_q[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s_q[j] = s_scale_q[min(col + j, BN - 1)];
+      if (INT8) {
+        int acc[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int s2 = 0; s2 < SS; ++s2)
+          if (S > 0 || s2 < nsl) {
+            acc[0] += static_cast<int>(x[b][s2].x);
+            acc[1] += static_cast<int>(x[b][s2].y);
+            acc[2] += static_cast<int>(x[b][s2].z);
+            acc[3] += static_cast<int>(x[b][s2].w);
+          }
+        store4s<SWAP, OutT>(prm, un.p0 + row, un.q0 + col, qvalid - col, acc, s_p, s_q);
+      } else {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s2 = 0; s2 < SS; ++s2)
+          if (S > 0 || s2 < nsl) {
+            acc[0] += __uint_as_float(x[b][s2].x);
+            acc[1] += __uint_as_float(x[b][s2].y);
+            acc[2] += __uint_as_float(x[b][s2].z);
+            acc[3] += __uint_as_float(x[b][s2].w);
+          }
+        store4s<SWAP, OutT>(prm, un.p0 + row, un.q0 + col, qvalid - col, acc, s_p, s_q);
+      }
+    }
+  }
+}
+
 // Narrow tiles run two CTAs per SM (the dispatch sizes their shared memory
 // for that); cap their registers so that two fit (<= 168 per thread).
 __host__ __device__ constexpr int min_ctas_for(int bn, bool int8) { return (bn <= 64 || (int8 && bn <= 128)) ? 2 : 1; }
@@ -293,6 +356,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   // bars: full[stages], empty[stages], unit_full[2], unit_empty[2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 4);
   __shared__ int s_is_last;
+  __shared__ float s_scale_p[kTileP];  // the unit's P-side row scales
+  __shared__ float s_scale_q[BN];      // the unit's Q-side column scales
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -428,11 +493,24 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
       // columns of this tile inside the problem (the Q side is M with swap)
       const int qvalid = min(BN, (SWAP ? prm.M : prm.N) - un.q0);
       const int qv4 = (qvalid + 3) & ~3;  // row stride of a partial tile (floats)
-      float s_lane;
-      if (!SWAP)
-        s_lane = (lane_idx < prm.M) ? (prm.a_per_row ? __ldg(prm.scale_a + lane_idx) : __ldg(prm.scale_a)) : 0.f;
-      else
-        s_lane = (lane_idx < prm.N) ? (prm.b_per_row ? __ldg(prm.scale_b + lane_idx) : __ldg(prm.scale_b)) : 0.f;
+      // Stage this unit's scales in shared memory now, while its MMAs run:
+      // P-side row scales and Q-side column scales (clamped to the problem;
+      // out-of-range rows/columns are never stored).  The previous unit's
+      // readers are done (barrier), and the tile's scales are ready before
+      // the accumulator is.
+      epi_bar_sync();
+      {
+        const float* ps = SWAP ? prm.scale_b : prm.scale_a;
+        const int pp = SWAP ? prm.b_per_row : prm.a_per_row;
+        const int plim = SWAP ? prm.N : prm.M;
+        const float* qs = SWAP ? prm.scale_a : prm.scale_b;
+        const int qp = SWAP ? prm.a_per_row : prm.b_per_row;
+        const int qlim = SWAP ? prm.M : prm.N;
+        s_scale_p[et] = pp ? __ldg(ps + min(un.p0 + et, plim - 1)) : __ldg(ps);
+        for (int i = et; i < BN; i += kEpiThreads) s_scale_q[i] = qp ? __ldg(qs + min(un.q0 + i, qlim - 1)) : __ldg(qs);
+      }
+      epi_bar_sync();
+      const float s_lane = s_scale_p[row];
       // Partial tile of a split unit, row-major with row stride part_ld:
       // in the workspace, or -- with a cluster split -- in this CTA's shared
       // memory over the stage ring (free once the unit's MMAs completed: the
@@ -457,6 +535,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
         tc_fence_after();
         const bool last = (c == nch - 1);
         if (cl && last) fence_proxy_async_shared();  // the stage ring becomes the partial tile
+        if (last && et == 0) trace_stamp(prm, T_ACC_READY);
         const uint32_t acc_addr = lane_base + static_cast<uint32_t>(b * BN);
         const uint32_t tot_addr = lane_base + static_cast<uint32_t>(kBufs * BN);
         if (INT8) {
@@ -491,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
                 int v[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] = static_cast<int>(t[bb][j]);
-                store16<SWAP, OutT>(prm, lane_idx, un.q0 + g * 16, v, s_lane);
+                store16<SWAP, OutT>(prm, lane_idx, un.q0 + g * 16, g * 16, v, s_lane, s_scale_q);
               }
             }
           }
@@ -507,13 +586,14 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
               float v[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-              store16<SWAP, OutT>(prm, lane_idx, un.q0 + g * 16, v, s_lane);
+              store16<SWAP, OutT>(prm, lane_idx, un.q0 + g * 16, g * 16, v, s_lane, s_scale_q);
             }
           }
         }
         if (INT8 && !last) tmem_st_wait();
         tc_fence_before();
         mbar_arrive(uempty_bar(b));
+        if (last && et == 0) trace_stamp(prm, T_DRAINED);
       }
       if (!ok) break;
 
@@ -550,16 +630,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
               const int v = vv[h] < nvec ? vv[h] : v0;
               const int row_r = (v * 4) / qv4;
               const int col = v * 4 - row_r * qv4;
-              const int p = un.p0 + row_r;
-              const float* ps = SWAP ? prm.scale_b : prm.scale_a;
-              const int pp = SWAP ? prm.b_per_row : prm.a_per_row;
-              const int plim = SWAP ? prm.N : prm.M;
-              sp[h] = pp ? __ldg(ps + min(p, plim - 1)) : __ldg(ps);
-              const float* qs = SWAP ? prm.scale_a : prm.scale_b;
-              const int qp = SWAP ? prm.a_per_row : prm.b_per_row;
+              sp[h] = s_scale_p[row_r];
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                sq[h][j] = qp ? __ldg(qs + min(un.q0 + col + j, un.q0 + qvalid - 1)) : __ldg(qs);
+              for (int j = 0; j < 4; ++j) sq[h][j] = s_scale_q[min(col + j, BN - 1)];
             }
             float fa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             int ia[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
@@ -614,6 +687,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
     // 0..S-1, so the result does not depend on scheduling) and finishes
     // those outputs.
     cluster_sync();
+    if (threadIdx.x == 2 * 32) trace_stamp(prm, T_SYNCED);
     if (warp >= 2) {
       const int et = threadIdx.x - 2 * 32;
       const Unit un = unit_of(w_first, prm, group, BN);
@@ -625,50 +699,14 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
       const int vpr = (qvalid + 3) / 4;  // float4s per row
       const int nvec = (r1 - r0) * vpr;
       const uint32_t red = smem_addr(smem);
-      const float* ps = SWAP ? prm.scale_b : prm.scale_a;
-      const int pp = SWAP ? prm.b_per_row : prm.a_per_row;
-      const int plim = SWAP ? prm.N : prm.M;
-      const float* qs = SWAP ? prm.scale_a : prm.scale_b;
-      const int qp = SWAP ? prm.a_per_row : prm.b_per_row;
-      for (int v = et; v < nvec; v += kEpiThreads) {
-        const int rr = v / vpr;
-        const int row = r0 + rr;
-        const int col = (v - rr * vpr) * 4;
-        const uint32_t off = red + static_cast<uint32_t>((row * kRedLd + col) * 4);
-        uint4 x[kMaxClusterSplits];
-#pragma unroll
-        for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
-          if (s2 < S) x[s2] = ld_dsmem_v4(mapa_shared(off, static_cast<uint32_t>(s2)));
-        const int p = un.p0 + row;
-        const float s_p = pp ? __ldg(ps + min(p, plim - 1)) : __ldg(ps);
-        float s_q[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) s_q[j] = qp ? __ldg(qs + min(un.q0 + col + j, un.q0 + qvalid - 1)) : __ldg(qs);
-        if (INT8) {
-          int acc[4] = {0, 0, 0, 0};
-#pragma unroll
-          for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
-            if (s2 < S) {
-              acc[0] += static_cast<int>(x[s2].x);
-              acc[1] += static_cast<int>(x[s2].y);
-              acc[2] += static_cast<int>(x[s2].z);
-              acc[3] += static_cast<int>(x[s2].w);
-            }
-          store4s<SWAP, OutT>(prm, p, un.q0 + col, qvalid - col, acc, s_p, s_q);
-        } else {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
-            if (s2 < S) {
-              acc[0] += __uint_as_float(x[s2].x);
-              acc[1] += __uint_as_float(x[s2].y);
-              acc[2] += __uint_as_float(x[s2].z);
-              acc[3] += __uint_as_float(x[s2].w);
-            }
-          store4s<SWAP, OutT>(prm, p, un.q0 + col, qvalid - col, acc, s_p, s_q);
-        }
+      switch (S) {  // compile-time slice counts: every load of a pass in flight together
+        case 2: cluster_reduce_rows<2, 8, BN, SWAP, INT8, OutT>(prm, un, red, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q); break;
+        case 4: cluster_reduce_rows<4, 4, BN, SWAP, INT8, OutT>(prm, un, red, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q); break;
+        case 8: cluster_reduce_rows<8, 2, BN, SWAP, INT8, OutT>(prm, un, red, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q); break;
+        default: cluster_reduce_rows<0, 1, BN, SWAP, INT8, OutT>(prm, un, red, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q, S); break;
       }
     }
+    if (threadIdx.x == 2 * 32) trace_stamp(prm, T_REDUCED);
     // no CTA leaves (freeing its shared memory) while a peer still reads it
     cluster_sync();
   }
