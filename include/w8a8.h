@@ -206,11 +206,12 @@ W8A8_API w8a8_status w8a8_scaled_mm(const void* a_q, int64_t lda, const void* b_
  *            W8A8_REDUCE_GLOBAL  partial tiles in the workspace, the last
  *                                slice to arrive sums them;
  *            W8A8_REDUCE_CLUSTER the slices of a tile run as one
- *                                thread-block cluster and sum each other's
- *                                partial tiles from shared memory (split_k
- *                                <= 8; no workspace);
- *            W8A8_REDUCE_AUTO    the cluster reduction when split_k <= 8
- *                                and the stage ring holds a fp32 tile,
+ *                                thread-block cluster: each writes its
+ *                                partial tile to the workspace and, after
+ *                                a cluster barrier, sums 1/split_k of the
+ *                                tile's rows over all partials (split_k
+ *                                <= 8);
+ *            W8A8_REDUCE_AUTO    the cluster reduction when split_k <= 8,
  *                                else the global one.
  * Fields set to 0 (except swap_ab) mean "choose automatically". */
 #define W8A8_REDUCE_AUTO 0

@@ -248,14 +248,12 @@ Plan make_plan(long long M, long long N, long long K, int q_dtype, const w8a8_mm
   p.kb_per_split = static_cast<int>(ceil_div(p.kb, sp));
   p.splits = static_cast<int>(ceil_div(p.kb, p.kb_per_split));  // every slice non-empty
   p.stages = cfg.stages > 0 ? cfg.stages : auto_stages(cfg.block_n, q_dtype, smem_optin);
-  p.cluster = p.splits > 1 && cfg.reduce != W8A8_REDUCE_GLOBAL && p.splits <= kMaxClusterSplit &&
-              cluster_reduce_fits(cfg.block_n, p.stages);
+  p.cluster = p.splits > 1 && cfg.reduce != W8A8_REDUCE_GLOBAL && p.splits <= kMaxClusterSplit;
   const size_t tiles = static_cast<size_t>(p.tiles_p) * p.tiles_q;
-  const bool global_split = p.splits > 1 && !p.cluster;
-  const bool need_ws = global_split || q_dtype == W8A8_INT8;
+  const bool need_ws = p.splits > 1 || q_dtype == W8A8_INT8;
   size_t off = need_ws ? kCounterRegion : 0;
   p.off_counters = 0;
-  if (global_split) {
+  if (p.splits > 1) {
     p.off_partial = off;
     off = align256(off + tiles * p.splits * 128 * cfg.block_n * sizeof(float));
   }
@@ -288,9 +286,6 @@ w8a8_status validate_config(const w8a8_mm_config& c, int q_dtype, int smem_optin
                 c.block_n, gemm_smem_bytes(c.block_n, st), smem_optin);
   if (c.reduce == W8A8_REDUCE_CLUSTER && c.split_k > kMaxClusterSplit)
     return fail(W8A8_ERR_UNSUPPORTED, "the cluster reduction takes split_k <= %d", kMaxClusterSplit);
-  if (c.reduce == W8A8_REDUCE_CLUSTER && !cluster_reduce_fits(c.block_n, st))
-    return fail(W8A8_ERR_UNSUPPORTED, "the cluster reduction needs the %d-stage ring to hold a 128 x %d fp32 tile",
-                st, c.block_n);
   return W8A8_OK;
 }
 
@@ -399,7 +394,7 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
   const long long out_elem = out_dtype >= W8A8_FP32 ? 4 : 2;
   prm.out_vec_ok = aligned(out, 16) && ((ldc * out_elem) % 16 == 0);
   prm.cluster = plan.cluster ? 1 : 0;
-  prm.partial = plan.splits > 1 && !plan.cluster ? reinterpret_cast<float*>(wsb + plan.off_partial) : nullptr;
+  prm.partial = plan.splits > 1 ? reinterpret_cast<float*>(wsb + plan.off_partial) : nullptr;
   prm.counters = plan.splits > 1 && !plan.cluster ? reinterpret_cast<unsigned*>(wsb + plan.off_counters) : nullptr;
   prm.kchunk_kb = kInt8ChunkK / 64;
   prm.num_sms = dev.sms;

@@ -263,33 +263,30 @@ __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.
 // unit overlaps the MMAs of the next.
 // Cluster split-K, final sum of rows [r0, r0 + nvec / vpr) of a tile: each
 // epilogue thread takes B float4 vectors per pass and requests all B * S
-// partial vectors (distributed shared memory of the S CTAs) before using
-// any, sums each in slice order 0..S-1 from zero (the order of the
-// workspace reduction, so both give the same bits) and stores its four
-// outputs with the staged scales.  S == 0: s_rt slices (any count up to
+// partial vectors (L2: the partial tiles are `slice_stride` words apart in
+// the workspace, `base` points at row r0 of slice 0) before using any, sums
+// each in slice order 0..S-1 from zero (the order of the last-arriver
+// reduction, so both give the same bits) and stores its four outputs with
+// the staged scales.  S == 0: s_rt slices (any count up to
 // kMaxClusterSplits), one vector per pass.
 template <int S, int B, int BN, bool SWAP, bool INT8, typename OutT>
-__device__ __forceinline__ void cluster_reduce_rows(const MmParams& prm, const Unit& un, uint32_t red, int r0,
-                                                    int vpr, int nvec, int et, int qvalid, const float* s_scale_p,
-                                                    const float* s_scale_q, int s_rt = 0) {
-  constexpr int kLd = BN + 4;  // row stride (words) of the partial tiles
+__device__ __forceinline__ void cluster_reduce_rows(const MmParams& prm, const Unit& un, const uint32_t* base,
+                                                    size_t slice_stride, int r0, int vpr, int nvec, int et,
+                                                    int qvalid, const float* s_scale_p, const float* s_scale_q,
+                                                    int s_rt = 0) {
   constexpr int SS = S > 0 ? S : kMaxClusterSplits;
   const int nsl = S > 0 ? S : s_rt;
   for (int v0 = et; v0 < nvec; v0 += B * kEpiThreads) {
     uint4 x[B][SS];
-    uint32_t off[B];
 #pragma unroll
     for (int b = 0; b < B; ++b) {
       const int v = v0 + b * kEpiThreads;
       const int vc = v < nvec ? v : v0;  // past the end: load an in-range vector, store nothing
-      const int rr = vc / vpr;
-      off[b] = red + static_cast<uint32_t>(((r0 + rr) * kLd + (vc - rr * vpr) * 4) * 4);
-    }
-#pragma unroll
-    for (int b = 0; b < B; ++b)
 #pragma unroll
       for (int s2 = 0; s2 < SS; ++s2)
-        if (S > 0 || s2 < nsl) x[b][s2] = ld_dsmem_v4(mapa_shared(off[b], static_cast<uint32_t>(s2)));
+        if (S > 0 || s2 < nsl)
+          x[b][s2] = __ldcg(reinterpret_cast<const uint4*>(base + s2 * slice_stride) + vc);
+    }
 #pragma unroll
     for (int b = 0; b < B; ++b) {
       const int v = v0 + b * kEpiThreads;
@@ -343,7 +340,6 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   constexpr uint32_t kIdesc = make_idesc(kTileP, BN, 0);
   constexpr int kTmemCols = tmem_cols_for(BN, INT8);
   constexpr int kGroups = BN / 16;
-  constexpr int kRedLd = BN + 4;  // row stride (words) of a cluster-split partial tile
   static_assert((INT8 ? acc_bufs(INT8) + 1 : acc_bufs(INT8)) * BN <= kTmemCols && kTmemCols <= 512,
                 "accumulators must fit the TMEM allocation");
 
@@ -511,22 +507,12 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
       }
       epi_bar_sync();
       const float s_lane = s_scale_p[row];
-      // Partial tile of a split unit, row-major with row stride part_ld:
-      // in the workspace, or -- with a cluster split -- in this CTA's shared
-      // memory over the stage ring (free once the unit's MMAs completed: the
-      // CTA has no further unit), padded so a warp's row-wise 16-byte stores
-      // hit distinct banks.
+      // Partial tile of a split unit in the workspace, row-major, row stride
+      // = valid columns rounded up to 4 (coalesced float4 rows).
       uint32_t* part = nullptr;
-      int part_ld = qv4;
-      if (prm.splits > 1) {
-        if (cl) {
-          part = reinterpret_cast<uint32_t*>(smem);
-          part_ld = kRedLd;
-        } else {
-          part = reinterpret_cast<uint32_t*>(prm.partial) +
-                 (static_cast<size_t>(un.tile_lin) * prm.splits + un.split) * tile_elems;
-        }
-      }
+      if (prm.splits > 1)
+        part = reinterpret_cast<uint32_t*>(prm.partial) +
+               (static_cast<size_t>(un.tile_lin) * prm.splits + un.split) * tile_elems;
 
       for (int c = 0; c < nch; ++c, ++u) {
         constexpr int kBufs = acc_bufs(INT8);
@@ -534,7 +520,6 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
         if (!mbar_wait(ufull_bar(b), (u / kBufs) & 1)) { ok = false; break; }
         tc_fence_after();
         const bool last = (c == nch - 1);
-        if (cl && last) fence_proxy_async_shared();  // the stage ring becomes the partial tile
         if (last && et == 0) trace_stamp(prm, T_ACC_READY);
         const uint32_t acc_addr = lane_base + static_cast<uint32_t>(b * BN);
         const uint32_t tot_addr = lane_base + static_cast<uint32_t>(kBufs * BN);
@@ -565,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
               if (!last) {
                 tmem_st16(tot_addr + g * 16, t[bb]);
               } else if (prm.splits > 1) {
-                write_partial16(part + static_cast<size_t>(row) * part_ld, g * 16, qvalid, t[bb]);
+                write_partial16(part + static_cast<size_t>(row) * qv4, g * 16, qvalid, t[bb]);
               } else {
                 int v[16];
 #pragma unroll
@@ -581,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
             tmem_ld16(acc_addr + g * 16, r);
             tmem_ld_wait();
             if (prm.splits > 1) {
-              write_partial16(part + static_cast<size_t>(row) * part_ld, g * 16, qvalid, r);
+              write_partial16(part + static_cast<size_t>(row) * qv4, g * 16, qvalid, r);
             } else {
               float v[16];
 #pragma unroll
@@ -681,11 +666,13 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
 
   if (warp == 1 && lane == 0) trace_stamp(prm, T_MMA_ISSUED);
   if (cl && prm.splits > 1) {
-    // Cluster split-K: every slice's partial tile now sits in its CTA's
-    // shared memory.  The CTA of rank r sums rows [r*128/S, (r+1)*128/S) of
-    // the tile over the S CTAs (distributed shared memory loads, slice order
-    // 0..S-1, so the result does not depend on scheduling) and finishes
-    // those outputs.
+    // Cluster split-K: every slice has written its partial tile to the
+    // workspace; the cluster barrier (release / acquire at cluster scope)
+    // makes them visible to the other CTAs of the tile.  The CTA of rank r
+    // then sums rows [r*128/S, (r+1)*128/S) over the S partials from L2
+    // (slice order 0..S-1, so the result does not depend on scheduling) and
+    // finishes those outputs.  The partials stay in the workspace: no CTA
+    // waits for another after this point.
     cluster_sync();
     if (threadIdx.x == 2 * 32) trace_stamp(prm, T_SYNCED);
     if (warp >= 2) {
@@ -696,19 +683,20 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
       const int r0 = (rank * kTileP) / S;
       const int r1 = ((rank + 1) * kTileP) / S;
       const int qvalid = min(BN, (SWAP ? prm.M : prm.N) - un.q0);
-      const int vpr = (qvalid + 3) / 4;  // float4s per row
+      const int qv4 = (qvalid + 3) & ~3;
+      const int vpr = qv4 / 4;  // float4s per row
       const int nvec = (r1 - r0) * vpr;
-      const uint32_t red = smem_addr(smem);
+      const size_t tile_elems = static_cast<size_t>(kTileP) * BN;
+      const uint32_t* base = reinterpret_cast<const uint32_t*>(prm.partial) +
+                             static_cast<size_t>(un.tile_lin) * S * tile_elems + static_cast<size_t>(r0) * qv4;
       switch (S) {  // compile-time slice counts: every load of a pass in flight together
-        case 2: cluster_reduce_rows<2, 8, BN, SWAP, INT8, OutT>(prm, un, red, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q); break;
-        case 4: cluster_reduce_rows<4, 4, BN, SWAP, INT8, OutT>(prm, un, red, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q); break;
-        case 8: cluster_reduce_rows<8, 2, BN, SWAP, INT8, OutT>(prm, un, red, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q); break;
-        default: cluster_reduce_rows<0, 1, BN, SWAP, INT8, OutT>(prm, un, red, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q, S); break;
+        case 2: cluster_reduce_rows<2, 8, BN, SWAP, INT8, OutT>(prm, un, base, tile_elems, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q); break;
+        case 4: cluster_reduce_rows<4, 4, BN, SWAP, INT8, OutT>(prm, un, base, tile_elems, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q); break;
+        case 8: cluster_reduce_rows<8, 2, BN, SWAP, INT8, OutT>(prm, un, base, tile_elems, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q); break;
+        default: cluster_reduce_rows<0, 1, BN, SWAP, INT8, OutT>(prm, un, base, tile_elems, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q, S); break;
       }
     }
     if (threadIdx.x == 2 * 32) trace_stamp(prm, T_REDUCED);
-    // no CTA leaves (freeing its shared memory) while a peer still reads it
-    cluster_sync();
   }
   if (threadIdx.x == 2 * 32) trace_stamp(prm, T_EPI_DONE);
   tc_fence_before();
@@ -755,8 +743,7 @@ cudaError_t launch_one(const CUtensorMap& tp, const CUtensorMap& tq, const MmPar
   if (p.max_ctas_per_sm > 0) occ = min(occ, p.max_ctas_per_sm);
   const int units = p.tiles_p * p.tiles_q * p.splits;
   const bool cl = p.cluster != 0 && p.splits > 1;
-  if (cl && (p.splits > kMaxClusterSplits || !cluster_reduce_fits(BN, stages)))
-    return cudaErrorInvalidValue;  // the host validates this first
+  if (cl && p.splits > kMaxClusterSplits) return cudaErrorInvalidValue;  // the host validates this first
   // persistent grid; with a cluster split one CTA per unit (clusters of
   // `splits` consecutive CTAs)
   const int grid = cl ? units : max(1, min(units, p.num_sms * occ));
@@ -864,10 +851,6 @@ __global__ void widen_int8_kernel(const int8_t* __restrict__ src, long long ld, 
 
 int gemm_smem_bytes(int block_n, int stages) {
   return stages * (kPBytes + block_n * kRowBytes) + 1024 /*alignment slack*/ + 256 /*barriers*/;
-}
-
-bool cluster_reduce_fits(int block_n, int stages) {
-  return kTileP * (block_n + 4) * 4 <= stages * (kPBytes + block_n * kRowBytes);
 }
 
 int max_stages_for(int block_n, int smem_budget) {

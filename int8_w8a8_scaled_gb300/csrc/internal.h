@@ -19,8 +19,9 @@ struct MmParams {
   int num_kb;            // K blocks of 128 bytes
   int kb_per_split;      // K blocks per split
   int splits;            // >= 1; > 1 reduces fp32 partials in split order
-  int cluster;           // 1: the splits of a tile form one thread-block cluster
-                         // and reduce through distributed shared memory
+  int cluster;           // 1: the splits of a tile form one thread-block cluster;
+                         // after a cluster barrier each CTA sums 1/splits of the
+                         // tile's rows from the workspace partials
   const float* scale_a;
   int a_per_row;
   const float* scale_b;
@@ -28,7 +29,7 @@ struct MmParams {
   void* out;
   long long ldc;
   int out_vec_ok;        // 16-byte vector stores allowed along n
-  float* partial;        // [tiles][splits][128 * block_n] fp32 (splits > 1, no cluster)
+  float* partial;        // [tiles][splits][128 * block_n] fp32 / int32 (splits > 1)
   unsigned* counters;    // [tiles] arrival counters (splits > 1, no cluster), left zero
   int kchunk_kb;         // int8 path: K blocks per exact fp32 chunk
   int num_sms;           // persistent grid = min(units, num_sms * resident CTAs per SM)
@@ -71,9 +72,6 @@ cudaError_t read_clear_quant_status(int* flags);
 int gemm_smem_bytes(int block_n, int stages);
 // Largest split_k the cluster reduction takes (one portable cluster).
 constexpr int kMaxClusterSplit = 8;
-// The cluster reduction keeps a 128 x (block_n + 4) fp32 partial tile over
-// the stage ring: does a `stages`-deep ring hold it?
-bool cluster_reduce_fits(int block_n, int stages);
 int max_stages_for(int block_n, int smem_budget);
 
 // Quantiser / dequantiser launchers.

@@ -128,9 +128,13 @@ __global__ void __launch_bounds__(kRowThreads)
   extern __shared__ __align__(16) uint4 row_s[];
   __shared__ uint64_t bar;
   __shared__ float red[kRowThreads / 32];
-  allow_dependents();
   const long long row = blockIdx.x;
   const uint32_t bytes = static_cast<uint32_t>(cols * 2);
+  // Start the row's trip into L2 before waiting on the preceding kernel (a
+  // prefetch only reads: whatever that kernel writes, the copy below reads
+  // after the wait), then trigger / wait as every kernel here does.
+  if (threadIdx.x == 0) bulk_prefetch_l2(x + row * ld_x, bytes);
+  allow_dependents();
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(&bar), 1);
     fence_barrier_init();

@@ -94,37 +94,13 @@ __device__ __forceinline__ uint32_t cluster_id_x() {
   return r;
 }
 
-// The shared::cluster address of the variable at CTA-local shared address
-// `addr` in the cluster's CTA `rank`.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-
-// 16-byte load from distributed shared memory (any CTA of the cluster).
-__device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
 // Cluster-wide barrier over every thread of every CTA in the cluster: the
-// release/acquire pair makes each CTA's shared-memory writes before the
-// barrier visible to the other CTAs' reads after it.  Like __syncthreads it
+// release/acquire pair (cluster scope) makes each CTA's memory writes before
+// the barrier visible to the other CTAs' reads after it.  Like __syncthreads it
 // has no timeout; every thread of the kernel reaches it on a path whose
 // waits are all bounded.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
-// Order this thread's earlier async-proxy (TMA / tensor core) accesses of
-// shared memory with its later generic ones.
-__device__ __forceinline__ void fence_proxy_async_shared() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ TMA
@@ -152,6 +128,13 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// Prefetch `bytes` bytes of global memory into L2 (address 16-byte aligned,
+// bytes a multiple of 16).  Reads only; no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
 }
 
 // Same with an L2 eviction-priority cache policy (createpolicy result).
