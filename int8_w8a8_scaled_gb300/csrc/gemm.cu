@@ -155,13 +155,17 @@ __device__ __forceinline__ void store16(const MmParams& prm, int lane_idx, int c
 }
 
 // Split-K partial of one TMEM lane: 16 consecutive accumulator columns
-// starting at col0, written as float4s into the lane's row of the partial
-// tile (row stride = valid columns rounded up to 4).
-__device__ __forceinline__ void write_partial16(uint32_t* prow, int col0, int qvalid, const uint32_t (&v)[16]) {
+// starting at col0 of row `row`.  A partial tile is stored float4-column-
+// major: float4 (row, c4) at c4 * 128 + row, so a warp (32 consecutive rows)
+// writes 512 contiguous bytes per store.  Float4s wholly past the valid
+// columns are not written.
+__device__ __forceinline__ void write_partial16(uint32_t* tile, int row, int col0, int qvalid,
+                                                const uint32_t (&v)[16]) {
+  uint4* t4 = reinterpret_cast<uint4*>(tile);
 #pragma unroll
   for (int j = 0; j < 4; ++j)
     if (col0 + 4 * j < qvalid)
-      *reinterpret_cast<uint4*>(prow + col0 + 4 * j) = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      t4[(col0 / 4 + j) * kTileP + row] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
 }
 
 // Epilogue store of four reduced accumulators at P row p and Q columns
@@ -261,73 +265,148 @@ __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.
 // Accumulation units (one per work unit for e4m3, one per <= 1024-K chunk
 // for int8) alternate between two TMEM accumulators, so the epilogue of one
 // unit overlaps the MMAs of the next.
-// Cluster split-K, final sum of rows [r0, r0 + nvec / vpr) of a tile: each
-// epilogue thread takes B float4 vectors per pass and requests all B * S
-// partial vectors (L2: the partial tiles are `slice_stride` words apart in
-// the workspace, `base` points at row r0 of slice 0) before using any, sums
-// each in slice order 0..S-1 from zero (the order of the last-arriver
-// reduction, so both give the same bits) and stores its four outputs with
-// the staged scales.  S == 0: s_rt slices (any count up to
-// kMaxClusterSplits), one vector per pass.
+// Split-K, final sum of rows [r0, r0 + nrows) of a tile (both reductions):
+// the vector -> (row, float4 column) map.  Vectors map to threads so that a
+// warp's stores are contiguous: with swap the P rows are output columns, so
+// consecutive threads take consecutive rows (their loads are contiguous
+// too); without swap consecutive threads take consecutive columns of a row.
+template <bool SWAP>
+__device__ __forceinline__ void reduce_pos(int v, int nrows, int vpr, int& rr, int& c4) {
+  if (SWAP) {
+    rr = v % nrows;
+    c4 = v / nrows;
+  } else {
+    rr = v / vpr;
+    c4 = v - rr * vpr;
+  }
+}
+
+// Epilogue of one reduced float4 (four outputs at row r0 + rr, column c4*4).
+template <int BN, bool SWAP, bool INT8, typename OutT, typename V>
+__device__ __forceinline__ void reduce_store(const MmParams& prm, const Unit& un, int row, int c4, int qvalid,
+                                             const V (&acc)[4], const float* s_scale_p, const float* s_scale_q) {
+  const int col = c4 * 4;
+  float s_q[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) s_q[j] = s_scale_q[min(col + j, BN - 1)];
+  store4s<SWAP, OutT>(prm, un.p0 + row, un.q0 + col, qvalid - col, acc, s_scale_p[row], s_q);
+}
+
+// Each epilogue thread takes B float4 vectors per pass and requests all
+// B * S partial vectors (L2; the slices' partial tiles are `slice_stride`
+// words apart from `tile0`, float4-column-major) before using any, then sums
+// each in slice order 0..S-1 from zero -- the order of both reductions, so
+// they give the same bits -- and stores its four outputs with the staged
+// scales.
 template <int S, int B, int BN, bool SWAP, bool INT8, typename OutT>
-__device__ __forceinline__ void cluster_reduce_rows(const MmParams& prm, const Unit& un, const uint32_t* base,
-                                                    size_t slice_stride, int r0, int vpr, int nvec, int et,
-                                                    int qvalid, const float* s_scale_p, const float* s_scale_q,
-                                                    int s_rt = 0) {
-  constexpr int SS = S > 0 ? S : kMaxClusterSplits;
-  const int nsl = S > 0 ? S : s_rt;
+__device__ __forceinline__ void reduce_rows(const MmParams& prm, const Unit& un, const uint32_t* tile0,
+                                            size_t slice_stride, int r0, int nrows, int qvalid, int et,
+                                            const float* s_scale_p, const float* s_scale_q) {
+  const int vpr = (qvalid + 3) / 4;  // valid float4 columns
+  const int nvec = nrows * vpr;
   for (int v0 = et; v0 < nvec; v0 += B * kEpiThreads) {
-    uint4 x[B][SS];
+    uint4 x[B][S];
 #pragma unroll
     for (int b = 0; b < B; ++b) {
       const int v = v0 + b * kEpiThreads;
-      const int vc = v < nvec ? v : v0;  // past the end: load an in-range vector, store nothing
+      int rr, c4;
+      reduce_pos<SWAP>(v < nvec ? v : v0, nrows, vpr, rr, c4);  // past the end: an in-range load, no store
+      const size_t idx = static_cast<size_t>(c4) * kTileP + r0 + rr;
 #pragma unroll
-      for (int s2 = 0; s2 < SS; ++s2)
-        if (S > 0 || s2 < nsl)
-          x[b][s2] = __ldcg(reinterpret_cast<const uint4*>(base + s2 * slice_stride) + vc);
+      for (int s2 = 0; s2 < S; ++s2) x[b][s2] = __ldcg(reinterpret_cast<const uint4*>(tile0 + s2 * slice_stride) + idx);
     }
 #pragma unroll
     for (int b = 0; b < B; ++b) {
       const int v = v0 + b * kEpiThreads;
       if (v >= nvec) break;
-      const int rr = v / vpr;
-      const int row = r0 + rr;
-      const int col = (v - rr * vpr) * 4;
-      const float s_p = s_scale_p[row];
-      float s_q[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) s_q[j] = s_scale_q[min(col + j, BN - 1)];
+      int rr, c4;
+      reduce_pos<SWAP>(v, nrows, vpr, rr, c4);
       if (INT8) {
         int acc[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int s2 = 0; s2 < SS; ++s2)
-          if (S > 0 || s2 < nsl) {
-            acc[0] += static_cast<int>(x[b][s2].x);
-            acc[1] += static_cast<int>(x[b][s2].y);
-            acc[2] += static_cast<int>(x[b][s2].z);
-            acc[3] += static_cast<int>(x[b][s2].w);
-          }
-        store4s<SWAP, OutT>(prm, un.p0 + row, un.q0 + col, qvalid - col, acc, s_p, s_q);
+        for (int s2 = 0; s2 < S; ++s2) {
+          acc[0] += static_cast<int>(x[b][s2].x);
+          acc[1] += static_cast<int>(x[b][s2].y);
+          acc[2] += static_cast<int>(x[b][s2].z);
+          acc[3] += static_cast<int>(x[b][s2].w);
+        }
+        reduce_store<BN, SWAP, INT8, OutT>(prm, un, r0 + rr, c4, qvalid, acc, s_scale_p, s_scale_q);
       } else {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int s2 = 0; s2 < SS; ++s2)
-          if (S > 0 || s2 < nsl) {
-            acc[0] += __uint_as_float(x[b][s2].x);
-            acc[1] += __uint_as_float(x[b][s2].y);
-            acc[2] += __uint_as_float(x[b][s2].z);
-            acc[3] += __uint_as_float(x[b][s2].w);
-          }
-        store4s<SWAP, OutT>(prm, un.p0 + row, un.q0 + col, qvalid - col, acc, s_p, s_q);
+        for (int s2 = 0; s2 < S; ++s2) {
+          acc[0] += __uint_as_float(x[b][s2].x);
+          acc[1] += __uint_as_float(x[b][s2].y);
+          acc[2] += __uint_as_float(x[b][s2].z);
+          acc[3] += __uint_as_float(x[b][s2].w);
+        }
+        reduce_store<BN, SWAP, INT8, OutT>(prm, un, r0 + rr, c4, qvalid, acc, s_scale_p, s_scale_q);
       }
     }
   }
 }
 
+// Any slice count: a running sum per vector in slice order (the loop is
+// unrolled so several slices' loads are in flight).
+template <int BN, bool SWAP, bool INT8, typename OutT>
+__device__ __forceinline__ void reduce_rows_n(const MmParams& prm, const Unit& un, const uint32_t* tile0,
+                                              size_t slice_stride, int S, int r0, int nrows, int qvalid, int et,
+                                              const float* s_scale_p, const float* s_scale_q) {
+  const int vpr = (qvalid + 3) / 4;
+  const int nvec = nrows * vpr;
+  for (int v = et; v < nvec; v += kEpiThreads) {
+    int rr, c4;
+    reduce_pos<SWAP>(v, nrows, vpr, rr, c4);
+    const uint4* src = reinterpret_cast<const uint4*>(tile0) + static_cast<size_t>(c4) * kTileP + r0 + rr;
+    if (INT8) {
+      int acc[4] = {0, 0, 0, 0};
+#pragma unroll 4
+      for (int s2 = 0; s2 < S; ++s2) {
+        const uint4 x = __ldcg(src + s2 * (slice_stride / 4));
+        acc[0] += static_cast<int>(x.x);
+        acc[1] += static_cast<int>(x.y);
+        acc[2] += static_cast<int>(x.z);
+        acc[3] += static_cast<int>(x.w);
+      }
+      reduce_store<BN, SWAP, INT8, OutT>(prm, un, r0 + rr, c4, qvalid, acc, s_scale_p, s_scale_q);
+    } else {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int s2 = 0; s2 < S; ++s2) {
+        const uint4 x = __ldcg(src + s2 * (slice_stride / 4));
+        acc[0] += __uint_as_float(x.x);
+        acc[1] += __uint_as_float(x.y);
+        acc[2] += __uint_as_float(x.z);
+        acc[3] += __uint_as_float(x.w);
+      }
+      reduce_store<BN, SWAP, INT8, OutT>(prm, un, r0 + rr, c4, qvalid, acc, s_scale_p, s_scale_q);
+    }
+  }
+}
+
+// Dispatch on the slice count: 2, 4 and 8 keep every load of a pass in
+// registers (fewer vectors per pass where two CTAs share the SM's registers).
+template <int BN, bool SWAP, bool INT8, typename OutT>
+__device__ __forceinline__ void reduce_rows_any(const MmParams& prm, const Unit& un, const uint32_t* tile0,
+                                                size_t slice_stride, int S, int r0, int nrows, int qvalid, int et,
+                                                const float* s_scale_p, const float* s_scale_q);
+
 // Narrow tiles run two CTAs per SM (the dispatch sizes their shared memory
 // for that); cap their registers so that two fit (<= 168 per thread).
 __host__ __device__ constexpr int min_ctas_for(int bn, bool int8) { return (bn <= 64 || (int8 && bn <= 128)) ? 2 : 1; }
+
+template <int BN, bool SWAP, bool INT8, typename OutT>
+__device__ __forceinline__ void reduce_rows_any(const MmParams& prm, const Unit& un, const uint32_t* tile0,
+                                                size_t slice_stride, int S, int r0, int nrows, int qvalid, int et,
+                                                const float* s_scale_p, const float* s_scale_q) {
+  constexpr int kTight = min_ctas_for(BN, INT8) == 2 ? 2 : 1;
+  switch (S) {
+    case 2: reduce_rows<2, 8 / kTight, BN, SWAP, INT8, OutT>(prm, un, tile0, slice_stride, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
+    case 4: reduce_rows<4, 4 / kTight, BN, SWAP, INT8, OutT>(prm, un, tile0, slice_stride, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
+    case 8: reduce_rows<8, 2 / kTight, BN, SWAP, INT8, OutT>(prm, un, tile0, slice_stride, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
+    default: reduce_rows_n<BN, SWAP, INT8, OutT>(prm, un, tile0, slice_stride, S, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
+  }
+}
 
 template <int BN, bool SWAP, bool INT8, typename OutT>
 __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
@@ -550,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
               if (!last) {
                 tmem_st16(tot_addr + g * 16, t[bb]);
               } else if (prm.splits > 1) {
-                write_partial16(part + static_cast<size_t>(row) * qv4, g * 16, qvalid, t[bb]);
+                write_partial16(part, row, g * 16, qvalid, t[bb]);
               } else {
                 int v[16];
 #pragma unroll
@@ -566,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
             tmem_ld16(acc_addr + g * 16, r);
             tmem_ld_wait();
             if (prm.splits > 1) {
-              write_partial16(part + static_cast<size_t>(row) * qv4, g * 16, qvalid, r);
+              write_partial16(part, row, g * 16, qvalid, r);
             } else {
               float v[16];
 #pragma unroll
@@ -593,71 +672,11 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
         epi_bar_sync();
         if (s_is_last) {
           __threadfence();
-          // the 128 epilogue threads sweep the tile's partials with
-          // independent float4 loads (slice order 0..S-1 per element) and
-          // each finishes four outputs
-          const uint32_t* base = reinterpret_cast<const uint32_t*>(prm.partial) +
-                                 static_cast<size_t>(un.tile_lin) * prm.splits * tile_elems;
-          const int nvec = kTileP * qv4 / 4;
-          // slices requested per batch: fewer where two CTAs share an SM's
-          // registers
-          constexpr int kRedBatch = min_ctas_for(BN, INT8) == 2 ? 4 : 8;
-          // Each thread finishes two float4s of the tile per pass.  All
-          // loads of a pass -- the slices' partials (in batches of four
-          // or eight slices) and the scales the four outputs need -- are requested
-          // before any is used, so a pass costs about one L2 round trip; the
-          // sum runs in slice order 0..S-1.
-          for (int v0 = et; v0 < nvec; v0 += 2 * kEpiThreads) {
-            int vv[2] = {v0, v0 + kEpiThreads};
-            float sp[2], sq[2][4];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int v = vv[h] < nvec ? vv[h] : v0;
-              const int row_r = (v * 4) / qv4;
-              const int col = v * 4 - row_r * qv4;
-              sp[h] = s_scale_p[row_r];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) sq[h][j] = s_scale_q[min(col + j, BN - 1)];
-            }
-            float fa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            int ia[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
-            for (int sl0 = 0; sl0 < prm.splits; sl0 += kRedBatch) {
-              uint4 x[2][kRedBatch];
-#pragma unroll
-              for (int k = 0; k < kRedBatch; ++k)
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                  if (sl0 + k < prm.splits && vv[h] < nvec)
-                    x[h][k] = __ldcg(reinterpret_cast<const uint4*>(base + (sl0 + k) * tile_elems) + vv[h]);
-#pragma unroll
-              for (int k = 0; k < kRedBatch; ++k)
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                  if (sl0 + k < prm.splits && vv[h] < nvec) {
-                    if (INT8) {
-                      ia[h][0] += static_cast<int>(x[h][k].x);
-                      ia[h][1] += static_cast<int>(x[h][k].y);
-                      ia[h][2] += static_cast<int>(x[h][k].z);
-                      ia[h][3] += static_cast<int>(x[h][k].w);
-                    } else {
-                      fa[h][0] += __uint_as_float(x[h][k].x);
-                      fa[h][1] += __uint_as_float(x[h][k].y);
-                      fa[h][2] += __uint_as_float(x[h][k].z);
-                      fa[h][3] += __uint_as_float(x[h][k].w);
-                    }
-                  }
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              if (vv[h] >= nvec) continue;
-              const int row_r = (vv[h] * 4) / qv4;
-              const int col = vv[h] * 4 - row_r * qv4;
-              if (INT8)
-                store4s<SWAP, OutT>(prm, un.p0 + row_r, un.q0 + col, qvalid - col, ia[h], sp[h], sq[h]);
-              else
-                store4s<SWAP, OutT>(prm, un.p0 + row_r, un.q0 + col, qvalid - col, fa[h], sp[h], sq[h]);
-            }
-          }
+          // the 128 epilogue threads sum the whole tile over the slices
+          const uint32_t* tile0 = reinterpret_cast<const uint32_t*>(prm.partial) +
+                                  static_cast<size_t>(un.tile_lin) * prm.splits * tile_elems;
+          reduce_rows_any<BN, SWAP, INT8, OutT>(prm, un, tile0, tile_elems, prm.splits, 0, kTileP, qvalid, et,
+                                                s_scale_p, s_scale_q);
           if (et == 0) prm.counters[un.tile_lin] = 0u;
         }
       }
@@ -683,18 +702,11 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
       const int r0 = (rank * kTileP) / S;
       const int r1 = ((rank + 1) * kTileP) / S;
       const int qvalid = min(BN, (SWAP ? prm.M : prm.N) - un.q0);
-      const int qv4 = (qvalid + 3) & ~3;
-      const int vpr = qv4 / 4;  // float4s per row
-      const int nvec = (r1 - r0) * vpr;
       const size_t tile_elems = static_cast<size_t>(kTileP) * BN;
-      const uint32_t* base = reinterpret_cast<const uint32_t*>(prm.partial) +
-                             static_cast<size_t>(un.tile_lin) * S * tile_elems + static_cast<size_t>(r0) * qv4;
-      switch (S) {  // compile-time slice counts: every load of a pass in flight together
-        case 2: cluster_reduce_rows<2, 8, BN, SWAP, INT8, OutT>(prm, un, base, tile_elems, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q); break;
-        case 4: cluster_reduce_rows<4, 4, BN, SWAP, INT8, OutT>(prm, un, base, tile_elems, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q); break;
-        case 8: cluster_reduce_rows<8, 2, BN, SWAP, INT8, OutT>(prm, un, base, tile_elems, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q); break;
-        default: cluster_reduce_rows<0, 1, BN, SWAP, INT8, OutT>(prm, un, base, tile_elems, r0, vpr, nvec, et, qvalid, s_scale_p, s_scale_q, S); break;
-      }
+      const uint32_t* tile0 = reinterpret_cast<const uint32_t*>(prm.partial) +
+                              static_cast<size_t>(un.tile_lin) * S * tile_elems;
+      reduce_rows_any<BN, SWAP, INT8, OutT>(prm, un, tile0, tile_elems, S, r0, r1 - r0, qvalid, et, s_scale_p,
+                                            s_scale_q);
     }
     if (threadIdx.x == 2 * 32) trace_stamp(prm, T_REDUCED);
   }
