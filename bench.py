@@ -125,9 +125,10 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def traffic_for(kernel_key: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (the source hash must match)."""
+def traffic_ratio_for(kernel_key: str):
+    """DRAM bytes / algorithmic bytes of a kernel from the committed ncu
+    capture (profiles/traffic.json), if it was taken on the current kernel
+    source (the source hash must match); None otherwise."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -144,7 +145,7 @@ def traffic_for(kernel_key: str):
         return None
     if h != ent.get("source_sha256_16"):
         return None
-    return ent.get("dram_bytes_per_launch_scaled")
+    return ent.get("dram_over_algorithmic")
 
 
 def max_over_ranks(t_local: float, device=None) -> float:
@@ -233,6 +234,9 @@ class DecodeWorkload:
 
     def launches_per_step(self):
         return 2 * len(self.items)
+
+    def gemms_per_step(self):
+        return len(self.items)
 
 
 def graph_of(fn, stream):
@@ -775,7 +779,10 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "kernel": "w8a8_gemm_kernel (decode GEMMs, all 16 per step)",
                          "achieved": gemm_gbs, "peak": hbm, "unit": "GB/s", "frac": gemm_gbs / hbm,
                          "peak_kind": pk_kind + " (MEASURED_PEAKS.json hbm_gbs)" if pk_kind == "measured" else pk_kind,
-                         "traffic": traffic_for("decode_gemm"),
+                         "traffic": (None if traffic_ratio_for("decode_gemm") is None else
+                                     traffic_ratio_for("decode_gemm") * wl.gemm_bytes() / wl.gemms_per_step()),
+                         "traffic_note": "DRAM read+write bytes per launch (average decode GEMM): the ncu "
+                                         "dram/algorithmic ratio of profiles/traffic.json x algorithmic bytes",
                          "bytes_note": "algorithmic: N*K + M*K + 2*M*N + 4*(M+scales) per GEMM"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
