@@ -155,17 +155,28 @@ __device__ __forceinline__ void store16(const MmParams& prm, int lane_idx, int c
 }
 
 // Split-K partial of one TMEM lane: 16 consecutive accumulator columns
-// starting at col0 of row `row`.  A partial tile is stored float4-column-
-// major: float4 (row, c4) at c4 * 128 + row, so a warp (32 consecutive rows)
-// writes 512 contiguous bytes per store.  Float4s wholly past the valid
-// columns are not written.
+// starting at col0 of row `row`, as float4s (those wholly past the valid
+// columns are not written).  The layout of a partial tile follows the
+// output's: with swap the P rows are output columns, and the tile is
+// float4-column-major -- float4 (row, c4) at c4 * 128 + row -- so a warp (32
+// consecutive rows) writes 512 contiguous bytes per store and the final sum
+// walks down rows; without swap it is row-major -- (row, c4) at row * vpr +
+// c4, vpr = valid columns / 4 rounded up -- and the final sum walks along
+// rows, matching the output rows it stores.
+template <bool SWAP>
+__device__ __forceinline__ size_t partial_index(int row, int c4, int vpr) {
+  return SWAP ? static_cast<size_t>(c4) * kTileP + row : static_cast<size_t>(row) * vpr + c4;
+}
+
+template <bool SWAP>
 __device__ __forceinline__ void write_partial16(uint32_t* tile, int row, int col0, int qvalid,
                                                 const uint32_t (&v)[16]) {
   uint4* t4 = reinterpret_cast<uint4*>(tile);
+  const int vpr = (qvalid + 3) / 4;
 #pragma unroll
   for (int j = 0; j < 4; ++j)
     if (col0 + 4 * j < qvalid)
-      t4[(col0 / 4 + j) * kTileP + row] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      t4[partial_index<SWAP>(row, col0 / 4 + j, vpr)] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
 }
 
 // Epilogue store of four reduced accumulators at P row p and Q columns
@@ -266,10 +277,9 @@ __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.
 // for int8) alternate between two TMEM accumulators, so the epilogue of one
 // unit overlaps the MMAs of the next.
 // Split-K, final sum of rows [r0, r0 + nrows) of a tile (both reductions):
-// the vector -> (row, float4 column) map.  Vectors map to threads so that a
-// warp's stores are contiguous: with swap the P rows are output columns, so
-// consecutive threads take consecutive rows (their loads are contiguous
-// too); without swap consecutive threads take consecutive columns of a row.
+// the vector -> (row, float4 column) map that walks the partial tiles in
+// their storage order (see write_partial16), so that a warp's loads and its
+// output stores are both contiguous.
 template <bool SWAP>
 __device__ __forceinline__ void reduce_pos(int v, int nrows, int vpr, int& rr, int& c4) {
   if (SWAP) {
@@ -311,7 +321,7 @@ __device__ __forceinline__ void reduce_rows(const MmParams& prm, const Unit& un,
       const int v = v0 + b * kEpiThreads;
       int rr, c4;
       reduce_pos<SWAP>(v < nvec ? v : v0, nrows, vpr, rr, c4);  // past the end: an in-range load, no store
-      const size_t idx = static_cast<size_t>(c4) * kTileP + r0 + rr;
+      const size_t idx = partial_index<SWAP>(r0 + rr, c4, vpr);
 #pragma unroll
       for (int s2 = 0; s2 < S; ++s2) x[b][s2] = __ldcg(reinterpret_cast<const uint4*>(tile0 + s2 * slice_stride) + idx);
     }
@@ -357,7 +367,7 @@ __device__ __forceinline__ void reduce_rows_n(const MmParams& prm, const Unit& u
   for (int v = et; v < nvec; v += kEpiThreads) {
     int rr, c4;
     reduce_pos<SWAP>(v, nrows, vpr, rr, c4);
-    const uint4* src = reinterpret_cast<const uint4*>(tile0) + static_cast<size_t>(c4) * kTileP + r0 + rr;
+    const uint4* src = reinterpret_cast<const uint4*>(tile0) + partial_index<SWAP>(r0 + rr, c4, vpr);
     if (INT8) {
       int acc[4] = {0, 0, 0, 0};
 #pragma unroll 4
@@ -629,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
               if (!last) {
                 tmem_st16(tot_addr + g * 16, t[bb]);
               } else if (prm.splits > 1) {
-                write_partial16(part, row, g * 16, qvalid, t[bb]);
+                write_partial16<SWAP>(part, row, g * 16, qvalid, t[bb]);
               } else {
                 int v[16];
 #pragma unroll
@@ -645,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
             tmem_ld16(acc_addr + g * 16, r);
             tmem_ld_wait();
             if (prm.splits > 1) {
-              write_partial16(part, row, g * 16, qvalid, r);
+              write_partial16<SWAP>(part, row, g * 16, qvalid, r);
             } else {
               float v[16];
 #pragma unroll
