@@ -192,6 +192,42 @@ W8A8_API w8a8_status w8a8_scaled_mm(const void* a_q, int64_t lda, const void* b_
                            int q_dtype, int out_dtype, void* workspace,
                            size_t workspace_bytes, w8a8_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * w8a8_quant_scaled_mm -- dynamic per-token activation quantiser and scaled
+ * matmul in one call: scale_a[m] = absmax_k |x[m, k]| / 448 (e4m3) or / 127
+ * (int8), 1 for an all-zero row; A_q = sat_round(x / scale_a); then
+ * out = w8a8_scaled_mm(A_q, b_q, scale_a (per row), scale_b).  The result
+ * is bit for bit that of w8a8_scaled_quant (W8A8_PER_ROW, W8A8_DYNAMIC)
+ * followed by w8a8_scaled_mm.  ("[Kernel] Support Fp8 Checkpoints (Dynamic
+ * + Static)": dynamic per-token activation scales; "[Kernel] Add w8a8
+ * CUTLASS kernels": the scaled matmul.)
+ *
+ *  x         [M, K] BF16 or FP16 activations (x_dtype), row stride ld_x
+ *            elements (ld_x >= K).
+ *  b_q, ldb, scale_b, b_gran, out, ldc, M, N, K, q_dtype, out_dtype
+ *            as for w8a8_scaled_mm.
+ *  scale_a_out  [M] fp32, receives the per-token scales; may be NULL.
+ *  workspace   device scratch of at least
+ *            w8a8_quant_scaled_mm_workspace_size(M, N, K, q_dtype) bytes,
+ *            256-byte aligned (the quantised activations when the two
+ *            steps run separately, split-K partials).  Split-K arrival
+ *            counters live at its head: zero-fill it once before first use;
+ *            every call leaves them zero.
+ *
+ * Decode shapes (e4m3, every token in one narrow matmul tile, x 16-byte
+ * aligned with ld_x * 2 a multiple of 16, K a multiple of 16) run as ONE
+ * kernel that quantises its own activations; the rest run the quantiser into
+ * the workspace and then the matmul.  Errors as for w8a8_scaled_mm and
+ * w8a8_scaled_quant.
+ * ---------------------------------------------------------------------- */
+W8A8_API size_t w8a8_quant_scaled_mm_workspace_size(int64_t M, int64_t N, int64_t K, int q_dtype);
+
+W8A8_API w8a8_status w8a8_quant_scaled_mm(const void* x, int x_dtype, int64_t ld_x, const void* b_q,
+                                 int64_t ldb, const float* scale_b, int b_gran, void* out,
+                                 int64_t ldc, int64_t M, int64_t N, int64_t K, int q_dtype,
+                                 int out_dtype, float* scale_a_out, void* workspace,
+                                 size_t workspace_bytes, w8a8_stream_t stream);
+
 /* Kernel configuration of one scaled_mm call (tests and tuning).
  *  swap_ab   1: the weight rows N are the 128-row MMA side and the tokens M
  *            the narrow side (small-M / decode regime); 0: tokens M on the

@@ -45,6 +45,8 @@ EXPORTS = (
     "w8a8_scaled_mm_noalloc_max_scratch",
     "w8a8_scaled_mm_noalloc",
     "w8a8_debug_mm_trace",
+    "w8a8_quant_scaled_mm_workspace_size",
+    "w8a8_quant_scaled_mm",
 )
 
 
@@ -113,6 +115,10 @@ def load(build_if_needed: bool = True):
         lib.w8a8_scaled_mm_noalloc.argtypes = [P, I64, P, I64, P, I, P, I, P, I64, I64, I64, I64, I, I, P]
         lib.w8a8_debug_mm_trace.restype = I
         lib.w8a8_debug_mm_trace.argtypes = [P, SZ]
+        lib.w8a8_quant_scaled_mm_workspace_size.restype = SZ
+        lib.w8a8_quant_scaled_mm_workspace_size.argtypes = [I64, I64, I64, I]
+        lib.w8a8_quant_scaled_mm.restype = I
+        lib.w8a8_quant_scaled_mm.argtypes = [P, I, I64, P, I64, P, I, P, I64, I64, I64, I64, I, I, P, P, SZ, P]
         lib.w8a8_device_status.restype = I
         lib.w8a8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
         _lib = lib

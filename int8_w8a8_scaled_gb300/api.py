@@ -27,7 +27,7 @@ from ._lib import (BF16, DYNAMIC, E4M3, FP16, FP32, INT8, INT32, PER_ROW, PER_TE
 
 __all__ = [
     "scaled_quant", "scaled_dequant", "scaled_mm", "mm_workspace_size",
-    "quant_workspace_size", "pick_config", "device_status", "Workspace",
+    "quant_workspace_size", "pick_config", "device_status", "Workspace", "quant_scaled_mm",
     "expand_shard_scales", "requant_shards",
     "W8A8Error", "MmConfig",
 ]
@@ -230,6 +230,50 @@ def scaled_mm(a_q: torch.Tensor, b_q: torch.Tensor, scale_a: torch.Tensor, scale
         check(lib.w8a8_scaled_mm(*args, _stream(stream)))
     else:
         check(lib.w8a8_scaled_mm_with_config(*args, ctypes.byref(c), _stream(stream)))
+    return out
+
+
+def quant_scaled_mm(x: torch.Tensor, b_q: torch.Tensor, scale_b: torch.Tensor, out: torch.Tensor,
+                    scale_a_out: torch.Tensor | None = None, workspace: torch.Tensor | Workspace | None = None,
+                    stream=None) -> torch.Tensor:
+    """Dynamic per-token quantisation of x and the scaled matmul in one call:
+    the bits of ``scaled_quant(x, ..., per_token=True, dynamic=True)``
+    followed by ``scaled_mm``.
+
+    x: [M, K] bf16 / fp16, rows contiguous.  b_q: [N, K] e4m3 / int8 (the
+    operand type).  scale_b: [N] or [1] fp32.  out: [M, N] bf16 / fp16 (or
+    float32 with e4m3 weights).  scale_a_out: optional [M] fp32 that receives
+    the per-token scales.  Decode shapes run as one kernel.
+    """
+    _cuda(x, b_q, scale_b, out)
+    lib = _lib.load()
+    M, K = x.shape
+    N, K2 = b_q.shape
+    if K != K2:
+        raise ValueError("x is [M, K] and b_q is [N, K]: K must match")
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out must be [M, N]")
+    if scale_b.dtype != torch.float32 or not scale_b.is_contiguous():
+        raise ValueError("scale_b must be a contiguous float32 tensor")
+    b_gran = PER_ROW if scale_b.numel() == N and N > 1 else PER_TENSOR
+    if b_gran == PER_TENSOR and scale_b.numel() != 1:
+        raise ValueError("scale_b must have 1 or N elements")
+    if scale_a_out is not None:
+        _cuda(scale_a_out)
+        if scale_a_out.dtype != torch.float32 or scale_a_out.numel() != M or not scale_a_out.is_contiguous():
+            raise ValueError("scale_a_out must be a contiguous float32 tensor of M elements")
+    qk = _qkind(b_q)
+    need = lib.w8a8_quant_scaled_mm_workspace_size(M, N, K, qk)
+    if isinstance(workspace, Workspace):
+        workspace = workspace.ensure(need).buf
+    elif workspace is None and need:
+        workspace = _default_workspace(x.device, need, "mm").buf
+    ws_ptr = _ptr(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(lib.w8a8_quant_scaled_mm(_ptr(x), _fkind(x), _ld(x), _ptr(b_q), _ld(b_q), _ptr(scale_b), b_gran,
+                                   _ptr(out), _ld(out), M, N, K, qk, _fkind(out, wide=True),
+                                   _ptr(scale_a_out) if scale_a_out is not None else None, ws_ptr, ws_bytes,
+                                   _stream(stream)))
     return out
 
 

@@ -323,11 +323,32 @@ w8a8_status validate_mm(const void* a_q, long long lda, const void* b_q, long lo
   return W8A8_OK;
 }
 
+// Activations the matmul quantises itself (dynamic per token, e4m3).
+struct FusedAct {
+  const void* x;
+  long long ld_x;
+  int x_fp16;
+  float* scale_out;
+};
+
+// Whether the decode matmul can quantise its own activations under `cfg`:
+// e4m3, swap-AB with every token in one tile, and K slices that one CTA or
+// one cluster covers (the per-token absmax needs the whole row).
+bool fused_quant_ok(const w8a8_mm_config& cfg, long long M, long long K, int q_dtype) {
+  if (q_dtype != W8A8_E4M3 || !cfg.swap_ab || cfg.block_n > 64 || M > cfg.block_n || K % 16 != 0) return false;
+  return cfg.split_k == 1 || (cfg.split_k <= kMaxClusterSplit && cfg.reduce != W8A8_REDUCE_GLOBAL);
+}
+
 w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ldb, const float* sa, int a_gran,
                    const float* sb, int b_gran, void* out, long long ldc, long long M, long long N, long long K,
                    int q_dtype, int out_dtype, void* ws, size_t ws_bytes, const w8a8_mm_config* user_cfg,
-                   cudaStream_t stream) {
-  w8a8_status st = validate_mm(a_q, lda, b_q, ldb, sa, a_gran, sb, b_gran, out, ldc, M, N, K, q_dtype, out_dtype);
+                   cudaStream_t stream, const FusedAct* fa = nullptr) {
+  // with fused activations the A operand is x (validated by the caller): give
+  // the operand checks a stand-in that passes them
+  static const uint4 kAligned = {};
+  w8a8_status st = validate_mm(fa ? static_cast<const void*>(&kAligned) : a_q, fa ? K : lda, b_q, ldb,
+                               fa ? reinterpret_cast<const float*>(&kAligned) : sa, fa ? W8A8_PER_ROW : a_gran, sb,
+                               b_gran, out, ldc, M, N, K, q_dtype, out_dtype);
   if (st != W8A8_OK) return st;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != W8A8_OK) return st;
@@ -342,6 +363,8 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
     auto_config(M, N, K, q_dtype, dev.sms, &cfg);
   }
   if ((st = validate_config(cfg, q_dtype, dev.smem_optin)) != W8A8_OK) return st;
+  if (fa && !fused_quant_ok(cfg, M, K, q_dtype))
+    return fail(W8A8_ERR_UNSUPPORTED, "this configuration cannot quantise the activations inside the matmul");
   const Plan plan = make_plan(M, N, K, q_dtype, cfg, dev.smem_optin);
   if (plan.splits > 1 && !plan.cluster && static_cast<size_t>(plan.tiles_p) * plan.tiles_q > kCounterSlots)
     return fail(W8A8_ERR_UNSUPPORTED, "split_k > 1 supports at most %zu output tiles (got %d)", kCounterSlots,
@@ -379,7 +402,7 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
   const long long p_ld = cfg.swap_ab ? ldb_b : lda_b;
   const long long q_ld = cfg.swap_ab ? lda_b : ldb_b;
   if ((st = make_operand_map(&tp, p_base, i8, p_rows, K, p_ld, 128)) != W8A8_OK) return st;
-  if ((st = make_operand_map(&tq, q_base, i8, q_rows, K, q_ld, cfg.block_n)) != W8A8_OK) return st;
+  if (!fa && (st = make_operand_map(&tq, q_base, i8, q_rows, K, q_ld, cfg.block_n)) != W8A8_OK) return st;
 
   MmParams prm{};
   prm.M = static_cast<int>(M);
@@ -411,8 +434,17 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
   prm.trace = g_trace_buf.load();
   prm.trace_ctas = g_trace_ctas.load();
   const int out_kind = out_dtype == W8A8_BF16 ? OUT_BF16 : out_dtype == W8A8_FP16 ? OUT_FP16 : OUT_RAW;
-  e = i8 ? launch_int8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream)
-         : launch_fp8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream);
+  if (fa) {
+    prm.scale_a = nullptr;
+    prm.x = fa->x;
+    prm.ld_x = fa->ld_x;
+    prm.x_fp16 = fa->x_fp16;
+    prm.scale_a_out = fa->scale_out;
+    e = launch_fused_quant_gemm(tp, prm, cfg.block_n, out_kind, plan.stages, stream);
+  } else {
+    e = i8 ? launch_int8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream)
+           : launch_fp8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "scaled_mm kernel launch");
   return ok();
 }
@@ -548,6 +580,60 @@ w8a8_status w8a8_scaled_mm(const void* a_q, int64_t lda, const void* b_q, int64_
                            size_t workspace_bytes, w8a8_stream_t stream) {
   return run_mm(a_q, lda, b_q, ldb, scale_a, a_gran, scale_b, b_gran, out, ldc, M, N, K, q_dtype, out_dtype,
                 workspace, workspace_bytes, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Activation quantiser + scaled matmul in one call.  The decode shapes (e4m3,
+// every token in one narrow tile) run as one kernel that quantises its own
+// activations; the rest run the quantiser into the workspace, then the
+// matmul.  Both give the bits of w8a8_scaled_quant (dynamic, per row)
+// followed by w8a8_scaled_mm.
+size_t w8a8_quant_scaled_mm_workspace_size(int64_t M, int64_t N, int64_t K, int q_dtype) {
+  if (M < 1 || N < 1 || K < 1) return 0;
+  const size_t mm = w8a8_scaled_mm_workspace_size(M, N, K, q_dtype);
+  const size_t ldq = static_cast<size_t>((K + 15) & ~15LL);
+  const size_t two_step = align256(static_cast<size_t>(M) * ldq) + align256(static_cast<size_t>(M) * 4) + mm;
+  return std::max(mm, two_step);
+}
+
+w8a8_status w8a8_quant_scaled_mm(const void* x, int x_dtype, int64_t ld_x, const void* b_q, int64_t ldb,
+                                 const float* scale_b, int b_gran, void* out, int64_t ldc, int64_t M, int64_t N,
+                                 int64_t K, int q_dtype, int out_dtype, float* scale_a_out, void* workspace,
+                                 size_t workspace_bytes, w8a8_stream_t stream) {
+  if (!x) return fail(W8A8_ERR_INVALID_ARG, "null pointer argument");
+  if (x_dtype != W8A8_BF16 && x_dtype != W8A8_FP16) return fail(W8A8_ERR_INVALID_ARG, "x_dtype must be BF16 or FP16");
+  if (M < 1 || N < 1 || K < 1) return fail(W8A8_ERR_INVALID_ARG, "M, N, K must be >= 1 (got %lld, %lld, %lld)",
+                                           static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K));
+  if (ld_x < K) return fail(W8A8_ERR_INVALID_ARG, "ld_x must be >= K");
+  if (!aligned(x, 2) || (scale_a_out && !aligned(scale_a_out, 4))) return fail(W8A8_ERR_MISALIGNED, "x or scale_a_out misaligned");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (q_dtype == W8A8_E4M3 && aligned(x, 16) && (ld_x * 2) % 16 == 0) {
+    DeviceInfo dev;
+    w8a8_status s0 = device_info(&dev);
+    if (s0 != W8A8_OK) return s0;
+    w8a8_mm_config cfg;
+    auto_config(M, N, K, q_dtype, dev.sms, &cfg);
+    if (fused_quant_ok(cfg, M, K, q_dtype)) {
+      const FusedAct fa{x, static_cast<long long>(ld_x), x_dtype == W8A8_FP16 ? 1 : 0, scale_a_out};
+      return run_mm(nullptr, K, b_q, ldb, nullptr, W8A8_PER_ROW, scale_b, b_gran, out, ldc, M, N, K, q_dtype,
+                    out_dtype, workspace, workspace_bytes, &cfg, st, &fa);
+    }
+  }
+  // two steps: codes (rows padded to 16 bytes) and per-token scales into the
+  // workspace, then the matmul
+  const long long ldq = (K + 15) & ~15LL;
+  const size_t a_bytes = align256(static_cast<size_t>(M) * static_cast<size_t>(ldq));
+  const size_t s_bytes = align256(static_cast<size_t>(M) * 4);
+  if (!workspace || workspace_bytes < a_bytes + s_bytes)
+    return fail(W8A8_ERR_WORKSPACE, "this problem needs %zu bytes of workspace",
+                w8a8_quant_scaled_mm_workspace_size(M, N, K, q_dtype));
+  if (!aligned(workspace, 256)) return fail(W8A8_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  float* sa = scale_a_out ? scale_a_out : reinterpret_cast<float*>(wsb + a_bytes);
+  w8a8_status s1 = w8a8_scaled_quant(x, x_dtype, M, K, ld_x, wsb, q_dtype, ldq, sa, W8A8_PER_ROW, W8A8_DYNAMIC,
+                                     nullptr, 0, stream);
+  if (s1 != W8A8_OK) return s1;
+  return run_mm(wsb, ldq, b_q, ldb, sa, W8A8_PER_ROW, scale_b, b_gran, out, ldc, M, N, K, q_dtype, out_dtype,
+                wsb + a_bytes + s_bytes, workspace_bytes - a_bytes - s_bytes, nullptr, st);
 }
 
 w8a8_status w8a8_scaled_mm_with_config(const void* a_q, int64_t lda, const void* b_q, int64_t ldb,

@@ -38,6 +38,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "quant_math.cuh"
 #include "sm103_ptx.cuh"
 
 namespace w8a8 {
@@ -401,6 +402,151 @@ __device__ __forceinline__ void reduce_rows_any(const MmParams& prm, const Unit&
                                                 size_t slice_stride, int S, int r0, int nrows, int qvalid, int et,
                                                 const float* s_scale_p, const float* s_scale_q);
 
+// ---------------------------------------------------------------- fused activation quantiser
+// The decode matmul that quantises its own activations (swap-AB, e4m3, all
+// M tokens in one tile).  The per-token dynamic scale is absmax / 448 over
+// the token's whole row and every code is the quantiser's own arithmetic
+// (quant_math.cuh), so the result equals the two calls quantiser + scaled
+// matmul bit for bit ("[Kernel] Support Fp8 Checkpoints (Dynamic + Static)",
+// dynamic per-token activation scales).  The epilogue warps, idle during the
+// main loop, compute the scales and then fill the token slot of each stage
+// with codes in the layout a 128-byte-swizzled TMA load would have written,
+// while TMA streams the weights into the other slot.
+
+// 16 consecutive x[m, k..k+15] (16-byte aligned: ld_x and K multiples of 16)
+__device__ __forceinline__ void fq_load16(const MmParams& prm, int m, int k, uint4& a, uint4& b) {
+  const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(prm.x) +
+                                                  static_cast<size_t>(m) * prm.ld_x + k);
+  a = p[0];
+  b = p[1];
+}
+
+template <int XK>
+__device__ __forceinline__ float fq_absmax16(const uint4& a, const uint4& b) {
+  float f[8], g[8];
+  unpack8<XK>(a, f);
+  unpack8<XK>(b, g);
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m = fmaxf(m, fmaxf(fabsf(f[j]), fabsf(g[j])));
+  return m;
+}
+
+template <int XK>
+__device__ __forceinline__ uint4 fq_quant16(const uint4& a, const uint4& b, float s, float y, bool ok) {
+  float f[8], g[8];
+  unpack8<XK>(a, f);
+  unpack8<XK>(b, g);
+  uint4 o;
+  o.x = enc4<0>(div_by(f[0], s, y, ok), div_by(f[1], s, y, ok), div_by(f[2], s, y, ok), div_by(f[3], s, y, ok));
+  o.y = enc4<0>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
+  o.z = enc4<0>(div_by(g[0], s, y, ok), div_by(g[1], s, y, ok), div_by(g[2], s, y, ok), div_by(g[3], s, y, ok));
+  o.w = enc4<0>(div_by(g[4], s, y, ok), div_by(g[5], s, y, ok), div_by(g[6], s, y, ok), div_by(g[7], s, y, ok));
+  return o;
+}
+
+// Per-token scales of the CTA's token tile (rows 0..M-1), by the 128
+// epilogue threads: absmax over this CTA's K range, combined over the
+// cluster's K slices (each CTA arrives on every peer's `amax_bar` and reads
+// the peers' partial maxima from distributed shared memory: BN words each),
+// then scale = absmax / 448 (1 for an all-zero row).  The reciprocal and its
+// validity feed the correctly rounded quotient (div_by).  False if a wait
+// timed out.
+template <int BN>
+__device__ bool fq_token_scales(const MmParams& prm, const Unit& un, bool cl, int et, uint32_t amax_bar,
+                                uint32_t* s_amax, float* s_tok, float* s_rcp, int* s_rok) {
+  const int M = prm.M;
+  const int k_lo = un.kb_begin * 128;
+  const int k_hi = min(prm.K, (un.kb_begin + un.nkb) * 128);
+  const int n16 = (k_hi - k_lo) / 16;
+  const int total = M * n16;
+  for (int m = et; m < BN; m += kEpiThreads) s_amax[m] = 0u;
+  epi_bar_sync();
+  for (int base = et; base < total; base += 4 * kEpiThreads) {
+    uint4 a[4], b[4];
+    int mm[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int idx = base + j * kEpiThreads;
+      mm[j] = -1;
+      if (idx < total) {
+        const int m = idx / n16;
+        mm[j] = m;
+        fq_load16(prm, m, k_lo + (idx - m * n16) * 16, a[j], b[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (mm[j] >= 0) {
+        const float v = prm.x_fp16 ? fq_absmax16<1>(a[j], b[j]) : fq_absmax16<0>(a[j], b[j]);
+        atomicMax(s_amax + mm[j], __float_as_uint(v));  // non-negative floats order as their bits
+      }
+  }
+  epi_bar_sync();
+  bool ok = true;
+  if (cl) {
+    if (et == 0) {
+      fence_acq_rel_cluster();
+      for (int r = 0; r < prm.splits; ++r) mbar_arrive_remote(mapa_shared(amax_bar, static_cast<uint32_t>(r)));
+    }
+    ok = mbar_wait_cluster(amax_bar, 0);
+  }
+  for (int m = et; m < BN; m += kEpiThreads) {
+    float s = 1.f;
+    if (m < M) {
+      uint32_t bits = s_amax[m];
+      if (cl) {
+        bits = 0u;
+        for (int r = 0; r < prm.splits; ++r)
+          bits = max(bits, ld_dsmem_u32(mapa_shared(smem_addr(s_amax + m), static_cast<uint32_t>(r))));
+      }
+      s = scale_from_amax<0>(__uint_as_float(bits));
+    }
+    float y;
+    s_rok[m] = recip_ok(s, &y) ? 1 : 0;
+    s_tok[m] = s;
+    s_rcp[m] = y;
+  }
+  epi_bar_sync();
+  if (prm.scale_a_out && (cl ? (cluster_ctarank() == 0 && cluster_id_x() == 0) : blockIdx.x == 0))
+    for (int m = et; m < M; m += kEpiThreads) prm.scale_a_out[m] = s_tok[m];
+  return ok;
+}
+
+// One warp fills the token slot of a stage (K block kb, BN rows x 128 codes,
+// 128-byte swizzle: 16-byte chunk c of row r at r * 128 + (c ^ (r & 7)) * 16)
+// with codes; rows >= M and columns >= K are zero.
+template <int BN>
+__device__ __forceinline__ void fq_fill_stage(const MmParams& prm, int kb, uint8_t* dst, const float* s_tok,
+                                              const float* s_rcp, const int* s_rok, int lane) {
+  constexpr int kPer = BN * 8 / 32;  // 16-code chunks per lane: 4 (BN 16) .. 16 (BN 64)
+  constexpr int kBatch = kPer < 8 ? kPer : 8;
+  const int k0 = kb * 128;
+#pragma unroll
+  for (int j0 = 0; j0 < kPer; j0 += kBatch) {
+    uint4 a[kBatch], b[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int ch = lane + 32 * (j0 + j);
+      const int r = ch >> 3;
+      const int k = k0 + (ch & 7) * 16;
+      if (r < prm.M && k < prm.K) fq_load16(prm, r, k, a[j], b[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int ch = lane + 32 * (j0 + j);
+      const int r = ch >> 3;
+      const int c = ch & 7;
+      const int k = k0 + c * 16;
+      uint4 q = make_uint4(0u, 0u, 0u, 0u);
+      if (r < prm.M && k < prm.K)
+        q = prm.x_fp16 ? fq_quant16<1>(a[j], b[j], s_tok[r], s_rcp[r], s_rok[r] != 0)
+                       : fq_quant16<0>(a[j], b[j], s_tok[r], s_rcp[r], s_rok[r] != 0);
+      *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = q;
+    }
+  }
+}
+
 // Narrow tiles run two CTAs per SM (the dispatch sizes their shared memory
 // for that); cap their registers so that two fit (<= 168 per thread).
 __host__ __device__ constexpr int min_ctas_for(int bn, bool int8) { return (bn <= 64 || (int8 && bn <= 128)) ? 2 : 1; }
@@ -418,7 +564,7 @@ __device__ __forceinline__ void reduce_rows_any(const MmParams& prm, const Unit&
   }
 }
 
-template <int BN, bool SWAP, bool INT8, typename OutT>
+template <int BN, bool SWAP, bool INT8, typename OutT, bool FQ = false>
 __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
     w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_p,
                      const __grid_constant__ CUtensorMap tmap_q, const MmParams prm, int stages,
@@ -431,6 +577,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   constexpr int kGroups = BN / 16;
   static_assert((INT8 ? acc_bufs(INT8) + 1 : acc_bufs(INT8)) * BN <= kTmemCols && kTmemCols <= 512,
                 "accumulators must fit the TMEM allocation");
+  static_assert(!FQ || (SWAP && !INT8 && BN <= 64), "the fused quantiser is the swap-AB e4m3 decode path");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -438,9 +585,14 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   uint8_t* sp = smem;
   uint8_t* sq = smem + stages * kPBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sq + stages * kQBytes);
-  // bars: full[stages], empty[stages], unit_full[2], unit_empty[2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 4);
+  // bars: full[stages], empty[stages], unit_full[2], unit_empty[2], amax
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 5);
   __shared__ int s_is_last;
+  // fused quantiser: per-token partial absmax (float bits), scales, reciprocals
+  __shared__ uint32_t s_amax[FQ ? BN : 1];
+  __shared__ float s_tok[FQ ? BN : 1];
+  __shared__ float s_rcp[FQ ? BN : 1];
+  __shared__ int s_rok[FQ ? BN : 1];
   __shared__ float s_scale_p[kTileP];  // the unit's P-side row scales
   __shared__ float s_scale_q[BN];      // the unit's Q-side column scales
 
@@ -473,14 +625,17 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   auto empty_bar = [&](int s) { return smem_addr(bars + stages + s); };
   auto ufull_bar = [&](int b) { return smem_addr(bars + 2 * stages + b); };
   auto uempty_bar = [&](int b) { return smem_addr(bars + 2 * stages + 2 + b); };
+  const uint32_t amax_bar = smem_addr(bars + 2 * stages + 4);
 
   if (threadIdx.x == 0) {
     prefetch_tensormap(&tmap_p);
     prefetch_tensormap(&tmap_q);
     for (int s = 0; s < stages; ++s) {
-      mbar_init(full_bar(s), 1);
+      // fused quantiser: the weights' TMA and the warp writing the codes
+      mbar_init(full_bar(s), FQ ? 2 : 1);
       mbar_init(empty_bar(s), 1);
     }
+    if (FQ) mbar_init(amax_bar, cl ? prm.splits : 1);
     mbar_init(ufull_bar(0), 1);
     mbar_init(ufull_bar(1), 1);
     mbar_init(uempty_bar(0), kEpiThreads);
@@ -495,6 +650,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the cluster's peers arrive on amax_bar: its initialisation must be
+  // visible to them first
+  if (FQ && cl) cluster_sync();
   if (threadIdx.x == 0) trace_stamp(prm, T_PROLOGUE);
   // Let the next kernel be scheduled (after this CTA holds its TMEM, so a
   // later kernel never takes TMEM ahead of an earlier one), then wait for the
@@ -513,10 +671,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
           const int s = it % stages;
           const uint32_t ph = (it / stages) & 1;
           if (!mbar_wait(empty_bar(s), ph ^ 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+          mbar_arrive_expect_tx(full_bar(s), FQ ? kPBytes : kStageBytes);
           const int kx = (un.kb_begin + i) * kKbElems;
           tma_load_2d(smem_addr(sp + s * kPBytes), &tmap_p, full_bar(s), kx, un.p0);
-          tma_load_2d(smem_addr(sq + s * kQBytes), &tmap_q, full_bar(s), kx, un.q0);
+          if (!FQ) tma_load_2d(smem_addr(sq + s * kQBytes), &tmap_q, full_bar(s), kx, un.q0);
         }
       }
     }
@@ -569,9 +727,29 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     const size_t tile_elems = static_cast<size_t>(kTileP) * BN;
     uint32_t u = 0;
+    uint32_t ait = 0;  // fused quantiser: stage iterations so far (the producer's count)
     bool ok = true;
+    if constexpr (FQ) {
+      // every unit of this CTA has the same tokens (one token tile) and the
+      // same K range (one slice per CTA, or the whole K)
+      if (w_first < units) ok = fq_token_scales<BN>(prm, unit_of(w_first, prm, group, BN), cl, et, amax_bar, s_amax,
+                                                      s_tok, s_rcp, s_rok);
+    }
     for (int w = w_first; w < units && ok; w += w_step) {
       const Unit un = unit_of(w, prm, group, BN);
+      if constexpr (FQ) {
+        // warp `quarter` writes the token codes of K blocks quarter, +4, ...
+        for (int i = quarter; i < un.nkb; i += 4) {
+          const uint32_t itg = ait + static_cast<uint32_t>(i);
+          const int s = static_cast<int>(itg % stages);
+          if (!mbar_wait(empty_bar(s), ((itg / stages) & 1) ^ 1)) { ok = false; break; }
+          fq_fill_stage<BN>(prm, un.kb_begin + i, sq + s * kQBytes, s_tok, s_rcp, s_rok, lane);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full_bar(s));
+        }
+        ait += static_cast<uint32_t>(un.nkb);
+      }
       const int chunk = INT8 ? prm.kchunk_kb : un.nkb;
       const int nch = (un.nkb + chunk - 1) / chunk;
       const int lane_idx = un.p0 + row;  // global P row of this thread
@@ -592,7 +770,11 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
         const int qp = SWAP ? prm.a_per_row : prm.b_per_row;
         const int qlim = SWAP ? prm.M : prm.N;
         s_scale_p[et] = pp ? __ldg(ps + min(un.p0 + et, plim - 1)) : __ldg(ps);
-        for (int i = et; i < BN; i += kEpiThreads) s_scale_q[i] = qp ? __ldg(qs + min(un.q0 + i, qlim - 1)) : __ldg(qs);
+        if constexpr (FQ) {
+          for (int i = et; i < BN; i += kEpiThreads) s_scale_q[i] = s_tok[i];  // the tokens' own scales
+        } else {
+          for (int i = et; i < BN; i += kEpiThreads) s_scale_q[i] = qp ? __ldg(qs + min(un.q0 + i, qlim - 1)) : __ldg(qs);
+        }
       }
       epi_bar_sync();
       const float s_lane = s_scale_p[row];
@@ -735,10 +917,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   }
 }
 
-template <int BN, bool SWAP, bool INT8, typename OutT>
+template <int BN, bool SWAP, bool INT8, typename OutT, bool FQ = false>
 cudaError_t launch_one(const CUtensorMap& tp, const CUtensorMap& tq, const MmParams& p, int stages,
                        cudaStream_t stream) {
-  auto kern = w8a8_gemm_kernel<BN, SWAP, INT8, OutT>;
+  auto kern = w8a8_gemm_kernel<BN, SWAP, INT8, OutT, FQ>;
   const int smem = gemm_smem_bytes(BN, stages);
   // the attribute is per function and device; setting it again is harmless
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -843,6 +1025,16 @@ cudaError_t dispatch(const CUtensorMap& tp, const CUtensorMap& tq, const MmParam
   }
 }
 
+template <int BN>
+cudaError_t launch_fq(const CUtensorMap& tp, const MmParams& p, int out_kind, int stages, cudaStream_t stream) {
+  switch (out_kind) {
+    case OUT_BF16: return launch_one<BN, true, false, __nv_bfloat16, true>(tp, tp, p, stages, stream);
+    case OUT_FP16: return launch_one<BN, true, false, __half, true>(tp, tp, p, stages, stream);
+    case OUT_RAW: return launch_one<BN, true, false, float, true>(tp, tp, p, stages, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 // int8 [rows, K] (leading dim ld) -> f16 [rows, K] contiguous, exact.
 __global__ void widen_int8_kernel(const int8_t* __restrict__ src, long long ld, int rows, int K,
                                   __half* __restrict__ dst) {
@@ -883,6 +1075,16 @@ int max_stages_for(int block_n, int smem_budget) {
 cudaError_t launch_fp8_gemm(const CUtensorMap& tmap_p, const CUtensorMap& tmap_q, const MmParams& p,
                             int block_n, bool swap, int out_kind, int stages, cudaStream_t stream) {
   return dispatch<false>(tmap_p, tmap_q, p, block_n, swap, out_kind, stages, stream);
+}
+
+cudaError_t launch_fused_quant_gemm(const CUtensorMap& tmap_p, const MmParams& p, int block_n, int out_kind,
+                                    int stages, cudaStream_t stream) {
+  switch (block_n) {
+    case 16: return launch_fq<16>(tmap_p, p, out_kind, stages, stream);
+    case 32: return launch_fq<32>(tmap_p, p, out_kind, stages, stream);
+    case 64: return launch_fq<64>(tmap_p, p, out_kind, stages, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_int8_gemm(const CUtensorMap& tmap_p, const CUtensorMap& tmap_q, const MmParams& p,

@@ -36,6 +36,12 @@ struct MmParams {
   int pdl;               // launch with programmatic stream serialisation
   int prefetch_kb;       // weight K blocks of the first unit prefetched into L2 early
   int max_ctas_per_sm;   // 0: as many as fit; else cap the persistent grid per SM
+  // fused activation quantiser (swap-AB e4m3 decode, one token tile): the
+  // kernel quantises x itself (scale_a is then unused)
+  const void* x;         // [M, K] bf16 / fp16 activations
+  long long ld_x;        // row stride of x in elements
+  int x_fp16;            // 1: x is fp16, 0: bf16
+  float* scale_a_out;    // [M] per-token scales the kernel computed (nullable)
   unsigned long long* trace;  // debug: per-CTA phase stamps (null = off)
   int trace_ctas;             // CTAs the trace buffer has room for
 };
@@ -59,6 +65,10 @@ cudaError_t launch_fp8_gemm(const CUtensorMap& tmap_p, const CUtensorMap& tmap_q
 // accumulator is exact; each chunk is drained into an int32 total.
 cudaError_t launch_int8_widen(const void* src, long long ld_src, int rows, int K,
                               void* dst_f16, cudaStream_t stream);
+// The decode matmul that quantises its own activations (prm.x); tmap_p maps
+// the weights (swap-AB).  block_n 16 / 32 / 64, e4m3 weights.
+cudaError_t launch_fused_quant_gemm(const CUtensorMap& tmap_p, const MmParams& p, int block_n, int out_kind,
+                                    int stages, cudaStream_t stream);
 cudaError_t launch_int8_gemm(const CUtensorMap& tmap_p, const CUtensorMap& tmap_q,
                              const MmParams& p, int block_n, bool swap, int out_kind,
                              int stages, cudaStream_t stream);

@@ -94,6 +94,58 @@ __device__ __forceinline__ uint32_t cluster_id_x() {
   return r;
 }
 
+// The shared::cluster address of the variable at CTA-local shared address
+// `addr` in the cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// 4-byte load from distributed shared memory (any CTA of the cluster).
+__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Arrive on an mbarrier of any CTA of the cluster (shared::cluster address),
+// releasing this thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+// Bounded wait on a local mbarrier phase, acquiring at cluster scope what the
+// (possibly remote) arrivals released.  False (and the device status flag)
+// after W8A8_WAIT_NS.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((++spins & 255u) == 0 && global_timer_ns() - t0 > W8A8_WAIT_NS) {
+      atomicOr(&g_device_status, 1);
+      return false;
+    }
+  }
+}
+
+// Order this thread's generic-proxy writes to shared memory before later
+// async-proxy (tensor core) reads of them.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Cluster-wide barrier over every thread of every CTA in the cluster: the
 // release/acquire pair (cluster scope) makes each CTA's memory writes before
 // the barrier visible to the other CTAs' reads after it.  Like __syncthreads it
