@@ -196,8 +196,14 @@ class DecodeWorkload:
                 cfg = None
                 if override:
                     cfg = dict(w8.pick_config(M, N, K, w8.E4M3), **override)
-                self.items.append({"M": M, "name": name, "x": x, "aq": aq, "sa": sa, "out": out, "cfg": cfg})
-                ws_need = max(ws_need, w8.mm_workspace_size(M, N, K, w8.E4M3, cfg))
+                auto = w8.pick_config(M, N, K, w8.E4M3)
+                # quantiser + matmul (the automatic route of quant_scaled_mm;
+                # `fused` items would run its one-kernel route)
+                fused = False
+                self.items.append({"M": M, "name": name, "x": x, "aq": aq, "sa": sa, "out": out, "cfg": cfg,
+                                   "fused": fused})
+                ws_need = max(ws_need, w8.mm_workspace_size(M, N, K, w8.E4M3, cfg),
+                              w8._lib.load().w8a8_quant_scaled_mm_workspace_size(M, N, K, w8.E4M3))
         self.ws = w8.Workspace(ws_need, dev)
         torch.cuda.synchronize()
 
@@ -205,35 +211,50 @@ class DecodeWorkload:
         return sum(2.0 * it["M"] * self.weights[it["name"]][2] * self.weights[it["name"]][3] for it in self.items)
 
     def gemm_bytes(self):
-        # algorithmic: 1-byte operands once, 16-bit output, fp32 scales
+        # algorithmic bytes of the matmul kernels: 1-byte weights once, the
+        # activations once (16-bit x where the kernel quantises them itself,
+        # 1-byte codes otherwise), 16-bit output, fp32 scales
         tot = 0
         for it in self.items:
             _, sw, N, K = self.weights[it["name"]]
             M = it["M"]
-            tot += N * K + M * K + 2 * M * N + 4 * (M + sw.numel())
+            tot += N * K + (2 if it["fused"] else 1) * M * K + 2 * M * N + 4 * (M + sw.numel())
         return tot
 
     def quant_bytes(self):
-        # 2 B read + 1 B write per element, 4 B scale per row
-        return sum(it["M"] * it["x"].shape[1] * 3 + 4 * it["M"] for it in self.items)
+        # the separate quantiser kernels: 2 B read + 1 B write per element, 4 B scale per row
+        return sum(it["M"] * it["x"].shape[1] * 3 + 4 * it["M"] for it in self.items if not it["fused"])
 
     def run_quant(self):
         for it in self.items:
-            self.w8.scaled_quant(it["x"], it["aq"], it["sa"], per_token=True, dynamic=True)
+            if not it["fused"]:
+                self.w8.scaled_quant(it["x"], it["aq"], it["sa"], per_token=True, dynamic=True)
+
+    def _fused(self, it):
+        wq, sw, _, _ = self.weights[it["name"]]
+        self.w8.quant_scaled_mm(it["x"], wq, sw, it["out"], scale_a_out=it["sa"], workspace=self.ws)
 
     def run_gemm(self):
+        # the matmul kernels of a step (those that quantise their own
+        # activations included); the others read codes quantised beforehand
         for it in self.items:
             wq, sw, _, _ = self.weights[it["name"]]
-            self.w8.scaled_mm(it["aq"], wq, it["sa"], sw, it["out"], workspace=self.ws, config=it["cfg"])
+            if it["fused"]:
+                self._fused(it)
+            else:
+                self.w8.scaled_mm(it["aq"], wq, it["sa"], sw, it["out"], workspace=self.ws, config=it["cfg"])
 
     def run_step(self):
         for it in self.items:
             wq, sw, _, _ = self.weights[it["name"]]
-            self.w8.scaled_quant(it["x"], it["aq"], it["sa"], per_token=True, dynamic=True)
-            self.w8.scaled_mm(it["aq"], wq, it["sa"], sw, it["out"], workspace=self.ws, config=it["cfg"])
+            if it["fused"]:
+                self._fused(it)
+            else:
+                self.w8.scaled_quant(it["x"], it["aq"], it["sa"], per_token=True, dynamic=True)
+                self.w8.scaled_mm(it["aq"], wq, it["sa"], sw, it["out"], workspace=self.ws, config=it["cfg"])
 
     def launches_per_step(self):
-        return 2 * len(self.items)
+        return sum(1 if it["fused"] else 2 for it in self.items)
 
     def gemms_per_step(self):
         return len(self.items)
@@ -754,6 +775,7 @@ def run_ours(args):
         "gemm_us_per_step": t_gemm * 1e6, "quant_us_per_step": t_quant * 1e6,
         "gemm_gbs": gemm_gbs, "gemm_frac_hbm": gemm_gbs / hbm,
         "quant_gbs": quant_gbs, "quant_frac_hbm": quant_gbs / hbm,
+        "fused_quant": [f"M{it['M']}_{it['name']}" for it in wl.items if it["fused"]],
         "configs": {f"M{it['M']}_{it['name']}": w8.pick_config(it["M"], *wl.weights[it["name"]][2:4][::1],
                                                                w8.E4M3) for it in wl.items},
     }
@@ -774,16 +796,20 @@ def run_ours(args):
                                    "per-tensor scale]/O[4096x4096]/gate-up[28672x4096]/down[4096x14336]; "
                                    "dynamic per-token act, per-channel weight e4m3, bf16 out",
                        "l2": "inputs larger than L2 (218 MB of weights per step vs 129 MB L2)",
-                       "graph": "one CUDA graph per step (32 kernels)",
+                       "graph": f"one CUDA graph per step ({wl.launches_per_step()} kernels: "
+                                f"{sum(1 for it in wl.items if it['fused'])} matmuls that quantise their own "
+                                f"activations, the rest quantiser + matmul)",
                        "parallelism": "replicas" if ws_n > 1 else "single GPU"},
-            "roofline": {"bound": "hbm", "kernel": "w8a8_gemm_kernel (decode GEMMs, all 16 per step)",
+            "roofline": {"bound": "hbm", "kernel": "w8a8_gemm_kernel (the 16 decode matmuls of a step, "
+                                                   "activation quantisation fused where it runs inside them)",
                          "achieved": gemm_gbs, "peak": hbm, "unit": "GB/s", "frac": gemm_gbs / hbm,
                          "peak_kind": pk_kind + " (MEASURED_PEAKS.json hbm_gbs)" if pk_kind == "measured" else pk_kind,
                          "traffic": (None if traffic_ratio_for("decode_gemm") is None else
                                      traffic_ratio_for("decode_gemm") * wl.gemm_bytes() / wl.gemms_per_step()),
                          "traffic_note": "DRAM read+write bytes per launch (average decode GEMM): the ncu "
                                          "dram/algorithmic ratio of profiles/traffic.json x algorithmic bytes",
-                         "bytes_note": "algorithmic: N*K + M*K + 2*M*N + 4*(M+scales) per GEMM"},
+                         "bytes_note": "algorithmic: N*K + M*K*(2 where the kernel quantises bf16 x itself, "
+                                       "else 1) + 2*M*N + 4*(M+scales) per matmul"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": wl.launches_per_step() * args.steps,

@@ -207,6 +207,10 @@ W8A8_API w8a8_status w8a8_scaled_mm(const void* a_q, int64_t lda, const void* b_
  *  b_q, ldb, scale_b, b_gran, out, ldc, M, N, K, q_dtype, out_dtype
  *            as for w8a8_scaled_mm.
  *  scale_a_out  [M] fp32, receives the per-token scales; may be NULL.
+ *  route     W8A8_ROUTE_AUTO: one kernel where it pays (below), else two
+ *            steps; W8A8_ROUTE_ONE_KERNEL: one kernel, W8A8_ERR_UNSUPPORTED
+ *            where it cannot run; W8A8_ROUTE_TWO_STEP: quantiser, then
+ *            matmul.
  *  workspace   device scratch of at least
  *            w8a8_quant_scaled_mm_workspace_size(M, N, K, q_dtype) bytes,
  *            256-byte aligned (the quantised activations when the two
@@ -214,18 +218,23 @@ W8A8_API w8a8_status w8a8_scaled_mm(const void* a_q, int64_t lda, const void* b_
  *            counters live at its head: zero-fill it once before first use;
  *            every call leaves them zero.
  *
- * Decode shapes (e4m3, every token in one narrow matmul tile, x 16-byte
- * aligned with ld_x * 2 a multiple of 16, K a multiple of 16) run as ONE
- * kernel that quantises its own activations; the rest run the quantiser into
- * the workspace and then the matmul.  Errors as for w8a8_scaled_mm and
+ * The one-kernel route (e4m3, every token in one narrow matmul tile, x 16-byte
+ * aligned with ld_x * 2 a multiple of 16, K a multiple of 16) quantises the
+ * activations inside the matmul.  The two-step route runs the quantiser into
+ * the workspace and then the matmul; AUTO takes it (measured faster on
+ * GB300 at every decode shape).  Errors as for w8a8_scaled_mm and
  * w8a8_scaled_quant.
  * ---------------------------------------------------------------------- */
+#define W8A8_ROUTE_AUTO 0
+#define W8A8_ROUTE_ONE_KERNEL 1
+#define W8A8_ROUTE_TWO_STEP 2
+
 W8A8_API size_t w8a8_quant_scaled_mm_workspace_size(int64_t M, int64_t N, int64_t K, int q_dtype);
 
 W8A8_API w8a8_status w8a8_quant_scaled_mm(const void* x, int x_dtype, int64_t ld_x, const void* b_q,
                                  int64_t ldb, const float* scale_b, int b_gran, void* out,
                                  int64_t ldc, int64_t M, int64_t N, int64_t K, int q_dtype,
-                                 int out_dtype, float* scale_a_out, void* workspace,
+                                 int out_dtype, float* scale_a_out, int route, void* workspace,
                                  size_t workspace_bytes, w8a8_stream_t stream);
 
 /* Kernel configuration of one scaled_mm call (tests and tuning).

@@ -16,6 +16,7 @@ E4M3, INT8, BF16, FP16, FP32, INT32 = 0, 1, 2, 3, 4, 5
 PER_TENSOR, PER_ROW = 0, 1
 DYNAMIC, STATIC = 0, 1
 REDUCE_AUTO, REDUCE_GLOBAL, REDUCE_CLUSTER = 0, 1, 2
+ROUTES = {"auto": 0, "one_kernel": 1, "two_step": 2}
 
 STATUS_NAMES = {
     0: "W8A8_OK",
@@ -118,7 +119,7 @@ def load(build_if_needed: bool = True):
         lib.w8a8_quant_scaled_mm_workspace_size.restype = SZ
         lib.w8a8_quant_scaled_mm_workspace_size.argtypes = [I64, I64, I64, I]
         lib.w8a8_quant_scaled_mm.restype = I
-        lib.w8a8_quant_scaled_mm.argtypes = [P, I, I64, P, I64, P, I, P, I64, I64, I64, I64, I, I, P, P, SZ, P]
+        lib.w8a8_quant_scaled_mm.argtypes = [P, I, I64, P, I64, P, I, P, I64, I64, I64, I64, I, I, P, I, P, SZ, P]
         lib.w8a8_device_status.restype = I
         lib.w8a8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
         _lib = lib

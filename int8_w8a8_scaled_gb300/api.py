@@ -235,7 +235,7 @@ def scaled_mm(a_q: torch.Tensor, b_q: torch.Tensor, scale_a: torch.Tensor, scale
 
 def quant_scaled_mm(x: torch.Tensor, b_q: torch.Tensor, scale_b: torch.Tensor, out: torch.Tensor,
                     scale_a_out: torch.Tensor | None = None, workspace: torch.Tensor | Workspace | None = None,
-                    stream=None) -> torch.Tensor:
+                    route: str = "auto", stream=None) -> torch.Tensor:
     """Dynamic per-token quantisation of x and the scaled matmul in one call:
     the bits of ``scaled_quant(x, ..., per_token=True, dynamic=True)``
     followed by ``scaled_mm``.
@@ -243,7 +243,8 @@ def quant_scaled_mm(x: torch.Tensor, b_q: torch.Tensor, scale_b: torch.Tensor, o
     x: [M, K] bf16 / fp16, rows contiguous.  b_q: [N, K] e4m3 / int8 (the
     operand type).  scale_b: [N] or [1] fp32.  out: [M, N] bf16 / fp16 (or
     float32 with e4m3 weights).  scale_a_out: optional [M] fp32 that receives
-    the per-token scales.  Decode shapes run as one kernel.
+    the per-token scales.  route: "auto", "one_kernel" (the matmul
+    quantises its own activations; decode shapes only) or "two_step".
     """
     _cuda(x, b_q, scale_b, out)
     lib = _lib.load()
@@ -272,8 +273,8 @@ def quant_scaled_mm(x: torch.Tensor, b_q: torch.Tensor, scale_b: torch.Tensor, o
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     check(lib.w8a8_quant_scaled_mm(_ptr(x), _fkind(x), _ld(x), _ptr(b_q), _ld(b_q), _ptr(scale_b), b_gran,
                                    _ptr(out), _ld(out), M, N, K, qk, _fkind(out, wide=True),
-                                   _ptr(scale_a_out) if scale_a_out is not None else None, ws_ptr, ws_bytes,
-                                   _stream(stream)))
+                                   _ptr(scale_a_out) if scale_a_out is not None else None,
+                                   _lib.ROUTES[route], ws_ptr, ws_bytes, _stream(stream)))
     return out
 
 

@@ -339,6 +339,17 @@ bool fused_quant_ok(const w8a8_mm_config& cfg, long long M, long long K, int q_d
   return cfg.split_k == 1 || (cfg.split_k <= kMaxClusterSplit && cfg.reduce != W8A8_REDUCE_GLOBAL);
 }
 
+// Whether w8a8_quant_scaled_mm's automatic route takes the one-kernel path.
+// Measured on GB300 in the Llama-3-8B decode step, the one kernel is slower
+// than quantiser + matmul even at M = 1: it removes the quantiser's launch
+// and kernel boundary (2-4 us) but its own start -- the token scales (with a
+// cluster exchange under split-K) and the first token stage written by the
+// epilogue warps -- costs 4.6-9 us from the dependency release to the first
+// MMA, against 1.5-2.3 us for a matmul whose codes arrive by TMA.  So the
+// automatic route is the two-step one; the one-kernel route is there on
+// request (W8A8_ROUTE_ONE_KERNEL).
+bool fused_quant_preferred(const w8a8_mm_config&, long long, long long, int) { return false; }
+
 w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ldb, const float* sa, int a_gran,
                    const float* sb, int b_gran, void* out, long long ldc, long long M, long long N, long long K,
                    int q_dtype, int out_dtype, void* ws, size_t ws_bytes, const w8a8_mm_config* user_cfg,
@@ -597,22 +608,29 @@ size_t w8a8_quant_scaled_mm_workspace_size(int64_t M, int64_t N, int64_t K, int 
 
 w8a8_status w8a8_quant_scaled_mm(const void* x, int x_dtype, int64_t ld_x, const void* b_q, int64_t ldb,
                                  const float* scale_b, int b_gran, void* out, int64_t ldc, int64_t M, int64_t N,
-                                 int64_t K, int q_dtype, int out_dtype, float* scale_a_out, void* workspace,
-                                 size_t workspace_bytes, w8a8_stream_t stream) {
+                                 int64_t K, int q_dtype, int out_dtype, float* scale_a_out, int route,
+                                 void* workspace, size_t workspace_bytes, w8a8_stream_t stream) {
   if (!x) return fail(W8A8_ERR_INVALID_ARG, "null pointer argument");
   if (x_dtype != W8A8_BF16 && x_dtype != W8A8_FP16) return fail(W8A8_ERR_INVALID_ARG, "x_dtype must be BF16 or FP16");
   if (M < 1 || N < 1 || K < 1) return fail(W8A8_ERR_INVALID_ARG, "M, N, K must be >= 1 (got %lld, %lld, %lld)",
                                            static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K));
   if (ld_x < K) return fail(W8A8_ERR_INVALID_ARG, "ld_x must be >= K");
   if (!aligned(x, 2) || (scale_a_out && !aligned(scale_a_out, 4))) return fail(W8A8_ERR_MISALIGNED, "x or scale_a_out misaligned");
+  if (route != W8A8_ROUTE_AUTO && route != W8A8_ROUTE_ONE_KERNEL && route != W8A8_ROUTE_TWO_STEP)
+    return fail(W8A8_ERR_INVALID_ARG, "route must be W8A8_ROUTE_AUTO, _ONE_KERNEL or _TWO_STEP");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (q_dtype == W8A8_E4M3 && aligned(x, 16) && (ld_x * 2) % 16 == 0) {
+  if (route != W8A8_ROUTE_TWO_STEP) {
     DeviceInfo dev;
     w8a8_status s0 = device_info(&dev);
     if (s0 != W8A8_OK) return s0;
     w8a8_mm_config cfg;
     auto_config(M, N, K, q_dtype, dev.sms, &cfg);
-    if (fused_quant_ok(cfg, M, K, q_dtype)) {
+    const bool possible = q_dtype == W8A8_E4M3 && aligned(x, 16) && (ld_x * 2) % 16 == 0 &&
+                          fused_quant_ok(cfg, M, K, q_dtype);
+    if (route == W8A8_ROUTE_ONE_KERNEL && !possible)
+      return fail(W8A8_ERR_UNSUPPORTED,
+                  "the one-kernel route needs e4m3, M <= 64 in one token tile, K %% 16 == 0 and 16-byte aligned x rows");
+    if (possible && (route == W8A8_ROUTE_ONE_KERNEL || fused_quant_preferred(cfg, M, K, q_dtype))) {
       const FusedAct fa{x, static_cast<long long>(ld_x), x_dtype == W8A8_FP16 ? 1 : 0, scale_a_out};
       return run_mm(nullptr, K, b_q, ldb, nullptr, W8A8_PER_ROW, scale_b, b_gran, out, ldc, M, N, K, q_dtype,
                     out_dtype, workspace, workspace_bytes, &cfg, st, &fa);

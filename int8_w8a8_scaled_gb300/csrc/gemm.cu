@@ -615,6 +615,15 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   // weight stream starts while the preceding kernel is still running.
   if (threadIdx.x == 0 && w_first < units) {
     const Unit un = unit_of(w_first, prm, group, BN);
+    if constexpr (FQ) {
+      // the activations this CTA quantises go first: once the weight stream
+      // fills the HBM queues, a read behind it waits microseconds
+      const int k_lo = un.kb_begin * 128;
+      const int k_hi = min(prm.K, (un.kb_begin + un.nkb) * 128);
+      for (int m = 0; m < prm.M; ++m)
+        bulk_prefetch_l2(static_cast<const uint16_t*>(prm.x) + static_cast<size_t>(m) * prm.ld_x + k_lo,
+                         static_cast<uint32_t>((k_hi - k_lo) * 2));
+    }
     const CUtensorMap* wmap = SWAP ? &tmap_p : &tmap_q;
     const int w_row = SWAP ? un.p0 : un.q0;
     const int n_pf = min(un.nkb, prm.prefetch_kb);

@@ -55,7 +55,7 @@ def test_fused_equals_two_calls_and_oracle(shape, x_dtype):
     for out_dtype in (torch.bfloat16, torch.float32):
         out = torch.empty(M, N, dtype=out_dtype, device="cuda")
         sa_out = torch.empty(M, dtype=torch.float32, device="cuda")
-        w8.quant_scaled_mm(xg, b_g, sb_g, out, scale_a_out=sa_out)
+        w8.quant_scaled_mm(xg, b_g, sb_g, out, scale_a_out=sa_out, route="one_kernel")
         ref_out, ref_sa = two_step(xg, b_g, sb_g, out_dtype, M, N)
         torch.cuda.synchronize()
         assert torch.equal(sa_out, ref_sa)
@@ -84,7 +84,7 @@ def test_fused_per_tensor_weight_scale_and_special_rows():
     sb_g = torch.from_numpy(sb).cuda()
     out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     sa_out = torch.empty(M, dtype=torch.float32, device="cuda")
-    w8.quant_scaled_mm(xg, b_g, sb_g, out, scale_a_out=sa_out)
+    w8.quant_scaled_mm(xg, b_g, sb_g, out, scale_a_out=sa_out, route="one_kernel")
     ref_out, ref_sa = two_step(xg, b_g, sb_g, torch.bfloat16, M, N)
     torch.cuda.synchronize()
     assert torch.equal(sa_out, ref_sa) and sa_out[2].item() == 1.0
@@ -112,7 +112,7 @@ def test_two_step_route(case):
     od = torch.bfloat16 if qd == oracle.E4M3 else torch.float16
     out = torch.empty(M, N, dtype=od, device="cuda")
     sa_out = torch.empty(M, dtype=torch.float32, device="cuda")
-    w8.quant_scaled_mm(xg, b_g, sb_g, out, scale_a_out=sa_out)
+    w8.quant_scaled_mm(xg, b_g, sb_g, out, scale_a_out=sa_out)   # auto: the two-step route here
     aq = torch.empty(M, K, dtype=torch.float8_e4m3fn if qd == oracle.E4M3 else torch.int8, device="cuda")
     sa = torch.empty(M, dtype=torch.float32, device="cuda")
     w8.scaled_quant(xg, aq, sa, per_token=True, dynamic=True)
@@ -138,11 +138,11 @@ def test_fused_in_cuda_graph_back_to_back():
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         for xg, b_g, sb_g, out in items:      # warm-up (lazy initialisation outside capture)
-            w8.quant_scaled_mm(xg, b_g, sb_g, out, workspace=ws, stream=s)
+            w8.quant_scaled_mm(xg, b_g, sb_g, out, workspace=ws, route="one_kernel", stream=s)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             for xg, b_g, sb_g, out in items:
-                w8.quant_scaled_mm(xg, b_g, sb_g, out, workspace=ws, stream=s)
+                w8.quant_scaled_mm(xg, b_g, sb_g, out, workspace=ws, route="one_kernel", stream=s)
     for out in (it[3] for it in items):
         out.zero_()
     g.replay()
@@ -153,3 +153,25 @@ def test_fused_in_cuda_graph_back_to_back():
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     assert w8.device_status() == 0
+
+
+def test_route_one_kernel_refused_where_it_cannot_run():
+    M, N, K = 100, 512, 1024      # tokens span more than one narrow tile
+    xg, _, _, B, sb = problem(M, N, K, seed=21)
+    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(w8.W8A8Error):
+        w8.quant_scaled_mm(xg, to_gpu_codes(B, oracle.E4M3), torch.from_numpy(sb).cuda(), out, route="one_kernel")
+
+
+@pytest.mark.parametrize("shape", [(1, 6144, 4096), (16, 4096, 4096)], ids=lambda s: "x".join(map(str, s)))
+def test_auto_route_equals_both_routes(shape):
+    M, N, K = shape
+    xg, _, _, B, sb = problem(M, N, K, seed=31)
+    b_g, sb_g = to_gpu_codes(B, oracle.E4M3), torch.from_numpy(sb).cuda()
+    outs = {}
+    for route in ("auto", "one_kernel", "two_step"):
+        outs[route] = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        w8.quant_scaled_mm(xg, b_g, sb_g, outs[route], route=route)
+    torch.cuda.synchronize()
+    assert torch.equal(outs["auto"].view(torch.int16), outs["one_kernel"].view(torch.int16))
+    assert torch.equal(outs["auto"].view(torch.int16), outs["two_step"].view(torch.int16))
