@@ -142,7 +142,10 @@ int num_kb(long long K, int q_dtype) { return static_cast<int>(ceil_div(K, q_dty
 // `bench.py --sweep-decode / --sweep-large` on GB300:
 //  - M <= 64: weights on the 128-row MMA side (swap), block_n the smallest of
 //    16 / 32 / 64 that holds all M tokens -- one token tile, so every weight
-//    byte crosses L2 once, and two CTAs resident per SM;
+//    byte crosses L2 once, and two CTAs resident per SM -- except for
+//    32 < M <= 64 with enough weight tiles to fill the GPU unsplit (the
+//    gate-up projection), where tokens on the 128-row side win (22.8 us
+//    against 25.5 us at M = 64);
 //  - M > 64: tokens on the 128-row side, the widest block_n in {256, 128, 64}
 //    that still gives >= 0.6 tiles per SM;
 //  - split-K: the largest power of two of K slices that fits one wave of
@@ -168,7 +171,8 @@ int resident_per_sm(int block_n, int q_dtype) {
 
 void auto_config(long long M, long long N, long long K, int q_dtype, int sms, w8a8_mm_config* c) {
   const int kb = num_kb(K, q_dtype);
-  if (M <= 64) {
+  const long long slots2 = 2LL * sms;  // resident narrow-tile CTAs
+  if (M <= 64 && !(M > 32 && ceil_div(N, 128) * 2 >= slots2)) {
     // all tokens in one narrow tile: the weights stream through L2 once
     c->swap_ab = 1;
     c->block_n = M <= 16 ? 16 : M <= 32 ? 32 : 64;
@@ -209,7 +213,8 @@ void auto_config(long long M, long long N, long long K, int q_dtype, int sms, w8
   // few token tiles and a long K (the decode down projection, K = 14336 at
   // M = 256): the widest tile split over K beats narrow tiles, which re-read
   // every activation K block once per 64 output columns (sweep: 25.4 us for
-  // 256 x 4 slices against 30.1 us for 64 x 2)
+  // 256 x 4 slices against 30.1 us for 64 x 2; in the decode step it also
+  // beat all 256 tokens in one swap-AB tile, 28.2 against 31.4 us)
   if (!c->swap_ab && q_dtype == W8A8_E4M3 && M <= 256 && K >= 8192) c->block_n = 256;
   const long long tiles = c->swap_ab ? ceil_div(N, 128) * ceil_div(M, c->block_n)
                                      : ceil_div(M, 128) * ceil_div(N, c->block_n);

@@ -555,11 +555,14 @@ template <int BN, bool SWAP, bool INT8, typename OutT>
 __device__ __forceinline__ void reduce_rows_any(const MmParams& prm, const Unit& un, const uint32_t* tile0,
                                                 size_t slice_stride, int S, int r0, int nrows, int qvalid, int et,
                                                 const float* s_scale_p, const float* s_scale_q) {
-  constexpr int kTight = min_ctas_for(BN, INT8) == 2 ? 2 : 1;
+  // loads per pass: 16 (one CTA per SM) or 8 (two share the registers);
+  // 32 measured slower (the decode M = 256 down projection's reduction took
+  // 11 us instead of 8)
+  constexpr int kLoads = min_ctas_for(BN, INT8) == 2 ? 8 : 16;
   switch (S) {
-    case 2: reduce_rows<2, 8 / kTight, BN, SWAP, INT8, OutT>(prm, un, tile0, slice_stride, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
-    case 4: reduce_rows<4, 4 / kTight, BN, SWAP, INT8, OutT>(prm, un, tile0, slice_stride, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
-    case 8: reduce_rows<8, 2 / kTight, BN, SWAP, INT8, OutT>(prm, un, tile0, slice_stride, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
+    case 2: reduce_rows<2, kLoads / 2, BN, SWAP, INT8, OutT>(prm, un, tile0, slice_stride, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
+    case 4: reduce_rows<4, kLoads / 4, BN, SWAP, INT8, OutT>(prm, un, tile0, slice_stride, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
+    case 8: reduce_rows<8, kLoads / 8, BN, SWAP, INT8, OutT>(prm, un, tile0, slice_stride, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
     default: reduce_rows_n<BN, SWAP, INT8, OutT>(prm, un, tile0, slice_stride, S, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
   }
 }
@@ -960,7 +963,17 @@ cudaError_t launch_one(const CUtensorMap& tp, const CUtensorMap& tq, const MmPar
   // persistent grid; with a cluster split one CTA per unit (clusters of
   // `splits` consecutive CTAs)
   const int grid = cl ? units : max(1, min(units, p.num_sms * occ));
-  const int group = SWAP ? 1 : 8;
+  // Rasterisation: groups of `group` P tiles, Q tiles fastest within a group
+  // (tile_coords).  Without swap the P side is the tokens: a group holds as
+  // many 128-row token slabs as fit in 48 MB of L2, so they stay resident
+  // while the weights stream past once per group (prefill: all 32 M tiles in
+  // one group, the weights read once; int8 at M = 8192: 24 M tiles).  With
+  // swap the P side is the weights, streamed once anyway.
+  const long long slab = static_cast<long long>(kTileP) * p.K * (INT8 ? 2 : 1);
+  long long g_tiles = (48LL << 20) / slab;
+  if (g_tiles > p.tiles_p) g_tiles = p.tiles_p;
+  if (g_tiles < 1) g_tiles = 1;
+  const int group = SWAP ? 1 : static_cast<int>(g_tiles);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

@@ -80,6 +80,7 @@ FP8_CONFIGS = [
     {"swap_ab": 1, "block_n": 16, "split_k": 7, "reduce": w8.REDUCE_CLUSTER},
     {"swap_ab": 0, "block_n": 256, "split_k": 2, "stages": 2, "reduce": w8.REDUCE_CLUSTER},
     {"swap_ab": 0, "block_n": 128, "split_k": 4, "reduce": w8.REDUCE_CLUSTER},
+    {"swap_ab": 1, "block_n": 256, "split_k": 4},
 ]
 
 
@@ -393,8 +394,9 @@ def test_back_to_back_graph_of_gemms_with_overlap():
     (oracle.E4M3, (16, 4096, 14336), {"swap_ab": 1, "block_n": 32}),
     (oracle.E4M3, (50, 1000, 3008), {"swap_ab": 1, "block_n": 32}),
     (oracle.E4M3, (256, 4096, 4096), {"swap_ab": 0, "block_n": 64}),
+    (oracle.E4M3, (256, 4096, 14336), {"swap_ab": 1, "block_n": 256}),
     (oracle.INT8, (7, 2048, 4096), {"swap_ab": 1, "block_n": 16}),
-], ids=["M1_qkv", "M16_down", "ragged", "M256_o", "int8_M7"])
+], ids=["M1_qkv", "M16_down", "ragged", "M256_o", "M256_down_swap", "int8_M7"])
 @pytest.mark.parametrize("splits", [2, 3, 6, 8])
 def test_cluster_and_global_reductions_agree_bitwise(qd, shape, base, splits):
     """Both reductions start from zero and add the slices in the order
