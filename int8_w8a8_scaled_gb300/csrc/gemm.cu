@@ -215,6 +215,19 @@ __device__ __forceinline__ void store4s(const MmParams& prm, int p, int q, int n
                                         const float (&s_q)[4]) {
   OutT* out = reinterpret_cast<OutT*>(prm.out);
   if (p >= (SWAP ? prm.N : prm.M)) return;
+  if (!SWAP && nvalid >= 4 && prm.out_vec_ok) {
+    // four consecutive outputs of one row in one store (q is a multiple of
+    // 4 and the rows are 16-byte aligned)
+    alignas(16) OutT o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = OutConv<OutT>::conv(v[j], s_p, s_q[j]);
+    OutT* dst = out + static_cast<long long>(p) * prm.ldc + q;
+    if (sizeof(OutT) == 2)
+      *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(o);
+    else
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
+    return;
+  }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     if (j < nvalid) {
