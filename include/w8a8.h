@@ -366,7 +366,9 @@ W8A8_API w8a8_status w8a8_scaled_mm_noalloc(const void* a_q, int64_t lda, const 
  * stage landed [3], when its last MMA was issued [4], when its epilogue
  * finished [5], at exit [6], its SM id [7], and for its last unit: when the
  * accumulator was complete [8] and drained [9], and with a cluster split,
- * after the cluster barrier [10] and its share of the reduction [11]; unused
+ * after the cluster barrier [10] and its share of the reduction [11]; in a
+ * matmul that quantises its own activations, when the token maxima [12],
+ * the token scales [13] and the first token stage [14] were ready; unused
  * words are left as they were.  Each launch overwrites the buffer.  NULL turns tracing off (the
  * default).  Not for production use: concurrent launches share the buffer. */
 W8A8_API w8a8_status w8a8_debug_mm_trace(void* buf, size_t bytes);

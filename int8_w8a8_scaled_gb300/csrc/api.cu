@@ -126,6 +126,7 @@ w8a8_status make_operand_map(CUtensorMap* map, const void* base, bool f16, long 
 
 constexpr int kSmemTwoPerSm = 113 * 1024;   // budget that lets two CTAs share an SM
 constexpr int kInt8ChunkK = 1024;           // exact fp32 accumulation bound: 1024 * 128 * 128 = 2^24
+constexpr long long kFusedRowsMaxBytes = 32768;  // one-kernel quant_scaled_mm: rows staged in shared memory
 
 bool valid_block_n(int bn, int q_dtype, int swap_ab) {
   if (bn == 16 || bn == 32 || bn == 64 || bn == 128) return true;
@@ -456,7 +457,20 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
     prm.ld_x = fa->ld_x;
     prm.x_fp16 = fa->x_fp16;
     prm.scale_a_out = fa->scale_out;
-    e = launch_fused_quant_gemm(tp, prm, cfg.block_n, out_kind, plan.stages, stream);
+    // rows mode: the tokens' whole rows (<= 32 KB) go to shared memory once,
+    // at the cost of stages where the budget requires it
+    int stages = plan.stages;
+    const long long x_bytes = M * K * 2;
+    if (x_bytes <= kFusedRowsMaxBytes) {
+      const int budget = resident_per_sm(cfg.block_n, q_dtype) == 2 ? kSmemTwoPerSm : dev.smem_optin;
+      const int stage_bytes = gemm_smem_bytes(cfg.block_n, 2) - gemm_smem_bytes(cfg.block_n, 1);
+      const int fit = (budget - static_cast<int>(x_bytes) - gemm_smem_bytes(cfg.block_n, 0)) / stage_bytes;
+      if (fit >= 2) {
+        prm.fq_rows = 1;
+        stages = std::min(stages, fit);
+      }
+    }
+    e = launch_fused_quant_gemm(tp, prm, cfg.block_n, out_kind, stages, stream);
   } else {
     e = i8 ? launch_int8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream)
            : launch_fp8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream);

@@ -52,6 +52,7 @@ constexpr int kMaxClusterSplits = kMaxClusterSplit;  // split_k limit of the clu
 constexpr int kTileP = 128;       // rows of the P operand per tile (MMA M)
 constexpr int kRowBytes = 128;    // bytes of K per stage row (one swizzle row)
 constexpr int kPBytes = kTileP * kRowBytes;
+constexpr int kBarBlockBytes = 256;  // mbarriers and the TMEM slot after the stage ring
 
 // e4m3: accumulation units alternate between two fp32 accumulators (columns
 // 0 and bn) so the epilogue of one unit overlaps the next unit's MMAs.
@@ -265,7 +266,7 @@ __device__ __forceinline__ Unit unit_of(int w, const MmParams& prm, int group, i
 constexpr int kTraceSlots = 16;
 enum TraceSlot {
   T_START = 0, T_PROLOGUE, T_DEP_RELEASED, T_FIRST_DATA, T_MMA_ISSUED, T_EPI_DONE, T_END, T_SMID,
-  T_ACC_READY, T_DRAINED, T_SYNCED, T_REDUCED
+  T_ACC_READY, T_DRAINED, T_SYNCED, T_REDUCED, T_FQ_AMAX, T_FQ_SCALES, T_FQ_STAGE0
 };
 
 __device__ __forceinline__ void trace_stamp(const MmParams& prm, int slot) {
@@ -496,6 +497,7 @@ __device__ bool fq_token_scales(const MmParams& prm, const Unit& un, bool cl, in
       }
   }
   epi_bar_sync();
+  if (et == 0) trace_stamp(prm, T_FQ_AMAX);
   bool ok = true;
   if (cl) {
     if (et == 0) {
@@ -521,6 +523,7 @@ __device__ bool fq_token_scales(const MmParams& prm, const Unit& un, bool cl, in
     s_rcp[m] = y;
   }
   epi_bar_sync();
+  if (et == 0) trace_stamp(prm, T_FQ_SCALES);
   if (prm.scale_a_out && (cl ? (cluster_ctarank() == 0 && cluster_id_x() == 0) : blockIdx.x == 0))
     for (int m = et; m < M; m += kEpiThreads) prm.scale_a_out[m] = s_tok[m];
   return ok;
@@ -557,6 +560,80 @@ __device__ __forceinline__ void fq_fill_stage(const MmParams& prm, int kb, uint8
                        : fq_quant16<0>(a[j], b[j], s_tok[r], s_rcp[r], s_rok[r] != 0);
       *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = q;
     }
+  }
+}
+
+// Single-token decode variant of the token scales: the CTA's tokens' whole
+// rows sit in shared memory (xs, row stride K elements, one bulk copy per
+// row after the dependency wait), so the absmax is the full row's -- no
+// exchange between the K slices of a cluster -- and the token stages are
+// written from shared memory.  One global round trip in all.
+template <int BN>
+__device__ bool fq_token_scales_rows(const MmParams& prm, int et, uint32_t x_bar, const uint16_t* xs,
+                                     uint32_t* s_amax, float* s_tok, float* s_rcp, int* s_rok) {
+  const int M = prm.M;
+  const int n16 = prm.K / 16;
+  const int total = M * n16;
+  for (int m = et; m < BN; m += kEpiThreads) s_amax[m] = 0u;
+  if (et == 0) {
+    mbar_arrive_expect_tx(x_bar, static_cast<uint32_t>(M * prm.K * 2));
+    for (int m = 0; m < M; ++m)
+      bulk_load(smem_addr(xs + static_cast<size_t>(m) * prm.K),
+                static_cast<const uint16_t*>(prm.x) + static_cast<size_t>(m) * prm.ld_x,
+                static_cast<uint32_t>(prm.K * 2), x_bar);
+  }
+  epi_bar_sync();
+  if (!mbar_wait(x_bar, 0)) return false;
+  if (et == 0) trace_stamp(prm, T_FQ_AMAX);
+  float mx = 0.f;
+  int cur = -1;
+  for (int idx = et; idx < total; idx += kEpiThreads) {
+    const int m = idx / n16;
+    const uint4* p = reinterpret_cast<const uint4*>(xs + static_cast<size_t>(m) * prm.K + (idx - m * n16) * 16);
+    const float v = prm.x_fp16 ? fq_absmax16<1>(p[0], p[1]) : fq_absmax16<0>(p[0], p[1]);
+    if (m != cur) {
+      if (cur >= 0) atomicMax(s_amax + cur, __float_as_uint(mx));
+      cur = m;
+      mx = 0.f;
+    }
+    mx = fmaxf(mx, v);
+  }
+  if (cur >= 0) atomicMax(s_amax + cur, __float_as_uint(mx));
+  epi_bar_sync();
+  for (int m = et; m < BN; m += kEpiThreads) {
+    const float s = m < M ? scale_from_amax<0>(__uint_as_float(s_amax[m])) : 1.f;
+    float y;
+    s_rok[m] = recip_ok(s, &y) ? 1 : 0;
+    s_tok[m] = s;
+    s_rcp[m] = y;
+  }
+  epi_bar_sync();
+  if (et == 0) trace_stamp(prm, T_FQ_SCALES);
+  if (prm.scale_a_out && (prm.cluster ? (cluster_ctarank() == 0 && cluster_id_x() == 0) : blockIdx.x == 0))
+    for (int m = et; m < M; m += kEpiThreads) prm.scale_a_out[m] = s_tok[m];
+  return true;
+}
+
+// fq_fill_stage with the tokens' rows in shared memory.
+template <int BN>
+__device__ __forceinline__ void fq_fill_stage_rows(const MmParams& prm, int kb, uint8_t* dst, const uint16_t* xs,
+                                                   const float* s_tok, const float* s_rcp, const int* s_rok,
+                                                   int lane) {
+  constexpr int kPer = BN * 8 / 32;
+  const int k0 = kb * 128;
+#pragma unroll 4
+  for (int j = 0; j < kPer; ++j) {
+    const int ch = lane + 32 * j;
+    const int r = ch >> 3;
+    const int c = ch & 7;
+    const int k = k0 + c * 16;
+    uint4 q = make_uint4(0u, 0u, 0u, 0u);
+    if (r < prm.M && k < prm.K) {
+      const uint4* p = reinterpret_cast<const uint4*>(xs + static_cast<size_t>(r) * prm.K + k);
+      q = prm.x_fp16 ? fq_quant16<1>(p[0], p[1], s_tok[r], s_rcp[r], s_rok[r] != 0)
+                     : fq_quant16<0>(p[0], p[1], s_tok[r], s_rcp[r], s_rok[r] != 0);
+    }
+    *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = q;
   }
 }
 
@@ -601,8 +678,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   uint8_t* sp = smem;
   uint8_t* sq = smem + stages * kPBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sq + stages * kQBytes);
-  // bars: full[stages], empty[stages], unit_full[2], unit_empty[2], amax
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 5);
+  // bars: full[stages], empty[stages], unit_full[2], unit_empty[2], amax, x
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 6);
+  // fused quantiser, rows mode: the tokens' rows after the barrier block
+  const uint16_t* xs = reinterpret_cast<const uint16_t*>(reinterpret_cast<uint8_t*>(bars) + kBarBlockBytes);
   __shared__ int s_is_last;
   // fused quantiser: per-token partial absmax (float bits), scales, reciprocals
   __shared__ uint32_t s_amax[FQ ? BN : 1];
@@ -651,6 +730,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   auto ufull_bar = [&](int b) { return smem_addr(bars + 2 * stages + b); };
   auto uempty_bar = [&](int b) { return smem_addr(bars + 2 * stages + 2 + b); };
   const uint32_t amax_bar = smem_addr(bars + 2 * stages + 4);
+  const uint32_t x_bar = smem_addr(bars + 2 * stages + 5);
 
   if (threadIdx.x == 0) {
     prefetch_tensormap(&tmap_p);
@@ -660,7 +740,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
       mbar_init(full_bar(s), FQ ? 2 : 1);
       mbar_init(empty_bar(s), 1);
     }
-    if (FQ) mbar_init(amax_bar, cl ? prm.splits : 1);
+    if (FQ) {
+      mbar_init(amax_bar, cl ? prm.splits : 1);
+      mbar_init(x_bar, 1);
+    }
     mbar_init(ufull_bar(0), 1);
     mbar_init(ufull_bar(1), 1);
     mbar_init(uempty_bar(0), kEpiThreads);
@@ -677,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   const uint32_t tmem_base = *tmem_slot;
   // the cluster's peers arrive on amax_bar: its initialisation must be
   // visible to them first
-  if (FQ && cl) cluster_sync();
+  if (FQ && cl && !prm.fq_rows) cluster_sync();
   if (threadIdx.x == 0) trace_stamp(prm, T_PROLOGUE);
   // Let the next kernel be scheduled (after this CTA holds its TMEM, so a
   // later kernel never takes TMEM ahead of an earlier one), then wait for the
@@ -757,8 +840,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
     if constexpr (FQ) {
       // every unit of this CTA has the same tokens (one token tile) and the
       // same K range (one slice per CTA, or the whole K)
-      if (w_first < units) ok = fq_token_scales<BN>(prm, unit_of(w_first, prm, group, BN), cl, et, amax_bar, s_amax,
-                                                      s_tok, s_rcp, s_rok);
+      if (w_first < units)
+        ok = prm.fq_rows ? fq_token_scales_rows<BN>(prm, et, x_bar, xs, s_amax, s_tok, s_rcp, s_rok)
+                         : fq_token_scales<BN>(prm, unit_of(w_first, prm, group, BN), cl, et, amax_bar, s_amax, s_tok,
+                                               s_rcp, s_rok);
     }
     for (int w = w_first; w < units && ok; w += w_step) {
       const Unit un = unit_of(w, prm, group, BN);
@@ -768,10 +853,14 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
           const uint32_t itg = ait + static_cast<uint32_t>(i);
           const int s = static_cast<int>(itg % stages);
           if (!mbar_wait(empty_bar(s), ((itg / stages) & 1) ^ 1)) { ok = false; break; }
-          fq_fill_stage<BN>(prm, un.kb_begin + i, sq + s * kQBytes, s_tok, s_rcp, s_rok, lane);
+          if (prm.fq_rows)
+            fq_fill_stage_rows<BN>(prm, un.kb_begin + i, sq + s * kQBytes, xs, s_tok, s_rcp, s_rok, lane);
+          else
+            fq_fill_stage<BN>(prm, un.kb_begin + i, sq + s * kQBytes, s_tok, s_rcp, s_rok, lane);
           fence_proxy_async_shared();
           __syncwarp();
           if (lane == 0) mbar_arrive(full_bar(s));
+          if (itg == 0 && lane == 0) trace_stamp(prm, T_FQ_STAGE0);
         }
         ait += static_cast<uint32_t>(un.nkb);
       }
@@ -946,7 +1035,8 @@ template <int BN, bool SWAP, bool INT8, typename OutT, bool FQ = false>
 cudaError_t launch_one(const CUtensorMap& tp, const CUtensorMap& tq, const MmParams& p, int stages,
                        cudaStream_t stream) {
   auto kern = w8a8_gemm_kernel<BN, SWAP, INT8, OutT, FQ>;
-  const int smem = gemm_smem_bytes(BN, stages);
+  // rows mode of the fused quantiser: the tokens' rows follow the barriers
+  const int smem = gemm_smem_bytes(BN, stages) + (FQ && p.fq_rows ? p.M * p.K * 2 : 0);
   // the attribute is per function and device; setting it again is harmless
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -1099,7 +1189,7 @@ __global__ void widen_int8_kernel(const int8_t* __restrict__ src, long long ld, 
 }  // namespace
 
 int gemm_smem_bytes(int block_n, int stages) {
-  return stages * (kPBytes + block_n * kRowBytes) + 1024 /*alignment slack*/ + 256 /*barriers*/;
+  return stages * (kPBytes + block_n * kRowBytes) + 1024 /*alignment slack*/ + kBarBlockBytes;
 }
 
 int max_stages_for(int block_n, int smem_budget) {

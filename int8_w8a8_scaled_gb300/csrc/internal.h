@@ -42,6 +42,7 @@ struct MmParams {
   long long ld_x;        // row stride of x in elements
   int x_fp16;            // 1: x is fp16, 0: bf16
   float* scale_a_out;    // [M] per-token scales the kernel computed (nullable)
+  int fq_rows;           // 1: the tokens' whole rows are staged in shared memory
   unsigned long long* trace;  // debug: per-CTA phase stamps (null = off)
   int trace_ctas;             // CTAs the trace buffer has room for
 };
