@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kRowThreads)
 // q = enc(x / s) over a contiguous tensor, s from the absmax word (dynamic)
 // or from scale[0] (static).  16 elements per thread per step.
 template <int XK, int QK>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
     quant_flat_kernel(const uint16_t* __restrict__ x, long long n, uint8_t* __restrict__ q,
                       float* __restrict__ scale, const unsigned* __restrict__ word, int dynamic) {
   allow_dependents();
@@ -346,13 +346,18 @@ __global__ void __launch_bounds__(256)
   const bool ok = recip_ok(s, &y);
   const long long n16 = n / 16;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  // The grid walks the tensor back to front: after the absmax pass (front to
+  // back) the tail it read last is still in L2, so a tensor up to about the
+  // L2 size is read from DRAM once.  rv(v) is the 16-element group visited
+  // at virtual position v.
+  auto rv = [n16](long long v) { return n16 - 1 - v; };
   long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
   for (; v + stride < n16; v += 2 * stride) {
     uint4 w[4];
-    w[0] = __ldcs(reinterpret_cast<const uint4*>(x) + 2 * v);
-    w[1] = __ldcs(reinterpret_cast<const uint4*>(x) + 2 * v + 1);
-    w[2] = __ldcs(reinterpret_cast<const uint4*>(x) + 2 * (v + stride));
-    w[3] = __ldcs(reinterpret_cast<const uint4*>(x) + 2 * (v + stride) + 1);
+    w[0] = __ldcs(reinterpret_cast<const uint4*>(x) + 2 * rv(v));
+    w[1] = __ldcs(reinterpret_cast<const uint4*>(x) + 2 * rv(v) + 1);
+    w[2] = __ldcs(reinterpret_cast<const uint4*>(x) + 2 * rv(v + stride));
+    w[3] = __ldcs(reinterpret_cast<const uint4*>(x) + 2 * rv(v + stride) + 1);
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       float f[16];
@@ -363,19 +368,19 @@ __global__ void __launch_bounds__(256)
       o.y = enc4<QK>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
       o.z = enc4<QK>(div_by(f[8], s, y, ok), div_by(f[9], s, y, ok), div_by(f[10], s, y, ok), div_by(f[11], s, y, ok));
       o.w = enc4<QK>(div_by(f[12], s, y, ok), div_by(f[13], s, y, ok), div_by(f[14], s, y, ok), div_by(f[15], s, y, ok));
-      __stcs(reinterpret_cast<uint4*>(q) + (u == 0 ? v : v + stride), o);
+      __stcs(reinterpret_cast<uint4*>(q) + rv(u == 0 ? v : v + stride), o);
     }
   }
   for (; v < n16; v += stride) {
     float f[16];
-    unpack8<XK>(__ldcs(reinterpret_cast<const uint4*>(x) + 2 * v), *reinterpret_cast<float(*)[8]>(f));
-    unpack8<XK>(__ldcs(reinterpret_cast<const uint4*>(x) + 2 * v + 1), *reinterpret_cast<float(*)[8]>(f + 8));
+    unpack8<XK>(__ldcs(reinterpret_cast<const uint4*>(x) + 2 * rv(v)), *reinterpret_cast<float(*)[8]>(f));
+    unpack8<XK>(__ldcs(reinterpret_cast<const uint4*>(x) + 2 * rv(v) + 1), *reinterpret_cast<float(*)[8]>(f + 8));
     uint4 o;
     o.x = enc4<QK>(div_by(f[0], s, y, ok), div_by(f[1], s, y, ok), div_by(f[2], s, y, ok), div_by(f[3], s, y, ok));
     o.y = enc4<QK>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
     o.z = enc4<QK>(div_by(f[8], s, y, ok), div_by(f[9], s, y, ok), div_by(f[10], s, y, ok), div_by(f[11], s, y, ok));
     o.w = enc4<QK>(div_by(f[12], s, y, ok), div_by(f[13], s, y, ok), div_by(f[14], s, y, ok), div_by(f[15], s, y, ok));
-    __stcs(reinterpret_cast<uint4*>(q) + v, o);
+    __stcs(reinterpret_cast<uint4*>(q) + rv(v), o);
   }
   for (long long j = n16 * 16 + blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; j < n;
        j += stride)
