@@ -602,7 +602,7 @@ def sweep_large(out_path: str, reps: int = 5):
     print(f"wrote {len(lines)} lines to {out_path}")
 
 
-def sweep_decode(out_path: str, reps: int = 20):
+def sweep_decode(out_path: str, reps: int = 20, ms=None):
     """Time every decode GEMM shape under a grid of kernel configurations
     (CUDA graph of 8 launches cycling over 4 weight copies, so weights come
     from HBM).  Writes one JSON line per (shape, config)."""
@@ -612,7 +612,7 @@ def sweep_decode(out_path: str, reps: int = 20):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
     lines = []
-    for M in DECODE_MS:
+    for M in (ms or DECODE_MS):
         for name, N, K, shared in LLAMA8B:
             g = torch.Generator(device=dev)
             g.manual_seed(M * 7 + N)
@@ -840,6 +840,7 @@ def main():
                          "(experiments; the default run uses the library's choice)")
     ap.add_argument("--sweep-decode", metavar="OUT", default=None,
                     help="time the decode GEMM shapes under a grid of configurations, write JSON lines to OUT")
+    ap.add_argument("--sweep-ms", default=None, help="token counts for --sweep-decode, e.g. 64,256")
     ap.add_argument("--sweep-large", metavar="OUT", default=None,
                     help="time the prefill / int8 70B shapes under large-M configurations")
     args = ap.parse_args()
@@ -847,7 +848,7 @@ def main():
         sweep_large(args.sweep_large)
         return 0
     if args.sweep_decode:
-        sweep_decode(args.sweep_decode)
+        sweep_decode(args.sweep_decode, ms=[int(m) for m in args.sweep_ms.split(",")] if args.sweep_ms else None)
         return 0
     if args.profile_case:
         run_profile_case(args.profile_case, args.launches, json.loads(args.override) if args.override else None)
