@@ -142,7 +142,13 @@ __global__ void __launch_bounds__(kRowThreads)
     bulk_load(smem_addr(row_s), x + row * ld_x, bytes, smem_addr(&bar));
   }
   __syncthreads();
-  if (!mbar_wait(smem_addr(&bar), 0)) return;  // flagged in the device status
+  // on a timeout (flagged in the device status) every thread leaves together,
+  // before the block-wide reductions below, once the copy in flight has had a
+  // second bounded wait to land
+  if (!__syncthreads_and(mbar_wait(smem_addr(&bar), 0))) {
+    if (threadIdx.x == 0) mbar_wait(smem_addr(&bar), 0);
+    return;
+  }
   const int nvec = static_cast<int>(cols / 8);
   float s;
   if (dynamic) {
@@ -447,6 +453,88 @@ __global__ void __launch_bounds__(256)
     y[j] = out16<YK>(dec1<QK>(q[j]) * s);
 }
 
+// Streaming dequantiser for a contiguous tensor (n % 16 == 0, 16-byte
+// aligned): each CTA walks chunks of kDqChunk codes with a two-deep ring.
+// One thread pulls the next chunk into shared memory with a bulk copy while
+// all threads convert the current one into a shared output buffer, which one
+// bulk store writes back.  No per-thread global loads or stores: the bulk
+// engine keeps whole chunks in flight in both directions.
+constexpr int kDqChunk = 4096;  // codes per chunk: 4 KB in, 8 KB out
+
+template <int QK, int YK>
+__global__ void __launch_bounds__(256)
+    dequant_bulk_kernel(const uint8_t* __restrict__ q, long long n, const float* __restrict__ scale,
+                        uint16_t* __restrict__ y) {
+  __shared__ __align__(128) uint8_t in_buf[2][kDqChunk];
+  __shared__ __align__(128) uint16_t out_buf[2][kDqChunk];
+  __shared__ uint64_t bar[2];
+  allow_dependents();
+  const float s = __ldg(scale);
+  const long long nchunks = (n + kDqChunk - 1) / kDqChunk;
+  const long long step = gridDim.x;
+  auto chunk_bytes = [&](long long c) {
+    const long long rem = n - c * kDqChunk;
+    return static_cast<uint32_t>(rem < kDqChunk ? rem : kDqChunk);
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar[0]), 1);
+    mbar_init(smem_addr(&bar[1]), 1);
+    fence_barrier_init();
+    const long long c0 = blockIdx.x;
+    if (c0 < nchunks) {
+      mbar_arrive_expect_tx(smem_addr(&bar[0]), chunk_bytes(c0));
+      bulk_load(smem_addr(in_buf[0]), q + c0 * kDqChunk, chunk_bytes(c0), smem_addr(&bar[0]));
+    }
+  }
+  __syncthreads();
+  int i = 0;
+  bool failed = false, next_issued = false;
+  for (long long c = blockIdx.x; c < nchunks; c += step, ++i) {
+    const int b = i & 1;
+    next_issued = false;
+    if (threadIdx.x == 0) {
+      const long long next = c + step;
+      next_issued = next < nchunks;
+      if (next_issued) {  // in_buf[b ^ 1] was consumed last iteration
+        mbar_arrive_expect_tx(smem_addr(&bar[b ^ 1]), chunk_bytes(next));
+        bulk_load(smem_addr(in_buf[b ^ 1]), q + next * kDqChunk, chunk_bytes(next), smem_addr(&bar[b ^ 1]));
+      }
+      bulk_wait_read<1>();  // the store two chunks back has read out_buf[b]
+    }
+    // every thread waits for the chunk; on a timeout (flagged in the device
+    // status) all of them leave together
+    const bool got = mbar_wait(smem_addr(&bar[b]), (i >> 1) & 1);
+    if (!__syncthreads_and(got)) {
+      failed = true;
+      break;
+    }
+    const uint4 w = reinterpret_cast<const uint4*>(in_buf[b])[threadIdx.x];
+    const uint8_t* bb = reinterpret_cast<const uint8_t*>(&w);
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      o[j] = static_cast<uint32_t>(out16<YK>(dec1<QK>(bb[2 * j]) * s)) |
+             (static_cast<uint32_t>(out16<YK>(dec1<QK>(bb[2 * j + 1]) * s)) << 16);
+    uint4* d = reinterpret_cast<uint4*>(out_buf[b]) + 2 * threadIdx.x;
+    d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    fence_proxy_async_shared();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      bulk_store(y + c * kDqChunk, smem_addr(out_buf[b]), chunk_bytes(c) * 2);
+      bulk_commit();
+    }
+  }
+  if (threadIdx.x == 0) {
+    if (failed) {
+      // let this CTA's copies in flight land (bounded) before it exits
+      mbar_wait(smem_addr(&bar[i & 1]), (i >> 1) & 1);
+      if (next_issued) mbar_wait(smem_addr(&bar[(i & 1) ^ 1]), ((i + 1) >> 1) & 1);
+    }
+    bulk_wait_all();
+  }
+}
+
 template <int QK, int YK>
 __global__ void __launch_bounds__(kRowThreads)
     dequant_rows_kernel(const uint8_t* __restrict__ q, long long ld_q, long long cols,
@@ -536,6 +624,12 @@ cudaError_t launch_dequant_t(const DequantArgs& a, int num_sms, cudaStream_t st)
   const bool contiguous = (a.ld_q == a.cols && a.ld_y == a.cols) || a.rows == 1;
   if (!a.per_row && contiguous && a.vec) {
     const long long n = a.rows * a.cols;
+    if (n % 16 == 0) {
+      const long long chunks = (n + kDqChunk - 1) / kDqChunk;
+      const long long cap = static_cast<long long>(num_sms) * 8;
+      return launch_pdl(dequant_bulk_kernel<QK, YK>, dim3(static_cast<unsigned>(chunks < cap ? chunks : cap)),
+                        dim3(256), st, q, n, a.scale, y);
+    }
     return launch_pdl(dequant_flat_kernel<QK, YK>, dim3(flat_blocks(n / 16, num_sms)), dim3(256), st, q, n, a.scale, y);
   }
   return launch_pdl(dequant_rows_kernel<QK, YK>, dim3(static_cast<unsigned>(a.rows)), dim3(kRowThreads), st, q, a.ld_q,
