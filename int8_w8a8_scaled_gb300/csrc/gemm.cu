@@ -678,8 +678,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   uint8_t* sp = smem;
   uint8_t* sq = smem + stages * kPBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sq + stages * kQBytes);
-  // bars: full[stages], empty[stages], unit_full[2], unit_empty[2], amax, x
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 6);
+  // bars: full[stages], empty[stages], unit_full[2], unit_empty[2], amax, x,
+  // mma_drain (failure path only)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 7);
   // fused quantiser, rows mode: the tokens' rows after the barrier block
   const uint16_t* xs = reinterpret_cast<const uint16_t*>(reinterpret_cast<uint8_t*>(bars) + kBarBlockBytes);
   __shared__ int s_is_last;
@@ -731,6 +732,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   auto uempty_bar = [&](int b) { return smem_addr(bars + 2 * stages + 2 + b); };
   const uint32_t amax_bar = smem_addr(bars + 2 * stages + 4);
   const uint32_t x_bar = smem_addr(bars + 2 * stages + 5);
+  const uint32_t drain_bar = smem_addr(bars + 2 * stages + 6);
 
   if (threadIdx.x == 0) {
     prefetch_tensormap(&tmap_p);
@@ -744,6 +746,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
       mbar_init(amax_bar, cl ? prm.splits : 1);
       mbar_init(x_bar, 1);
     }
+    mbar_init(drain_bar, 1);
     mbar_init(ufull_bar(0), 1);
     mbar_init(ufull_bar(1), 1);
     mbar_init(uempty_bar(0), kEpiThreads);
@@ -785,6 +788,12 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
           if (!FQ) tma_load_2d(smem_addr(sq + s * kQBytes), &tmap_q, full_bar(s), kx, un.q0);
         }
       }
+      if (!ok) {
+        // a wait gave up: let the stage loads still in flight land (bounded)
+        // before the CTA leaves and its shared memory is released
+        for (uint32_t j = it > static_cast<uint32_t>(stages) ? it - stages : 0u; j < it; ++j)
+          mbar_wait(full_bar(static_cast<int>(j % stages)), (j / stages) & 1);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -824,6 +833,12 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
           }
           mma_commit(ufull_bar(b));
         }
+      }
+      if (!ok) {
+        // a wait gave up: the MMAs already issued finish (bounded wait on a
+        // commit behind them) before the accumulators' TMEM is released
+        mma_commit(drain_bar);
+        mbar_wait(drain_bar, 0);
       }
     }
     __syncwarp();

@@ -453,6 +453,171 @@ __global__ void __launch_bounds__(256)
     y[j] = out16<YK>(dec1<QK>(q[j]) * s);
 }
 
+// Streaming per-tensor quantiser passes for a contiguous tensor (n % 16 == 0,
+// 16-byte aligned), in the dequantiser's pattern: chunks of kQzChunk
+// elements pulled into shared memory by bulk copies (two-deep ring, one
+// thread issuing), all threads working from shared memory.
+constexpr int kQzChunk = 4096;  // elements per chunk: 8 KB of bf16 / fp16
+
+// Pass 1: absmax of the whole tensor (front to back) into the word.
+template <int XK>
+__global__ void __launch_bounds__(256)
+    absmax_bulk_kernel(const uint16_t* __restrict__ x, long long n, unsigned* __restrict__ word) {
+  __shared__ __align__(128) uint16_t in_buf[2][kQzChunk];
+  __shared__ uint64_t bar[2];
+  __shared__ float red[8];
+  allow_dependents();
+  const long long nchunks = (n + kQzChunk - 1) / kQzChunk;
+  const long long step = gridDim.x;
+  auto chunk_elems = [&](long long c) {
+    const long long rem = n - c * kQzChunk;
+    return static_cast<int>(rem < kQzChunk ? rem : kQzChunk);
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar[0]), 1);
+    mbar_init(smem_addr(&bar[1]), 1);
+    fence_barrier_init();
+    const long long c0 = blockIdx.x;
+    if (c0 < nchunks) {
+      mbar_arrive_expect_tx(smem_addr(&bar[0]), chunk_elems(c0) * 2);
+      bulk_load(smem_addr(in_buf[0]), x + c0 * kQzChunk, chunk_elems(c0) * 2, smem_addr(&bar[0]));
+    }
+  }
+  __syncthreads();
+  float amax = 0.f;
+  int i = 0;
+  bool failed = false, next_issued = false;
+  for (long long c = blockIdx.x; c < nchunks; c += step, ++i) {
+    const int b = i & 1;
+    next_issued = false;
+    if (threadIdx.x == 0) {
+      const long long next = c + step;
+      next_issued = next < nchunks;
+      if (next_issued) {  // in_buf[b ^ 1] was consumed last iteration
+        mbar_arrive_expect_tx(smem_addr(&bar[b ^ 1]), chunk_elems(next) * 2);
+        bulk_load(smem_addr(in_buf[b ^ 1]), x + next * kQzChunk, chunk_elems(next) * 2, smem_addr(&bar[b ^ 1]));
+      }
+    }
+    const bool got = mbar_wait(smem_addr(&bar[b]), (i >> 1) & 1);
+    if (!__syncthreads_and(got)) {
+      failed = true;
+      break;
+    }
+    const int e0 = threadIdx.x * 16;
+    if (e0 < chunk_elems(c)) {
+      const uint4* p = reinterpret_cast<const uint4*>(in_buf[b] + e0);
+      float f[8];
+      unpack8<XK>(p[0], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+      unpack8<XK>(p[1], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    }
+    __syncthreads();  // in_buf[b] is refilled next iteration
+  }
+  if (threadIdx.x == 0 && failed) {
+    // let this CTA's copies in flight land (bounded) before it exits
+    mbar_wait(smem_addr(&bar[i & 1]), (i >> 1) & 1);
+    if (next_issued) mbar_wait(smem_addr(&bar[(i & 1) ^ 1]), ((i + 1) >> 1) & 1);
+  }
+  amax = warp_max(amax);
+  const int w = threadIdx.x / 32, l = threadIdx.x % 32;
+  if (l == 0) red[w] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float r = (l < 8) ? red[l] : 0.f;
+    r = warp_max(r);
+    // non-negative, non-NaN floats order like their bit patterns
+    if (l == 0 && r > 0.f) atomicMax(word, __float_as_uint(r));
+  }
+}
+
+// Pass 2: codes of the whole tensor with the scale from the word (dynamic)
+// or scale[0] (static).  The chunks are visited back to front, so a tensor
+// about the size of L2 finds the tail pass 1 read last still there.
+template <int XK, int QK>
+__global__ void __launch_bounds__(256)
+    quant_bulk_kernel(const uint16_t* __restrict__ x, long long n, uint8_t* __restrict__ q,
+                      float* __restrict__ scale, const unsigned* __restrict__ word, int dynamic) {
+  __shared__ __align__(128) uint16_t in_buf[2][kQzChunk];
+  __shared__ __align__(128) uint8_t out_buf[2][kQzChunk];
+  __shared__ uint64_t bar[2];
+  allow_dependents();
+  float s;
+  if (dynamic) {
+    s = scale_from_amax<QK>(__uint_as_float(*word));
+    if (blockIdx.x == 0 && threadIdx.x == 0) scale[0] = s;
+  } else {
+    s = __ldg(scale);
+  }
+  float y;
+  const bool ok = recip_ok(s, &y);
+  const long long nchunks = (n + kQzChunk - 1) / kQzChunk;
+  const long long step = gridDim.x;
+  auto phys = [&](long long c) { return nchunks - 1 - c; };  // back to front
+  auto chunk_elems = [&](long long c) {
+    const long long rem = n - phys(c) * kQzChunk;
+    return static_cast<int>(rem < kQzChunk ? rem : kQzChunk);
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar[0]), 1);
+    mbar_init(smem_addr(&bar[1]), 1);
+    fence_barrier_init();
+    const long long c0 = blockIdx.x;
+    if (c0 < nchunks) {
+      mbar_arrive_expect_tx(smem_addr(&bar[0]), chunk_elems(c0) * 2);
+      bulk_load(smem_addr(in_buf[0]), x + phys(c0) * kQzChunk, chunk_elems(c0) * 2, smem_addr(&bar[0]));
+    }
+  }
+  __syncthreads();
+  int i = 0;
+  bool failed = false, next_issued = false;
+  for (long long c = blockIdx.x; c < nchunks; c += step, ++i) {
+    const int b = i & 1;
+    next_issued = false;
+    if (threadIdx.x == 0) {
+      const long long next = c + step;
+      next_issued = next < nchunks;
+      if (next_issued) {  // in_buf[b ^ 1] was consumed last iteration
+        mbar_arrive_expect_tx(smem_addr(&bar[b ^ 1]), chunk_elems(next) * 2);
+        bulk_load(smem_addr(in_buf[b ^ 1]), x + phys(next) * kQzChunk, chunk_elems(next) * 2,
+                  smem_addr(&bar[b ^ 1]));
+      }
+      bulk_wait_read<1>();  // the store two chunks back has read out_buf[b]
+    }
+    const bool got = mbar_wait(smem_addr(&bar[b]), (i >> 1) & 1);
+    if (!__syncthreads_and(got)) {
+      failed = true;
+      break;
+    }
+    const uint4* p = reinterpret_cast<const uint4*>(in_buf[b] + threadIdx.x * 16);
+    float f[16];
+    unpack8<XK>(p[0], *reinterpret_cast<float(*)[8]>(f));
+    unpack8<XK>(p[1], *reinterpret_cast<float(*)[8]>(f + 8));
+    uint4 o;
+    o.x = enc4<QK>(div_by(f[0], s, y, ok), div_by(f[1], s, y, ok), div_by(f[2], s, y, ok), div_by(f[3], s, y, ok));
+    o.y = enc4<QK>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
+    o.z = enc4<QK>(div_by(f[8], s, y, ok), div_by(f[9], s, y, ok), div_by(f[10], s, y, ok), div_by(f[11], s, y, ok));
+    o.w = enc4<QK>(div_by(f[12], s, y, ok), div_by(f[13], s, y, ok), div_by(f[14], s, y, ok), div_by(f[15], s, y, ok));
+    reinterpret_cast<uint4*>(out_buf[b])[threadIdx.x] = o;
+    fence_proxy_async_shared();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      bulk_store(q + phys(c) * kQzChunk, smem_addr(out_buf[b]), static_cast<uint32_t>(chunk_elems(c)));
+      bulk_commit();
+    }
+  }
+  if (threadIdx.x == 0) {
+    if (failed) {
+      // let this CTA's copies in flight land (bounded) before it exits
+      mbar_wait(smem_addr(&bar[i & 1]), (i >> 1) & 1);
+      if (next_issued) mbar_wait(smem_addr(&bar[(i & 1) ^ 1]), ((i + 1) >> 1) & 1);
+    }
+    bulk_wait_all();
+  }
+}
+
 // Streaming dequantiser for a contiguous tensor (n % 16 == 0, 16-byte
 // aligned): each CTA walks chunks of kDqChunk codes with a two-deep ring.
 // One thread pulls the next chunk into shared memory with a bulk copy while
@@ -592,9 +757,17 @@ cudaError_t launch_quant_t(const QuantArgs& a, int num_sms, cudaStream_t st) {
   const bool contiguous = (a.ld_x == a.cols && a.ld_q == a.cols) || a.rows == 1;
   const dim3 b256(256);
   if (a.per_row) return launch_rows<XK, QK>(a, st);
+  auto bulk_grid = [&](long long n) {
+    const long long chunks = (n + kQzChunk - 1) / kQzChunk;
+    const long long cap = static_cast<long long>(num_sms) * 8;
+    return dim3(static_cast<unsigned>(chunks < cap ? chunks : cap));
+  };
   if (!a.dynamic) {
     if (contiguous && a.vec) {
       const long long n = a.rows * a.cols;
+      if (n % 16 == 0)
+        return launch_pdl(quant_bulk_kernel<XK, QK>, bulk_grid(n), b256, st, x, n, q, a.scale,
+                          static_cast<const unsigned*>(nullptr), 0);
       return launch_pdl(quant_flat_kernel<XK, QK>, dim3(flat_blocks(n / 16, num_sms)), b256, st, x, n, q, a.scale,
                         static_cast<const unsigned*>(nullptr), 0);
     }
@@ -603,6 +776,13 @@ cudaError_t launch_quant_t(const QuantArgs& a, int num_sms, cudaStream_t st) {
   // dynamic per-tensor: absmax pass, then quantise pass
   cudaError_t e = cudaMemsetAsync(a.amax_word, 0, sizeof(unsigned), st);
   if (e != cudaSuccess) return e;
+  if (contiguous && a.vec && (a.rows * a.cols) % 16 == 0) {
+    const long long n = a.rows * a.cols;
+    e = launch_pdl(absmax_bulk_kernel<XK>, bulk_grid(n), b256, st, x, n, a.amax_word);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(quant_bulk_kernel<XK, QK>, bulk_grid(n), b256, st, x, n, q, a.scale,
+                      static_cast<const unsigned*>(a.amax_word), 1);
+  }
   if (contiguous && a.vec) {
     const long long n = a.rows * a.cols;
     e = launch_pdl(absmax_flat_kernel<XK>, dim3(flat_blocks(n / 8, num_sms)), b256, st, x, n, a.amax_word);
