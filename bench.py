@@ -244,8 +244,14 @@ class DecodeWorkload:
             else:
                 self.w8.scaled_mm(it["aq"], wq, it["sa"], sw, it["out"], workspace=self.ws, config=it["cfg"])
 
-    def run_step(self):
-        for it in self.items:
+    def second_set(self):
+        """The step's activations, codes, scales and outputs once more (the
+        weights and workspace are shared), for double-buffered host copies."""
+        return [dict(it, x=it["x"].clone(), aq=it["aq"].clone(), sa=it["sa"].clone(), out=it["out"].clone())
+                for it in self.items]
+
+    def run_step(self, items=None):
+        for it in (items if items is not None else self.items):
             wq, sw, _, _ = self.weights[it["name"]]
             if it["fused"]:
                 self._fused(it)
@@ -734,33 +740,54 @@ def run_ours(args):
     gemm_gbs = gemm_bytes / t_gemm / 1e9
     quant_gbs = wl.quant_bytes() / t_quant / 1e9
 
-    # end to end through the public API with host buffers: pinned host
-    # activations copied in, the step, outputs copied back
+    # end to end through the public API with host buffers: every step copies
+    # its activations in from pinned host memory and reads its outputs back.
+    # Pipelined over two device buffer sets: step k+1's upload and step k-1's
+    # download run on copy streams while step k computes (the computes stay
+    # in order on one stream, so they share the workspace safely).
+    sets = [wl.items, wl.second_set()]
+    graphs = [g_step, graph_of(lambda: wl.run_step(sets[1]), stream)]
     host_x = [it["x"].cpu().pin_memory() for it in wl.items]
-    host_o = [torch.empty(it["out"].shape, dtype=it["out"].dtype).pin_memory() for it in wl.items]
+    host_o = [[torch.empty(it["out"].shape, dtype=it["out"].dtype).pin_memory() for it in wl.items]
+              for _ in range(2)]
     h2d = sum(h.numel() * h.element_size() for h in host_x)
-    d2h = sum(h.numel() * h.element_size() for h in host_o)
+    d2h = sum(h.numel() * h.element_size() for h in host_o[0])
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_up = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_down = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for it, hx in zip(wl.items, host_x):
-            it["x"].copy_(hx, non_blocking=True)
-        g_step.replay()
-        for it, ho in zip(wl.items, host_o):
-            ho.copy_(it["out"], non_blocking=True)
+    def e2e_step(k):
+        b = k % 2
+        up.wait_event(ev_comp[b])          # set b's activations are free again
+        with torch.cuda.stream(up):
+            for it, hx in zip(sets[b], host_x):
+                it["x"].copy_(hx, non_blocking=True)
+            ev_up[b].record(up)
+        stream.wait_event(ev_up[b])
+        stream.wait_event(ev_down[b])      # set b's outputs have been read back
+        with torch.cuda.stream(stream):
+            graphs[b].replay()
+            ev_comp[b].record(stream)
+        down.wait_event(ev_comp[b])
+        with torch.cuda.stream(down):
+            for it, ho in zip(sets[b], host_o[b]):
+                ho.copy_(it["out"], non_blocking=True)
+            ev_down[b].record(down)
 
-    e2e_steps = max(1, min(args.steps, 200))
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            e2e_step()
+    e2e_steps = max(2, min(args.steps, 200))
+    for k in range(args.warmup):
+        e2e_step(k)
     torch.cuda.synchronize()
     if barrier:
         barrier()
     s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        s_ev.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e_ev.record(stream)
+    s_ev.record(up)                        # the first upload is inside the timed region
+    for k in range(e2e_steps):
+        e2e_step(k)
+    for b in range(2):
+        stream.wait_event(ev_down[b])      # ... and so is the last download
+    e_ev.record(stream)
     torch.cuda.synchronize()
     t_e2e = max_over_ranks(s_ev.elapsed_time(e_ev) / 1e3, dev)
     e2e_val = aggregate_tflops(flops_step, e2e_steps, t_e2e, ws_n)
@@ -811,7 +838,9 @@ def run_ours(args):
                          "bytes_note": "algorithmic: N*K + M*K*(2 where the kernel quantises bf16 x itself, "
                                        "else 1) + 2*M*N + 4*(M+scales) per matmul"},
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "note": "public API with pinned host buffers; each step uploads its activations and downloads "
+                            "its outputs, overlapped with the neighbouring steps' compute (two device buffer sets)"},
             "gpu_launches": wl.launches_per_step() * args.steps,
             "clocks": clocks,
             "workloads": workloads,
