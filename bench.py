@@ -559,9 +559,10 @@ def run_profile_case(name: str, launches: int, override=None):
 
 # ---------------------------------------------------------------- config sweep
 
-def sweep_large(out_path: str, reps: int = 5):
+def sweep_large(out_path: str, reps: int = 5, only=None):
     """Time the prefill (M=4096) fp8 shapes and the int8 70B shapes (M=8192)
-    under a grid of large-M kernel configurations."""
+    under a grid of large-M kernel configurations (`only`: "e4m3" or "int8"
+    restricts the sweep to one of the two)."""
     import torch
     import int8_w8a8_scaled_gb300 as w8
     dev = torch.device("cuda", 0)
@@ -569,6 +570,8 @@ def sweep_large(out_path: str, reps: int = 5):
     stream = torch.cuda.Stream(device=dev)
     lines = []
     cases = [(4096, N, K, w8.E4M3) for _, N, K, _ in LLAMA8B] + [(8192, N, K, w8.INT8) for _, N, K in LLAMA70B]
+    if only is not None:
+        cases = [c for c in cases if (c[3] == w8.E4M3) == (only == "e4m3")]
     for M, N, K, qd in cases:
         qt = torch.float8_e4m3fn if qd == w8.E4M3 else torch.int8
         g = torch.Generator(device=dev)
@@ -579,7 +582,7 @@ def sweep_large(out_path: str, reps: int = 5):
         sa = torch.rand(M, device=dev) * 0.01
         sb = torch.rand(N, device=dev) * 0.01
         out = torch.empty(M, N, dtype=torch.bfloat16 if qd == w8.E4M3 else torch.float16, device=dev)
-        bns = (128, 160, 192, 224, 256) if qd == w8.E4M3 else (64, 128, 256)
+        bns = (128, 160, 192, 224, 256) if qd == w8.E4M3 else (128, 160, 256)
         cfgs = [None] + [{"swap_ab": 0, "block_n": bn, "split_k": sp, "stages": st}
                          for bn in bns for sp in (1, 2) for st in (0, 3)]
         flops = 2.0 * M * N * K
@@ -872,9 +875,11 @@ def main():
     ap.add_argument("--sweep-ms", default=None, help="token counts for --sweep-decode, e.g. 64,256")
     ap.add_argument("--sweep-large", metavar="OUT", default=None,
                     help="time the prefill / int8 70B shapes under large-M configurations")
+    ap.add_argument("--sweep-q", choices=("e4m3", "int8"), default=None,
+                    help="restrict --sweep-large to the e4m3 or the int8 shapes")
     args = ap.parse_args()
     if args.sweep_large:
-        sweep_large(args.sweep_large)
+        sweep_large(args.sweep_large, only=args.sweep_q)
         return 0
     if args.sweep_decode:
         sweep_decode(args.sweep_decode, ms=[int(m) for m in args.sweep_ms.split(",")] if args.sweep_ms else None)

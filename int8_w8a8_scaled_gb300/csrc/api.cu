@@ -130,7 +130,7 @@ constexpr long long kFusedRowsMaxBytes = 32768;  // one-kernel quant_scaled_mm: 
 
 bool valid_block_n(int bn, int q_dtype, int swap_ab) {
   if (bn == 16 || bn == 32 || bn == 64 || bn == 128) return true;
-  if (q_dtype == W8A8_INT8) return bn == 256 && !swap_ab;
+  if (q_dtype == W8A8_INT8) return (bn == 160 || bn == 256) && !swap_ab;
   if (bn == 256) return true;
   return !swap_ab && (bn == 160 || bn == 192 || bn == 224);
 }
@@ -167,7 +167,8 @@ int one_wave_split(long long tiles, int kb, long long slots) {
 }
 
 int resident_per_sm(int block_n, int q_dtype) {
-  return (block_n <= 64 || (q_dtype == W8A8_INT8 && block_n <= 128)) ? 2 : 1;
+  (void)q_dtype;
+  return block_n <= 64 ? 2 : 1;
 }
 
 void auto_config(long long M, long long N, long long K, int q_dtype, int sms, w8a8_mm_config* c) {
@@ -282,7 +283,7 @@ w8a8_status validate_config(const w8a8_mm_config& c, int q_dtype, int smem_optin
   if (c.swap_ab != 0 && c.swap_ab != 1) return fail(W8A8_ERR_UNSUPPORTED, "swap_ab must be 0 or 1");
   if (!valid_block_n(c.block_n, q_dtype, c.swap_ab))
     return fail(W8A8_ERR_UNSUPPORTED,
-                "block_n %d not supported (16, 32, 64, 128, 256; 160/192/224 for e4m3 without swap; 256 for int8 without swap)",
+                "block_n %d not supported (16, 32, 64, 128, 256; 160/192/224 for e4m3 without swap; 160/256 for int8 without swap)",
                 c.block_n);
   if (c.split_k < 1 || c.split_k > 16) return fail(W8A8_ERR_UNSUPPORTED, "split_k must be in [1, 16]");
   if (c.stages != 0 && (c.stages < 2 || c.stages > 8))

@@ -56,13 +56,15 @@ constexpr int kBarBlockBytes = 256;  // mbarriers and the TMEM slot after the st
 
 // e4m3: accumulation units alternate between two fp32 accumulators (columns
 // 0 and bn) so the epilogue of one unit overlaps the next unit's MMAs.
-// int8: one fp32 chunk accumulator (column 0) and the int32 total (column
-// bn) -- 2 * bn columns, so two CTAs share an SM and one CTA's MMAs fill the
-// tensor pipe while the other drains a chunk.
-__host__ __device__ constexpr int acc_bufs(bool int8) { return int8 ? 1 : 2; }
+// int8: fp32 chunk accumulators (columns 0, bn) and the int32 total after
+// them.  Up to 160 columns two chunk accumulators and the total fit the 512
+// TMEM columns (3 * bn), so one chunk's MMAs run while the previous chunk
+// drains; at 256 columns one chunk accumulator and the total fill TMEM and
+// the MMAs wait for each drain.
+__host__ __device__ constexpr int acc_bufs(int bn, bool int8) { return (int8 && 3 * bn > 512) ? 1 : 2; }
 
 __host__ __device__ constexpr int tmem_cols_for(int bn, bool int8) {
-  const int need = acc_bufs(int8) * bn + (int8 ? bn : 0);
+  const int need = acc_bufs(bn, int8) * bn + (int8 ? bn : 0);
   int c = 32;
   while (c < need) c *= 2;
   return c;
@@ -639,7 +641,13 @@ __device__ __forceinline__ void fq_fill_stage_rows(const MmParams& prm, int kb, 
 
 // Narrow tiles run two CTAs per SM (the dispatch sizes their shared memory
 // for that); cap their registers so that two fit (<= 168 per thread).
-__host__ __device__ constexpr int min_ctas_for(int bn, bool int8) { return (bn <= 64 || (int8 && bn <= 128)) ? 2 : 1; }
+__host__ __device__ constexpr int min_ctas_for(int bn, bool) { return bn <= 64 ? 2 : 1; }
+
+// int8 drain: 16-column groups per batch, the largest count <= cap that
+// divides the tile's groups (160 columns: 10 groups, batches of 2)
+__host__ __device__ constexpr int drain_batch(int groups, int cap) {
+  return cap <= 1 ? 1 : (groups % cap == 0 ? cap : drain_batch(groups, cap - 1));
+}
 
 template <int BN, bool SWAP, bool INT8, typename OutT>
 __device__ __forceinline__ void reduce_rows_any(const MmParams& prm, const Unit& un, const uint32_t* tile0,
@@ -668,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
   constexpr uint32_t kIdesc = make_idesc(kTileP, BN, 0);
   constexpr int kTmemCols = tmem_cols_for(BN, INT8);
   constexpr int kGroups = BN / 16;
-  static_assert((INT8 ? acc_bufs(INT8) + 1 : acc_bufs(INT8)) * BN <= kTmemCols && kTmemCols <= 512,
+  static_assert((INT8 ? acc_bufs(BN, INT8) + 1 : acc_bufs(BN, INT8)) * BN <= kTmemCols && kTmemCols <= 512,
                 "accumulators must fit the TMEM allocation");
   static_assert(!FQ || (SWAP && !INT8 && BN <= 64), "the fused quantiser is the swap-AB e4m3 decode path");
 
@@ -805,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
         const int chunk = INT8 ? prm.kchunk_kb : un.nkb;
         const int nch = (un.nkb + chunk - 1) / chunk;
         for (int c = 0; c < nch && ok; ++c, ++u) {
-          constexpr int kBufs = acc_bufs(INT8);
+          constexpr int kBufs = acc_bufs(BN, INT8);
           const int b = static_cast<int>(u % kBufs);
           if (u >= static_cast<uint32_t>(kBufs)) {
             if (!mbar_wait(uempty_bar(b), ((u - kBufs) / kBufs) & 1)) { ok = false; break; }
@@ -915,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
                (static_cast<size_t>(un.tile_lin) * prm.splits + un.split) * tile_elems;
 
       for (int c = 0; c < nch; ++c, ++u) {
-        constexpr int kBufs = acc_bufs(INT8);
+        constexpr int kBufs = acc_bufs(BN, INT8);
         const int b = static_cast<int>(u % kBufs);
         if (!mbar_wait(ufull_bar(b), (u / kBufs) & 1)) { ok = false; break; }
         tc_fence_after();
@@ -928,8 +936,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
           // 16-column groups: all TMEM loads
           // of a batch are in flight together (one wait per batch), so the
           // drain of a 1024-K chunk stays shorter than the next chunk's MMAs
-          constexpr int kBatchMax = min_ctas_for(BN, INT8) == 2 ? 2 : 4;  // register budget
-          constexpr int kBatch = kGroups < kBatchMax ? kGroups : kBatchMax;
+          constexpr int kBatch = drain_batch(kGroups, min_ctas_for(BN, INT8) == 2 ? 2 : 4);  // register budget
 #pragma unroll 1
           for (int g0 = 0; g0 < kGroups; g0 += kBatch) {
             uint32_t r[kBatch][16], t[kBatch][16];
@@ -1051,24 +1058,32 @@ cudaError_t launch_one(const CUtensorMap& tp, const CUtensorMap& tq, const MmPar
                        cudaStream_t stream) {
   auto kern = w8a8_gemm_kernel<BN, SWAP, INT8, OutT, FQ>;
   // rows mode of the fused quantiser: the tokens' rows follow the barriers
-  const int smem = gemm_smem_bytes(BN, stages) + (FQ && p.fq_rows ? p.M * p.K * 2 : 0);
-  // the attribute is per function and device; setting it again is harmless
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  // all of the unified L1/shared storage as shared memory, so that two
-  // CTAs of the narrow (decode) configurations fit on one SM
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  if (e != cudaSuccess) return e;
+  int smem = gemm_smem_bytes(BN, stages) + (FQ && p.fq_rows ? p.M * p.K * 2 : 0);
   // resident CTAs per SM from the kernel's own resources (shared memory,
   // registers, threads, TMEM columns)
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, kern);
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
   int dev = 0, smem_sm = 0, reserved = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
-  const int per_cta_smem = smem + static_cast<int>(fa.sharedSizeBytes) + reserved;
+  // The block scheduler does not see TMEM: a CTA that finds its SM's columns
+  // taken blocks in tcgen05.alloc until the holder exits.  Pad the shared
+  // memory (few stages) so that no more CTAs fit an SM than its TMEM holds;
+  // otherwise two CTAs of one split-K cluster could share an SM and the
+  // one holding the columns would wait at the cluster barrier for the other.
+  const int tmem_occ = 512 / tmem_cols_for(BN, INT8);
+  const int fixed = static_cast<int>(fa.sharedSizeBytes) + reserved;
+  if (smem_sm / (smem + fixed) > tmem_occ) smem = ((smem_sm / (tmem_occ + 1) + 1 - fixed) + 1023) & ~1023;
+  // the attribute is per function and device; setting it again is harmless
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  // all of the unified L1/shared storage as shared memory, so that two
+  // CTAs of the narrow (decode) configurations fit on one SM
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return e;
+  const int per_cta_smem = smem + fixed;
   const int regs_per_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
   int occ = smem_sm / per_cta_smem;
   occ = min(occ, 65536 / (regs_per_warp * (kThreads / 32)));
@@ -1153,7 +1168,8 @@ cudaError_t dispatch(const CUtensorMap& tp, const CUtensorMap& tq, const MmParam
     // wave-balancing widths for the large-M e4m3 regime (tokens on the
     // 128-row side only)
     case 160:
-      if (INT8 || swap) return cudaErrorInvalidValue;
+      if (swap) return cudaErrorInvalidValue;
+      if (INT8) return launch_out<160, false, true>(tp, tq, p, out_kind, stages, stream);
       return launch_out<160, false, false>(tp, tq, p, out_kind, stages, stream);
     case 192:
       if (INT8 || swap) return cudaErrorInvalidValue;

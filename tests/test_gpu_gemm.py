@@ -196,6 +196,8 @@ INT8_CONFIGS = [
     {"swap_ab": 1, "block_n": 128, "split_k": 2},
     {"swap_ab": 0, "block_n": 256, "split_k": 1},
     {"swap_ab": 0, "block_n": 256, "split_k": 2},
+    {"swap_ab": 0, "block_n": 160, "split_k": 1},
+    {"swap_ab": 0, "block_n": 160, "split_k": 2, "stages": 2},
     {"swap_ab": 1, "block_n": 16, "split_k": 3, "reduce": w8.REDUCE_GLOBAL},
     {"swap_ab": 0, "block_n": 256, "split_k": 2, "reduce": w8.REDUCE_GLOBAL},
     {"swap_ab": 1, "block_n": 32, "split_k": 8, "reduce": w8.REDUCE_CLUSTER},
@@ -219,6 +221,7 @@ def test_int8_variants_bit_exact(cfg, shape):
 
 @pytest.mark.parametrize("cfg", [None, {"swap_ab": 0, "block_n": 128, "split_k": 1},
                                  {"swap_ab": 0, "block_n": 256, "split_k": 1},
+                                 {"swap_ab": 0, "block_n": 160, "split_k": 1},
                                  {"swap_ab": 1, "block_n": 16, "split_k": 4}])
 def test_int8_worst_case_magnitudes_exact(cfg):
     """+-127 / -128 everywhere at a long K: every 1024-long chunk reaches

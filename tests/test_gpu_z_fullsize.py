@@ -138,6 +138,32 @@ def test_int8_llama70b(proj):
     assert w8.device_status() == 0
 
 
+@pytest.mark.parametrize("block_n", [160, 256])
+def test_int8_llama70b_qkv_tile_widths(block_n):
+    """Both int8 accumulator layouts at full size, many tiles per persistent
+    CTA: two chunk accumulators alternating (160 columns) and one chunk
+    accumulator (256 columns)."""
+    name, N, K = LLAMA70B[0]
+    M = 8192
+    wt = si.normal((N, K), seed=1500 + block_n, std=0.02)
+    x = si.normal_with_outliers((M, K), seed=1600 + block_n)
+    wq, sw = gpu_quant(wt, oracle.INT8, per_token=True)
+    aq, sa = gpu_quant(x, oracle.INT8, per_token=True)
+    owq, osw = check_quant(wt, wq, sw, oracle.INT8, True)
+    oaq, osa = check_quant(x, aq, sa, oracle.INT8, True)
+    del wt, x
+    cfg = {"swap_ab": 0, "block_n": block_n, "split_k": 1}
+    acc = torch.empty(M, N, dtype=torch.int32, device="cuda")
+    w8.scaled_mm(aq, wq, sa, sw, acc, config=cfg)
+    torch.cuda.synchronize()
+    im, inn = sample_points(M, N, seed=block_n)
+    ref = oracle.scaled_mm_sample(oaq.view(np.int8), owq.view(np.int8), osa, osw, oracle.INT8, oracle.FP16,
+                                  im, inn)
+    gacc = acc.cpu().numpy()[im, inn].astype(np.int64)
+    assert np.array_equal(gacc, ref["iacc"]), f"{(gacc != ref['iacc']).sum()} int32 accumulators differ ({name})"
+    assert w8.device_status() == 0
+
+
 def test_kv_cache_fp8_round_trip_full():
     T, H, D = 65536, 8, 128
     for j in range(2):  # K then V, each with its own per-tensor scale
