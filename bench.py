@@ -429,6 +429,45 @@ def measure_kv(dev, steps, warmup, stream, pk):
                          "bytes_note": "quant 5 B/element (absmax read 2 + read 2 + write 1), dequant 3 B/element"}}
 
 
+def measure_kv_attention(dev, steps, warmup, stream, pk):
+    """Decode attention reading an e4m3 KV cache with per-tensor K / V scales:
+    16 sequences x 4096 tokens, 32 query heads over 8 KV heads of 128
+    (Llama-3-8B), one query token per sequence.  Two cache sets alternate
+    (268 MB, larger than L2), so every call streams its cache from HBM."""
+    import torch
+    import int8_w8a8_scaled_gb300 as w8
+    import synthetic_inputs as si
+    B, T, Hkv, Hq, D = 16, 4096, 8, 32, 128
+    def finite_codes(seed):
+        c = si.random_codes((B, T, Hkv, D), seed=seed, device=dev)
+        return torch.where((c & 0x7F) == 0x7F, c - 1, c)     # NaN codes -> +-448
+
+    sets = []
+    for j in range(2):
+        kc = finite_codes(5000 + 2 * j)
+        vc = finite_codes(5001 + 2 * j)
+        q = si.normal((B, Hq, D), seed=5100 + j, device=dev)
+        out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev)
+        sets.append((q, kc, vc, out))
+    lens = torch.full((B,), T, dtype=torch.int32, device=dev)
+    ks = torch.full((1,), 0.02, dtype=torch.float32, device=dev)
+    vs = torch.full((1,), 0.01, dtype=torch.float32, device=dev)
+    ws = w8.Workspace(w8.attention_workspace_size(B, Hq, T), dev)
+
+    def step():
+        for q, kc, vc, out in sets:
+            w8.fp8_kv_decode_attention(q, kc, vc, lens, ks, vs, out, workspace=ws, stream=stream)
+
+    t = time_graph(graph_of(step, stream), stream, steps, warmup) / steps / len(sets)
+    byts = 2 * B * T * Hkv * D + 2 * 2 * B * Hq * D   # codes of K and V, q and out (bf16)
+    hbm = pk["hbm_gbs"]
+    gbs = byts / t / 1e9
+    return {"workload": "decode attention over an e4m3 KV cache, 16 seqs x 4096 tokens, 32 q / 8 kv heads x 128",
+            "value": gbs, "unit": "GB/s", "us_per_call": t * 1e6,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                         "bytes_note": "1 B per K and V code + q and out (bf16); per-tensor scales"}}
+
+
 # ---------------------------------------------------------------- CPU baseline (oracle)
 
 _ORACLE_WEIGHTS = {}
@@ -487,6 +526,7 @@ PROFILE_CASES = {
     "dequant_kv": "e4m3 -> bf16 dequantiser, KV [524288 x 128]",
     "decode_step": "the decode step (16 quantisers + 16 GEMMs), eager launches",
     "quant_decode": "per-token dynamic e4m3 quantiser of one decode token, [1 x 4096] bf16",
+    "attention": "decode attention over an e4m3 KV cache, 16 seqs x 4096 tokens, 32 q / 8 kv heads x 128",
 }
 
 
@@ -539,6 +579,16 @@ def run_profile_case(name: str, launches: int, override=None):
         s = torch.empty(4096, dtype=torch.float32, device=dev)
         for _ in range(launches):
             w8.scaled_quant(x, q, s, per_token=True, dynamic=True)
+    elif name == "attention":
+        B, T, Hkv, Hq, D = 16, 4096, 8, 32, 128
+        kc = si.random_codes((B, T, Hkv, D), seed=5000, device=dev)
+        vc = si.random_codes((B, T, Hkv, D), seed=5001, device=dev)
+        q = si.normal((B, Hq, D), seed=5100, device=dev)
+        out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev)
+        lens = torch.full((B,), T, dtype=torch.int32, device=dev)
+        ks = torch.full((1,), 0.02, dtype=torch.float32, device=dev)
+        for _ in range(launches):
+            w8.fp8_kv_decode_attention(q, kc, vc, lens, ks, ks, out)
     elif name in ("quant_kv", "dequant_kv"):
         x = si.kv_with_spikes(65536, 8, 128, seed=4, device=dev).reshape(-1, 128)
         q = torch.empty(x.shape, dtype=torch.float8_e4m3fn, device=dev)
@@ -801,6 +851,7 @@ def run_ours(args):
         workloads["prefill_fp8_static"] = measure_prefill_fp8(dev, extra_steps, max(3, args.warmup), stream, pk)
         workloads["int8_70b"] = measure_int8_70b(dev, extra_steps, max(3, args.warmup), stream, pk)
         workloads["kv_cache_fp8"] = measure_kv(dev, extra_steps, max(3, args.warmup), stream, pk)
+        workloads["kv_fp8_attention"] = measure_kv_attention(dev, extra_steps, max(3, args.warmup), stream, pk)
     workloads["decode_fp8_detail"] = {
         "gemm_us_per_step": t_gemm * 1e6, "quant_us_per_step": t_quant * 1e6,
         "gemm_gbs": gemm_gbs, "gemm_frac_hbm": gemm_gbs / hbm,

@@ -322,6 +322,45 @@ W8A8_API w8a8_status w8a8_requant_shards(const void* q, int q_dtype, int64_t col
                                          float* scale_out, w8a8_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Decode attention over an fp8 (e4m3) KV cache
+ *
+ * "Enable scaled FP8 (e4m3fn) KV cache on ROCm (AMD GPU)", section
+ * "Scaling semantics": the cache holds e4m3 codes written with one
+ * per-tensor scaling factor for K and one for V (absmax / 448), and the
+ * paged attention kernel dequantises as decode(code) * kv_scale.  For one
+ * query token per sequence and every query head h (KV head h / G,
+ * G = num_q_heads / num_kv_heads):
+ *   s_t = sm_scale * sum_d q[b,h,d] * (decode(K[t,d]) * k_scale)
+ *   out[b,h,:] = sum_t softmax(s)_t * (decode(V[t,:]) * v_scale)
+ * over the tokens t < seq_lens[b] (an empty sequence gives zeros).
+ *
+ * Layouts (all DEVICE memory, caller-owned, 16-byte aligned caches):
+ *   q, out        [batch, num_q_heads, 128] contiguous, bf16 or fp16
+ *   k/v_cache     e4m3 token rows of num_kv_heads * 128 bytes.  Without a
+ *                 block table (block_table NULL) token t of sequence b is
+ *                 row b * max_seq_len + t.  With one (int32
+ *                 [batch, max_blocks], the paged cache) it is row
+ *                 block_table[b * max_blocks + t / block_size] * block_size
+ *                 + t % block_size, and num_blocks blocks exist; tokens
+ *                 whose block id is outside [0, num_blocks) are skipped.
+ *   seq_lens      int32 [batch], clamped to [0, max_seq_len]
+ *   k_scale, v_scale  fp32 [1]
+ * head_dim must be 128 and G one of 1, 2, 4, 8.  The workspace holds the
+ * per-chunk partial results (w8a8_fp8_kv_attention_workspace_size).  No
+ * allocation, no synchronisation; graph-capturable.  Errors: INVALID_ARG
+ * (null pointer, sizes, head_dim, G), MISALIGNED (cache base not 16-byte
+ * aligned), WORKSPACE (too small), CUDA (launch). */
+W8A8_API size_t w8a8_fp8_kv_attention_workspace_size(int64_t batch, int64_t num_q_heads,
+                                                     int64_t max_seq_len);
+
+W8A8_API w8a8_status w8a8_fp8_kv_decode_attention(
+    const void* q, int q_dtype, int64_t batch, int64_t num_q_heads, int64_t num_kv_heads,
+    int64_t head_dim, const void* k_cache, const void* v_cache, int64_t max_seq_len,
+    const int32_t* block_table, int64_t block_size, int64_t max_blocks, int64_t num_blocks,
+    const int32_t* seq_lens, const float* k_scale, const float* v_scale, float sm_scale,
+    void* out, int out_dtype, void* workspace, size_t workspace_bytes, w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Scaled matmul without a caller-provided workspace
  *
  * No counterpart on the source pages: this entry point exists for callers

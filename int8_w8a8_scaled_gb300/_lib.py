@@ -48,6 +48,8 @@ EXPORTS = (
     "w8a8_debug_mm_trace",
     "w8a8_quant_scaled_mm_workspace_size",
     "w8a8_quant_scaled_mm",
+    "w8a8_fp8_kv_attention_workspace_size",
+    "w8a8_fp8_kv_decode_attention",
 )
 
 
@@ -120,6 +122,11 @@ def load(build_if_needed: bool = True):
         lib.w8a8_quant_scaled_mm_workspace_size.argtypes = [I64, I64, I64, I]
         lib.w8a8_quant_scaled_mm.restype = I
         lib.w8a8_quant_scaled_mm.argtypes = [P, I, I64, P, I64, P, I, P, I64, I64, I64, I64, I, I, P, I, P, SZ, P]
+        lib.w8a8_fp8_kv_attention_workspace_size.restype = SZ
+        lib.w8a8_fp8_kv_attention_workspace_size.argtypes = [I64, I64, I64]
+        lib.w8a8_fp8_kv_decode_attention.restype = I
+        lib.w8a8_fp8_kv_decode_attention.argtypes = [P, I, I64, I64, I64, I64, P, P, I64, P, I64, I64, I64,
+                                                     P, P, P, ctypes.c_float, P, I, P, SZ, P]
         lib.w8a8_device_status.restype = I
         lib.w8a8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
         _lib = lib

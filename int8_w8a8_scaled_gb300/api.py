@@ -28,7 +28,7 @@ from ._lib import (BF16, DYNAMIC, E4M3, FP16, FP32, INT8, INT32, PER_ROW, PER_TE
 __all__ = [
     "scaled_quant", "scaled_dequant", "scaled_mm", "mm_workspace_size",
     "quant_workspace_size", "pick_config", "device_status", "Workspace", "quant_scaled_mm",
-    "expand_shard_scales", "requant_shards",
+    "expand_shard_scales", "requant_shards", "fp8_kv_decode_attention", "attention_workspace_size",
     "W8A8Error", "MmConfig",
 ]
 
@@ -311,3 +311,69 @@ def device_status() -> int:
     v = ctypes.c_int(0)
     check(_lib.load().w8a8_device_status(ctypes.byref(v)))
     return v.value
+
+
+def attention_workspace_size(batch: int, num_q_heads: int, max_seq_len: int) -> int:
+    return int(_lib.load().w8a8_fp8_kv_attention_workspace_size(batch, num_q_heads, max_seq_len))
+
+
+def fp8_kv_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            seq_lens: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                            out: torch.Tensor, sm_scale: float | None = None,
+                            block_table: torch.Tensor | None = None, workspace=None, stream=None) -> None:
+    """Decode attention reading an e4m3 KV cache with per-tensor scales
+    ("Enable scaled FP8 (e4m3fn) KV cache on ROCm", "Scaling semantics").
+
+    q, out: [batch, num_q_heads, 128] bf16 / fp16.  Without block_table the
+    caches are [batch, max_seq_len, num_kv_heads, 128]; with block_table
+    (int32 [batch, max_blocks]) they are [num_blocks, block_size,
+    num_kv_heads, 128] (the paged cache).  Codes are float8_e4m3fn (or uint8
+    views).  seq_lens: int32 [batch]; k_scale, v_scale: float32 [1].
+    sm_scale defaults to 1/sqrt(128)."""
+    _cuda(q, k_cache, v_cache, seq_lens, k_scale, v_scale, out)
+    lib = _lib.load()
+    if q.dim() != 3 or not q.is_contiguous() or tuple(out.shape) != tuple(q.shape) or not out.is_contiguous():
+        raise ValueError("q and out must be contiguous [batch, num_q_heads, head_dim] tensors")
+    batch, hq, d = q.shape
+    if k_cache.dim() != 4 or tuple(k_cache.shape) != tuple(v_cache.shape):
+        raise ValueError("k_cache and v_cache must be 4-d tensors of one shape")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("caches must be contiguous")
+    for c in (k_cache, v_cache):
+        if c.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise TypeError("caches must hold float8_e4m3fn codes (or uint8 views)")
+    hkv = k_cache.shape[2]
+    if k_cache.shape[3] != d:
+        raise ValueError("cache head_dim must equal q's")
+    if seq_lens.dtype != torch.int32 or seq_lens.numel() != batch or not seq_lens.is_contiguous():
+        raise ValueError("seq_lens must be a contiguous int32 tensor of batch entries")
+    for s_ in (k_scale, v_scale):
+        if s_.dtype != torch.float32 or s_.numel() != 1:
+            raise ValueError("k_scale and v_scale must be float32 tensors of one element")
+    if block_table is None:
+        if k_cache.shape[0] != batch:
+            raise ValueError("without a block table the caches are [batch, max_seq_len, num_kv_heads, head_dim]")
+        max_seq = k_cache.shape[1]
+        bt, bsz, maxb, nblk = None, 0, 0, 0
+    else:
+        if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != batch \
+                or not block_table.is_contiguous():
+            raise ValueError("block_table must be a contiguous int32 [batch, max_blocks] tensor")
+        _cuda(block_table)
+        nblk, bsz = k_cache.shape[0], k_cache.shape[1]
+        maxb = block_table.shape[1]
+        max_seq = maxb * bsz
+        bt = _ptr(block_table)
+    need = lib.w8a8_fp8_kv_attention_workspace_size(batch, hq, max_seq)
+    if isinstance(workspace, Workspace):
+        wbuf = workspace.ensure(need).buf
+    elif workspace is None:
+        wbuf = _default_workspace(q.device, need, "attention").buf
+    else:
+        wbuf = workspace
+    if sm_scale is None:
+        sm_scale = 1.0 / float(d) ** 0.5
+    check(lib.w8a8_fp8_kv_decode_attention(
+        _ptr(q), _fkind(q), batch, hq, hkv, d, _ptr(k_cache), _ptr(v_cache), max_seq, bt, bsz, maxb, nblk,
+        _ptr(seq_lens), _ptr(k_scale), _ptr(v_scale), float(sm_scale), _ptr(out), _fkind(out),
+        _ptr(wbuf), wbuf.numel(), _stream(stream)))

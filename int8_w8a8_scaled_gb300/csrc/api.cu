@@ -736,6 +736,82 @@ w8a8_status w8a8_requant_shards(const void* q, int q_dtype, int64_t cols, int64_
   return ok();
 }
 
+namespace {
+// Tokens per CTA of the attention: the largest of 256 / 128 / 64 that still
+// gives two CTAs per SM; the workspace is sized for 64.
+int attn_chunk_for(long long batch, long long kv_heads, long long max_seq, int sms) {
+  int chunk = w8a8::attn_max_chunk();
+  while (chunk > 64 && batch * kv_heads * ((max_seq + chunk - 1) / chunk) < 2LL * sms) chunk /= 2;
+  return chunk;
+}
+}  // namespace
+
+size_t w8a8_fp8_kv_attention_workspace_size(int64_t batch, int64_t num_q_heads, int64_t max_seq_len) {
+  if (batch < 1 || num_q_heads < 1 || max_seq_len < 1) return 0;
+  return static_cast<size_t>(batch) * num_q_heads * ((max_seq_len + 63) / 64) * w8a8::attn_part_stride() *
+         sizeof(float);
+}
+
+w8a8_status w8a8_fp8_kv_decode_attention(const void* q, int q_dtype, int64_t batch, int64_t num_q_heads,
+                                         int64_t num_kv_heads, int64_t head_dim, const void* k_cache,
+                                         const void* v_cache, int64_t max_seq_len, const int32_t* block_table,
+                                         int64_t block_size, int64_t max_blocks, int64_t num_blocks,
+                                         const int32_t* seq_lens, const float* k_scale, const float* v_scale,
+                                         float sm_scale, void* out, int out_dtype, void* workspace,
+                                         size_t workspace_bytes, w8a8_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !seq_lens || !k_scale || !v_scale || !out)
+    return fail(W8A8_ERR_INVALID_ARG, "null pointer argument");
+  if ((q_dtype != W8A8_BF16 && q_dtype != W8A8_FP16) || (out_dtype != W8A8_BF16 && out_dtype != W8A8_FP16))
+    return fail(W8A8_ERR_INVALID_ARG, "q and out must be BF16 or FP16");
+  if (head_dim != 128) return fail(W8A8_ERR_INVALID_ARG, "head_dim must be 128");
+  if (batch < 1 || num_q_heads < 1 || num_kv_heads < 1 || max_seq_len < 1)
+    return fail(W8A8_ERR_INVALID_ARG, "batch, head counts and max_seq_len must be >= 1");
+  if (batch > 65535 || num_kv_heads > 65535 || max_seq_len > (1LL << 30) || num_q_heads > 65535)
+    return fail(W8A8_ERR_INVALID_ARG, "sizes exceed the launch grid");
+  if (num_q_heads % num_kv_heads != 0) return fail(W8A8_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
+  const long long G = num_q_heads / num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return fail(W8A8_ERR_INVALID_ARG, "num_q_heads / num_kv_heads must be 1, 2, 4 or 8");
+  if (block_table && (block_size < 1 || max_blocks < 1 || num_blocks < 1 || max_blocks * block_size < max_seq_len))
+    return fail(W8A8_ERR_INVALID_ARG, "a block table needs block_size, max_blocks, num_blocks >= 1 and "
+                                      "max_blocks * block_size >= max_seq_len");
+  if (block_table && (block_size > (1 << 30) || max_blocks > (1 << 30) || num_blocks > (1LL << 31) / block_size))
+    return fail(W8A8_ERR_INVALID_ARG, "block table sizes out of range");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return fail(W8A8_ERR_MISALIGNED, "caches must be 16-byte aligned");
+  if (!aligned(seq_lens, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4) || (block_table && !aligned(block_table, 4)) ||
+      !aligned(q, 2) || !aligned(out, 2))
+    return fail(W8A8_ERR_MISALIGNED, "misaligned q, out, scale, length or block table pointer");
+  const size_t need = w8a8_fp8_kv_attention_workspace_size(batch, num_q_heads, max_seq_len);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 16))
+    return fail(W8A8_ERR_WORKSPACE, "workspace must be 16-byte aligned and hold %zu bytes", need);
+  w8a8_status st;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != W8A8_OK) return st;
+  w8a8::AttnParams p{};
+  p.q = q;
+  p.q_fp16 = q_dtype == W8A8_FP16;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_table = block_table;
+  p.block_size = block_table ? static_cast<int>(block_size) : 1;
+  p.max_blocks = block_table ? static_cast<int>(max_blocks) : 1;
+  p.num_blocks = block_table ? static_cast<int>(num_blocks) : 1;
+  p.seq_lens = seq_lens;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.sm_scale = sm_scale;
+  p.out = out;
+  p.out_fp16 = out_dtype == W8A8_FP16;
+  p.partial = static_cast<float*>(workspace);
+  p.batch = static_cast<int>(batch);
+  p.num_q_heads = static_cast<int>(num_q_heads);
+  p.num_kv_heads = static_cast<int>(num_kv_heads);
+  p.max_seq_len = static_cast<int>(max_seq_len);
+  p.chunk = attn_chunk_for(batch, num_kv_heads, max_seq_len, dev.sms);
+  cudaError_t e = w8a8::launch_fp8kv_attention(p, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fp8 KV attention launch");
+  return ok();
+}
+
 w8a8_status w8a8_debug_mm_trace(void* buf, size_t bytes) {
   if (buf && !aligned(buf, 8)) return fail(W8A8_ERR_MISALIGNED, "trace buffer must be 8-byte aligned");
   const size_t per_cta = 16 * sizeof(unsigned long long);

@@ -85,6 +85,31 @@ int gemm_smem_bytes(int block_n, int stages);
 constexpr int kMaxClusterSplit = 8;
 int max_stages_for(int block_n, int smem_budget);
 
+// Decode attention over an e4m3 KV cache (attention.cu).  Caches hold
+// token rows of num_kv_heads * 128 codes; token t of sequence b sits in row
+// b * max_seq_len + t, or with a block table in row
+// block_table[b * max_blocks + t / block_size] * block_size + t % block_size.
+struct AttnParams {
+  const void* q;        // [batch, num_q_heads, 128] bf16 / fp16
+  int q_fp16;
+  const void* k_cache;  // e4m3 rows
+  const void* v_cache;
+  const int* block_table;  // null: contiguous per-sequence rows
+  int block_size, max_blocks, num_blocks;
+  const int* seq_lens;  // [batch], clamped to [0, max_seq_len]
+  const float* k_scale; // [1]
+  const float* v_scale; // [1]
+  float sm_scale;
+  void* out;            // [batch, num_q_heads, 128] bf16 / fp16
+  int out_fp16;
+  float* partial;       // [batch, num_q_heads, chunks, attn_part_stride()] fp32
+  int batch, num_q_heads, num_kv_heads, max_seq_len;
+  int chunk;            // tokens per CTA, <= attn_max_chunk()
+};
+int attn_part_stride();
+int attn_max_chunk();
+cudaError_t launch_fp8kv_attention(const AttnParams& p, cudaStream_t stream);
+
 // Quantiser / dequantiser launchers.
 struct QuantArgs {
   const void* x;

@@ -1,0 +1,147 @@
+"""Decode attention over an fp8 (e4m3) KV cache: the CUDA path against the
+oracle ("Enable scaled FP8 (e4m3fn) KV cache on ROCm", section "Scaling
+semantics": K and V dequantised as decode(code) * per-tensor scale inside the
+attention).
+
+The caches are seeded bf16 KV with rare spikes, quantised per tensor by the
+oracle on the CPU; both sides read the same codes.  Tolerance: the kernel
+computes in fp32 (exact code decoding, fp32 dot products and sums, exp2) and
+rounds the output to bf16 / fp16, so |gpu - ref| <= 2^-8 |ref| + 2^-14 r,
+where r is the same attention over |V| (the softmax-weighted mean of |V|,
+the scale of the fp32 rounding in the sums): half an output ulp is
+2^-9 |ref|, and fp32 score and sum errors stay near 1e-6 r.  A dropped or
+repeated token moves an output by about r / T, above the bound for every
+length tested but the 65536-token one."""
+import numpy as np
+import pytest
+import torch
+
+import int8_w8a8_scaled_gb300 as w8
+import oracle
+import synthetic_inputs as si
+from oracle import attention as oa
+from gpu_util import bits_np, out_to_f32
+
+pytestmark = pytest.mark.gpu
+
+
+def kv_codes(B, T, Hkv, D, seed):
+    """Seeded bf16 K and V [B, T, Hkv, D] quantised per tensor (oracle)."""
+    out = []
+    for j in range(2):
+        x = si.kv_with_spikes(B * T, Hkv, D, seed=seed + j)
+        codes, s = oracle.quant(si.bits16(x).reshape(B * T, Hkv * D), oracle.BF16, oracle.E4M3, oracle.PER_TENSOR)
+        out.append((codes.reshape(B, T, Hkv, D), np.float32(s[0])))
+    return out
+
+
+def run_case(B, Hq, Hkv, T, lens, seed, q_dtype=torch.bfloat16, out_dtype=torch.bfloat16, paged_bs=0,
+             check_b=None):
+    D = 128
+    (k, ks), (v, vs) = kv_codes(B, T, Hkv, D, seed)
+    q = si.normal((B, Hq, D), seed=seed + 7, dtype=q_dtype)
+    qkind = oracle.BF16 if q_dtype == torch.bfloat16 else oracle.FP16
+    lens = np.asarray(lens, np.int32)
+    table = None
+    kc, vc = k, v
+    if paged_bs:
+        nbps = T // paged_bs
+        nb = B * nbps + 3                      # a few blocks no sequence uses
+        perm = np.random.default_rng(seed).permutation(nb)[:B * nbps]
+        table = perm.reshape(B, nbps).astype(np.int32)
+        kc = np.zeros((nb, paged_bs, Hkv, D), np.uint8)
+        vc = np.zeros((nb, paged_bs, Hkv, D), np.uint8)
+        for b in range(B):
+            for j in range(nbps):
+                kc[table[b, j]] = k[b, j * paged_bs:(j + 1) * paged_bs]
+                vc[table[b, j]] = v[b, j * paged_bs:(j + 1) * paged_bs]
+    dev = "cuda"
+    out = torch.empty(B, Hq, D, dtype=out_dtype, device=dev)
+    w8.fp8_kv_decode_attention(q.to(dev), torch.from_numpy(kc).to(dev), torch.from_numpy(vc).to(dev),
+                               torch.from_numpy(lens).to(dev), torch.tensor([ks], device=dev),
+                               torch.tensor([vs], device=dev), out,
+                               block_table=None if table is None else torch.from_numpy(table).to(dev))
+    torch.cuda.synchronize()
+    okind = oracle.BF16 if out_dtype == torch.bfloat16 else oracle.FP16
+    got = out_to_f32(bits_np(out), okind).astype(np.float64)
+    bsel = list(range(B)) if check_b is None else check_b
+    qb = si.bits16(q)[bsel]
+    ref = oa.fp8_kv_decode_attention(qb, qkind, k[bsel], v[bsel], lens[bsel], ks, vs, 1.0 / np.sqrt(D))
+    # the same weights over |V| (clearing an e4m3 code's sign bit gives |value|)
+    r_abs = oa.fp8_kv_decode_attention(qb, qkind, k[bsel], v[bsel] & 0x7F, lens[bsel], ks, vs, 1.0 / np.sqrt(D))
+    err = np.abs(got[bsel] - ref)
+    bound = 2.0 ** -8 * np.abs(ref) + 2.0 ** -14 * r_abs
+    bad = err > bound
+    assert not bad.any(), f"{int(bad.sum())} outputs off; worst {float((err - bound).max())}"
+    for b in bsel:
+        if lens[b] == 0:
+            assert np.all(got[b] == 0.0)
+    return got, ref
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_grouped_heads_ragged_lengths(G):
+    Hkv = 2
+    # one token, a chunk boundary, a ragged tail, the maximum length
+    run_case(B=4, Hq=Hkv * G, Hkv=Hkv, T=600, lens=[1, 256, 333, 600], seed=100 + G)
+
+
+def test_paged_cache_and_empty_sequence():
+    run_case(B=3, Hq=8, Hkv=2, T=512, lens=[512, 0, 77], seed=200, paged_bs=16)
+
+
+def test_fp16_query_and_output():
+    run_case(B=2, Hq=8, Hkv=2, T=300, lens=[300, 129], seed=300, q_dtype=torch.float16, out_dtype=torch.float16)
+
+
+def test_llama3_8b_decode_shape_sampled():
+    """16 sequences x 4096 tokens, 32 query / 8 KV heads (the benchmark's
+    shape), every output of four sequences checked."""
+    run_case(B=16, Hq=32, Hkv=8, T=4096, lens=[4096] * 15 + [1000], seed=400, check_b=[0, 7, 14, 15])
+
+
+def test_long_single_sequence():
+    """One sequence of 65536 tokens: 8 KV heads x 128 (the KV-cache tensor
+    of the quantiser benchmark), many chunks combined."""
+    run_case(B=1, Hq=32, Hkv=8, T=65536, lens=[65536], seed=500)
+
+
+def test_graph_capture_and_determinism():
+    """Same inputs twice inside one CUDA graph: identical bits (no atomics)."""
+    B, Hq, Hkv, T, D = 4, 16, 4, 1024, 128
+    (k, ks), (v, vs) = kv_codes(B, T, Hkv, D, 600)
+    dev = "cuda"
+    q = si.normal((B, Hq, D), seed=601).to(dev)
+    kc, vc = torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev)
+    lens = torch.tensor([1024, 999, 1, 512], dtype=torch.int32, device=dev)
+    ksc, vsc = torch.tensor([ks], device=dev), torch.tensor([vs], device=dev)
+    outs = [torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    ws = w8.Workspace(w8.attention_workspace_size(B, Hq, T))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        w8.fp8_kv_decode_attention(q, kc, vc, lens, ksc, vsc, outs[0], workspace=ws, stream=s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for o in outs:
+                w8.fp8_kv_decode_attention(q, kc, vc, lens, ksc, vsc, o, workspace=ws, stream=s)
+    for o in outs:
+        o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_argument_errors():
+    dev = "cuda"
+    q = torch.zeros(2, 6, 128, dtype=torch.bfloat16, device=dev)
+    kc = torch.zeros(2, 16, 4, 128, dtype=torch.uint8, device=dev)
+    lens = torch.ones(2, dtype=torch.int32, device=dev)
+    sc = torch.ones(1, device=dev)
+    out = torch.empty_like(q)
+    with pytest.raises(w8.W8A8Error):    # 6 query heads over 4 KV heads
+        w8.fp8_kv_decode_attention(q, kc, kc, lens, sc, sc, out)
+    q64 = torch.zeros(2, 8, 64, dtype=torch.bfloat16, device=dev)
+    kc64 = torch.zeros(2, 16, 4, 64, dtype=torch.uint8, device=dev)
+    with pytest.raises(w8.W8A8Error):    # head_dim 64
+        w8.fp8_kv_decode_attention(q64, kc64, kc64, lens, sc, sc, torch.empty_like(q64))
