@@ -119,3 +119,30 @@ def test_pick_config_regimes(M):
         assert c["split_k"] == 1 and c["block_n"] >= 128   # many tiles: no split, wide tile
     c8 = w8.pick_config(M, 4096, 4096, w8.INT8)
     assert c8["block_n"] <= 128 or (c8["block_n"] in (160, 256) and not c8["swap_ab"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), 1), (dict(kc=None), 1), (dict(lens=None), 1), (dict(out=None), 1),
+    (dict(qd=w8.E4M3), 1), (dict(od=w8.INT8), 1), (dict(hd=64), 1), (dict(hq=12), 1), (dict(hq=24, hkv=8), 1),
+    (dict(batch=0), 1), (dict(maxseq=0), 1),
+    (dict(bt=FAKE, bs=16, maxb=2, nblk=8), 1),          # max_blocks * block_size < max_seq_len
+    (dict(kc=FAKE_ODD), 3), (dict(ws=None), 4), (dict(wsb=16), 4),
+])
+def test_attention_rejects_bad_arguments(kw, status):
+    """w8a8_fp8_kv_decode_attention validates everything before any CUDA call."""
+    lib = _lib.load()
+    a = dict(q=FAKE, qd=w8.BF16, batch=2, hq=32, hkv=8, hd=128, kc=FAKE, vc=FAKE, maxseq=4096, bt=None, bs=0,
+             maxb=0, nblk=0, lens=FAKE, ks=FAKE, vs=FAKE, out=FAKE, od=w8.BF16, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    st = lib.w8a8_fp8_kv_decode_attention(a["q"], a["qd"], a["batch"], a["hq"], a["hkv"], a["hd"], a["kc"], a["vc"],
+                                          a["maxseq"], a["bt"], a["bs"], a["maxb"], a["nblk"], a["lens"], a["ks"],
+                                          a["vs"], 0.088, a["out"], a["od"], a["ws"], a["wsb"], None)
+    assert st == status
+    assert lib.w8a8_last_error()
+
+
+def test_attention_workspace_size():
+    # 64-token chunks at most: [batch, q heads, chunks, 132 floats]
+    assert w8.attention_workspace_size(16, 32, 4096) == 16 * 32 * 64 * 132 * 4
+    assert w8.attention_workspace_size(1, 8, 1) == 8 * 1 * 132 * 4
+    assert w8.attention_workspace_size(0, 8, 10) == 0
