@@ -5,10 +5,10 @@ the package smoke check and the CPU-baseline leg of the benchmark may use it.
 
 What it computes, in float64, straight from the definitions:
   * dequantisation, "Enable scaled FP8 (e4m3fn) KV cache on ROCm (AMD GPU)",
-    section "Scaling semantics": higher precision = fp8_dequant(code) *
-    scaling_factor, one per-tensor factor for K and one for V (the kv_scale of
-    the paged attention kernel).  fp8_dequant is the exact value of the OCP
-    e4m3fn code (``oracle.e4m3_value``).
+    section "Scaling semantics": a cached code stands for its e4m3 value
+    times the tensor's scaling factor, with one per-tensor factor for K and
+    one for V (the kv_scale of the paged attention kernel).  The e4m3 value
+    is the exact value of the OCP e4m3fn code (``oracle.e4m3_value``).
   * attention: the pages name the kernel (paged attention) but not its
     arithmetic; the plain reading is textbook scaled-dot-product attention
     of one query token per sequence over the cached tokens t < seq_len,
