@@ -74,8 +74,10 @@ __device__ __forceinline__ int seq_len_of(const AttnParams& p, int b) {
   return len < 0 ? 0 : (len > p.max_seq_len ? p.max_seq_len : len);
 }
 
+// Up to 4 heads per KV head the kernel fits 96 registers without spilling,
+// so 5 CTAs (20 warps) share an SM instead of 4; at 8 heads a cap spills.
 template <int G>
-__global__ void __launch_bounds__(kAttnThreads) fp8kv_attn_chunk_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kAttnThreads, G <= 4 ? 5 : 1) fp8kv_attn_chunk_kernel(const AttnParams p) {
   const int b = blockIdx.z;
   const int kvh = blockIdx.y;
   const int ch = blockIdx.x;
