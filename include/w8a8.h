@@ -349,7 +349,8 @@ W8A8_API w8a8_status w8a8_requant_shards(const void* q, int q_dtype, int64_t col
  * per-chunk partial results (w8a8_fp8_kv_attention_workspace_size).  No
  * allocation, no synchronisation; graph-capturable.  Errors: INVALID_ARG
  * (null pointer, sizes, head_dim, G), MISALIGNED (cache base not 16-byte
- * aligned), WORKSPACE (too small), CUDA (launch). */
+ * aligned), WORKSPACE (too small), CUDA (launch).  The workspace size is
+ * 0 for invalid sizes, including a size beyond 2^62 bytes. */
 W8A8_API size_t w8a8_fp8_kv_attention_workspace_size(int64_t batch, int64_t num_q_heads,
                                                      int64_t max_seq_len);
 

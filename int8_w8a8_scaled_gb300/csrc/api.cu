@@ -748,6 +748,10 @@ int attn_chunk_for(long long batch, long long kv_heads, long long max_seq, int s
 
 size_t w8a8_fp8_kv_attention_workspace_size(int64_t batch, int64_t num_q_heads, int64_t max_seq_len) {
   if (batch < 1 || num_q_heads < 1 || max_seq_len < 1) return 0;
+  // 0 as well when the size does not fit 2^62 bytes (no wrap-around)
+  const long double bytes = static_cast<long double>(batch) * num_q_heads * ((max_seq_len + 63) / 64) *
+                            w8a8::attn_part_stride() * sizeof(float);
+  if (bytes > static_cast<long double>(1ULL << 62)) return 0;
   return static_cast<size_t>(batch) * num_q_heads * ((max_seq_len + 63) / 64) * w8a8::attn_part_stride() *
          sizeof(float);
 }
@@ -781,6 +785,7 @@ w8a8_status w8a8_fp8_kv_decode_attention(const void* q, int q_dtype, int64_t bat
       !aligned(q, 2) || !aligned(out, 2))
     return fail(W8A8_ERR_MISALIGNED, "misaligned q, out, scale, length or block table pointer");
   const size_t need = w8a8_fp8_kv_attention_workspace_size(batch, num_q_heads, max_seq_len);
+  if (need == 0) return fail(W8A8_ERR_INVALID_ARG, "batch x heads x max_seq_len too large");
   if (!workspace || workspace_bytes < need || !aligned(workspace, 16))
     return fail(W8A8_ERR_WORKSPACE, "workspace must be 16-byte aligned and hold %zu bytes", need);
   w8a8_status st;

@@ -146,3 +146,9 @@ def test_attention_workspace_size():
     assert w8.attention_workspace_size(16, 32, 4096) == 16 * 32 * 64 * 132 * 4
     assert w8.attention_workspace_size(1, 8, 1) == 8 * 1 * 132 * 4
     assert w8.attention_workspace_size(0, 8, 10) == 0
+    # a product beyond 2^62 bytes is refused, not wrapped around
+    assert w8.attention_workspace_size(65535, 65535, 1 << 30) == 0
+    lib = _lib.load()
+    st = lib.w8a8_fp8_kv_decode_attention(FAKE, w8.BF16, 65535, 65535, 65535, 128, FAKE, FAKE, 1 << 30, None, 0, 0, 0,
+                                          FAKE, FAKE, FAKE, 0.088, FAKE, w8.BF16, FAKE, 1 << 40, None)
+    assert st == 1
