@@ -16,11 +16,16 @@ What it computes, in float64, straight from the definitions:
     reading KV head h // (num_q_heads // num_kv_heads).  An empty sequence
     gives zeros.
   * paging: token t of sequence b lives in cache row
-    block_table[b, t // block_size] * block_size + t % block_size.
+    block_table[b, t // block_size] * block_size + t % block_size.  A
+    table entry outside [0, num_blocks) marks padding: the tokens it would
+    hold are not attended to (the usual -1 padding of a block table, and
+    any id past the end of the cache alike).  A sequence with no attended
+    token gives zeros, as an empty one does.
 
 Pinned by ``tests/test_oracle_attention.py``: brute force with Python
 scalars on tiny inputs, closed forms (one token, equal keys, a dominant
-key), the paged layout against the contiguous one, and grouped heads against
+key), the paged layout against the contiguous one, padding entries against
+the contiguous sequence with those tokens removed, and grouped heads against
 one head at a time.
 """
 from __future__ import annotations
@@ -41,13 +46,16 @@ def e4m3_table() -> np.ndarray:
 
 
 def gather_rows(cache: np.ndarray, b: int, n: int, block_table=None) -> np.ndarray:
-    """Rows of tokens 0..n-1 of sequence b: [n, num_kv_heads, head_dim]."""
+    """Rows of the attended tokens among 0..n-1 of sequence b, in token
+    order: [n', num_kv_heads, head_dim].  Without a block table all n; with
+    one, the tokens whose block id lies in [0, num_blocks)."""
     if block_table is None:
         return cache[b, :n]
-    bs = cache.shape[1]
+    num_blocks, bs = cache.shape[0], cache.shape[1]
     t = np.arange(n)
-    blk = np.asarray(block_table)[b, t // bs]
-    return cache[blk, t % bs]
+    blk = np.asarray(block_table, dtype=np.int64)[b, t // bs]
+    keep = (blk >= 0) & (blk < num_blocks)
+    return cache[blk[keep], (t % bs)[keep]]
 
 
 def fp8_kv_decode_attention(q_bits, q_dtype: int, k_codes, v_codes, seq_lens, k_scale: float,
@@ -65,8 +73,10 @@ def fp8_kv_decode_attention(q_bits, q_dtype: int, k_codes, v_codes, seq_lens, k_
         n = int(seq_lens[b])
         if n <= 0:
             continue
-        K = tab[gather_rows(k_codes, b, n, block_table)] * float(k_scale)   # [n, Hkv, D]
+        K = tab[gather_rows(k_codes, b, n, block_table)] * float(k_scale)   # [n', Hkv, D]
         V = tab[gather_rows(v_codes, b, n, block_table)] * float(v_scale)
+        if K.shape[0] == 0:
+            continue                      # every token is padding: zeros
         for h in range(Hq):
             g = h // G
             s = (K[:, g, :] @ q[b, h]) * float(sm_scale)                      # [n]

@@ -136,3 +136,77 @@ def test_scales_enter_linearly():
     a = oa.fp8_kv_decode_attention(q_bits, oracle.BF16, k, v, lens, 0.5, 1.0, 0.25)
     b = oa.fp8_kv_decode_attention(q_bits, oracle.BF16, k, v, lens, 0.25, 4.0, 0.5)
     np.testing.assert_allclose(b, 4.0 * a, rtol=1e-13, atol=1e-300)
+
+
+def _scatter_paged(k, v, bs, table, nb):
+    B, T = k.shape[:2]
+    kp = np.zeros((nb, bs) + k.shape[2:], np.uint8)
+    vp = np.zeros((nb, bs) + v.shape[2:], np.uint8)
+    for b in range(B):
+        for j in range(T // bs):
+            if 0 <= table[b, j] < nb:
+                kp[table[b, j]] = k[b, j * bs:(j + 1) * bs]
+                vp[table[b, j]] = v[b, j * bs:(j + 1) * bs]
+    return kp, vp
+
+
+@pytest.mark.parametrize("pad_id", [-1, -7, 10_000])
+def test_padding_block_ids_drop_their_tokens(pad_id):
+    """A block-table entry outside [0, num_blocks) (the -1 padding of a paged
+    cache, or an id past its end) holds no tokens: the result equals the
+    contiguous sequence with that block's tokens removed, checked against
+    brute force over the remaining tokens."""
+    B, Hq, Hkv, T, D, bs = 2, 4, 2, 16, 8, 4
+    q_bits, k, v = random_case(B, Hq, Hkv, T, D, seed=11)
+    lens = np.array([16, 11], np.int32)
+    nb = B * (T // bs)
+    table = np.random.default_rng(12).permutation(nb).reshape(B, T // bs).astype(np.int32)
+    table[0, 1] = pad_id                 # tokens 4..7 of sequence 0
+    table[1, 2] = pad_id                 # tokens 8..10 of sequence 1 (ragged tail)
+    kp, vp = _scatter_paged(k, v, bs, table, nb)
+    ks, vs, sm = 0.0625, 0.25, 0.3
+    got = oa.fp8_kv_decode_attention(q_bits, oracle.BF16, kp, vp, lens, ks, vs, sm, block_table=table)
+    q = oracle.bits16_to_f32(q_bits, oracle.BF16)
+    tab = [oracle.e4m3_value(c) for c in range(256)]
+    kept = {0: [t for t in range(16) if not 4 <= t < 8], 1: [t for t in range(11) if t < 8]}
+    for b in range(B):
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            K = [[tab[int(c)] * ks for c in k[b, t, g]] for t in kept[b]]
+            V = [[tab[int(c)] * vs for c in v[b, t, g]] for t in kept[b]]
+            ref = oa.attention_bruteforce([float(x) for x in q[b, h]], K, V, sm)
+            np.testing.assert_allclose(got[b, h], ref, rtol=1e-12, atol=1e-15)
+    # and the contiguous oracle over the compacted sequences agrees exactly
+    kc = np.zeros_like(k)
+    vc = np.zeros_like(v)
+    for b in range(B):
+        kc[b, :len(kept[b])] = k[b, kept[b]]
+        vc[b, :len(kept[b])] = v[b, kept[b]]
+    compact = oa.fp8_kv_decode_attention(q_bits, oracle.BF16, kc, vc, np.array([len(kept[0]), len(kept[1])], np.int32),
+                                         ks, vs, sm)
+    np.testing.assert_array_equal(got, compact)
+
+
+def test_all_blocks_padding_gives_zeros():
+    B, Hq, Hkv, T, D, bs = 1, 2, 1, 8, 8, 4
+    q_bits, k, v = random_case(B, Hq, Hkv, T, D, seed=13)
+    table = np.array([[-1, 5]], np.int32)      # 2 blocks exist: id 5 is past the end
+    kp, vp = _scatter_paged(k, v, bs, np.array([[0, 1]], np.int32), 2)
+    out = oa.fp8_kv_decode_attention(q_bits, oracle.BF16, kp, vp, np.array([8], np.int32), 1.0, 1.0, 0.5,
+                                     block_table=table)
+    assert np.all(out == 0.0)
+
+
+def test_uniform_weights_count_every_token_exactly():
+    """Equal (zero) keys give every token weight 1/n; V marks dim d with 1.0
+    on tokens [4d, 4d + 4): every output is exactly 4/n (a closed form that a
+    dropped or repeated token changes)."""
+    B, Hq, Hkv, D = 1, 2, 1, 8
+    T = 4 * D
+    q_bits, _, _ = random_case(B, Hq, Hkv, T, D, seed=14)
+    k = np.zeros((B, T, Hkv, D), np.uint8)
+    v = np.zeros((B, T, Hkv, D), np.uint8)
+    for d in range(D):
+        v[0, 4 * d:4 * d + 4, 0, d] = 0x38           # e4m3 1.0
+    out = oa.fp8_kv_decode_attention(q_bits, oracle.BF16, k, v, np.array([T], np.int32), 1.0, 0.5, 0.9)
+    np.testing.assert_array_equal(out, np.full((B, Hq, D), 4.0 / T * 0.5))
