@@ -36,7 +36,9 @@ def kv_codes(B, T, Hkv, D, seed):
 
 
 def run_case(B, Hq, Hkv, T, lens, seed, q_dtype=torch.bfloat16, out_dtype=torch.bfloat16, paged_bs=0,
-             check_b=None):
+             check_b=None, pad=()):
+    """pad: (sequence, block index, id) entries written into the block table
+    after the cache is laid out: ids outside [0, num_blocks) are padding."""
     D = 128
     (k, ks), (v, vs) = kv_codes(B, T, Hkv, D, seed)
     q = si.normal((B, Hq, D), seed=seed + 7, dtype=q_dtype)
@@ -55,6 +57,8 @@ def run_case(B, Hq, Hkv, T, lens, seed, q_dtype=torch.bfloat16, out_dtype=torch.
             for j in range(nbps):
                 kc[table[b, j]] = k[b, j * paged_bs:(j + 1) * paged_bs]
                 vc[table[b, j]] = v[b, j * paged_bs:(j + 1) * paged_bs]
+        for b, j, blk in pad:
+            table[b, j] = blk
     dev = "cuda"
     out = torch.empty(B, Hq, D, dtype=out_dtype, device=dev)
     w8.fp8_kv_decode_attention(q.to(dev), torch.from_numpy(kc).to(dev), torch.from_numpy(vc).to(dev),
@@ -66,9 +70,15 @@ def run_case(B, Hq, Hkv, T, lens, seed, q_dtype=torch.bfloat16, out_dtype=torch.
     got = out_to_f32(bits_np(out), okind).astype(np.float64)
     bsel = list(range(B)) if check_b is None else check_b
     qb = si.bits16(q)[bsel]
-    ref = oa.fp8_kv_decode_attention(qb, qkind, k[bsel], v[bsel], lens[bsel], ks, vs, 1.0 / np.sqrt(D))
-    # the same weights over |V| (clearing an e4m3 code's sign bit gives |value|)
-    r_abs = oa.fp8_kv_decode_attention(qb, qkind, k[bsel], v[bsel] & 0x7F, lens[bsel], ks, vs, 1.0 / np.sqrt(D))
+    if table is None:
+        ref = oa.fp8_kv_decode_attention(qb, qkind, k[bsel], v[bsel], lens[bsel], ks, vs, 1.0 / np.sqrt(D))
+        # the same weights over |V| (clearing an e4m3 code's sign bit gives |value|)
+        r_abs = oa.fp8_kv_decode_attention(qb, qkind, k[bsel], v[bsel] & 0x7F, lens[bsel], ks, vs, 1.0 / np.sqrt(D))
+    else:
+        ref = oa.fp8_kv_decode_attention(qb, qkind, kc, vc, lens[bsel], ks, vs, 1.0 / np.sqrt(D),
+                                         block_table=table[bsel])
+        r_abs = oa.fp8_kv_decode_attention(qb, qkind, kc, vc & 0x7F, lens[bsel], ks, vs, 1.0 / np.sqrt(D),
+                                           block_table=table[bsel])
     err = np.abs(got[bsel] - ref)
     bound = 2.0 ** -8 * np.abs(ref) + 2.0 ** -14 * r_abs
     bad = err > bound
@@ -90,6 +100,16 @@ def test_paged_cache_and_empty_sequence():
     run_case(B=3, Hq=8, Hkv=2, T=512, lens=[512, 0, 77], seed=200, paged_bs=16)
 
 
+@pytest.mark.parametrize("pad_id", [-1, 1 << 20])
+def test_paged_cache_padding_entries(pad_id):
+    """Block-table entries outside the cache (-1 padding, or an id past its
+    end) hold no tokens, on the GPU as in the oracle: a whole middle block,
+    the block of a ragged tail, and every block of one sequence."""
+    nbps = 512 // 16
+    pad = [(0, 5, pad_id), (1, 77 // 16, pad_id)] + [(2, j, pad_id) for j in range(nbps)]
+    run_case(B=3, Hq=8, Hkv=2, T=512, lens=[512, 77, 300], seed=210, paged_bs=16, pad=pad)
+
+
 def test_fp16_query_and_output():
     run_case(B=2, Hq=8, Hkv=2, T=300, lens=[300, 129], seed=300, q_dtype=torch.float16, out_dtype=torch.float16)
 
@@ -104,6 +124,79 @@ def test_long_single_sequence():
     """One sequence of 65536 tokens: 8 KV heads x 128 (the KV-cache tensor
     of the quantiser benchmark), many chunks combined."""
     run_case(B=1, Hq=32, Hkv=8, T=65536, lens=[65536], seed=500)
+
+
+def _long_case_inputs(T, Hkv, Hq, D):
+    dev = "cuda"
+    lens = torch.tensor([T], dtype=torch.int32, device=dev)
+    ks = torch.tensor([2.0 ** -3], device=dev)
+    vs = torch.tensor([2.0 ** -4], device=dev)
+    return dev, lens, ks, vs
+
+
+def test_long_sequence_counts_every_token_exactly():
+    """65536 tokens, all keys zero: every token weighs 1/65536.  V marks dim
+    d of every KV head with 1.0 on tokens [512 d, 512 d + 512), so every
+    output is exactly 512/65536 * v_scale, a value that a dropped or repeated
+    token (or chunk) changes.  The fp32 sums of ones are exact, so the GPU
+    must match the oracle bit for bit."""
+    B, T, Hkv, Hq, D = 1, 65536, 8, 32, 128
+    dev, lens, ks, vs = _long_case_inputs(T, Hkv, Hq, D)
+    k = np.zeros((B, T, Hkv, D), np.uint8)
+    v = np.zeros((B, T, Hkv, D), np.uint8)
+    for d in range(D):
+        v[0, 512 * d:512 * (d + 1), :, d] = 0x38          # e4m3 1.0
+    q = si.normal((B, Hq, D), seed=700)
+    out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev)
+    w8.fp8_kv_decode_attention(q.to(dev), torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev), lens, ks, vs,
+                               out)
+    torch.cuda.synchronize()
+    ref = oa.fp8_kv_decode_attention(si.bits16(q), oracle.BF16, k, v, np.array([T], np.int32), 2.0 ** -3,
+                                     2.0 ** -4, 1.0 / np.sqrt(D))
+    assert np.all(ref == 2.0 ** -7 * 2.0 ** -4)
+    got = out_to_f32(bits_np(out), oracle.BF16).astype(np.float64)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_long_sequence_dominant_key_per_head():
+    """65536 tokens; query head h is one-hot on dim d_h and only token t_h has
+    a key on that dim (448): its score leads every other by more than 200, so
+    head h returns token t_h's value row exactly.  The t_h sit on the first
+    and last tokens and on both sides of 64/128/256/512-token boundaries."""
+    B, T, Hkv, Hq, D = 1, 65536, 8, 32, 128
+    G = Hq // Hkv
+    dev, lens, ks, vs = _long_case_inputs(T, Hkv, Hq, D)
+    rng = np.random.default_rng(701)
+    k = np.zeros((B, T, Hkv, D), np.uint8)
+    v = rng.integers(0, 0x7F, (B, T, Hkv, D), dtype=np.uint8) | (rng.integers(0, 2, (B, T, Hkv, D), dtype=np.uint8) << 7)
+    spots = [0, T - 1, 63, 64, 127, 128, 255, 256, 511, 512, 4095, 4096, 30000, 32767, 32768, 65535 - 256,
+             65535 - 255, 1, 1000, 2047, 2048, 8191, 8192, 16383, 16384, 40000, 50000, 60000, 65000, 65280, 12345, 777]
+    qf = np.zeros((B, Hq, D), np.float32)
+    t_of = {}
+    for h in range(Hq):
+        g, j = divmod(h, G)
+        d = 16 * j + 3
+        t = spots[h]
+        k[0, t, g, d] = 0x7E                                  # 448
+        qf[0, h, d] = 4.0                                     # score 4 * 448 / 8 / sqrt(128) ~ 19.8 ...
+        t_of[h] = (t, g)
+    qf *= 16.0                                                # ... x16: ~317 above every other token
+    q_bits = oracle.f32_to_bf16_bits(qf)
+    q = torch.from_numpy(q_bits.view(np.int16)).view(torch.bfloat16)
+    out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev)
+    w8.fp8_kv_decode_attention(q.to(dev), torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev), lens, ks, vs,
+                               out)
+    torch.cuda.synchronize()
+    got = out_to_f32(bits_np(out), oracle.BF16).astype(np.float64)
+    ref = oa.fp8_kv_decode_attention(q_bits, oracle.BF16, k, v, np.array([T], np.int32), 2.0 ** -3, 2.0 ** -4,
+                                     1.0 / np.sqrt(D))
+    tab = oa.e4m3_table()
+    for h in range(Hq):
+        t, g = t_of[h]
+        want = tab[v[0, t, g]] * 2.0 ** -4                   # exact in bf16
+        # the oracle (fp64) keeps the other tokens' weights of ~1e-138
+        np.testing.assert_allclose(ref[0, h], want, rtol=1e-12, atol=1e-120)
+        np.testing.assert_array_equal(got[0, h], want, err_msg=f"head {h} (token {t})")
 
 
 def test_graph_capture_and_determinism():
