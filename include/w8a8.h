@@ -95,7 +95,13 @@ enum {
   W8A8_ERR_NO_DEVICE = 6    /* current device is not an sm_103 GPU */
 };
 
-/* Device status bits reported by w8a8_device_status(). */
+/* Device status bits reported by w8a8_device_status().
+ *
+ * No call returns a timeout status: calls only enqueue work and never wait
+ * for the GPU, so a call cannot see a kernel's wait give up.  Every wait
+ * inside a kernel is bounded instead (about 2 s); one that gives up lets its
+ * kernel finish without hanging the GPU and sets W8A8_DEVICE_TIMEOUT in the
+ * device status word, which w8a8_device_status() reads. */
 enum { W8A8_DEVICE_TIMEOUT = 1 };
 
 /* Message for the last failing call on this host thread ("" if none).
@@ -382,12 +388,15 @@ W8A8_API w8a8_status w8a8_fp8_kv_decode_attention(
  *    this covers e4m3 at every size (large M needs no scratch) and int8 only
  *    where its widened operand planes fit.
  *  - The array is shared by every call on a device and keeps the previous
- *    call's contents; each call clears the counters it relies on (an
- *    asynchronous memset on `stream`).  Calls that may overlap on the GPU
- *    (different streams without ordering) race on the array: serialise them.
- *  - The first call on a device looks up the array's device address (a host
- *    query, once per device, with that device current); make that first call
- *    before any stream capture.
+ *    call's contents.  A call that uses split-K arrival counters clears
+ *    them first (an asynchronous memset of those counters on `stream`);
+ *    every other byte it reads it has written itself.  Calls that may
+ *    overlap on the GPU (different streams without ordering) race on the
+ *    array: serialise them.
+ *  - The first call on a device (and again after the device's context has
+ *    been replaced, e.g. by cudaDeviceReset) looks up the array's device
+ *    address with a host query, with that device current; make that first
+ *    call before any stream capture.
  */
 W8A8_API size_t w8a8_scaled_mm_noalloc_max_scratch(void);
 

@@ -241,12 +241,10 @@ struct Plan {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Workspace layout.  The split-K arrival counters live in a fixed region at
-// the head of every workspace and nothing else is ever written there: each
-// call that uses them leaves them zero, so a zero-filled workspace stays valid
-// across calls of any shape and configuration (scratch data -- split-K
-// partials, int8 f16 planes -- always lives after the region).
-constexpr size_t kCounterSlots = 16384;
-constexpr size_t kCounterRegion = kCounterSlots * sizeof(unsigned);
+// the head of every workspace (kCounterRegion) and nothing else is ever
+// written there: each call that uses them leaves them zero, so a zero-filled
+// workspace stays valid across calls of any shape and configuration (scratch
+// data -- split-K partials, int8 f16 planes -- always lives after the region).
 
 Plan make_plan(long long M, long long N, long long K, int q_dtype, const w8a8_mm_config& cfg, int smem_optin) {
   Plan p{};
@@ -483,6 +481,16 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
 }  // namespace
 
 void w8a8::set_last_error(const char* msg) { t_last_error = msg ? msg : ""; }
+
+size_t w8a8::mm_counter_bytes(long long M, long long N, long long K, int q_dtype) {
+  DeviceInfo dev;
+  if (device_info(&dev) != W8A8_OK) return kCounterRegion;  // unknown: the whole region
+  w8a8_mm_config cfg;
+  auto_config(M, N, K, q_dtype, dev.sms, &cfg);
+  const Plan plan = make_plan(M, N, K, q_dtype, cfg, dev.smem_optin);
+  if (plan.splits <= 1 || plan.cluster) return 0;
+  return std::min(kCounterRegion, static_cast<size_t>(plan.tiles_p) * plan.tiles_q * sizeof(unsigned));
+}
 
 extern "C" {
 

@@ -142,6 +142,17 @@ cudaError_t launch_dequant(const DequantArgs& a, int num_sms, cudaStream_t strea
 // Sets the message returned by w8a8_last_error() on this host thread.
 void set_last_error(const char* msg);
 
+// Split-K arrival counters: a fixed region at the head of every matmul
+// workspace (one 32-bit counter per output tile), left zero by every call
+// that uses it.  Scratch data always lives after the region.
+constexpr size_t kCounterSlots = 16384;
+constexpr size_t kCounterRegion = kCounterSlots * sizeof(unsigned);
+
+// Bytes at the head of the workspace whose counters the automatic
+// configuration of this matmul uses (0 when it uses none), on the current
+// device.
+size_t mm_counter_bytes(long long M, long long N, long long K, int q_dtype);
+
 // Row shards of a merged weight: cumulative row ends.
 constexpr int kMaxShards = 16;
 struct ShardTable {

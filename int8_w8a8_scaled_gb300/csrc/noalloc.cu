@@ -9,6 +9,7 @@
 // split-K partial tiles) in one file-scope device array of fixed size, which
 // the CUDA runtime creates when the library is loaded on a device and keeps
 // until the process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -17,8 +18,8 @@
 
 #include "internal.h"
 
-// 8 MiB of split-K partials plus the 64 KiB counter region at the head.
-static constexpr size_t kScratchBytes = (8u << 20) + (64u << 10);
+// 8 MiB of split-K partials plus the counter region at the head.
+static constexpr size_t kScratchBytes = (8u << 20) + w8a8::kCounterRegion;
 
 // The scratch itself: one per device that loads the library, zero at load.
 static __device__ __align__(256) unsigned char g_w8a8_static_scratch[kScratchBytes];
@@ -26,29 +27,65 @@ static __device__ __align__(256) unsigned char g_w8a8_static_scratch[kScratchByt
 namespace {
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the array, per device, remembered together with the
+// context it was looked up in: a context created later on the same device
+// (after cudaDeviceReset, say) holds the array at another address, and the
+// lookup is then made again.
+struct ScratchAddr {
+  CUcontext ctx = nullptr;
+  void* ptr = nullptr;
+};
+ScratchAddr g_scratch[kMaxDevices];
 std::mutex g_scratch_mu;
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
 // Device address of the scratch array on the current device.  The array's
-// name in host code is only a host-side handle, so the address is looked up
-// once per device, with that device current, and cached.
+// name in host code is only a host-side handle, so its address is looked up
+// with cudaGetSymbolAddress, with the device current, the first time a
+// device (in a given context) is used.
 w8a8_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
+    w8a8::set_last_error("scaled_mm_noalloc: no usable current CUDA device");
     return W8A8_ERR_NO_DEVICE;
   }
+  CtxGetCurrentFn get = ctx_get_current_fn();
+  if (!get) {
+    w8a8::set_last_error("scaled_mm_noalloc: cuCtxGetCurrent is not available from the driver");
+    return W8A8_ERR_CUDA;
+  }
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) ctx = nullptr;  // none yet: the lookup below creates the runtime's
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  ScratchAddr& s = g_scratch[dev];
+  if (!ctx || !s.ptr || s.ctx != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_w8a8_static_scratch) != cudaSuccess || !p) {
       cudaGetLastError();
       w8a8::set_last_error("scaled_mm_noalloc: cudaGetSymbolAddress of the scratch array failed");
       return W8A8_ERR_CUDA;
     }
-    g_scratch_ptr[dev] = p;
+    if (get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+    s.ptr = p;
+    s.ctx = ctx;
   }
-  *out = g_scratch_ptr[dev];
+  *out = s.ptr;
   return W8A8_OK;
 }
 
@@ -75,14 +112,15 @@ w8a8_status w8a8_scaled_mm_noalloc(const void* a_q, int64_t lda, const void* b_q
   void* scratch = nullptr;
   w8a8_status st = scratch_address(&scratch);
   if (st != W8A8_OK) return st;
-  if (need > 0) {
-    // The array keeps whatever the previous call left; the split-K arrival
-    // counters at its head must start at zero.
-    if (cudaMemsetAsync(scratch, 0, 64u << 10, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
-      cudaGetLastError();
-      w8a8::set_last_error("scaled_mm_noalloc: clearing the split-K counters failed");
-      return W8A8_ERR_CUDA;
-    }
+  // The array keeps whatever the previous call left.  The split-K arrival
+  // counters this problem uses must start at zero: a successful call leaves
+  // them zero, but a call whose kernel gave up on a wait may not, so they
+  // are cleared (only they, and only when the plan uses them).
+  const size_t ctr = need > 0 ? w8a8::mm_counter_bytes(M, N, K, q_dtype) : 0;
+  if (ctr > 0 && cudaMemsetAsync(scratch, 0, ctr, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    w8a8::set_last_error("scaled_mm_noalloc: clearing the split-K counters failed");
+    return W8A8_ERR_CUDA;
   }
   return w8a8_scaled_mm(a_q, lda, b_q, ldb, scale_a, a_gran, scale_b, b_gran, out, ldc, M, N, K, q_dtype, out_dtype,
                         need > 0 ? scratch : nullptr, need > 0 ? kScratchBytes : 0, stream);

@@ -4,9 +4,12 @@ w8a8_scaled_mm_noalloc serves callers that cannot allocate device memory
 where they run the matmul (allocator hooks, plug-ins given only operand and
 output buffers, processes whose memory another runtime has reserved): it
 keeps its scratch (split-K partials through the workspace, int8 operand
-planes) in a fixed array the library defines in device memory.  Checked here through the C ABI against w8a8_scaled_mm with a
-caller workspace, on two calls in a row, within the fp8 tolerance used by
-the other matmul tests.  This file is collected last.
+planes) in a fixed array the library defines in device memory.  Checked here
+through the C ABI against w8a8_scaled_mm with a caller workspace, on two
+calls in a row: both run the same kernel configuration with the same
+deterministic split-K order, so the outputs must be the same bits (e4m3 and
+int8 alike).  One shape is also checked against the oracle, within the fp8
+tolerance the other matmul tests use.  This file is collected last.
 """
 import ctypes
 
@@ -59,12 +62,33 @@ def test_noalloc_matches_workspace_entry_point_twice(M, N, K, qd):
                                         qd, od, stream)
         assert st == 0, lib.w8a8_last_error()
         torch.cuda.synchronize()
-        if qd == INT8:   # exact integer accumulation: the same bits
-            assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
-        else:
-            r = ref.float().cpu().numpy().astype(np.float64)
-            o = out.float().cpu().numpy().astype(np.float64)
-            assert np.all(np.abs(o - r) <= 2.0 ** -7 * np.abs(r) + 1e-3)
+        # same configuration, same slice order: the same bits
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+def test_noalloc_matches_the_oracle():
+    """M=16 tokens x the O projection [4096 x 4096] (a split-K decode shape):
+    bf16 outputs within |gpu - y| <= 2^-7 |y| + 1e-3 of the oracle's fp32 y."""
+    import oracle
+    import synthetic_inputs as si
+    lib = _lib.load()
+    M, N, K = 16, 4096, 4096
+    qa, sa = oracle.quant(si.bits16(si.normal_with_outliers((M, K), seed=31)), oracle.BF16, oracle.E4M3,
+                          oracle.PER_ROW)
+    qb, sb = oracle.quant(si.bits16(si.normal((N, K), seed=32, std=0.02)), oracle.BF16, oracle.E4M3, oracle.PER_ROW)
+    assert lib.w8a8_scaled_mm_workspace_size(M, N, K, E4M3) > 0      # the fixed array is in use
+    a = torch.from_numpy(qa).cuda()
+    b = torch.from_numpy(qb).cuda()
+    ga, gb = torch.from_numpy(sa).cuda(), torch.from_numpy(sb).cuda()
+    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st = lib.w8a8_scaled_mm_noalloc(_p(a), K, _p(b), K, _p(ga), PER_ROW, _p(gb), PER_ROW, _p(out), N, M, N, K,
+                                    E4M3, BF16, stream)
+    assert st == 0, lib.w8a8_last_error()
+    torch.cuda.synchronize()
+    y = oracle.scaled_mm(qa, qb, sa, sb, oracle.E4M3, oracle.BF16)["y"].astype(np.float64)
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - y) <= 2.0 ** -7 * np.abs(y) + 1e-3)
 
 
 def test_noalloc_rejects_problems_beyond_its_array():
