@@ -11,9 +11,17 @@ stay resident; the 218 MB of weights are larger than the 129 MB L2, so every
 step streams them from HBM.  The step is captured once in a CUDA graph and
 replayed.
 
-The JSON line also carries the other measured workloads (fp8 prefill at
-M = 4096 with static per-tensor scales, int8 w8a8 at Llama-3-70B shapes and
-M = 8192, and the scaled FP8 KV-cache round trip) under "workloads".
+Timing: W warm-up steps, then samples of exactly K steps, each bracketed by
+a device synchronisation (and a barrier over ranks) with CUDA events on the
+launching stream, repeated until at least half a second has been timed so
+that the clock sampler sees the load; the median sample is reported.
+
+The JSON line also carries the other configurations under "configs", each
+with its roofline and the oracle timed on the host cores on a bounded
+sample: fp8 prefill at M = 4096 with static per-tensor scales, int8 w8a8 at
+Llama-3-70B shapes and M = 8192, the scaled FP8 KV-cache round trip, decode
+attention over the e4m3 KV cache and the activation quantiser at prefill
+sizes.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -44,6 +52,12 @@ DECODE_MS = (1, 16, 64, 256)
 LLAMA8B = (("qkv", 6144, 4096, True), ("o", 4096, 4096, False),
            ("gate_up", 28672, 4096, False), ("down", 4096, 14336, False))
 LLAMA70B = (("qkv", 10240, 8192), ("gate_up", 57344, 8192), ("down", 8192, 28672))
+
+QUANT_PREFILL = ((4096, 4096), (4096, 14336), (8192, 8192), (8192, 28672))
+ATTN_SHAPE = (16, 4096, 8, 32, 128)   # sequences, tokens, KV heads, query heads, head dim
+MIN_TIMED_S = 0.5
+DECODE_WORKLOAD = ("Llama-3-8B decode fp8 e4m3: M in {1,16,64,256} x QKV/O/gate-up/down, dynamic per-token act, "
+                   "per-channel weights (QKV shared)")
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -171,7 +185,7 @@ def aggregate_tflops(flops_per_step_per_rank: float, steps: int, t_max: float, w
 class DecodeWorkload:
     """Llama-3-8B decode fp8: 4 token counts x 4 projections."""
 
-    def __init__(self, dev, seed=1000, override=None):
+    def __init__(self, dev, seed=1000):
         import torch
         import int8_w8a8_scaled_gb300 as w8
         import synthetic_inputs as si
@@ -194,9 +208,6 @@ class DecodeWorkload:
                 sa = torch.empty(M, dtype=torch.float32, device=dev)
                 out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
                 cfg = None
-                if override:
-                    cfg = dict(w8.pick_config(M, N, K, w8.E4M3), **override)
-                auto = w8.pick_config(M, N, K, w8.E4M3)
                 # quantiser + matmul (the automatic route of quant_scaled_mm;
                 # `fused` items would run its one-kernel route)
                 fused = False
@@ -277,11 +288,10 @@ def graph_of(fn, stream):
     return g
 
 
-def time_graph(g, stream, steps, warmup, barrier=None):
+def _time_once(run, stream, steps, barrier=None):
+    """Seconds for exactly `steps` calls of run() (CUDA events on `stream`,
+    device synchronised and ranks at a barrier on both sides)."""
     import torch
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            g.replay()
     torch.cuda.synchronize()
     if barrier:
         barrier()
@@ -291,12 +301,45 @@ def time_graph(g, stream, steps, warmup, barrier=None):
     with torch.cuda.stream(stream):
         start.record(stream)
         for _ in range(steps):
-            g.replay()
+            run()
         end.record(stream)
     torch.cuda.synchronize()
     if barrier:
         barrier()
-    return start.elapsed_time(end) / 1e3  # seconds
+    return start.elapsed_time(end) / 1e3
+
+
+def timed(run, stream, steps, warmup, min_s=MIN_TIMED_S, barrier=None, device=None):
+    """W warm-up calls, then timed samples of exactly `steps` calls each,
+    repeated until at least `min_s` seconds of timed work (so that the clock
+    sampler sees the load).  Every rank runs the same number of samples.
+    Returns (median seconds per sample, number of samples)."""
+    import math
+    with_stream(stream, lambda: [run() for _ in range(warmup)])
+    probe = _time_once(run, stream, steps, barrier)
+    n = max(1, min(10_000, math.ceil(min_s / max(probe, 1e-9))))
+    n = int(max_over_ranks(float(n), device))
+    ts = [_time_once(run, stream, steps, barrier) for _ in range(n)]
+    return statistics.median(ts), n
+
+
+def with_stream(stream, fn):
+    import torch
+    with torch.cuda.stream(stream):
+        return fn()
+
+
+def time_graph(g, stream, steps, warmup, barrier=None, device=None):
+    """Median seconds per step of graph replays (see timed())."""
+    t, n = timed(g.replay, stream, steps, warmup, barrier=barrier, device=device)
+    return t / steps, n
+
+
+def r4(x):
+    """Four significant digits (keeps the JSON line short)."""
+    if x is None:
+        return None
+    return float(f"{x:.4g}")
 
 
 def measure_prefill_fp8(dev, steps, warmup, stream, pk):
@@ -335,19 +378,16 @@ def measure_prefill_fp8(dev, steps, warmup, stream, pk):
             w8.scaled_mm(aq, wq, sa, sw, out, workspace=ws)
 
     flops = sum(2.0 * M * N * K for *_, N, K in items)
-    t_step = time_graph(graph_of(step, stream), stream, steps, warmup) / steps
-    t_gemm = time_graph(graph_of(gemm_only, stream), stream, steps, warmup) / steps
+    t_step, n1 = time_graph(graph_of(step, stream), stream, steps, warmup)
+    t_gemm, n2 = time_graph(graph_of(gemm_only, stream), stream, steps, warmup)
     fp8_peak = pk["bf16_tflops"] * 2.0  # nominal fp8 / bf16 ratio 4.5 / 2.25
     ach = flops / t_gemm / 1e12
-    res = {"workload": "Llama-3-8B prefill fp8 static, M=4096, QKV/O/gate-up/down",
-           "value": flops / t_step / 1e12, "unit": "TFLOP/s", "ms_per_step": t_step * 1e3,
-           "gemm_tflops": ach,
-           "roofline": {"bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s",
-                        "frac": ach / fp8_peak,
-                        "peak_note": "dense fp8 = 2 x measured bf16 burst peak (nominal fp8/bf16 ratio)"}}
     del items
     torch.cuda.empty_cache()
-    return res
+    return {"value": r4(flops / t_step / 1e12), "unit": "TFLOP/s", "ms_per_step": r4(t_step * 1e3),
+            "samples": n1 + n2,
+            "roofline": {"bound": "tensor", "achieved": r4(ach), "peak": r4(fp8_peak), "frac": r4(ach / fp8_peak),
+                         "kernel": "4 GEMMs"}}
 
 
 def measure_int8_70b(dev, steps, warmup, stream, pk):
@@ -377,19 +417,15 @@ def measure_int8_70b(dev, steps, warmup, stream, pk):
             w8.scaled_mm(aq, wq, sa, sw, out, workspace=ws)
 
     flops = sum(2.0 * M * N * K for *_, N, K in items)
-    st = max(1, min(steps, 20))
-    t_step = time_graph(graph_of(step, stream), stream, st, max(3, min(warmup, 3))) / st
+    # a step is ~13 ms: one step per sample
+    t_step, n = time_graph(graph_of(step, stream), stream, 1, warmup)
     ach = flops / t_step / 1e12
-    res = {"workload": "int8 w8a8 Llama-3-70B shapes, M=8192, QKV/gate-up/down, fp16 out",
-           "value": ach, "unit": "TFLOP/s", "ms_per_step": t_step * 1e3,
-           "roofline": {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                        "frac": ach / pk["bf16_tflops"],
-                        "peak_note": "route peak: int8 runs on tcgen05 kind::f16 (kind::i8 is not available "
-                                     "on sm_103a); measured bf16 burst peak; includes quantiser and int8->f16 widening",
-                        "frac_of_fp8_dense": ach / (2.0 * pk["bf16_tflops"])}}
     del items
     torch.cuda.empty_cache()
-    return res
+    return {"value": r4(ach), "unit": "TFLOP/s", "ms_per_step": r4(t_step * 1e3), "samples": n,
+            "roofline": {"bound": "tensor", "achieved": r4(ach), "peak": r4(pk["bf16_tflops"]),
+                         "frac": r4(ach / pk["bf16_tflops"]), "frac_fp8": r4(ach / (2.0 * pk["bf16_tflops"])),
+                         "kernel": "quant+GEMM, f16 route"}}
 
 
 def measure_kv(dev, steps, warmup, stream, pk):
@@ -417,16 +453,41 @@ def measure_kv(dev, steps, warmup, stream, pk):
         for x, q, s, y, wsq in bufs:
             w8.scaled_dequant(q, s, y)
 
-    tq = time_graph(graph_of(quant, stream), stream, steps, warmup) / steps
-    td = time_graph(graph_of(dequant, stream), stream, steps, warmup) / steps
+    tq, n1 = time_graph(graph_of(quant, stream), stream, steps, warmup)
+    td, n2 = time_graph(graph_of(dequant, stream), stream, steps, warmup)
     qb, db = 2 * n * 5, 2 * n * 3
     hbm = pk["hbm_gbs"]
-    return {"workload": "scaled FP8 KV cache, K and V bf16 [65536, 8, 128], per-tensor dynamic",
-            "quant_gbs": qb / tq / 1e9, "dequant_gbs": db / td / 1e9,
-            "quant_us": tq * 1e6, "dequant_us": td * 1e6, "unit": "GB/s",
-            "roofline": {"bound": "hbm", "quant_frac": qb / tq / 1e9 / hbm, "dequant_frac": db / td / 1e9 / hbm,
-                         "peak": hbm, "unit": "GB/s",
-                         "bytes_note": "quant 5 B/element (absmax read 2 + read 2 + write 1), dequant 3 B/element"}}
+    return {"value": r4(qb / tq / 1e9), "unit": "GB/s", "dequant_gbs": r4(db / td / 1e9),
+            "us": [r4(tq * 1e6), r4(td * 1e6)], "samples": n1 + n2,
+            "roofline": {"bound": "hbm", "frac": r4(qb / tq / 1e9 / hbm), "dequant_frac": r4(db / td / 1e9 / hbm),
+                         "peak": r4(hbm), "kernel": "5 B/elt, dequant 3"}}
+
+
+def measure_quant_prefill(dev, steps, warmup, stream, pk):
+    """The activation quantiser at prefill sizes: [4096, 4096], [4096,
+    14336], [8192, 8192], [8192, 28672] bf16, dynamic per token, e4m3."""
+    import torch
+    import int8_w8a8_scaled_gb300 as w8
+    import synthetic_inputs as si
+    bufs = []
+    for j, (R, C) in enumerate(QUANT_PREFILL):
+        x = si.normal_with_outliers((R, C), seed=6000 + j, device=dev)
+        q = torch.empty(R, C, dtype=torch.float8_e4m3fn, device=dev)
+        s = torch.empty(R, dtype=torch.float32, device=dev)
+        bufs.append((x, q, s))
+
+    def run():
+        for x, q, s in bufs:
+            w8.scaled_quant(x, q, s, per_token=True, dynamic=True)
+
+    t, n = time_graph(graph_of(run, stream), stream, steps, warmup)
+    byts = sum(R * C * 3 + 4 * R for R, C in QUANT_PREFILL)
+    gbs = byts / t / 1e9
+    del bufs
+    torch.cuda.empty_cache()
+    return {"value": r4(gbs), "unit": "GB/s", "us": r4(t * 1e6), "samples": n,
+            "roofline": {"bound": "hbm", "achieved": r4(gbs), "peak": r4(pk["hbm_gbs"]),
+                         "frac": r4(gbs / pk["hbm_gbs"]), "kernel": "3 B/elt + 4 B/row"}}
 
 
 def measure_kv_attention(dev, steps, warmup, stream, pk):
@@ -437,7 +498,8 @@ def measure_kv_attention(dev, steps, warmup, stream, pk):
     import torch
     import int8_w8a8_scaled_gb300 as w8
     import synthetic_inputs as si
-    B, T, Hkv, Hq, D = 16, 4096, 8, 32, 128
+    B, T, Hkv, Hq, D = ATTN_SHAPE
+
     def finite_codes(seed):
         c = si.random_codes((B, T, Hkv, D), seed=seed, device=dev)
         return torch.where((c & 0x7F) == 0x7F, c - 1, c)     # NaN codes -> +-448
@@ -458,17 +520,28 @@ def measure_kv_attention(dev, steps, warmup, stream, pk):
         for q, kc, vc, out in sets:
             w8.fp8_kv_decode_attention(q, kc, vc, lens, ks, vs, out, workspace=ws, stream=stream)
 
-    t = time_graph(graph_of(step, stream), stream, steps, warmup) / steps / len(sets)
-    byts = 2 * B * T * Hkv * D + 2 * 2 * B * Hq * D   # codes of K and V, q and out (bf16)
+    t, n = time_graph(graph_of(step, stream), stream, steps, warmup)
+    t /= len(sets)
+    byts = attention_bytes()
     hbm = pk["hbm_gbs"]
     gbs = byts / t / 1e9
-    return {"workload": "decode attention over an e4m3 KV cache, 16 seqs x 4096 tokens, 32 q / 8 kv heads x 128",
-            "value": gbs, "unit": "GB/s", "us_per_call": t * 1e6,
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                         "bytes_note": "1 B per K and V code + q and out (bf16); per-tensor scales"}}
+    del sets
+    torch.cuda.empty_cache()
+    return {"value": r4(gbs), "unit": "GB/s", "us": r4(t * 1e6), "samples": n,
+            "roofline": {"bound": "hbm", "achieved": r4(gbs), "peak": r4(hbm), "frac": r4(gbs / hbm),
+                         "kernel": "codes+q+out"}}
 
 
-# ---------------------------------------------------------------- CPU baseline (oracle)
+def attention_bytes():
+    B, T, Hkv, Hq, D = ATTN_SHAPE
+    return 2 * B * T * Hkv * D + 2 * 2 * B * Hq * D   # codes of K and V, q and out (bf16)
+
+
+# ---------------------------------------------------------------- CPU baselines (oracle)
+# The oracle as it stands, timed on the host cores on a bounded sample of
+# each workload.  Inputs are made on the CPU by synthetic_inputs (same laws
+# and shapes as the GPU workloads) and quantised by the oracle; the sample
+# is what the timer covers.
 
 _ORACLE_WEIGHTS = {}
 
@@ -512,6 +585,118 @@ def oracle_decode_sample(budget_s: float, seed=5000):
     return flops, elapsed, rows, oracle.num_threads()
 
 
+def _sample_pairs(M, N, rows=64, cols=64, tile_m=128, tile_n=128, seed=0):
+    """(m, n) pairs of the large-M oracle sample: `rows` full rows, `cols`
+    full columns and every (tile_m x tile_n) tile's four corners."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    rm = rng.choice(M, size=min(rows, M), replace=False)
+    cn = rng.choice(N, size=min(cols, N), replace=False)
+    mm = [np.repeat(rm, N), np.tile(np.arange(M), len(cn))]
+    nn = [np.tile(np.arange(N), len(rm)), np.repeat(cn, M)]
+    tm = np.arange(0, M, tile_m)
+    tn = np.arange(0, N, tile_n)
+    for dm in (0, tile_m - 1):
+        for dn in (0, tile_n - 1):
+            gm, gn = np.meshgrid(np.minimum(tm + dm, M - 1), np.minimum(tn + dn, N - 1), indexing="ij")
+            mm.append(gm.ravel())
+            nn.append(gn.ravel())
+    return np.concatenate(mm).astype(np.int64), np.concatenate(nn).astype(np.int64)
+
+
+def cpu_prefill_sample():
+    """Config 3 sample: the QKV projection at M = 4096 (static per-tensor
+    scales): quantise the activations with the calibration scale, then the
+    scaled matmul on 64 rows, 64 columns and the tile corners."""
+    import oracle
+    import synthetic_inputs as si
+    M, (name, N, K, _) = 4096, LLAMA8B[0]
+    wq, sw = oracle.quant(si.bits16(si.normal((N, K), seed=2000, std=0.02)), oracle.BF16, oracle.E4M3,
+                          oracle.PER_TENSOR)
+    _, sa = oracle.quant(si.bits16(si.student_t_columns((M, K), seed=2100)), oracle.BF16, oracle.E4M3,
+                         oracle.PER_TENSOR)
+    x = si.bits16(si.student_t_columns((M, K), seed=2200))
+    im, inn = _sample_pairs(M, N, seed=3)
+    t0 = time.perf_counter()
+    aq, _ = oracle.quant(x, oracle.BF16, oracle.E4M3, oracle.PER_TENSOR, scale=sa)
+    oracle.scaled_mm_sample(aq, wq, sa, sw, oracle.E4M3, oracle.BF16, im, inn)
+    t = time.perf_counter() - t0
+    return {"value": r4(2.0 * im.size * K / t / 1e12), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"QKV: quant, 64 rows+64 cols+corners, {t:.1f} s"}
+
+
+def cpu_int8_sample():
+    """Config 4 sample: the QKV-70B projection at M = 8192: per-token int8
+    activation quantisation of every row, then the exact scaled matmul on
+    64 rows, 64 columns and the tile corners."""
+    import oracle
+    import synthetic_inputs as si
+    M, (name, N, K) = 8192, LLAMA70B[0]
+    wq, sw = oracle.quant(si.bits16(si.normal((N, K), seed=3000, std=0.02)), oracle.BF16, oracle.INT8,
+                          oracle.PER_ROW)
+    x = si.bits16(si.normal_with_outliers((M, K), seed=3100))
+    im, inn = _sample_pairs(M, N, seed=4)
+    t0 = time.perf_counter()
+    aq, sa = oracle.quant(x, oracle.BF16, oracle.INT8, oracle.PER_ROW)
+    oracle.scaled_mm_sample(aq, wq, sa, sw, oracle.INT8, oracle.FP16, im, inn)
+    t = time.perf_counter() - t0
+    return {"value": r4(2.0 * im.size * K / t / 1e12), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"QKV: quant, 64 rows+64 cols+corners, {t:.1f} s"}
+
+
+def cpu_kv_full():
+    """Config 5 in full: per-tensor dynamic quantisation of K and V
+    [65536, 8, 128] and their dequantisation, by the oracle."""
+    import oracle
+    import synthetic_inputs as si
+    T, H, D = 65536, 8, 128
+    xs = [si.bits16(si.kv_with_spikes(T, H, D, seed=4000 + j).reshape(T * H, D)) for j in range(2)]
+    t0 = time.perf_counter()
+    for x in xs:
+        q, s = oracle.quant(x, oracle.BF16, oracle.E4M3, oracle.PER_TENSOR)
+        oracle.dequant(q, oracle.E4M3, s, oracle.PER_TENSOR, oracle.BF16)
+    t = time.perf_counter() - t0
+    n = T * H * D
+    return {"value": r4(2 * n * 8 / t / 1e9), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"full K,V quant+dequant, {t:.1f} s"}
+
+
+def cpu_quant_prefill_sample(rows=1024):
+    """Prefill quantiser sample: the first `rows` rows of each of the four
+    sizes, dynamic per token."""
+    import oracle
+    import synthetic_inputs as si
+    xs = [si.bits16(si.normal_with_outliers((rows, C), seed=6000 + j)) for j, (_, C) in enumerate(QUANT_PREFILL)]
+    t0 = time.perf_counter()
+    for x in xs:
+        oracle.quant(x, oracle.BF16, oracle.E4M3, oracle.PER_ROW)
+    t = time.perf_counter() - t0
+    byts = sum(rows * C * 3 + 4 * rows for _, C in QUANT_PREFILL)
+    return {"value": r4(byts / t / 1e9), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{rows} rows/size, {t:.2f} s"}
+
+
+def cpu_attention_sample():
+    """Attention sample: one sequence of 4096 tokens, all 32 query heads."""
+    import numpy as np
+    import oracle
+    import synthetic_inputs as si
+    from oracle import attention as oa
+    B, T, Hkv, Hq, D = ATTN_SHAPE
+    b = 4
+    kc = si.random_codes((b, T, Hkv, D), seed=5000).numpy()
+    vc = si.random_codes((b, T, Hkv, D), seed=5001).numpy()
+    kc = np.where((kc & 0x7F) == 0x7F, kc - 1, kc).astype(np.uint8)
+    vc = np.where((vc & 0x7F) == 0x7F, vc - 1, vc).astype(np.uint8)
+    q = si.bits16(si.normal((b, Hq, D), seed=5100))
+    t0 = time.perf_counter()
+    oa.fp8_kv_decode_attention(q, oracle.BF16, kc, vc, np.full(b, T, np.int32), 0.02, 0.01, 1.0 / np.sqrt(D))
+    t = time.perf_counter() - t0
+    byts = b * (2 * T * Hkv * D + 2 * 2 * Hq * D)
+    return {"value": r4(byts / t / 1e9), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{b}/{B} seqs, numpy, {t:.2f} s"}
+
+
 # ---------------------------------------------------------------- ncu cases
 
 PROFILE_CASES = {
@@ -530,7 +715,7 @@ PROFILE_CASES = {
 }
 
 
-def run_profile_case(name: str, launches: int, override=None):
+def run_profile_case(name: str, launches: int):
     """Run `launches` calls of one kernel family on a fixed small case (for
     ncu: capture with -k/-s/-c).  Prints the kernel configuration."""
     import torch
@@ -562,7 +747,7 @@ def run_profile_case(name: str, launches: int, override=None):
         a, sa = quantised((M, K), 1, qt, True, False)
         b, sb = quantised((N, K), 2, qt, True, True)
         out = torch.empty(M, N, dtype=torch.bfloat16 if qd == w8.E4M3 else torch.float16, device=dev)
-        cfg = dict(w8.pick_config(M, N, K, qd), **override) if override else None
+        cfg = None
         ws = w8.Workspace(w8.mm_workspace_size(M, N, K, qd, cfg), dev)
         print(json.dumps({"case": name, "config": cfg or w8.pick_config(M, N, K, qd)}), flush=True)
         for _ in range(launches):
@@ -607,116 +792,6 @@ def run_profile_case(name: str, launches: int, override=None):
         raise SystemExit("a kernel reported a pipeline timeout")
 
 
-# ---------------------------------------------------------------- config sweep
-
-def sweep_large(out_path: str, reps: int = 5, only=None):
-    """Time the prefill (M=4096) fp8 shapes and the int8 70B shapes (M=8192)
-    under a grid of large-M kernel configurations (`only`: "e4m3" or "int8"
-    restricts the sweep to one of the two)."""
-    import torch
-    import int8_w8a8_scaled_gb300 as w8
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.Stream(device=dev)
-    lines = []
-    cases = [(4096, N, K, w8.E4M3) for _, N, K, _ in LLAMA8B] + [(8192, N, K, w8.INT8) for _, N, K in LLAMA70B]
-    if only is not None:
-        cases = [c for c in cases if (c[3] == w8.E4M3) == (only == "e4m3")]
-    for M, N, K, qd in cases:
-        qt = torch.float8_e4m3fn if qd == w8.E4M3 else torch.int8
-        g = torch.Generator(device=dev)
-        g.manual_seed(M + N + K)
-        lo, hi = (0, 126) if qd == w8.E4M3 else (0, 256)
-        a = torch.randint(lo, hi, (M, K), generator=g, device=dev, dtype=torch.uint8).view(qt)
-        b = torch.randint(lo, hi, (N, K), generator=g, device=dev, dtype=torch.uint8).view(qt)
-        sa = torch.rand(M, device=dev) * 0.01
-        sb = torch.rand(N, device=dev) * 0.01
-        out = torch.empty(M, N, dtype=torch.bfloat16 if qd == w8.E4M3 else torch.float16, device=dev)
-        bns = (128, 160, 192, 224, 256) if qd == w8.E4M3 else (128, 160, 256)
-        cfgs = [None] + [{"swap_ab": 0, "block_n": bn, "split_k": sp, "stages": st}
-                         for bn in bns for sp in (1, 2) for st in (0, 3)]
-        flops = 2.0 * M * N * K
-        for cfg in cfgs:
-            ws = w8.Workspace(w8.mm_workspace_size(M, N, K, qd, cfg), dev)
-
-            def fn():
-                w8.scaled_mm(a, b, sa, sb, out, workspace=ws, config=cfg)
-            try:
-                gr = graph_of(fn, stream)
-                t = time_graph(gr, stream, reps, 2) / reps
-            except Exception as e:
-                lines.append({"M": M, "N": N, "K": K, "config": cfg, "error": str(e)[:200]})
-                continue
-            lines.append({"M": M, "N": N, "K": K, "q": "e4m3" if qd == w8.E4M3 else "int8",
-                          "config": cfg or {"auto": w8.pick_config(M, N, K, qd)}, "us": t * 1e6,
-                          "tflops": flops / t / 1e12})
-            del gr, ws
-        del a, b, out
-        torch.cuda.empty_cache()
-    if w8.device_status() != 0:
-        raise SystemExit("a kernel reported a pipeline timeout")
-    with open(out_path, "w") as f:
-        for ln in lines:
-            f.write(json.dumps(ln) + "\n")
-    print(f"wrote {len(lines)} lines to {out_path}")
-
-
-def sweep_decode(out_path: str, reps: int = 20, ms=None):
-    """Time every decode GEMM shape under a grid of kernel configurations
-    (CUDA graph of 8 launches cycling over 4 weight copies, so weights come
-    from HBM).  Writes one JSON line per (shape, config)."""
-    import torch
-    import int8_w8a8_scaled_gb300 as w8
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.Stream(device=dev)
-    lines = []
-    for M in (ms or DECODE_MS):
-        for name, N, K, shared in LLAMA8B:
-            g = torch.Generator(device=dev)
-            g.manual_seed(M * 7 + N)
-            copies = [torch.randint(0, 126, (N, K), generator=g, device=dev, dtype=torch.uint8).view(torch.float8_e4m3fn)
-                      for _ in range(4)]
-            a = torch.randint(0, 126, (M, K), generator=g, device=dev, dtype=torch.uint8).view(torch.float8_e4m3fn)
-            sa = torch.rand(M, device=dev) * 0.01
-            sb = torch.rand(1 if shared else N, device=dev) * 0.01
-            out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-            cfgs = []
-            bns = [b for b in (16, 32, 64, 128, 256) if b <= max(16, 2 * M) or b <= 64]
-            for bn in bns:
-                for sp in (1, 2, 3, 4, 6, 8, 12, 16):
-                    cfgs.append({"swap_ab": 1, "block_n": bn, "split_k": sp})
-            if M >= 64:
-                for bn in (64, 128, 160, 192, 224, 256):
-                    for sp in (1, 2, 4, 8):
-                        cfgs.append({"swap_ab": 0, "block_n": bn, "split_k": sp})
-            auto = w8.pick_config(M, N, K, w8.E4M3)
-            bytes_ = N * K + M * K + 2 * M * N
-            for cfg in [None] + cfgs:
-                ws = w8.Workspace(w8.mm_workspace_size(M, N, K, w8.E4M3, cfg), dev)
-
-                def fn():
-                    for i in range(8):
-                        w8.scaled_mm(a, copies[i % 4], sa, sb, out, workspace=ws, config=cfg)
-                try:
-                    gr = graph_of(fn, stream)
-                    t = time_graph(gr, stream, reps, 3) / (8 * reps)
-                except Exception as e:  # unsupported configuration
-                    lines.append({"M": M, "proj": name, "config": cfg, "error": str(e)[:200]})
-                    continue
-                lines.append({"M": M, "proj": name, "N": N, "K": K, "config": cfg or {"auto": auto},
-                              "us": t * 1e6, "gbs": bytes_ / t / 1e9})
-                del gr
-            del copies
-            torch.cuda.empty_cache()
-    if w8.device_status() != 0:
-        raise SystemExit("a kernel reported a pipeline timeout")
-    with open(out_path, "w") as f:
-        for ln in lines:
-            f.write(json.dumps(ln) + "\n")
-    print(f"wrote {len(lines)} lines to {out_path}")
-
-
 # ---------------------------------------------------------------- main paths
 
 def run_reference(args):
@@ -741,16 +816,78 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
         "data": "synthetic",
-        "config": {"workload": "Llama-3-8B decode fp8 (M in {1,16,64,256} x QKV/O/gate-up/down), "
-                               "dynamic per-token act, per-channel weight e4m3, bf16 out",
-                   "parallelism": "replicas"},
+        "config": {"workload": DECODE_WORKLOAD, "parallelism": "replicas"},
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"{tot_rows} full activation rows (M=1 each) through all four projections "
-                                   "per run: oracle quantisation + exact scaled matmul"},
+                         "sample": f"{tot_rows} activation rows (M=1) through all four projections: "
+                                   "oracle quantisation + exact scaled matmul"},
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def run_e2e(wl, stream, dev, steps, warmup, barrier):
+    """The decode step end to end through the public API with host buffers:
+    every step uploads its activations from pinned host memory and reads its
+    outputs back, pipelined over two device buffer sets (step k+1's upload
+    and step k-1's download run on copy streams while step k computes; the
+    computes stay in order on one stream, so they share the workspace)."""
+    import torch
+    sets = [wl.items, wl.second_set()]
+    graphs = [graph_of(lambda: wl.run_step(sets[0]), stream), graph_of(lambda: wl.run_step(sets[1]), stream)]
+    host_x = [it["x"].cpu().pin_memory() for it in wl.items]
+    host_o = [[torch.empty(it["out"].shape, dtype=it["out"].dtype).pin_memory() for it in wl.items]
+              for _ in range(2)]
+    h2d = sum(h.numel() * h.element_size() for h in host_x)
+    d2h = sum(h.numel() * h.element_size() for h in host_o[0])
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_up = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_down = [torch.cuda.Event() for _ in range(2)]
+    k = [0]
+
+    def e2e_step():
+        b = k[0] % 2
+        k[0] += 1
+        up.wait_event(ev_comp[b])          # set b's activations are free again
+        with torch.cuda.stream(up):
+            for it, hx in zip(sets[b], host_x):
+                it["x"].copy_(hx, non_blocking=True)
+            ev_up[b].record(up)
+        stream.wait_event(ev_up[b])
+        stream.wait_event(ev_down[b])      # set b's outputs have been read back
+        with torch.cuda.stream(stream):
+            graphs[b].replay()
+            ev_comp[b].record(stream)
+        down.wait_event(ev_comp[b])
+        with torch.cuda.stream(down):
+            for it, ho in zip(sets[b], host_o[b]):
+                ho.copy_(it["out"], non_blocking=True)
+            ev_down[b].record(down)
+
+    def sample():
+        torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_ev.record(up)                    # the first upload is inside the timed region
+        for _ in range(steps):
+            e2e_step()
+        for b in range(2):
+            stream.wait_event(ev_down[b])  # ... and so is the last download
+        e_ev.record(stream)
+        torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        return s_ev.elapsed_time(e_ev) / 1e3
+
+    import math
+    for _ in range(warmup):
+        e2e_step()
+    probe = sample()
+    n = int(max_over_ranks(float(max(1, math.ceil(MIN_TIMED_S / max(probe, 1e-9)))), dev))
+    t = statistics.median([sample() for _ in range(n)])
+    return t, n, h2d, d2h
 
 
 def run_ours(args):
@@ -771,135 +908,77 @@ def run_ours(args):
     pk, pk_kind = peaks()
     stream = torch.cuda.Stream(device=dev)
 
-    wl = DecodeWorkload(dev, override=json.loads(args.override) if args.override else None)
+    wl = DecodeWorkload(dev)
     g_step = graph_of(wl.run_step, stream)
     g_gemm = graph_of(wl.run_gemm, stream)
     g_quant = graph_of(wl.run_quant, stream)
 
     sampler = ClockSampler(local)
     sampler.start()
-    t = time_graph(g_step, stream, args.steps, args.warmup, barrier)
+    t_sample, n_samples = timed(g_step.replay, stream, args.steps, args.warmup, barrier=barrier, device=dev)
     clocks = sampler.stop()
-    t = max_over_ranks(t, dev)
+    t = max_over_ranks(t_sample, dev)
     flops_step = wl.flops()
     value = aggregate_tflops(flops_step, args.steps, t, ws_n)
     ms_per_step = t / args.steps * 1e3
 
-    # per-kernel-class timing over their own timed regions
-    t_gemm = time_graph(g_gemm, stream, args.steps, args.warmup) / args.steps
-    t_quant = time_graph(g_quant, stream, args.steps, args.warmup) / args.steps
-    gemm_bytes = wl.gemm_bytes()
+    # the step's two kernel classes, each over its own timed samples
+    t_gemm, _ = time_graph(g_gemm, stream, args.steps, args.warmup)
+    t_quant, _ = time_graph(g_quant, stream, args.steps, args.warmup)
     hbm = pk["hbm_gbs"]
-    gemm_gbs = gemm_bytes / t_gemm / 1e9
+    gemm_gbs = wl.gemm_bytes() / t_gemm / 1e9
     quant_gbs = wl.quant_bytes() / t_quant / 1e9
 
-    # end to end through the public API with host buffers: every step copies
-    # its activations in from pinned host memory and reads its outputs back.
-    # Pipelined over two device buffer sets: step k+1's upload and step k-1's
-    # download run on copy streams while step k computes (the computes stay
-    # in order on one stream, so they share the workspace safely).
-    sets = [wl.items, wl.second_set()]
-    graphs = [g_step, graph_of(lambda: wl.run_step(sets[1]), stream)]
-    host_x = [it["x"].cpu().pin_memory() for it in wl.items]
-    host_o = [[torch.empty(it["out"].shape, dtype=it["out"].dtype).pin_memory() for it in wl.items]
-              for _ in range(2)]
-    h2d = sum(h.numel() * h.element_size() for h in host_x)
-    d2h = sum(h.numel() * h.element_size() for h in host_o[0])
-    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_up = [torch.cuda.Event() for _ in range(2)]
-    ev_comp = [torch.cuda.Event() for _ in range(2)]
-    ev_down = [torch.cuda.Event() for _ in range(2)]
+    t_e2e, n_e2e, h2d, d2h = run_e2e(wl, stream, dev, args.steps, args.warmup, barrier)
+    t_e2e = max_over_ranks(t_e2e, dev)
+    e2e_val = aggregate_tflops(flops_step, args.steps, t_e2e, ws_n)
+    del g_step, g_gemm, g_quant
 
-    def e2e_step(k):
-        b = k % 2
-        up.wait_event(ev_comp[b])          # set b's activations are free again
-        with torch.cuda.stream(up):
-            for it, hx in zip(sets[b], host_x):
-                it["x"].copy_(hx, non_blocking=True)
-            ev_up[b].record(up)
-        stream.wait_event(ev_up[b])
-        stream.wait_event(ev_down[b])      # set b's outputs have been read back
-        with torch.cuda.stream(stream):
-            graphs[b].replay()
-            ev_comp[b].record(stream)
-        down.wait_event(ev_comp[b])
-        with torch.cuda.stream(down):
-            for it, ho in zip(sets[b], host_o[b]):
-                ho.copy_(it["out"], non_blocking=True)
-            ev_down[b].record(down)
-
-    e2e_steps = max(2, min(args.steps, 200))
-    for k in range(args.warmup):
-        e2e_step(k)
-    torch.cuda.synchronize()
-    if barrier:
-        barrier()
-    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s_ev.record(up)                        # the first upload is inside the timed region
-    for k in range(e2e_steps):
-        e2e_step(k)
-    for b in range(2):
-        stream.wait_event(ev_down[b])      # ... and so is the last download
-    e_ev.record(stream)
-    torch.cuda.synchronize()
-    t_e2e = max_over_ranks(s_ev.elapsed_time(e_ev) / 1e3, dev)
-    e2e_val = aggregate_tflops(flops_step, e2e_steps, t_e2e, ws_n)
-
-    workloads = {}
+    cfgs = {}
     if not args.main_only:
-        extra_steps = max(3, min(args.steps, 50))
-        workloads["prefill_fp8_static"] = measure_prefill_fp8(dev, extra_steps, max(3, args.warmup), stream, pk)
-        workloads["int8_70b"] = measure_int8_70b(dev, extra_steps, max(3, args.warmup), stream, pk)
-        workloads["kv_cache_fp8"] = measure_kv(dev, extra_steps, max(3, args.warmup), stream, pk)
-        workloads["kv_fp8_attention"] = measure_kv_attention(dev, extra_steps, max(3, args.warmup), stream, pk)
-    workloads["decode_fp8_detail"] = {
-        "gemm_us_per_step": t_gemm * 1e6, "quant_us_per_step": t_quant * 1e6,
-        "gemm_gbs": gemm_gbs, "gemm_frac_hbm": gemm_gbs / hbm,
-        "quant_gbs": quant_gbs, "quant_frac_hbm": quant_gbs / hbm,
-        "fused_quant": [f"M{it['M']}_{it['name']}" for it in wl.items if it["fused"]],
-        "configs": {f"M{it['M']}_{it['name']}": w8.pick_config(it["M"], *wl.weights[it["name"]][2:4][::1],
-                                                               w8.E4M3) for it in wl.items},
-    }
+        w = max(3, args.warmup)
+        st = max(3, min(args.steps, 50))
+        cfgs["c3_prefill_fp8"] = measure_prefill_fp8(dev, st, w, stream, pk)
+        cfgs["c4_int8_70b"] = measure_int8_70b(dev, st, w, stream, pk)
+        cfgs["c5_kv_fp8"] = measure_kv(dev, st, w, stream, pk)
+        cfgs["attn_fp8kv"] = measure_kv_attention(dev, st, w, stream, pk)
+        cfgs["quant_prefill"] = measure_quant_prefill(dev, st, w, stream, pk)
+    cfgs["c2_detail"] = {"gemm_us": r4(t_gemm * 1e6), "quant_us": r4(t_quant * 1e6),
+                         "quant_gbs": r4(quant_gbs), "quant_frac": r4(quant_gbs / hbm)}
 
     cpu = None
-    if rank == 0 and ws_n >= 1 and args.gpus == 1 and not args.no_cpu_baseline:
+    if rank == 0 and args.gpus == 1 and not args.no_cpu_baseline:
         f, tc, rows, cores = oracle_decode_sample(args.cpu_budget)
-        cpu = {"value": f / tc / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"{rows} full activation rows (M=1) through QKV/O/gate-up/down: oracle quantisation "
-                         f"+ exact scaled matmul, {tc:.1f} s"}
+        cpu = {"value": r4(f / tc / 1e12), "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{rows} rows (M=1) x 4 projections: quant + exact matmul, {tc:.1f} s"}
+        if not args.main_only:
+            for key, fn in (("c3_prefill_fp8", cpu_prefill_sample), ("c4_int8_70b", cpu_int8_sample),
+                            ("c5_kv_fp8", cpu_kv_full), ("attn_fp8kv", cpu_attention_sample),
+                            ("quant_prefill", cpu_quant_prefill_sample)):
+                cfgs[key]["cpu_baseline"] = fn()
 
     if rank == 0:
+        tr = traffic_ratio_for("decode_gemm")
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "metric": METRIC, "value": r4(value), "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": r4(ms_per_step), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-            "config": {"workload": "Llama-3-8B decode fp8: M in {1,16,64,256} x QKV[6144x4096, shared "
-                                   "per-tensor scale]/O[4096x4096]/gate-up[28672x4096]/down[4096x14336]; "
-                                   "dynamic per-token act, per-channel weight e4m3, bf16 out",
-                       "l2": "inputs larger than L2 (218 MB of weights per step vs 129 MB L2)",
-                       "graph": f"one CUDA graph per step ({wl.launches_per_step()} kernels: "
-                                f"{sum(1 for it in wl.items if it['fused'])} matmuls that quantise their own "
-                                f"activations, the rest quantiser + matmul)",
+            "config": {"workload": DECODE_WORKLOAD,
+                       "timing": f"CUDA graph of one step; median of {n_samples} samples of {args.steps} steps "
+                                 f"(>= {MIN_TIMED_S} s timed); inputs > L2 (218 MB weights/step)",
                        "parallelism": "replicas" if ws_n > 1 else "single GPU"},
-            "roofline": {"bound": "hbm", "kernel": "w8a8_gemm_kernel (the 16 decode matmuls of a step, "
-                                                   "activation quantisation fused where it runs inside them)",
-                         "achieved": gemm_gbs, "peak": hbm, "unit": "GB/s", "frac": gemm_gbs / hbm,
-                         "peak_kind": pk_kind + " (MEASURED_PEAKS.json hbm_gbs)" if pk_kind == "measured" else pk_kind,
-                         "traffic": (None if traffic_ratio_for("decode_gemm") is None else
-                                     traffic_ratio_for("decode_gemm") * wl.gemm_bytes() / wl.gemms_per_step()),
-                         "traffic_note": "DRAM read+write bytes per launch (average decode GEMM): the ncu "
-                                         "dram/algorithmic ratio of profiles/traffic.json x algorithmic bytes",
-                         "bytes_note": "algorithmic: N*K + M*K*(2 where the kernel quantises bf16 x itself, "
-                                       "else 1) + 2*M*N + 4*(M+scales) per matmul"},
+            "roofline": {"bound": "hbm", "kernel": "w8a8_gemm_kernel (16 decode GEMMs)",
+                         "achieved": r4(gemm_gbs), "peak": r4(hbm), "unit": "GB/s", "frac": r4(gemm_gbs / hbm),
+                         "peak_kind": pk_kind,
+                         "traffic": None if tr is None else r4(tr * wl.gemm_bytes() / wl.gemms_per_step())},
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "note": "public API with pinned host buffers; each step uploads its activations and downloads "
-                            "its outputs, overlapped with the neighbouring steps' compute (two device buffer sets)"},
+            "e2e": {"value": r4(e2e_val), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "samples": n_e2e},
             "gpu_launches": wl.launches_per_step() * args.steps,
             "clocks": clocks,
-            "workloads": workloads,
+            "configs": cfgs,
         }
-        print(json.dumps(line), flush=True)
+        print(json.dumps(line, separators=(",", ":")), flush=True)
     if ws_n > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -909,34 +988,18 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--main-only", action="store_true", help="skip the extra workloads")
+    ap.add_argument("--main-only", action="store_true", help="skip the other configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle time for the decode cpu_baseline")
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
                     help="run a few launches of one kernel on a small case (for ncu) and exit")
     ap.add_argument("--launches", type=int, default=5)
-    ap.add_argument("--override", default=None,
-                    help="JSON dict merged into the automatic matmul configuration of every decode GEMM "
-                         "(experiments; the default run uses the library's choice)")
-    ap.add_argument("--sweep-decode", metavar="OUT", default=None,
-                    help="time the decode GEMM shapes under a grid of configurations, write JSON lines to OUT")
-    ap.add_argument("--sweep-ms", default=None, help="token counts for --sweep-decode, e.g. 64,256")
-    ap.add_argument("--sweep-large", metavar="OUT", default=None,
-                    help="time the prefill / int8 70B shapes under large-M configurations")
-    ap.add_argument("--sweep-q", choices=("e4m3", "int8"), default=None,
-                    help="restrict --sweep-large to the e4m3 or the int8 shapes")
     args = ap.parse_args()
-    if args.sweep_large:
-        sweep_large(args.sweep_large, only=args.sweep_q)
-        return 0
-    if args.sweep_decode:
-        sweep_decode(args.sweep_decode, ms=[int(m) for m in args.sweep_ms.split(",")] if args.sweep_ms else None)
-        return 0
     if args.profile_case:
-        run_profile_case(args.profile_case, args.launches, json.loads(args.override) if args.override else None)
+        run_profile_case(args.profile_case, args.launches)
         return 0
     if args.warmup < 3:
         args.warmup = 3
