@@ -15,12 +15,34 @@
 // o = sum 2^(s - m) * decode(v); a second kernel combines the chunks:
 // out = (sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c) * v_scale.
 //
-// Work split inside a CTA (128 threads): 8 lanes per token, 16 head dims
-// (16 code bytes) per lane, so a warp's load covers four whole 128-byte
-// cache rows.  Scores: each lane multiplies its 16 dims by the G query rows
-// (kept in registers) and the 8 lanes of a token add their partial sums
-// with shuffles.  Output: each lane accumulates its 16 dims for the G heads
-// over its tokens; lanes with the same dims then add up across tokens.
+// Both products run on the tensor cores (mma.sync m16n8k16, f16 operands,
+// fp32 accumulation), 16 tokens at a time per warp:
+//   scores  S^T[16 tokens x 8 heads] = K[16 tokens x 128] . q^T[128 x 8]
+//   output  O^T[128 dims x 8 heads] += V^T[128 x 16 tokens] . P^T[16 tokens x 8]
+// e4m3 codes convert exactly to f16 (one cvt per two codes).  The query is
+// scaled by a power of two 2^e before its conversion to f16, so that its
+// largest element lies in [2^14, 2^15): every bf16 query element down to
+// 2^-31 of the largest converts exactly (f16 carries bf16's 8 significant
+// bits over that range), and the scores are multiplied by 2^-e after.  The
+// softmax weights p = 2^(s - m) <= 1 are carried as p * 2^15 = hi + lo, two
+// f16 values (hi = f16(p * 2^15), lo = f16(p * 2^15 - hi)), so a weight
+// keeps ~22 significant bits: for G <= 4 the lo halves take the four
+// padding columns of the 8-column MMA (no extra MMA), for G = 8 a second
+// MMA adds them.
+//
+// Register layout (lane = 4 g + t):
+//  - scores: A = K tile, rows g and g + 8 are tokens g and g + 8; thread t
+//    reads bytes [16t, 16t + 16) and [64 + 16t, 64 + 16t + 16) of a 128-byte
+//    cache row (the 8 lanes t = 0..3 of two instructions read whole rows),
+//    and k-block j (16 dims) takes 4 of those 32 bytes.  The dot product
+//    does not depend on the order of the dims, so q's fragment is laid out
+//    with the same permutation.
+//  - output: A = V^T tile, rows are dims; thread g reads bytes
+//    [16g, 16g + 16) of the rows of tokens 2t, 2t+1, 2t+8, 2t+9 and
+//    m-block i (16 dims) takes dims 16g + 2i (row g) and 16g + 2i + 1
+//    (row g + 8): byte permutes pair two tokens' codes of one dim.
+//  - P^T: the scores' accumulator layout transposed in registers
+//    (movmatrix), which is exactly the B fragment of the output MMA.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -32,28 +54,17 @@ namespace w8a8 {
 namespace {
 
 constexpr int kHeadDim = 128;
-constexpr int kAttnThreads = 128;
-constexpr int kLanesPerToken = 8;                              // 16 dims per lane
-constexpr int kTokPerPass = kAttnThreads / kLanesPerToken;    // 16 tokens per pass of the CTA
-constexpr int kUnroll = 4;                                     // passes whose loads are in flight together
-constexpr int kMaxChunk = 256;
-constexpr int kPartStride = kHeadDim + 4;                      // o[128], m, l, 2 pad (floats)
-
-// 16 e4m3 codes -> 16 floats (exact: e4m3 -> f16 -> f32 widen)
-__device__ __forceinline__ void decode16(const uint4& w, float (&f)[16]) {
-  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[i] & 0xFFFFu), __NV_E4M3);
-    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[i] >> 16), __NV_E4M3);
-    const float2 a = __half22float2(__half2(lo));
-    const float2 b = __half22float2(__half2(hi));
-    f[4 * i + 0] = a.x;
-    f[4 * i + 1] = a.y;
-    f[4 * i + 2] = b.x;
-    f[4 * i + 3] = b.y;
-  }
-}
+constexpr int kWarps = 4;                         // warps per CTA; each takes chunk / 4 tokens
+constexpr int kAttnThreads = 32 * kWarps;
+#ifndef W8A8_ATTN_MIN_CTAS
+#define W8A8_ATTN_MIN_CTAS 3
+#endif
+#ifndef W8A8_ATTN_MAX_CHUNK
+#define W8A8_ATTN_MAX_CHUNK 512
+#endif
+constexpr int kMaxChunk = W8A8_ATTN_MAX_CHUNK;
+constexpr int kPartStride = kHeadDim + 4;         // o[128], m, l, 2 pad (floats)
+constexpr float kPScale = 32768.f;                // weights enter the output MMA as p * 2^15
 
 __device__ __forceinline__ float load_q(const void* q, int q_fp16, size_t i) {
   if (q_fp16) return __half2float(static_cast<const __half*>(q)[i]);
@@ -74,10 +85,168 @@ __device__ __forceinline__ int seq_len_of(const AttnParams& p, int b) {
   return len < 0 ? 0 : (len > p.max_seq_len ? p.max_seq_len : len);
 }
 
-// Up to 4 heads per KV head the kernel fits 96 registers without spilling,
-// so 5 CTAs (20 warps) share an SM instead of 4; at 8 heads a cap spills.
+// two e4m3 codes (low byte first) -> f16x2 (exact), as a 32-bit register
+__device__ __forceinline__ uint32_t cvt2(uint32_t two_codes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
+  return static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+}
+
+// D += A . B for one m16n8k16 tile: f16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 matrix of 16-bit elements held one row pair per lane
+// (lane 4r + c holds row r, columns 2c and 2c + 1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint4 ld_stream16(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
+  return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+}
+
+// f16 weight pair hi + lo of x (hi = RN(x), lo = RN(x - hi)); `want_lo`
+// picks which of the two a lane contributes.
+__device__ __forceinline__ __half weight_part(float x, bool want_lo) {
+  const __half hi = __float2half_rn(x);
+  return want_lo ? __float2half_rn(x - __half2float(hi)) : hi;
+}
+
+// The codes one lane holds for a block of 16 tokens: K rows g and g + 8
+// (bytes 16t and 64 + 16t), V rows 2t, 2t + 1, 2t + 8, 2t + 9 (bytes 16g),
+// and whether K rows g, g + 8 are tokens of the sequence.
+struct KvBlock {
+  uint4 k[2][2];
+  uint4 v[4];
+  bool kval[2];
+};
+
+// Loads of the block at chunk position ib (tokens past `end` or in padding
+// blocks are not loaded: zeros, marked invalid).
+__device__ __forceinline__ void load_block(const AttnParams& p, int b, int t0, int ib, int end, int g, int t,
+                                           const uint8_t* kbase, const uint8_t* vbase, long long row_bytes,
+                                           KvBlock& x) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int i = ib + g + 8 * r;
+    const long long slot = i < end ? slot_of(p, b, t0 + i) : -1;
+    x.kval[r] = slot >= 0;
+    if (slot >= 0) {
+      const uint8_t* row = kbase + slot * row_bytes;
+      x.k[r][0] = ld_stream16(row + 16 * t);
+      x.k[r][1] = ld_stream16(row + 64 + 16 * t);
+    } else {
+      x.k[r][0] = x.k[r][1] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = ib + 2 * t + (r & 1) + 8 * (r >> 1);
+    const long long slot = i < end ? slot_of(p, b, t0 + i) : -1;
+    x.v[r] = slot >= 0 ? ld_stream16(vbase + slot * row_bytes + 16 * g) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Running softmax state of one lane: maxima and (lane-partial) sums of its
+// two columns, and the O^T accumulators of the 8 dim blocks.
+struct SoftmaxState {
+  float m[2], l[2];
+  float o[8][4];
+};
+
+// Scores, online softmax and output update for one block of 16 tokens.
+template <bool kPack>
+__device__ __forceinline__ void attend_block(const KvBlock& x, const uint32_t (&qf)[8][2], float cs, bool lo_lane,
+                                             SoftmaxState& st) {
+  // scores S^T[token g / g+8][column 2t / 2t+1]
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t w0r = word_of(x.k[0][j >> 2], j & 3);
+    const uint32_t w1r = word_of(x.k[1][j >> 2], j & 3);
+    mma16816(s, cvt2(w0r), cvt2(w1r), cvt2(w0r >> 16), cvt2(w1r >> 16), qf[j][0], qf[j][1]);
+  }
+  // lanes t >= 2 mirror their partner's columns (heads); invalid tokens -inf
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float v = __shfl_xor_sync(0xffffffffu, s[k], 2);
+    float y = lo_lane ? v : s[k];
+    y = x.kval[k >> 1] ? y * cs : -INFINITY;
+    s[k] = y;
+    mx[k & 1] = fmaxf(mx[k & 1], y);
+  }
+  float alpha[2], m_new[2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], off));
+    m_new[c] = fmaxf(st.m[c], mx[c]);
+    alpha[c] = m_new[c] == -INFINITY ? 1.f : exp2f(st.m[c] - m_new[c]);
+    st.m[c] = m_new[c];
+    st.l[c] *= alpha[c];
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    st.o[i][0] *= alpha[0];
+    st.o[i][1] *= alpha[1];
+    st.o[i][2] *= alpha[0];
+    st.o[i][3] *= alpha[1];
+  }
+  float pw[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float mc = m_new[k & 1];
+    pw[k] = (mc == -INFINITY) ? 0.f : exp2f(s[k] - mc);
+    st.l[k & 1] += pw[k];
+  }
+  // P^T fragments (tokens 2t.., column g) by transposing the accumulator layout
+  uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
+  if (kPack) {
+    bh0 = movmatrix_t(pack_half2(weight_part(pw[0] * kPScale, lo_lane), weight_part(pw[1] * kPScale, lo_lane)));
+    bh1 = movmatrix_t(pack_half2(weight_part(pw[2] * kPScale, lo_lane), weight_part(pw[3] * kPScale, lo_lane)));
+  } else {
+    bh0 = movmatrix_t(pack_half2(weight_part(pw[0] * kPScale, false), weight_part(pw[1] * kPScale, false)));
+    bh1 = movmatrix_t(pack_half2(weight_part(pw[2] * kPScale, false), weight_part(pw[3] * kPScale, false)));
+    bl0 = movmatrix_t(pack_half2(weight_part(pw[0] * kPScale, true), weight_part(pw[1] * kPScale, true)));
+    bl1 = movmatrix_t(pack_half2(weight_part(pw[2] * kPScale, true), weight_part(pw[3] * kPScale, true)));
+  }
+  // O^T[dims 16g+2i, 16g+2i+1][columns] += V^T . P^T
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+    const uint32_t p01 = __byte_perm(word_of(x.v[0], i >> 1), word_of(x.v[1], i >> 1), sel);
+    const uint32_t p23 = __byte_perm(word_of(x.v[2], i >> 1), word_of(x.v[3], i >> 1), sel);
+    const uint32_t a0 = cvt2(p01), a1 = cvt2(p01 >> 16), a2 = cvt2(p23), a3 = cvt2(p23 >> 16);
+    mma16816(st.o[i], a0, a1, a2, a3, bh0, bh1);
+    if (!kPack) mma16816(st.o[i], a0, a1, a2, a3, bl0, bl1);
+  }
+}
+
 template <int G>
-__global__ void __launch_bounds__(kAttnThreads, G <= 4 ? 5 : 1) fp8kv_attn_chunk_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kAttnThreads, W8A8_ATTN_MIN_CTAS) fp8kv_attn_chunk_kernel(const AttnParams p) {
+  // G <= 4: the lo halves of the weights ride in the padding columns 4..7
+  constexpr bool kPack = G <= 4;
   const int b = blockIdx.z;
   const int kvh = blockIdx.y;
   const int ch = blockIdx.x;
@@ -85,149 +254,131 @@ __global__ void __launch_bounds__(kAttnThreads, G <= 4 ? 5 : 1) fp8kv_attn_chunk
   const int t0 = ch * p.chunk;
   if (t0 >= len) return;  // uniform: the combine reads only chunks that hold tokens
   const int n = min(len - t0, p.chunk);
-
-  __shared__ float qs[G][kHeadDim];          // query rows * (sm_scale * k_scale * log2 e)
-  __shared__ float ps[G][kMaxChunk];         // scores, then 2^(s - m)
-  __shared__ float red[kAttnThreads / 32][G][kHeadDim];
-  __shared__ float s_m[G], s_l[G];
-
-  const float c = p.sm_scale * __ldg(p.k_scale) * 1.4426950408889634f;  // log2(e)
-  for (int i = threadIdx.x; i < G * kHeadDim; i += kAttnThreads) {
-    const int g = i / kHeadDim, d = i - g * kHeadDim;
-    qs[g][d] = load_q(p.q, p.q_fp16, (static_cast<size_t>(b) * p.num_q_heads + kvh * G + g) * kHeadDim + d) * c;
-  }
-  __syncthreads();
-
-  const int sub = threadIdx.x % kLanesPerToken;  // dims sub*16 .. +15
-  const int tok = threadIdx.x / kLanesPerToken;  // token within a pass
-  const uint8_t* kbase = static_cast<const uint8_t*>(p.k_cache) + kvh * kHeadDim + sub * 16;
-  const uint8_t* vbase = static_cast<const uint8_t*>(p.v_cache) + kvh * kHeadDim + sub * 16;
-  const long long row_bytes = static_cast<long long>(p.num_kv_heads) * kHeadDim;
-
-  // ---- scores
-  {
-    float qr[G][16];
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int j = 0; j < 16; ++j) qr[g][j] = qs[g][sub * 16 + j];
-    for (int i0 = 0; i0 < n; i0 += kTokPerPass * kUnroll) {
-      uint4 w[kUnroll];
-      bool valid[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int i = i0 + u * kTokPerPass + tok;
-        const long long slot = i < n ? slot_of(p, b, t0 + i) : -1;
-        valid[u] = slot >= 0;
-        w[u] = valid[u] ? __ldg(reinterpret_cast<const uint4*>(kbase + slot * row_bytes)) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        float f[16];
-        decode16(w[u], f);
-        float s[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float a = 0.f;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) a = fmaf(f[j], qr[g][j], a);
-          s[g] = a;
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          s[g] += __shfl_xor_sync(0xffffffffu, s[g], 4);
-          s[g] += __shfl_xor_sync(0xffffffffu, s[g], 2);
-          s[g] += __shfl_xor_sync(0xffffffffu, s[g], 1);
-        }
-        const int i = i0 + u * kTokPerPass + tok;
-        if (sub == 0 && i < n)
-#pragma unroll
-          for (int g = 0; g < G; ++g) ps[g][i] = valid[u] ? s[g] : -INFINITY;
-      }
-    }
-  }
-  __syncthreads();
-
-  // ---- chunk maximum and 2^(s - m), per head (warp w takes heads w, w+4)
-  {
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    for (int g = warp; g < G; g += kAttnThreads / 32) {
-      float m = -INFINITY;
-      for (int i = lane; i < n; i += 32) m = fmaxf(m, ps[g][i]);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      float l = 0.f;
-      for (int i = lane; i < n; i += 32) {
-        const float e = (m == -INFINITY) ? 0.f : exp2f(ps[g][i] - m);
-        ps[g][i] = e;
-        l += e;
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-      if (lane == 0) {
-        s_m[g] = m;
-        s_l[g] = l;
-      }
-    }
-  }
-  __syncthreads();
-
-  // ---- o = sum_t 2^(s_t - m) * decode(v_t), per head
-  float o[G][16];
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int j = 0; j < 16; ++j) o[g][j] = 0.f;
-  for (int i0 = 0; i0 < n; i0 += kTokPerPass * kUnroll) {
-    uint4 w[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int i = i0 + u * kTokPerPass + tok;
-      const long long slot = i < n ? slot_of(p, b, t0 + i) : -1;
-      w[u] = slot >= 0 ? __ldg(reinterpret_cast<const uint4*>(vbase + slot * row_bytes)) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int i = i0 + u * kTokPerPass + tok;
-      if (i >= n) continue;
-      float f[16];
-      decode16(w[u], f);
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float pg = ps[g][i];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) o[g][j] = fmaf(pg, f[j], o[g][j]);
-      }
-    }
-  }
-  // lanes with the same dims (sub) in a warp: tokens differ by lane bits 3, 4
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      o[g][j] += __shfl_xor_sync(0xffffffffu, o[g][j], 8);
-      o[g][j] += __shfl_xor_sync(0xffffffffu, o[g][j], 16);
-    }
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  if (lane < kLanesPerToken)
+  const int g = lane >> 2, t = lane & 3;
+
+  __shared__ __align__(16) __half qs[8][kHeadDim];   // q * 2^e in f16; zero rows for padding heads
+  __shared__ float s_qmax[kWarps];
+  __shared__ float s_m[kWarps][8], s_l[kWarps][8];
+  __shared__ float s_o[kWarps][G][kHeadDim];
+
+  // this warp's tokens of the chunk; the first block's codes are requested
+  // before the query is prepared
+  const uint8_t* kbase = static_cast<const uint8_t*>(p.k_cache) + kvh * kHeadDim;
+  const uint8_t* vbase = static_cast<const uint8_t*>(p.v_cache) + kvh * kHeadDim;
+  const long long row_bytes = static_cast<long long>(p.num_kv_heads) * kHeadDim;
+  const int per_warp = p.chunk / kWarps;
+  const int w0 = warp * per_warp;
+  const int w1 = min(n, w0 + per_warp);
+  KvBlock xa, xb;
+  load_block(p, b, t0, w0, w1, g, t, kbase, vbase, row_bytes, xa);
+
+  // ---- the query rows of the G heads, scaled by 2^e into [2^14, 2^15) and converted to f16
+  const size_t q0 = (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G) * kHeadDim;
+  float qmax = 0.f;
+  for (int i = threadIdx.x; i < G * kHeadDim; i += kAttnThreads) qmax = fmaxf(qmax, fabsf(load_q(p.q, p.q_fp16, q0 + i)));
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+  for (int off = 16; off > 0; off >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+  if (lane == 0) s_qmax[warp] = qmax;
+  __syncthreads();
+  qmax = s_qmax[0];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) red[warp][g][lane * 16 + j] = o[g][j];
+  for (int w = 1; w < kWarps; ++w) qmax = fmaxf(qmax, s_qmax[w]);
+  int e = 0;
+  if (qmax > 0.f && qmax <= 3.0e38f) {
+    int ex;
+    frexpf(qmax, &ex);  // qmax in [2^(ex-1), 2^ex)
+    e = min(100, max(-100, 15 - ex));
+  }
+  for (int i = threadIdx.x; i < 8 * kHeadDim; i += kAttnThreads) {
+    const int h = i / kHeadDim;
+    qs[h][i % kHeadDim] = h < G ? __float2half_rn(ldexpf(load_q(p.q, p.q_fp16, q0 + i), e)) : __float2half_rn(0.f);
+  }
+  __syncthreads();
+  // B fragment of k-block j: dims L_t[4j .. 4j+3] of head g, L_t = [16t, 16t+16) ++ [64+16t, 64+16t+16)
+  uint32_t qf[8][2];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int d = (j < 4 ? 16 * t : 64 + 16 * t) + 4 * (j & 3);
+    qf[j][0] = *reinterpret_cast<const uint32_t*>(&qs[g][d]);
+    qf[j][1] = *reinterpret_cast<const uint32_t*>(&qs[g][d + 2]);
+  }
+  // scores in the log2 domain: S' * (sm_scale * k_scale * log2 e) * 2^-e
+  const float cs = ldexpf(p.sm_scale * __ldg(p.k_scale) * 1.4426950408889634f, -e);
+
+  // columns 2t and 2t+1 of this lane: heads hc, hc + 1 (with packing the
+  // lanes t >= 2 hold the lo parts of the heads of lane t - 2)
+  const bool lo_lane = kPack && t >= 2;
+  SoftmaxState st;
+  st.m[0] = st.m[1] = -INFINITY;
+  st.l[0] = st.l[1] = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
+
+  // blocks of 16 tokens, the next block's codes in flight while one is used
+  for (int ib = w0; ib < w1; ib += 32) {
+    load_block(p, b, t0, ib + 16, w1, g, t, kbase, vbase, row_bytes, xb);
+    attend_block<kPack>(xa, qf, cs, lo_lane, st);
+    if (ib + 16 >= w1) break;
+    load_block(p, b, t0, ib + 32, w1, g, t, kbase, vbase, row_bytes, xa);
+    attend_block<kPack>(xb, qf, cs, lo_lane, st);
+  }
+  float (&o)[8][4] = st.o;
+  float (&m_run)[2] = st.m;
+  float (&l_run)[2] = st.l;
+
+  // ---- this warp's (m, l, o) per head into shared memory
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) l_run[c] += __shfl_xor_sync(0xffffffffu, l_run[c], off);
+  if (kPack) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[i][k] += __shfl_xor_sync(0xffffffffu, o[i][k], 2);  // hi + lo
+  }
+  const int hc = kPack ? 2 * (t & 1) : 2 * t;
+  if (!lo_lane) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int h = hc + c;
+      if (h < G) {
+        if (g == 0) {
+          s_m[warp][h] = m_run[c];
+          s_l[warp][h] = l_run[c];
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          s_o[warp][h][16 * g + 2 * i] = o[i][c];
+          s_o[warp][h][16 * g + 2 * i + 1] = o[i][2 + c];
+        }
+      }
+    }
+  }
   __syncthreads();
 
-  // ---- the chunk's partial result of each head: o[128], m, l
+  // ---- the chunk's partial result of each head: o[128], m, l (warps combined in order)
   const int nch = (p.max_seq_len + p.chunk - 1) / p.chunk;
-  for (int g = 0; g < G; ++g) {
-    float* part = p.partial + ((static_cast<size_t>(b) * p.num_q_heads + kvh * G + g) * nch + ch) * kPartStride;
-    const int d = threadIdx.x;
-    float acc = 0.f;
+  for (int idx = threadIdx.x; idx < G * kHeadDim; idx += kAttnThreads) {
+    const int h = idx / kHeadDim, d = idx % kHeadDim;
+    float M = s_m[0][h];
 #pragma unroll
-    for (int w2 = 0; w2 < kAttnThreads / 32; ++w2) acc += red[w2][g][d];
-    part[d] = acc;
+    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, s_m[w][h]);
+    float acc = 0.f, l = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float f = exp2f(s_m[w][h] - M);
+        acc = fmaf(f, s_o[w][h][d], acc);
+        l = fmaf(f, s_l[w][h], l);
+      }
+    }
+    float* part = p.partial + ((static_cast<size_t>(b) * p.num_q_heads + kvh * G + h) * nch + ch) * kPartStride;
+    part[d] = acc * (1.f / kPScale);
     if (d == 0) {
-      part[kHeadDim] = s_m[g];
-      part[kHeadDim + 1] = s_l[g];
+      part[kHeadDim] = M;
+      part[kHeadDim + 1] = l;
     }
   }
 }
