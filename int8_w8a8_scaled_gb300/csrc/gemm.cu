@@ -453,12 +453,9 @@ __device__ __forceinline__ uint4 fq_quant16(const uint4& a, const uint4& b, floa
   float f[8], g[8];
   unpack8<XK>(a, f);
   unpack8<XK>(b, g);
-  uint4 o;
-  o.x = enc4<0>(div_by(f[0], s, y, ok), div_by(f[1], s, y, ok), div_by(f[2], s, y, ok), div_by(f[3], s, y, ok));
-  o.y = enc4<0>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
-  o.z = enc4<0>(div_by(g[0], s, y, ok), div_by(g[1], s, y, ok), div_by(g[2], s, y, ok), div_by(g[3], s, y, ok));
-  o.w = enc4<0>(div_by(g[4], s, y, ok), div_by(g[5], s, y, ok), div_by(g[6], s, y, ok), div_by(g[7], s, y, ok));
-  return o;
+  // dynamic per-token scales: the quotients stay within the code range
+  const uint2 a8 = quant8<0>(f, s, y, ok, true), b8 = quant8<0>(g, s, y, ok, true);
+  return make_uint4(a8.x, a8.y, b8.x, b8.y);
 }
 
 // Per-token scales of the CTA's token tile (rows 0..M-1), by the 128

@@ -119,7 +119,10 @@ __device__ __forceinline__ float block_max(float v, float* red) {
 // one thread pulls the whole row into shared memory with a single bulk async
 // copy (no chain of dependent loads, which matters when a decode step has one
 // row per kernel), then all threads reduce absmax and convert from shared
-// memory in short loops (small code: the kernel runs cold on few SMs).
+// memory in short loops (small code: the kernel runs cold on few SMs).  One
+// CTA per row: with several CTAs per SM at different phases, one CTA's copy
+// is in flight while another converts.  (A persistent two-row ring per CTA
+// measured 6 % slower at the prefill sizes.)
 template <int XK, int QK>
 __global__ void __launch_bounds__(kRowThreads)
     quant_row_bulk_kernel(const uint16_t* __restrict__ x, long long ld_x, long long cols,
@@ -173,10 +176,7 @@ __global__ void __launch_bounds__(kRowThreads)
   for (int v = threadIdx.x; v < nvec; v += kRowThreads) {
     float f[8];
     unpack8<XK>(row_s[v], f);
-    uint2 o;
-    o.x = enc4<QK>(div_by(f[0], s, y, ok), div_by(f[1], s, y, ok), div_by(f[2], s, y, ok), div_by(f[3], s, y, ok));
-    o.y = enc4<QK>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
-    qr[v] = o;
+    qr[v] = quant8<QK>(f, s, y, ok, dynamic);
   }
 }
 
@@ -238,8 +238,7 @@ __global__ void __launch_bounds__(kRowThreads)
         float f[8];
         unpack8<XK>(cache[i], f);
         uint2 o;
-        o.x = enc4<QK>(div_by(f[0], s, y, ok), div_by(f[1], s, y, ok), div_by(f[2], s, y, ok), div_by(f[3], s, y, ok));
-        o.y = enc4<QK>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
+        o = quant8<QK>(f, s, y, ok, dynamic);
         reinterpret_cast<uint2*>(qr)[v] = o;
       }
     }
@@ -248,12 +247,11 @@ __global__ void __launch_bounds__(kRowThreads)
       float f[8];
       unpack8<XK>(__ldg(reinterpret_cast<const uint4*>(xr) + v), f);
       uint2 o;
-      o.x = enc4<QK>(div_by(f[0], s, y, ok), div_by(f[1], s, y, ok), div_by(f[2], s, y, ok), div_by(f[3], s, y, ok));
-      o.y = enc4<QK>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
+      o = quant8<QK>(f, s, y, ok, dynamic);
       reinterpret_cast<uint2*>(qr)[v] = o;
     }
     for (long long j = nvec * 8 + threadIdx.x; j < cols; j += kRowThreads)
-      qr[j] = enc1<QK>(div_by(cvt_in<XK>(xr[j]), s, y, ok));
+      qr[j] = quant1<QK>(cvt_in<XK>(xr[j]), s, y, ok, dynamic);
   } else {
     // scalar path for unaligned layouts
     float s;
@@ -270,7 +268,7 @@ __global__ void __launch_bounds__(kRowThreads)
     float y;
     const bool ok = recip_ok(s, &y);
     for (long long j = threadIdx.x; j < cols; j += kRowThreads)
-      qr[j] = enc1<QK>(div_by(cvt_in<XK>(xr[j]), s, y, ok));
+      qr[j] = quant1<QK>(cvt_in<XK>(xr[j]), s, y, ok, dynamic);
   }
 }
 
@@ -370,10 +368,7 @@ __global__ void __launch_bounds__(256, 4)
       unpack8<XK>(w[2 * u], *reinterpret_cast<float(*)[8]>(f));
       unpack8<XK>(w[2 * u + 1], *reinterpret_cast<float(*)[8]>(f + 8));
       uint4 o;
-      o.x = enc4<QK>(div_by(f[0], s, y, ok), div_by(f[1], s, y, ok), div_by(f[2], s, y, ok), div_by(f[3], s, y, ok));
-      o.y = enc4<QK>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
-      o.z = enc4<QK>(div_by(f[8], s, y, ok), div_by(f[9], s, y, ok), div_by(f[10], s, y, ok), div_by(f[11], s, y, ok));
-      o.w = enc4<QK>(div_by(f[12], s, y, ok), div_by(f[13], s, y, ok), div_by(f[14], s, y, ok), div_by(f[15], s, y, ok));
+      o = quant16<QK>(f, s, y, ok, dynamic);
       __stcs(reinterpret_cast<uint4*>(q) + rv(u == 0 ? v : v + stride), o);
     }
   }
@@ -382,15 +377,12 @@ __global__ void __launch_bounds__(256, 4)
     unpack8<XK>(__ldcs(reinterpret_cast<const uint4*>(x) + 2 * rv(v)), *reinterpret_cast<float(*)[8]>(f));
     unpack8<XK>(__ldcs(reinterpret_cast<const uint4*>(x) + 2 * rv(v) + 1), *reinterpret_cast<float(*)[8]>(f + 8));
     uint4 o;
-    o.x = enc4<QK>(div_by(f[0], s, y, ok), div_by(f[1], s, y, ok), div_by(f[2], s, y, ok), div_by(f[3], s, y, ok));
-    o.y = enc4<QK>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
-    o.z = enc4<QK>(div_by(f[8], s, y, ok), div_by(f[9], s, y, ok), div_by(f[10], s, y, ok), div_by(f[11], s, y, ok));
-    o.w = enc4<QK>(div_by(f[12], s, y, ok), div_by(f[13], s, y, ok), div_by(f[14], s, y, ok), div_by(f[15], s, y, ok));
+    o = quant16<QK>(f, s, y, ok, dynamic);
     __stcs(reinterpret_cast<uint4*>(q) + rv(v), o);
   }
   for (long long j = n16 * 16 + blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; j < n;
        j += stride)
-    q[j] = enc1<QK>(div_by(cvt_in<XK>(x[j]), s, y, ok));
+    q[j] = quant1<QK>(cvt_in<XK>(x[j]), s, y, ok, dynamic);
 }
 
 // Per-row quantiser driven by a per-tensor scale from the absmax word (the
@@ -407,7 +399,7 @@ __global__ void __launch_bounds__(kRowThreads)
   const bool ok = recip_ok(s, &y);
   const uint16_t* xr = x + static_cast<long long>(blockIdx.x) * ld_x;
   uint8_t* qr = q + static_cast<long long>(blockIdx.x) * ld_q;
-  for (long long j = threadIdx.x; j < cols; j += kRowThreads) qr[j] = enc1<QK>(div_by(cvt_in<XK>(xr[j]), s, y, ok));
+  for (long long j = threadIdx.x; j < cols; j += kRowThreads) qr[j] = quant1<QK>(cvt_in<XK>(xr[j]), s, y, ok, true);
 }
 
 // ---------------------------------------------------------------- dequantiser
@@ -454,58 +446,84 @@ __global__ void __launch_bounds__(256)
 }
 
 // Streaming per-tensor quantiser passes for a contiguous tensor (n % 16 == 0,
-// 16-byte aligned), in the dequantiser's pattern: chunks of kQzChunk
-// elements pulled into shared memory by bulk copies (two-deep ring, one
-// thread issuing), all threads working from shared memory.
+// 16-byte aligned): chunks of kQzChunk elements pulled into shared memory by
+// bulk copies, one thread issuing, kQzStages chunks in flight per CTA (a ring
+// of that depth), all threads working from shared memory.  With several
+// CTAs per SM that keeps ~100 KB per SM on its way from HBM.
 constexpr int kQzChunk = 4096;  // elements per chunk: 8 KB of bf16 / fp16
+#ifndef W8A8_QZ_ABS_STAGES
+#define W8A8_QZ_ABS_STAGES 4
+#endif
+#ifndef W8A8_QZ_CVT_STAGES
+#define W8A8_QZ_CVT_STAGES 2
+#endif
+// ring depths: the absmax pass only streams, so it keeps more chunks in
+// flight; the convert pass is bound by its per-element arithmetic and keeps
+// a shallow ring so that more CTAs (warps) fit an SM
+constexpr int kQzAbsStages = W8A8_QZ_ABS_STAGES;
+constexpr int kQzCvtStages = W8A8_QZ_CVT_STAGES;
+
+// Chunk ring shared by the two passes: chunk c of this CTA (its i-th) goes
+// to slot i % kQzStages; the loads run kQzStages - 1 chunks ahead.
+template <int kQzStages>
+struct QzRing {
+  long long n, nchunks, step;
+  bool reverse;  // visit the chunks back to front
+  __device__ long long phys(long long c) const { return reverse ? nchunks - 1 - c : c; }
+  __device__ uint32_t elems(long long c) const {
+    const long long rem = n - phys(c) * kQzChunk;
+    return static_cast<uint32_t>(rem < kQzChunk ? rem : kQzChunk);
+  }
+  // thread 0: issue the load of this CTA's i-th chunk, if it exists
+  __device__ bool issue(int i, const uint16_t* x, uint16_t (*buf)[kQzChunk], uint64_t* bar) const {
+    const long long c = blockIdx.x + static_cast<long long>(i) * step;
+    if (c >= nchunks) return false;
+    const int slot = i % kQzStages;
+    mbar_arrive_expect_tx(smem_addr(&bar[slot]), elems(c) * 2);
+    bulk_load(smem_addr(buf[slot]), x + phys(c) * kQzChunk, elems(c) * 2, smem_addr(&bar[slot]));
+    return true;
+  }
+  // thread 0, after a failed wait at chunk i: let the loads still in flight
+  // (chunks i .. i + kQzStages - 2 that were issued) land, bounded, before
+  // the CTA exits and its shared memory is released
+  __device__ void drain(int i, uint64_t* bar) const {
+    for (int j = i; j < i + kQzStages - 1; ++j) {
+      if (blockIdx.x + static_cast<long long>(j) * step >= nchunks) break;
+      mbar_wait(smem_addr(&bar[j % kQzStages]), (j / kQzStages) & 1);
+    }
+  }
+};
 
 // Pass 1: absmax of the whole tensor (front to back) into the word.
 template <int XK>
 __global__ void __launch_bounds__(256)
     absmax_bulk_kernel(const uint16_t* __restrict__ x, long long n, unsigned* __restrict__ word) {
-  __shared__ __align__(128) uint16_t in_buf[2][kQzChunk];
-  __shared__ uint64_t bar[2];
+  __shared__ __align__(128) uint16_t in_buf[kQzAbsStages][kQzChunk];
+  __shared__ uint64_t bar[kQzAbsStages];
   __shared__ float red[8];
   allow_dependents();
-  const long long nchunks = (n + kQzChunk - 1) / kQzChunk;
-  const long long step = gridDim.x;
-  auto chunk_elems = [&](long long c) {
-    const long long rem = n - c * kQzChunk;
-    return static_cast<int>(rem < kQzChunk ? rem : kQzChunk);
-  };
+  QzRing<kQzAbsStages> ring{n, (n + kQzChunk - 1) / kQzChunk, gridDim.x, false};
   if (threadIdx.x == 0) {
-    mbar_init(smem_addr(&bar[0]), 1);
-    mbar_init(smem_addr(&bar[1]), 1);
+    for (int j = 0; j < kQzAbsStages; ++j) mbar_init(smem_addr(&bar[j]), 1);
     fence_barrier_init();
-    const long long c0 = blockIdx.x;
-    if (c0 < nchunks) {
-      mbar_arrive_expect_tx(smem_addr(&bar[0]), chunk_elems(c0) * 2);
-      bulk_load(smem_addr(in_buf[0]), x + c0 * kQzChunk, chunk_elems(c0) * 2, smem_addr(&bar[0]));
-    }
+    for (int j = 0; j < kQzAbsStages - 1; ++j) ring.issue(j, x, in_buf, bar);
   }
   __syncthreads();
   float amax = 0.f;
   int i = 0;
-  bool failed = false, next_issued = false;
-  for (long long c = blockIdx.x; c < nchunks; c += step, ++i) {
-    const int b = i & 1;
-    next_issued = false;
-    if (threadIdx.x == 0) {
-      const long long next = c + step;
-      next_issued = next < nchunks;
-      if (next_issued) {  // in_buf[b ^ 1] was consumed last iteration
-        mbar_arrive_expect_tx(smem_addr(&bar[b ^ 1]), chunk_elems(next) * 2);
-        bulk_load(smem_addr(in_buf[b ^ 1]), x + next * kQzChunk, chunk_elems(next) * 2, smem_addr(&bar[b ^ 1]));
-      }
-    }
-    const bool got = mbar_wait(smem_addr(&bar[b]), (i >> 1) & 1);
+  bool failed = false;
+  for (long long c = blockIdx.x; c < ring.nchunks; c += ring.step, ++i) {
+    // the slot of chunk i + S - 1 was released by the barrier ending chunk i - 1
+    if (threadIdx.x == 0) ring.issue(i + kQzAbsStages - 1, x, in_buf, bar);
+    const int slot = i % kQzAbsStages;
+    const bool got = mbar_wait(smem_addr(&bar[slot]), (i / kQzAbsStages) & 1);
     if (!__syncthreads_and(got)) {
       failed = true;
       break;
     }
     const int e0 = threadIdx.x * 16;
-    if (e0 < chunk_elems(c)) {
-      const uint4* p = reinterpret_cast<const uint4*>(in_buf[b] + e0);
+    if (e0 < static_cast<int>(ring.elems(c))) {
+      const uint4* p = reinterpret_cast<const uint4*>(in_buf[slot] + e0);
       float f[8];
       unpack8<XK>(p[0], f);
 #pragma unroll
@@ -514,13 +532,9 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
       for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
     }
-    __syncthreads();  // in_buf[b] is refilled next iteration
+    __syncthreads();  // the slot is refilled S - 1 chunks on
   }
-  if (threadIdx.x == 0 && failed) {
-    // let this CTA's copies in flight land (bounded) before it exits
-    mbar_wait(smem_addr(&bar[i & 1]), (i >> 1) & 1);
-    if (next_issued) mbar_wait(smem_addr(&bar[(i & 1) ^ 1]), ((i + 1) >> 1) & 1);
-  }
+  if (threadIdx.x == 0 && failed) ring.drain(i, bar);
   amax = warp_max(amax);
   const int w = threadIdx.x / 32, l = threadIdx.x % 32;
   if (l == 0) red[w] = amax;
@@ -535,14 +549,15 @@ __global__ void __launch_bounds__(256)
 
 // Pass 2: codes of the whole tensor with the scale from the word (dynamic)
 // or scale[0] (static).  The chunks are visited back to front, so a tensor
-// about the size of L2 finds the tail pass 1 read last still there.
+// about the size of L2 finds the tail pass 1 read last still there.  Codes
+// leave through two output buffers, each written back by one bulk store.
 template <int XK, int QK>
 __global__ void __launch_bounds__(256)
     quant_bulk_kernel(const uint16_t* __restrict__ x, long long n, uint8_t* __restrict__ q,
                       float* __restrict__ scale, const unsigned* __restrict__ word, int dynamic) {
-  __shared__ __align__(128) uint16_t in_buf[2][kQzChunk];
+  __shared__ __align__(128) uint16_t in_buf[kQzCvtStages][kQzChunk];
   __shared__ __align__(128) uint8_t out_buf[2][kQzChunk];
-  __shared__ uint64_t bar[2];
+  __shared__ uint64_t bar[kQzCvtStages];
   allow_dependents();
   float s;
   if (dynamic) {
@@ -553,67 +568,43 @@ __global__ void __launch_bounds__(256)
   }
   float y;
   const bool ok = recip_ok(s, &y);
-  const long long nchunks = (n + kQzChunk - 1) / kQzChunk;
-  const long long step = gridDim.x;
-  auto phys = [&](long long c) { return nchunks - 1 - c; };  // back to front
-  auto chunk_elems = [&](long long c) {
-    const long long rem = n - phys(c) * kQzChunk;
-    return static_cast<int>(rem < kQzChunk ? rem : kQzChunk);
-  };
+  QzRing<kQzCvtStages> ring{n, (n + kQzChunk - 1) / kQzChunk, gridDim.x, true};
   if (threadIdx.x == 0) {
-    mbar_init(smem_addr(&bar[0]), 1);
-    mbar_init(smem_addr(&bar[1]), 1);
+    for (int j = 0; j < kQzCvtStages; ++j) mbar_init(smem_addr(&bar[j]), 1);
     fence_barrier_init();
-    const long long c0 = blockIdx.x;
-    if (c0 < nchunks) {
-      mbar_arrive_expect_tx(smem_addr(&bar[0]), chunk_elems(c0) * 2);
-      bulk_load(smem_addr(in_buf[0]), x + phys(c0) * kQzChunk, chunk_elems(c0) * 2, smem_addr(&bar[0]));
-    }
+    for (int j = 0; j < kQzCvtStages - 1; ++j) ring.issue(j, x, in_buf, bar);
   }
   __syncthreads();
   int i = 0;
-  bool failed = false, next_issued = false;
-  for (long long c = blockIdx.x; c < nchunks; c += step, ++i) {
-    const int b = i & 1;
-    next_issued = false;
+  bool failed = false;
+  for (long long c = blockIdx.x; c < ring.nchunks; c += ring.step, ++i) {
+    const int ob = i & 1;
     if (threadIdx.x == 0) {
-      const long long next = c + step;
-      next_issued = next < nchunks;
-      if (next_issued) {  // in_buf[b ^ 1] was consumed last iteration
-        mbar_arrive_expect_tx(smem_addr(&bar[b ^ 1]), chunk_elems(next) * 2);
-        bulk_load(smem_addr(in_buf[b ^ 1]), x + phys(next) * kQzChunk, chunk_elems(next) * 2,
-                  smem_addr(&bar[b ^ 1]));
-      }
-      bulk_wait_read<1>();  // the store two chunks back has read out_buf[b]
+      ring.issue(i + kQzCvtStages - 1, x, in_buf, bar);
+      bulk_wait_read<1>();  // the store two chunks back has read out_buf[ob]
     }
-    const bool got = mbar_wait(smem_addr(&bar[b]), (i >> 1) & 1);
+    const int slot = i % kQzCvtStages;
+    const bool got = mbar_wait(smem_addr(&bar[slot]), (i / kQzCvtStages) & 1);
     if (!__syncthreads_and(got)) {
       failed = true;
       break;
     }
-    const uint4* p = reinterpret_cast<const uint4*>(in_buf[b] + threadIdx.x * 16);
+    const uint4* p = reinterpret_cast<const uint4*>(in_buf[slot] + threadIdx.x * 16);
     float f[16];
     unpack8<XK>(p[0], *reinterpret_cast<float(*)[8]>(f));
     unpack8<XK>(p[1], *reinterpret_cast<float(*)[8]>(f + 8));
     uint4 o;
-    o.x = enc4<QK>(div_by(f[0], s, y, ok), div_by(f[1], s, y, ok), div_by(f[2], s, y, ok), div_by(f[3], s, y, ok));
-    o.y = enc4<QK>(div_by(f[4], s, y, ok), div_by(f[5], s, y, ok), div_by(f[6], s, y, ok), div_by(f[7], s, y, ok));
-    o.z = enc4<QK>(div_by(f[8], s, y, ok), div_by(f[9], s, y, ok), div_by(f[10], s, y, ok), div_by(f[11], s, y, ok));
-    o.w = enc4<QK>(div_by(f[12], s, y, ok), div_by(f[13], s, y, ok), div_by(f[14], s, y, ok), div_by(f[15], s, y, ok));
-    reinterpret_cast<uint4*>(out_buf[b])[threadIdx.x] = o;
+    o = quant16<QK>(f, s, y, ok, dynamic);
+    reinterpret_cast<uint4*>(out_buf[ob])[threadIdx.x] = o;
     fence_proxy_async_shared();
     __syncthreads();
     if (threadIdx.x == 0) {
-      bulk_store(q + phys(c) * kQzChunk, smem_addr(out_buf[b]), static_cast<uint32_t>(chunk_elems(c)));
+      bulk_store(q + ring.phys(c) * kQzChunk, smem_addr(out_buf[ob]), ring.elems(c));
       bulk_commit();
     }
   }
   if (threadIdx.x == 0) {
-    if (failed) {
-      // let this CTA's copies in flight land (bounded) before it exits
-      mbar_wait(smem_addr(&bar[i & 1]), (i >> 1) & 1);
-      if (next_issued) mbar_wait(smem_addr(&bar[(i & 1) ^ 1]), ((i + 1) >> 1) & 1);
-    }
+    if (failed) ring.drain(i, bar);
     bulk_wait_all();
   }
 }
@@ -715,6 +706,9 @@ __global__ void __launch_bounds__(kRowThreads)
 
 // ---------------------------------------------------------------- launch helpers
 
+// Shared memory of an SM (sm_100 family).
+constexpr long long kSmSmem = 228 * 1024;
+
 template <int XK, int QK>
 cudaError_t launch_rows(const QuantArgs& a, cudaStream_t st) {
   const uint16_t* x = static_cast<const uint16_t*>(a.x);
@@ -757,16 +751,22 @@ cudaError_t launch_quant_t(const QuantArgs& a, int num_sms, cudaStream_t st) {
   const bool contiguous = (a.ld_x == a.cols && a.ld_q == a.cols) || a.rows == 1;
   const dim3 b256(256);
   if (a.per_row) return launch_rows<XK, QK>(a, st);
-  auto bulk_grid = [&](long long n) {
+  // CTAs per SM: as many as the pass's chunk ring in shared memory allows
+  // (<= 8: 2048 threads), all resident at once
+  auto bulk_grid = [&](long long n, long long ring_bytes) {
     const long long chunks = (n + kQzChunk - 1) / kQzChunk;
-    const long long cap = static_cast<long long>(num_sms) * 8;
+    long long per_sm = kSmSmem / (ring_bytes + 1024);
+    per_sm = per_sm < 1 ? 1 : (per_sm > 8 ? 8 : per_sm);
+    const long long cap = static_cast<long long>(num_sms) * per_sm;
     return dim3(static_cast<unsigned>(chunks < cap ? chunks : cap));
   };
+  const long long abs_ring = static_cast<long long>(kQzAbsStages) * kQzChunk * 2;
+  const long long cvt_ring = static_cast<long long>(kQzCvtStages) * kQzChunk * 2 + 2 * kQzChunk;
   if (!a.dynamic) {
     if (contiguous && a.vec) {
       const long long n = a.rows * a.cols;
       if (n % 16 == 0)
-        return launch_pdl(quant_bulk_kernel<XK, QK>, bulk_grid(n), b256, st, x, n, q, a.scale,
+        return launch_pdl(quant_bulk_kernel<XK, QK>, bulk_grid(n, cvt_ring), b256, st, x, n, q, a.scale,
                           static_cast<const unsigned*>(nullptr), 0);
       return launch_pdl(quant_flat_kernel<XK, QK>, dim3(flat_blocks(n / 16, num_sms)), b256, st, x, n, q, a.scale,
                         static_cast<const unsigned*>(nullptr), 0);
@@ -778,9 +778,9 @@ cudaError_t launch_quant_t(const QuantArgs& a, int num_sms, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (contiguous && a.vec && (a.rows * a.cols) % 16 == 0) {
     const long long n = a.rows * a.cols;
-    e = launch_pdl(absmax_bulk_kernel<XK>, bulk_grid(n), b256, st, x, n, a.amax_word);
+    e = launch_pdl(absmax_bulk_kernel<XK>, bulk_grid(n, abs_ring), b256, st, x, n, a.amax_word);
     if (e != cudaSuccess) return e;
-    return launch_pdl(quant_bulk_kernel<XK, QK>, bulk_grid(n), b256, st, x, n, q, a.scale,
+    return launch_pdl(quant_bulk_kernel<XK, QK>, bulk_grid(n, cvt_ring), b256, st, x, n, q, a.scale,
                       static_cast<const unsigned*>(a.amax_word), 1);
   }
   if (contiguous && a.vec) {

@@ -43,6 +43,20 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return out;
 }
 
+// Four fp32 -> four e4m3 codes in one word (low byte = first).  The
+// satfinite conversion never gives 0x7F / 0xFF for a number (its largest
+// magnitude is 0x7E), so the NaN codes are exactly the bytes whose low seven
+// bits are all ones; their sign bit is cleared once for the whole word
+// (0x7F + 1 carries into the byte's top bit and no further).
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  const uint32_t w = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  const uint32_t nan_top = ((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
+  return w & ~nan_top;
+}
+
 __device__ __forceinline__ uint32_t int8x1(float a) {
   int i;
   asm("cvt.rni.s32.f32 %0, %1;" : "=r"(i) : "f"(a));  // RNE; NaN -> 0; saturates to int32
@@ -52,7 +66,7 @@ __device__ __forceinline__ uint32_t int8x1(float a) {
 
 template <int QK>
 __device__ __forceinline__ uint32_t enc4(float a, float b, float c, float d) {
-  if (QK == 0) return e4m3x2(a, b) | (e4m3x2(c, d) << 16);
+  if (QK == 0) return e4m3x4(a, b, c, d);
   return int8x1(a) | (int8x1(b) << 8) | (int8x1(c) << 16) | (int8x1(d) << 24);
 }
 
@@ -65,16 +79,21 @@ __device__ __forceinline__ uint8_t enc1(float a) {
 // Correctly rounded x / s without a per-element division.
 //
 // With y = RN(1/s) (one IEEE division per thread), q0 = RN(x*y) lies within
-// one ulp of x/s, so the remainder x - s*q0 is exact in one FMA and
-// RN(q0 + remainder*y) is the correctly rounded quotient RN(x/s)
+// one ulp of x/s, so the (negated) remainder q0*s - x is exact in one FMA
+// and RN(q0 - (q0*s - x)*y) is the correctly rounded quotient RN(x/s)
 // (Markstein's correction step for IEEE division with a correctly rounded
-// reciprocal).  Preconditions: s and y are normal finite floats (checked per
-// thread; otherwise the plain IEEE division is used) and no intermediate
-// overflows -- when x*y overflows, q0 = +-inf already gives the code of the
-// exact quotient (saturation), and the NaN the correction step would make is
-// replaced by q0.  A zero remainder means q0 is exact; it is returned as is
-// (q0 + 0 would turn -0 into +0).  Quotients in the fp32 subnormal range all
-// encode to a signed zero, whatever their last bits.
+// reciprocal).  Taking the remainder negated also gets the sign of a zero
+// quotient right: for x = -0 both addends of the correction are -0.
+// Preconditions: s and y are normal finite floats (checked per thread;
+// otherwise the plain IEEE division is used) and no intermediate overflows.
+// kBounded: the quotient is known to stay near the code range (dynamic
+// scales: s is absmax / 448 or absmax / 127, so |x / s| cannot exceed the
+// largest code by more than a rounding); otherwise quotients beyond
+// kSatQuot, far past the largest code, are taken as q0 uncorrected -- they
+// saturate whatever their last bits, and this covers q0 = +-inf (x*y
+// overflowed, or x is infinite), where the correction would make a NaN.
+// A NaN x gives a NaN quotient either way.  Quotients in the fp32 subnormal
+// range all encode to a signed zero, whatever their last bits.
 __device__ __forceinline__ bool recip_ok(float s, float* y) {
   const float r = __fdiv_rn(1.0f, s);
   *y = r;
@@ -82,14 +101,48 @@ __device__ __forceinline__ bool recip_ok(float s, float* y) {
   return es != 0u && es != 0xFFu && er != 0u && er != 0xFFu;
 }
 
+constexpr float kSatQuot = 1024.f;
+
+template <bool kBounded>
 __device__ __forceinline__ float div_by(float x, float s, float y, bool ok) {
   if (!ok) return __fdiv_rn(x, s);
   const float q0 = __fmul_rn(x, y);
-  const float rem = __fmaf_rn(-q0, s, x);
-  const float q1 = __fmaf_rn(rem, y, q0);
-  // rem == 0: q0 is the exact quotient (and keeps the sign of a zero, which
-  // q0 + 0 would lose for x = -0)
-  return (rem == 0.0f || q1 != q1) ? q0 : q1;
+  const float nrem = __fmaf_rn(q0, s, -x);
+  const float q1 = __fmaf_rn(-nrem, y, q0);
+  if (kBounded) return q1;
+  return fabsf(q0) < kSatQuot ? q1 : q0;
+}
+
+// Codes of 4 / 8 / 16 consecutive values and of one value; `bounded` picks
+// the division without the saturation guard (dynamic scales).
+template <int QK, bool kB>
+__device__ __forceinline__ uint32_t quant4(const float* f, float s, float y, bool ok) {
+  return enc4<QK>(div_by<kB>(f[0], s, y, ok), div_by<kB>(f[1], s, y, ok), div_by<kB>(f[2], s, y, ok),
+                  div_by<kB>(f[3], s, y, ok));
+}
+
+template <int QK>
+__device__ __forceinline__ uint2 quant8(const float* f, float s, float y, bool ok, bool bounded) {
+  uint2 o;
+  if (bounded) {
+    o.x = quant4<QK, true>(f, s, y, ok);
+    o.y = quant4<QK, true>(f + 4, s, y, ok);
+  } else {
+    o.x = quant4<QK, false>(f, s, y, ok);
+    o.y = quant4<QK, false>(f + 4, s, y, ok);
+  }
+  return o;
+}
+
+template <int QK>
+__device__ __forceinline__ uint4 quant16(const float* f, float s, float y, bool ok, bool bounded) {
+  const uint2 a = quant8<QK>(f, s, y, ok, bounded), b = quant8<QK>(f + 8, s, y, ok, bounded);
+  return make_uint4(a.x, a.y, b.x, b.y);
+}
+
+template <int QK>
+__device__ __forceinline__ uint8_t quant1(float x, float s, float y, bool ok, bool bounded) {
+  return enc1<QK>(bounded ? div_by<true>(x, s, y, ok) : div_by<false>(x, s, y, ok));
 }
 
 template <int QK>

@@ -227,3 +227,44 @@ def test_inputs_at_decision_points(qd, dtype):
         g1, _ = gpu_quant(xi.cuda(), qd, per_token=False, dynamic=False, scale=[scales[i]])
         o1, _ = oracle_quant(xi, qd, per_token=False, scale=np.array([scales[i]], np.float32))
         assert np.array_equal(g1, o1)
+
+
+def _patterns_up_to(dtype, amax):
+    """Every 16-bit pattern whose magnitude is <= amax (NaNs included: the
+    absmax ignores them), padded with zeros to 65536, plus amax itself."""
+    allp = all_patterns(dtype).reshape(-1)
+    f = allp.float()
+    keep = (f.abs() <= amax) | torch.isnan(f)
+    row = torch.zeros(65536, dtype=dtype)
+    sel = allp[keep]
+    row[:sel.numel()] = sel
+    row[-1] = torch.tensor(amax, dtype=torch.float32).to(dtype)
+    return row
+
+
+DYN_AMAX = {torch.bfloat16: [1.0, 0.37, 448.0, 2.5e-3, 7.1, 1.0e-30, 3.0e38, 127.0, 65504.0, 1.5e-38],
+            torch.float16: [1.0, 0.37, 448.0, 2.5e-3, 7.1, 65504.0, 127.0, 6.1e-5, 3.0e-7]}
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("qd", QDS)
+def test_dynamic_rows_of_every_pattern_below_their_absmax(dtype, qd):
+    """Dynamic per-row scales with every representable input at or below each
+    row's absmax: the codes of the whole sweep bit-exact against the oracle
+    (the quotient of a dynamic scale never leaves the code range)."""
+    x = torch.stack([_patterns_up_to(dtype, a) for a in DYN_AMAX[dtype]])
+    g, gs = gpu_quant(x.cuda(), qd, per_token=True, dynamic=True)
+    o, os_ = oracle_quant(x, qd, per_token=True)
+    assert np.array_equal(gs, os_)
+    assert np.array_equal(g, o)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("qd", QDS)
+@pytest.mark.parametrize("amax", [0.37, 448.0, 65504.0])
+def test_dynamic_tensor_of_every_pattern_below_its_absmax(dtype, qd, amax):
+    x = _patterns_up_to(dtype, amax).reshape(256, 256)
+    g, gs = gpu_quant(x.cuda(), qd, per_token=False, dynamic=True)
+    o, os_ = oracle_quant(x, qd, per_token=False)
+    assert gs[0] == os_[0]
+    assert np.array_equal(g, o)
