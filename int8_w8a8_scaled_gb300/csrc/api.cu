@@ -328,6 +328,20 @@ w8a8_status validate_mm(const void* a_q, long long lda, const void* b_q, long lo
   return W8A8_OK;
 }
 
+// Whether a cluster split keeps its partial tiles in the CTAs' shared memory
+// and sums them through distributed shared memory: a 128 x block_n fp32 tile
+// (rows padded by 16 bytes) must fit the stage ring, which is idle once the
+// CTA's single unit is accumulated.  Only with tokens on the 128-row side:
+// there a lane drains whole tile rows and the final sum walks along rows
+// (measured at M = 256: the down projection 28.0 -> 23.6 us, O 14.8 -> 13.5
+// us); the swap-AB decode tiles, whose final sum walks down the rows, were
+// slower that way (M = 64 QKV 10.8 -> 13.9 us) and keep the L2 reduction.
+bool dsmem_reduce_fits(const Plan& plan, int block_n, int stages) {
+  if (!plan.cluster || plan.splits < 2 || plan.cfg.swap_ab) return false;
+  const long long ring = static_cast<long long>(gemm_smem_bytes(block_n, stages)) - gemm_smem_bytes(block_n, 0);
+  return ring >= 128LL * (block_n + 4) * 4;
+}
+
 // Activations the matmul quantises itself (dynamic per token, e4m3).
 struct FusedAct {
   const void* x;
@@ -469,8 +483,10 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
         stages = std::min(stages, fit);
       }
     }
+    prm.dsmem_reduce = dsmem_reduce_fits(plan, cfg.block_n, stages);
     e = launch_fused_quant_gemm(tp, prm, cfg.block_n, out_kind, stages, stream);
   } else {
+    prm.dsmem_reduce = dsmem_reduce_fits(plan, cfg.block_n, plan.stages);
     e = i8 ? launch_int8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream)
            : launch_fp8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream);
   }
@@ -778,7 +794,8 @@ w8a8_status w8a8_fp8_kv_decode_attention(const void* q, int q_dtype, int64_t bat
   if (head_dim != 128) return fail(W8A8_ERR_INVALID_ARG, "head_dim must be 128");
   if (batch < 1 || num_q_heads < 1 || num_kv_heads < 1 || max_seq_len < 1)
     return fail(W8A8_ERR_INVALID_ARG, "batch, head counts and max_seq_len must be >= 1");
-  if (batch > 65535 || num_kv_heads > 65535 || max_seq_len > (1LL << 30) || num_q_heads > 65535)
+  if (batch > 65535 || num_kv_heads > 65535 || max_seq_len > (1LL << 30) || num_q_heads > 65535 ||
+      ((max_seq_len + 63) / 64) * num_kv_heads >= (1LL << 31))
     return fail(W8A8_ERR_INVALID_ARG, "sizes exceed the launch grid");
   if (num_q_heads % num_kv_heads != 0) return fail(W8A8_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
   const long long G = num_q_heads / num_kv_heads;
@@ -802,6 +819,7 @@ w8a8_status w8a8_fp8_kv_decode_attention(const void* q, int q_dtype, int64_t bat
   w8a8::AttnParams p{};
   p.q = q;
   p.q_fp16 = q_dtype == W8A8_FP16;
+  p.q_vec = aligned(q, 8) ? 1 : 0;
   p.k_cache = k_cache;
   p.v_cache = v_cache;
   p.block_table = block_table;
@@ -820,7 +838,18 @@ w8a8_status w8a8_fp8_kv_decode_attention(const void* q, int q_dtype, int64_t bat
   p.num_kv_heads = static_cast<int>(num_kv_heads);
   p.max_seq_len = static_cast<int>(max_seq_len);
   p.chunk = attn_chunk_for(batch, num_kv_heads, max_seq_len, dev.sms);
-  cudaError_t e = w8a8::launch_fp8kv_attention(p, reinterpret_cast<cudaStream_t>(stream));
+  // bulk-tensor copies of the 16-token blocks where the cache rows of a block
+  // are consecutive: a contiguous cache, or a paged one with 16 | block_size
+  CUtensorMap mk, mv;
+  const long long rows = block_table ? num_blocks * block_size : batch * max_seq_len;
+  bool tma = (!block_table || block_size % 16 == 0) && rows < (1LL << 31);
+  if (tma) {
+    tma = make_operand_map(&mk, k_cache, false, rows, num_kv_heads * 128, num_kv_heads * 128, 16) == W8A8_OK &&
+          make_operand_map(&mv, v_cache, false, rows, num_kv_heads * 128, num_kv_heads * 128, 16) == W8A8_OK;
+    if (!tma) t_last_error.clear();  // the per-lane path needs no tensor map
+  }
+  cudaError_t e = w8a8::launch_fp8kv_attention(p, tma ? &mk : nullptr, tma ? &mv : nullptr,
+                                               reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fp8 KV attention launch");
   return ok();
 }
@@ -839,6 +868,9 @@ w8a8_status w8a8_device_status(int* flags) {
   if (e != cudaSuccess) return cuda_fail(e, "device status read");
   int qf = 0;
   e = read_clear_quant_status(&qf);
+  if (e != cudaSuccess) return cuda_fail(e, "device status read");
+  *flags |= qf;
+  e = read_clear_attn_status(&qf);
   if (e != cudaSuccess) return cuda_fail(e, "device status read");
   *flags |= qf;
   return ok();

@@ -43,11 +43,22 @@
 //    (row g + 8): byte permutes pair two tokens' codes of one dim.
 //  - P^T: the scores' accumulator layout transposed in registers
 //    (movmatrix), which is exactly the B fragment of the output MMA.
+//
+// Work split: a CTA of 4 warps takes one (chunk, KV head, sequence); each
+// warp takes a quarter of the chunk's tokens, 16 at a time, and its lanes
+// stream their own 16-byte pieces of the next blocks into a per-warp
+// shared-memory ring with cp.async while the current block is used; the 4
+// warps' (m, l, o) are combined in shared memory at the end.  The KV heads of
+// a chunk are consecutive CTAs, so they read the same cache rows (each its
+// 128-byte slice) at about the same time.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <cstring>
+
 #include "internal.h"
+#include "sm103_ptx.cuh"
 
 namespace w8a8 {
 
@@ -56,8 +67,10 @@ namespace {
 constexpr int kHeadDim = 128;
 constexpr int kWarps = 4;                         // warps per CTA; each takes chunk / 4 tokens
 constexpr int kAttnThreads = 32 * kWarps;
+// Resident CTAs per SM the register budget is fitted to (4: <= 128
+// registers, 16 warps per SM; measured best with a 2-block ring).
 #ifndef W8A8_ATTN_MIN_CTAS
-#define W8A8_ATTN_MIN_CTAS 3
+#define W8A8_ATTN_MIN_CTAS 4
 #endif
 #ifndef W8A8_ATTN_MAX_CHUNK
 #define W8A8_ATTN_MAX_CHUNK 512
@@ -113,12 +126,8 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   return y;
 }
 
-__device__ __forceinline__ uint4 ld_stream16(const uint8_t* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+__device__ __forceinline__ uint32_t smem_addr_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
@@ -141,29 +150,120 @@ struct KvBlock {
   bool kval[2];
 };
 
-// Loads of the block at chunk position ib (tokens past `end` or in padding
-// blocks are not loaded: zeros, marked invalid).
-__device__ __forceinline__ void load_block(const AttnParams& p, int b, int t0, int ib, int end, int g, int t,
-                                           const uint8_t* kbase, const uint8_t* vbase, long long row_bytes,
-                                           KvBlock& x) {
+// Ring of blocks in flight per warp (shared memory, filled by cp.async).  A
+// lane copies its own eight 16-byte chunks of a block and later reads them
+// back itself, so the ring needs no synchronisation between lanes; chunk j
+// of lane L sits at (j * 32 + L) * 16 within the block's 4 KB, so a warp's
+// 16-byte reads of one chunk index touch 32 consecutive 16-byte words.
+#ifndef W8A8_ATTN_RING
+#define W8A8_ATTN_RING 2
+#endif
+constexpr int kRing = W8A8_ATTN_RING;
+static_assert(kRing >= 2 && kRing <= 8, "ring depth");
+constexpr int kBlockBytes = 32 * 8 * 16;  // one 16-token block of K and V codes
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  // invalid: no read, the 16 bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Requests the block at chunk position ib into ring slot `slot` (tokens past
+// `end` or in padding blocks are not read: zeros) and returns the validity
+// bits of K rows g, g + 8.
+__device__ __forceinline__ uint32_t issue_block(const AttnParams& p, int b, int t0, int ib, int end, int g, int t,
+                                                int lane, const uint8_t* kbase, const uint8_t* vbase,
+                                                long long row_bytes, uint32_t slot_addr) {
+  uint32_t kv = 0u;
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const int i = ib + g + 8 * r;
     const long long slot = i < end ? slot_of(p, b, t0 + i) : -1;
-    x.kval[r] = slot >= 0;
-    if (slot >= 0) {
-      const uint8_t* row = kbase + slot * row_bytes;
-      x.k[r][0] = ld_stream16(row + 16 * t);
-      x.k[r][1] = ld_stream16(row + 64 + 16 * t);
-    } else {
-      x.k[r][0] = x.k[r][1] = make_uint4(0u, 0u, 0u, 0u);
-    }
+    const bool ok = slot >= 0;
+    kv |= ok ? (1u << r) : 0u;
+    const uint8_t* row = kbase + (ok ? slot : 0) * row_bytes;
+    cp_async16(slot_addr + ((2 * r + 0) * 32 + lane) * 16, row + 16 * t, ok);
+    cp_async16(slot_addr + ((2 * r + 1) * 32 + lane) * 16, row + 64 + 16 * t, ok);
   }
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int i = ib + 2 * t + (r & 1) + 8 * (r >> 1);
     const long long slot = i < end ? slot_of(p, b, t0 + i) : -1;
-    x.v[r] = slot >= 0 ? ld_stream16(vbase + slot * row_bytes + 16 * g) : make_uint4(0u, 0u, 0u, 0u);
+    const bool ok = slot >= 0;
+    cp_async16(slot_addr + ((4 + r) * 32 + lane) * 16, vbase + (ok ? slot : 0) * row_bytes + 16 * g, ok);
+  }
+  return kv;
+}
+
+// The lane's chunks of a block, back from its ring slot.
+__device__ __forceinline__ void read_block(const uint8_t* slot_ptr, int lane, uint32_t kv, KvBlock& x) {
+  const uint4* c = reinterpret_cast<const uint4*>(slot_ptr) + lane;
+  x.k[0][0] = c[0 * 32];
+  x.k[0][1] = c[1 * 32];
+  x.k[1][0] = c[2 * 32];
+  x.k[1][1] = c[3 * 32];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) x.v[r] = c[(4 + r) * 32];
+  x.kval[0] = (kv & 1u) != 0u;
+  x.kval[1] = (kv & 2u) != 0u;
+}
+
+// ---- the bulk-tensor path: per 16-token block two TMA copies (the K and the
+// V rows of this KV head, 16 x 128 bytes each, 128-byte swizzled) into the
+// warp's ring slot, one mbarrier per slot.  Per-lane 16-byte copies keep at
+// most ~64 KB per SM in flight, whatever the ring depth; bulk copies do not
+// have that limit.  Chunk c of tile row r sits at r * 128 + (c ^ (r & 7)) * 16,
+// so a quarter-warp's fragment reads hit different banks.
+
+// Cache row of the 16-token block starting at token tb of sequence b (16 |
+// block_size with a table), or -1 for a padding block.
+__device__ __forceinline__ long long block_row(const AttnParams& p, int b, int tb) {
+  if (!p.block_table) return static_cast<long long>(b) * p.max_seq_len + tb;
+  const int blk = __ldg(p.block_table + static_cast<size_t>(b) * p.max_blocks + tb / p.block_size);
+  if (blk < 0 || blk >= p.num_blocks) return -1;
+  return static_cast<long long>(blk) * p.block_size + tb % p.block_size;
+}
+
+// lane 0: the two copies of the block at chunk position ib into slot `dst`
+__device__ __forceinline__ void tma_issue_block(const AttnParams& p, const CUtensorMap* mk, const CUtensorMap* mv,
+                                                int b, int t0, int ib, int kvh, uint32_t dst, uint32_t bar) {
+  const long long row = block_row(p, b, t0 + ib);
+  if (row < 0) {
+    mbar_arrive(bar);  // a padding block: nothing to copy
+    return;
+  }
+  mbar_arrive_expect_tx(bar, kBlockBytes);
+  tma_load_2d(dst, mk, bar, kvh * kHeadDim, static_cast<int32_t>(row));
+  tma_load_2d(dst + kBlockBytes / 2, mv, bar, kvh * kHeadDim, static_cast<int32_t>(row));
+}
+
+__device__ __forceinline__ uint32_t swz(int r, int c) { return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+// The lane's fragments of a block from its (swizzled) slot; tokens past
+// `end` or in a padding block are invalid: their K rows masked by kval,
+// their V codes zeroed (whatever the cache holds there, their weight is 0).
+__device__ __forceinline__ void read_block_tma(const uint8_t* slot, const AttnParams& p, int b, int t0, int ib,
+                                               int end, int g, int t, KvBlock& x) {
+  const bool blk_ok = block_row(p, b, t0 + ib) >= 0;
+  const uint8_t* kt = slot;
+  const uint8_t* vt = slot + kBlockBytes / 2;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int row = g + 8 * r;
+    x.k[r][0] = *reinterpret_cast<const uint4*>(kt + swz(row, t));
+    x.k[r][1] = *reinterpret_cast<const uint4*>(kt + swz(row, 4 + t));
+    x.kval[r] = blk_ok && ib + row < end;
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int row = 2 * t + (r & 1) + 8 * (r >> 1);
+    const uint4 v = *reinterpret_cast<const uint4*>(vt + swz(row, g));
+    x.v[r] = (blk_ok && ib + row < end) ? v : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -178,14 +278,21 @@ struct SoftmaxState {
 template <bool kPack>
 __device__ __forceinline__ void attend_block(const KvBlock& x, const uint32_t (&qf)[8][2], float cs, bool lo_lane,
                                              SoftmaxState& st) {
-  // scores S^T[token g / g+8][column 2t / 2t+1]
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  // scores S^T[token g / g+8][column 2t / 2t+1]: four independent
+  // accumulator chains of two k-blocks each (a single chain of eight MMAs
+  // would make the block wait for eight MMA latencies), summed after
+  float sp[4][4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) sp[c][0] = sp[c][1] = sp[c][2] = sp[c][3] = 0.f;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const uint32_t w0r = word_of(x.k[0][j >> 2], j & 3);
     const uint32_t w1r = word_of(x.k[1][j >> 2], j & 3);
-    mma16816(s, cvt2(w0r), cvt2(w1r), cvt2(w0r >> 16), cvt2(w1r >> 16), qf[j][0], qf[j][1]);
+    mma16816(sp[j & 3], cvt2(w0r), cvt2(w1r), cvt2(w0r >> 16), cvt2(w1r >> 16), qf[j][0], qf[j][1]);
   }
+  float s[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) s[k] = (sp[0][k] + sp[1][k]) + (sp[2][k] + sp[3][k]);
   // lanes t >= 2 mirror their partner's columns (heads); invalid tokens -inf
   float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -243,13 +350,17 @@ __device__ __forceinline__ void attend_block(const KvBlock& x, const uint32_t (&
   }
 }
 
-template <int G>
-__global__ void __launch_bounds__(kAttnThreads, W8A8_ATTN_MIN_CTAS) fp8kv_attn_chunk_kernel(const AttnParams p) {
+template <int G, bool kTma>
+__global__ void __launch_bounds__(kAttnThreads, W8A8_ATTN_MIN_CTAS)
+    fp8kv_attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap_k,
+                            const __grid_constant__ CUtensorMap tmap_v) {
   // G <= 4: the lo halves of the weights ride in the padding columns 4..7
   constexpr bool kPack = G <= 4;
-  const int b = blockIdx.z;
-  const int kvh = blockIdx.y;
-  const int ch = blockIdx.x;
+  // the KV heads of a chunk are consecutive CTAs: they run side by side and
+  // read the same cache rows (each its 128-byte slice) at about the same time
+  const int b = blockIdx.y;
+  const int kvh = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.num_kv_heads));
+  const int ch = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.num_kv_heads));
   const int len = seq_len_of(p, b);
   const int t0 = ch * p.chunk;
   if (t0 >= len) return;  // uniform: the combine reads only chunks that hold tokens
@@ -261,25 +372,76 @@ __global__ void __launch_bounds__(kAttnThreads, W8A8_ATTN_MIN_CTAS) fp8kv_attn_c
   __shared__ float s_qmax[kWarps];
   __shared__ float s_m[kWarps][8], s_l[kWarps][8];
   __shared__ float s_o[kWarps][G][kHeadDim];
+  extern __shared__ __align__(128) uint8_t ring_raw[];  // [kWarps][kRing][kBlockBytes], 1024-byte aligned
+  __shared__ uint64_t s_bar[kWarps][kRing];             // bulk-tensor path: one per ring slot
+  uint8_t* ring_smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ring_raw) + 1023) &
+                                                  ~static_cast<uintptr_t>(1023));
 
-  // this warp's tokens of the chunk; the first block's codes are requested
-  // before the query is prepared
+  // this warp's tokens of the chunk, in blocks of 16; the first kRing - 1
+  // blocks are requested before the query is prepared
   const uint8_t* kbase = static_cast<const uint8_t*>(p.k_cache) + kvh * kHeadDim;
   const uint8_t* vbase = static_cast<const uint8_t*>(p.v_cache) + kvh * kHeadDim;
   const long long row_bytes = static_cast<long long>(p.num_kv_heads) * kHeadDim;
   const int per_warp = p.chunk / kWarps;
   const int w0 = warp * per_warp;
   const int w1 = min(n, w0 + per_warp);
-  KvBlock xa, xb;
-  load_block(p, b, t0, w0, w1, g, t, kbase, vbase, row_bytes, xa);
+  const int nblk = w1 > w0 ? (w1 - w0 + 15) / 16 : 0;
+  uint8_t* ring = ring_smem + static_cast<size_t>(warp) * kRing * kBlockBytes;
+  const uint32_t ring_addr = smem_addr_u32(ring);
+  uint32_t kvbits = 0u;  // K-row validity, two bits per ring slot (per-lane copies)
+  if (kTma) {
+    if (lane == 0) {
+      for (int j = 0; j < kRing; ++j) mbar_init(smem_addr(&s_bar[warp][j]), 1);
+      fence_barrier_init();
+      prefetch_tensormap(&tmap_k);
+      prefetch_tensormap(&tmap_v);
+      for (int j = 0; j < kRing - 1 && j < nblk; ++j)
+        tma_issue_block(p, &tmap_k, &tmap_v, b, t0, w0 + 16 * j, kvh, ring_addr + j * kBlockBytes,
+                        smem_addr(&s_bar[warp][j]));
+    }
+    __syncwarp();
+  } else {
+#pragma unroll
+    for (int j = 0; j < kRing - 1; ++j) {
+      if (j < nblk)
+        kvbits |= issue_block(p, b, t0, w0 + 16 * j, w1, g, t, lane, kbase, vbase, row_bytes,
+                              ring_addr + j * kBlockBytes) << (2 * j);
+      cp_async_commit();  // one group per block, empty past the end
+    }
+  }
 
-  // ---- the query rows of the G heads, scaled by 2^e into [2^14, 2^15) and converted to f16
+  // ---- the query rows of the G heads, scaled by 2^e into [2^14, 2^15) and
+  // converted to f16: one pass of 8-byte loads (G * 128 values, 4 per thread
+  // and pass), the values kept in registers for the conversion
   const size_t q0 = (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G) * kHeadDim;
+  constexpr int kQPer = (G * kHeadDim) / (4 * kAttnThreads) > 0 ? (G * kHeadDim) / (4 * kAttnThreads) : 1;
+  float qv[kQPer][4];
   float qmax = 0.f;
-  for (int i = threadIdx.x; i < G * kHeadDim; i += kAttnThreads) qmax = fmaxf(qmax, fabsf(load_q(p.q, p.q_fp16, q0 + i)));
+#pragma unroll
+  for (int u = 0; u < kQPer; ++u) {
+    const int i = 4 * (threadIdx.x + u * kAttnThreads);
+    if (i < G * kHeadDim) {
+      if (p.q_vec) {  // q 8-byte aligned
+        const uint2 w = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.q) + q0 + i);
+        const uint16_t e4[4] = {static_cast<uint16_t>(w.x), static_cast<uint16_t>(w.x >> 16),
+                                static_cast<uint16_t>(w.y), static_cast<uint16_t>(w.y >> 16)};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          qv[u][c] = p.q_fp16 ? __half2float(__ushort_as_half(e4[c])) : __bfloat162float(__ushort_as_bfloat16(e4[c]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) qv[u][c] = load_q(p.q, p.q_fp16, q0 + i + c);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) qmax = fmaxf(qmax, fabsf(qv[u][c]));
+    }
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
   if (lane == 0) s_qmax[warp] = qmax;
+  // padding heads' rows of the fragment are zero
+  for (int i = G * kHeadDim + threadIdx.x; i < 8 * kHeadDim; i += kAttnThreads)
+    qs[i / kHeadDim][i % kHeadDim] = __float2half_rn(0.f);
   __syncthreads();
   qmax = s_qmax[0];
 #pragma unroll
@@ -290,9 +452,13 @@ __global__ void __launch_bounds__(kAttnThreads, W8A8_ATTN_MIN_CTAS) fp8kv_attn_c
     frexpf(qmax, &ex);  // qmax in [2^(ex-1), 2^ex)
     e = min(100, max(-100, 15 - ex));
   }
-  for (int i = threadIdx.x; i < 8 * kHeadDim; i += kAttnThreads) {
-    const int h = i / kHeadDim;
-    qs[h][i % kHeadDim] = h < G ? __float2half_rn(ldexpf(load_q(p.q, p.q_fp16, q0 + i), e)) : __float2half_rn(0.f);
+#pragma unroll
+  for (int u = 0; u < kQPer; ++u) {
+    const int i = 4 * (threadIdx.x + u * kAttnThreads);
+    if (i < G * kHeadDim) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) qs[(i + c) / kHeadDim][(i + c) % kHeadDim] = __float2half_rn(ldexpf(qv[u][c], e));
+    }
   }
   __syncthreads();
   // B fragment of k-block j: dims L_t[4j .. 4j+3] of head g, L_t = [16t, 16t+16) ++ [64+16t, 64+16t+16)
@@ -315,14 +481,45 @@ __global__ void __launch_bounds__(kAttnThreads, W8A8_ATTN_MIN_CTAS) fp8kv_attn_c
 #pragma unroll
   for (int i = 0; i < 8; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
 
-  // blocks of 16 tokens, the next block's codes in flight while one is used
-  for (int ib = w0; ib < w1; ib += 32) {
-    load_block(p, b, t0, ib + 16, w1, g, t, kbase, vbase, row_bytes, xb);
-    attend_block<kPack>(xa, qf, cs, lo_lane, st);
-    if (ib + 16 >= w1) break;
-    load_block(p, b, t0, ib + 32, w1, g, t, kbase, vbase, row_bytes, xa);
-    attend_block<kPack>(xb, qf, cs, lo_lane, st);
+  // blocks of 16 tokens, kRing - 1 blocks in flight ahead of the one used
+  bool ok = true;
+  int issued = kTma ? min(kRing - 1, nblk) : 0, consumed = 0;
+  for (int i = 0; i < nblk; ++i) {
+    const int jn = i + kRing - 1;  // its slot held block i - 1, already read back
+    const int sn = jn % kRing;
+    const int si = i % kRing;
+    KvBlock x;
+    if (kTma) {
+      __syncwarp();  // every lane is done with block i - 1's slot
+      if (lane == 0 && jn < nblk) {
+        fence_proxy_async_shared();  // its reads before the copy that overwrites it
+        tma_issue_block(p, &tmap_k, &tmap_v, b, t0, w0 + 16 * jn, kvh, ring_addr + sn * kBlockBytes,
+                        smem_addr(&s_bar[warp][sn]));
+      }
+      if (jn < nblk) ++issued;
+      if (!mbar_wait(smem_addr(&s_bar[warp][si]), (i / kRing) & 1)) {
+        ok = false;
+        break;
+      }
+      consumed = i + 1;
+      read_block_tma(ring + si * kBlockBytes, p, b, t0, w0 + 16 * i, w1, g, t, x);
+    } else {
+      kvbits &= ~(3u << (2 * sn));
+      if (jn < nblk)
+        kvbits |= issue_block(p, b, t0, w0 + 16 * jn, w1, g, t, lane, kbase, vbase, row_bytes,
+                              ring_addr + sn * kBlockBytes) << (2 * sn);
+      cp_async_commit();
+      cp_async_wait<kRing - 1>();  // block i's group has landed
+      read_block(ring + si * kBlockBytes, lane, (kvbits >> (2 * si)) & 3u, x);
+    }
+    attend_block<kPack>(x, qf, cs, lo_lane, st);
   }
+  if (kTma && !ok && lane == 0) {
+    // a wait gave up (flagged in the device status): let the copies still in
+    // flight land, bounded, before the CTA's shared memory is released
+    for (int j = consumed; j < issued; ++j) mbar_wait(smem_addr(&s_bar[warp][j % kRing]), (j / kRing) & 1);
+  }
+  if (!kTma) cp_async_wait<0>();
   float (&o)[8][4] = st.o;
   float (&m_run)[2] = st.m;
   float (&l_run)[2] = st.l;
@@ -412,11 +609,25 @@ __global__ void __launch_bounds__(kHeadDim) fp8kv_attn_combine_kernel(const Attn
     static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(y);
 }
 
-template <int G>
-cudaError_t launch_chunks(const AttnParams& p, cudaStream_t stream) {
-  const dim3 grid((p.max_seq_len + p.chunk - 1) / p.chunk, p.num_kv_heads, p.batch);
-  fp8kv_attn_chunk_kernel<G><<<grid, kAttnThreads, 0, stream>>>(p);
+template <int G, bool kTma>
+cudaError_t launch_chunks_t(const AttnParams& p, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t stream) {
+  const long long nch = (p.max_seq_len + p.chunk - 1) / p.chunk;
+  const dim3 grid(static_cast<unsigned>(nch * p.num_kv_heads), p.batch);
+  constexpr int smem = kWarps * kRing * kBlockBytes + 1024;  // + alignment slack
+  auto kern = fp8kv_attn_chunk_kernel<G, kTma>;
+  // the attribute is per function and device; setting it again is harmless
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kAttnThreads, smem, stream>>>(p, mk, mv);
   return cudaGetLastError();
+}
+
+template <int G>
+cudaError_t launch_chunks(const AttnParams& p, const CUtensorMap* mk, const CUtensorMap* mv, cudaStream_t stream) {
+  if (mk) return launch_chunks_t<G, true>(p, *mk, *mv, stream);
+  CUtensorMap none;
+  memset(&none, 0, sizeof(none));
+  return launch_chunks_t<G, false>(p, none, none, stream);
 }
 
 }  // namespace
@@ -424,14 +635,25 @@ cudaError_t launch_chunks(const AttnParams& p, cudaStream_t stream) {
 int attn_part_stride() { return kPartStride; }
 int attn_max_chunk() { return kMaxChunk; }
 
-cudaError_t launch_fp8kv_attention(const AttnParams& p, cudaStream_t stream) {
+cudaError_t read_clear_attn_status(int* flags) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int));
+  if (e != cudaSuccess) return e;
+  const int zero = 0;
+  e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+  *flags = v;
+  return e;
+}
+
+cudaError_t launch_fp8kv_attention(const AttnParams& p, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                                   cudaStream_t stream) {
   const int G = p.num_q_heads / p.num_kv_heads;
   cudaError_t e;
   switch (G) {
-    case 1: e = launch_chunks<1>(p, stream); break;
-    case 2: e = launch_chunks<2>(p, stream); break;
-    case 4: e = launch_chunks<4>(p, stream); break;
-    case 8: e = launch_chunks<8>(p, stream); break;
+    case 1: e = launch_chunks<1>(p, tmap_k, tmap_v, stream); break;
+    case 2: e = launch_chunks<2>(p, tmap_k, tmap_v, stream); break;
+    case 4: e = launch_chunks<4>(p, tmap_k, tmap_v, stream); break;
+    case 8: e = launch_chunks<8>(p, tmap_k, tmap_v, stream); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;

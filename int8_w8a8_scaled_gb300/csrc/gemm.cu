@@ -636,6 +636,88 @@ __device__ __forceinline__ void fq_fill_stage_rows(const MmParams& prm, int kb, 
   }
 }
 
+// Split-K partial tiles kept in shared memory (distributed-shared-memory
+// reduction): row-major in the idle stage ring, BN + 4 floats per row (the
+// pad spreads a warp's 16-byte stores of 32 consecutive rows over the banks).
+template <int BN>
+__device__ __forceinline__ void write_partial16_smem(uint32_t* tile, int row, int col0, const uint32_t (&v)[16]) {
+  uint4* dst = reinterpret_cast<uint4*>(tile + static_cast<size_t>(row) * (BN + 4) + col0);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) dst[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+}
+
+// Final sum of rows [r0, r0 + nrows) of a cluster-split tile from the S
+// partial tiles in the cluster's shared memory (slice s in the CTA of rank
+// s, at the same offset `tile_saddr`): B float4 vectors per pass, all B * S
+// loads requested before any is used, each vector summed in slice order
+// 0..S-1 from zero -- the order of the global reductions, so every form
+// gives the same bits.
+template <int S, int B, int BN, bool SWAP, bool INT8, typename OutT>
+__device__ __forceinline__ void reduce_rows_dsmem(const MmParams& prm, const Unit& un, uint32_t tile_saddr, int r0,
+                                                  int nrows, int qvalid, int et, const float* s_scale_p,
+                                                  const float* s_scale_q) {
+  const int vpr = (qvalid + 3) / 4;
+  const int nvec = nrows * vpr;
+  uint32_t peer[S];
+#pragma unroll
+  for (int s2 = 0; s2 < S; ++s2) peer[s2] = mapa_shared(tile_saddr, static_cast<uint32_t>(s2));
+  for (int v0 = et; v0 < nvec; v0 += B * kEpiThreads) {
+    uint4 x[B][S];
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int v = v0 + b * kEpiThreads;
+      int rr, c4;
+      reduce_pos<SWAP>(v < nvec ? v : v0, nrows, vpr, rr, c4);
+      const uint32_t off = static_cast<uint32_t>(((r0 + rr) * (BN + 4) + 4 * c4) * 4);
+#pragma unroll
+      for (int s2 = 0; s2 < S; ++s2) x[b][s2] = ld_dsmem_v4(peer[s2] + off);
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int v = v0 + b * kEpiThreads;
+      if (v >= nvec) break;
+      int rr, c4;
+      reduce_pos<SWAP>(v, nrows, vpr, rr, c4);
+      if (INT8) {
+        int acc[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int s2 = 0; s2 < S; ++s2) {
+          acc[0] += static_cast<int>(x[b][s2].x);
+          acc[1] += static_cast<int>(x[b][s2].y);
+          acc[2] += static_cast<int>(x[b][s2].z);
+          acc[3] += static_cast<int>(x[b][s2].w);
+        }
+        reduce_store<BN, SWAP, INT8, OutT>(prm, un, r0 + rr, c4, qvalid, acc, s_scale_p, s_scale_q);
+      } else {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s2 = 0; s2 < S; ++s2) {
+          acc[0] += __uint_as_float(x[b][s2].x);
+          acc[1] += __uint_as_float(x[b][s2].y);
+          acc[2] += __uint_as_float(x[b][s2].z);
+          acc[3] += __uint_as_float(x[b][s2].w);
+        }
+        reduce_store<BN, SWAP, INT8, OutT>(prm, un, r0 + rr, c4, qvalid, acc, s_scale_p, s_scale_q);
+      }
+    }
+  }
+}
+
+template <int BN, bool SWAP, bool INT8, typename OutT>
+__device__ __forceinline__ void reduce_rows_dsmem_any(const MmParams& prm, const Unit& un, uint32_t tile_saddr, int S,
+                                                      int r0, int nrows, int qvalid, int et, const float* s_scale_p,
+                                                      const float* s_scale_q) {
+  switch (S) {
+    case 2: reduce_rows_dsmem<2, 4, BN, SWAP, INT8, OutT>(prm, un, tile_saddr, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
+    case 3: reduce_rows_dsmem<3, 2, BN, SWAP, INT8, OutT>(prm, un, tile_saddr, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
+    case 4: reduce_rows_dsmem<4, 2, BN, SWAP, INT8, OutT>(prm, un, tile_saddr, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
+    case 5: reduce_rows_dsmem<5, 1, BN, SWAP, INT8, OutT>(prm, un, tile_saddr, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
+    case 6: reduce_rows_dsmem<6, 1, BN, SWAP, INT8, OutT>(prm, un, tile_saddr, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
+    case 7: reduce_rows_dsmem<7, 1, BN, SWAP, INT8, OutT>(prm, un, tile_saddr, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
+    default: reduce_rows_dsmem<8, 1, BN, SWAP, INT8, OutT>(prm, un, tile_saddr, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
+  }
+}
+
 // Narrow tiles run two CTAs per SM (the dispatch sizes their shared memory
 // for that); cap their registers so that two fit (<= 168 per thread).
 __host__ __device__ constexpr int min_ctas_for(int bn, bool) { return bn <= 64 ? 2 : 1; }
@@ -653,7 +735,7 @@ __device__ __forceinline__ void reduce_rows_any(const MmParams& prm, const Unit&
   // loads per pass: 16 (one CTA per SM) or 8 (two share the registers);
   // 32 measured slower (the decode M = 256 down projection's reduction took
   // 11 us instead of 8)
-  constexpr int kLoads = min_ctas_for(BN, INT8) == 2 ? 8 : 16;
+  constexpr int kLoads = 16;
   switch (S) {
     case 2: reduce_rows<2, kLoads / 2, BN, SWAP, INT8, OutT>(prm, un, tile0, slice_stride, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
     case 4: reduce_rows<4, kLoads / 4, BN, SWAP, INT8, OutT>(prm, un, tile0, slice_stride, r0, nrows, qvalid, et, s_scale_p, s_scale_q); break;
@@ -954,7 +1036,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
               if (!last) {
                 tmem_st16(tot_addr + g * 16, t[bb]);
               } else if (prm.splits > 1) {
-                write_partial16<SWAP>(part, row, g * 16, qvalid, t[bb]);
+                if (prm.dsmem_reduce)
+                  write_partial16_smem<BN>(reinterpret_cast<uint32_t*>(smem), row, g * 16, t[bb]);
+                else
+                  write_partial16<SWAP>(part, row, g * 16, qvalid, t[bb]);
               } else {
                 int v[16];
 #pragma unroll
@@ -970,7 +1055,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
             tmem_ld16(acc_addr + g * 16, r);
             tmem_ld_wait();
             if (prm.splits > 1) {
-              write_partial16<SWAP>(part, row, g * 16, qvalid, r);
+              if (prm.dsmem_reduce)
+                write_partial16_smem<BN>(reinterpret_cast<uint32_t*>(smem), row, g * 16, r);
+              else
+                write_partial16<SWAP>(part, row, g * 16, qvalid, r);
             } else {
               float v[16];
 #pragma unroll
@@ -1027,13 +1115,21 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
       const int r0 = (rank * kTileP) / S;
       const int r1 = ((rank + 1) * kTileP) / S;
       const int qvalid = min(BN, (SWAP ? prm.M : prm.N) - un.q0);
-      const size_t tile_elems = static_cast<size_t>(kTileP) * BN;
-      const uint32_t* tile0 = reinterpret_cast<const uint32_t*>(prm.partial) +
-                              static_cast<size_t>(un.tile_lin) * S * tile_elems;
-      reduce_rows_any<BN, SWAP, INT8, OutT>(prm, un, tile0, tile_elems, S, r0, r1 - r0, qvalid, et, s_scale_p,
-                                            s_scale_q);
+      if (prm.dsmem_reduce) {
+        reduce_rows_dsmem_any<BN, SWAP, INT8, OutT>(prm, un, smem_addr(smem), S, r0, r1 - r0, qvalid, et, s_scale_p,
+                                                    s_scale_q);
+      } else {
+        const size_t tile_elems = static_cast<size_t>(kTileP) * BN;
+        const uint32_t* tile0 = reinterpret_cast<const uint32_t*>(prm.partial) +
+                                static_cast<size_t>(un.tile_lin) * S * tile_elems;
+        reduce_rows_any<BN, SWAP, INT8, OutT>(prm, un, tile0, tile_elems, S, r0, r1 - r0, qvalid, et, s_scale_p,
+                                              s_scale_q);
+      }
     }
     if (threadIdx.x == 2 * 32) trace_stamp(prm, T_REDUCED);
+    // the peers read this CTA's partial tile from its shared memory: it
+    // stays allocated until every CTA of the cluster is done
+    if (prm.dsmem_reduce) cluster_sync();
   }
   if (threadIdx.x == 2 * 32) trace_stamp(prm, T_EPI_DONE);
   tc_fence_before();

@@ -22,6 +22,9 @@ struct MmParams {
   int cluster;           // 1: the splits of a tile form one thread-block cluster;
                          // after a cluster barrier each CTA sums 1/splits of the
                          // tile's rows from the workspace partials
+  int dsmem_reduce;      // cluster split whose partial tiles stay in each CTA's
+                         // shared memory (stage ring) and are summed from there
+                         // through distributed shared memory
   const float* scale_a;
   int a_per_row;
   const float* scale_b;
@@ -92,6 +95,7 @@ int max_stages_for(int block_n, int smem_budget);
 struct AttnParams {
   const void* q;        // [batch, num_q_heads, 128] bf16 / fp16
   int q_fp16;
+  int q_vec;            // q is 8-byte aligned (vector loads)
   const void* k_cache;  // e4m3 rows
   const void* v_cache;
   const int* block_table;  // null: contiguous per-sequence rows
@@ -108,7 +112,13 @@ struct AttnParams {
 };
 int attn_part_stride();
 int attn_max_chunk();
-cudaError_t launch_fp8kv_attention(const AttnParams& p, cudaStream_t stream);
+// tmap_k / tmap_v: 2-D uint8 tensor maps over the caches ({num_kv_heads *
+// 128, rows}, box {128, 16}, 128-byte swizzle) for the bulk-tensor path
+// (contiguous caches, or 16 | block_size), or null for per-lane copies.
+cudaError_t launch_fp8kv_attention(const AttnParams& p, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                                   cudaStream_t stream);
+// Reads and clears the attention kernels' status word (call after a sync).
+cudaError_t read_clear_attn_status(int* flags);
 
 // Quantiser / dequantiser launchers.
 struct QuantArgs {

@@ -109,6 +109,16 @@ __device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
   return v;
 }
 
+// 16-byte load from distributed shared memory (any CTA of the cluster).
+__device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // Arrive on an mbarrier of any CTA of the cluster (shared::cluster address),
 // releasing this thread's prior writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {

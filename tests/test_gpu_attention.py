@@ -110,6 +110,35 @@ def test_paged_cache_padding_entries(pad_id):
     run_case(B=3, Hq=8, Hkv=2, T=512, lens=[512, 77, 300], seed=210, paged_bs=16, pad=pad)
 
 
+@pytest.mark.parametrize("bs,T", [(8, 512), (48, 480), (32, 512)])
+def test_paged_block_sizes(bs, T):
+    """Block sizes that are not a multiple of 16 take per-lane copies; 32 and
+    48 take the bulk-tensor copies of 16-token blocks inside a cache block."""
+    run_case(B=3, Hq=8, Hkv=2, T=T, lens=[T, T - 37, 100], seed=220 + bs, paged_bs=bs,
+             pad=[(1, 2, -1)])
+
+
+def test_query_not_8_byte_aligned():
+    """A query view that starts 2 bytes into its storage takes the scalar
+    query loads; the result equals the aligned query's bit for bit."""
+    B, Hq, Hkv, T, D = 2, 8, 2, 200, 128
+    (k, ks), (v, vs) = kv_codes(B, T, Hkv, D, 230)
+    dev = "cuda"
+    q = si.normal((B, Hq, D), seed=231).to(dev)
+    store = torch.empty(B * Hq * D + 1, dtype=torch.bfloat16, device=dev)
+    qu = store[1:].view(B, Hq, D)
+    qu.copy_(q)
+    assert qu.data_ptr() % 8 != 0
+    kc, vc = torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev)
+    lens = torch.tensor([200, 77], dtype=torch.int32, device=dev)
+    ksc, vsc = torch.tensor([ks], device=dev), torch.tensor([vs], device=dev)
+    outs = [torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    w8.fp8_kv_decode_attention(q, kc, vc, lens, ksc, vsc, outs[0])
+    w8.fp8_kv_decode_attention(qu, kc, vc, lens, ksc, vsc, outs[1])
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
 def test_fp16_query_and_output():
     run_case(B=2, Hq=8, Hkv=2, T=300, lens=[300, 129], seed=300, q_dtype=torch.float16, out_dtype=torch.float16)
 
