@@ -65,14 +65,30 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
+def _stale(src: str) -> bool:
+    """An object is rebuilt when it is older than its source or than any
+    header of the library (every source includes the shared headers)."""
+    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+    if not os.path.exists(obj):
+        return True
+    t = os.path.getmtime(obj)
+    headers = (glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))
+               + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
+    return any(os.path.getmtime(d) > t for d in [src] + headers)
+
+
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile (if needed) and return the path of the shared library."""
+    """Compile what changed (everything with force) and return the path of
+    the shared library."""
     if not force and up_to_date():
         return LIB_PATH
     os.makedirs(BUILD, exist_ok=True)
     srcs = _sources()
-    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
+    todo = [s for s in srcs if force or verbose_ptxas or _stale(s)]
+    if todo:
+        with cf.ThreadPoolExecutor(max_workers=max(1, min(len(todo), os.cpu_count() or 4))) as ex:
+            list(ex.map(lambda s: _compile(s, verbose_ptxas), todo))
+    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-lrt", "-ldl", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
