@@ -68,7 +68,8 @@ constexpr int kHeadDim = 128;
 constexpr int kWarps = 4;                         // warps per CTA; each takes chunk / 4 tokens
 constexpr int kAttnThreads = 32 * kWarps;
 // Resident CTAs per SM the register budget is fitted to (4: <= 128
-// registers, 16 warps per SM; measured best with a 2-block ring).
+// registers, 16 warps per SM), with a ring of 2 blocks per warp: measured
+// best (a third slot, or 3 CTAs with deeper rings, ran 5-7 % slower).
 #ifndef W8A8_ATTN_MIN_CTAS
 #define W8A8_ATTN_MIN_CTAS 4
 #endif
@@ -303,22 +304,29 @@ __device__ __forceinline__ void attend_block(const KvBlock& x, const uint32_t (&
     s[k] = y;
     mx[k & 1] = fmaxf(mx[k & 1], y);
   }
-  float alpha[2], m_new[2];
+  // The running maxima only move when some score of the block exceeds them
+  // (rare once the first blocks are seen): then the new maxima are reduced
+  // over the 8 lanes of each column and the state rescaled by 2^(m_old -
+  // m_new); otherwise the factor would be exactly 1 and all of it is skipped.
+  float m_new[2] = {st.m[0], st.m[1]};
+  if (__any_sync(0xffffffffu, mx[0] > st.m[0] || mx[1] > st.m[1])) {
+    float alpha[2];
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < 2; ++c) {
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], off));
-    m_new[c] = fmaxf(st.m[c], mx[c]);
-    alpha[c] = m_new[c] == -INFINITY ? 1.f : exp2f(st.m[c] - m_new[c]);
-    st.m[c] = m_new[c];
-    st.l[c] *= alpha[c];
-  }
+      for (int off = 4; off < 32; off <<= 1) mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], off));
+      m_new[c] = fmaxf(st.m[c], mx[c]);
+      alpha[c] = m_new[c] == -INFINITY ? 1.f : exp2f(st.m[c] - m_new[c]);
+      st.m[c] = m_new[c];
+      st.l[c] *= alpha[c];
+    }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    st.o[i][0] *= alpha[0];
-    st.o[i][1] *= alpha[1];
-    st.o[i][2] *= alpha[0];
-    st.o[i][3] *= alpha[1];
+    for (int i = 0; i < 8; ++i) {
+      st.o[i][0] *= alpha[0];
+      st.o[i][1] *= alpha[1];
+      st.o[i][2] *= alpha[0];
+      st.o[i][3] *= alpha[1];
+    }
   }
   float pw[4];
 #pragma unroll
@@ -358,6 +366,10 @@ __global__ void __launch_bounds__(kAttnThreads, W8A8_ATTN_MIN_CTAS)
   constexpr bool kPack = G <= 4;
   // the KV heads of a chunk are consecutive CTAs: they run side by side and
   // read the same cache rows (each its 128-byte slice) at about the same time
+  // programmatic dependent launch: let the combine kernel be scheduled, then
+  // wait for the preceding kernel (and its memory) before reading anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.y;
   const int kvh = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.num_kv_heads));
   const int ch = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.num_kv_heads));
@@ -582,6 +594,8 @@ __global__ void __launch_bounds__(kAttnThreads, W8A8_ATTN_MIN_CTAS)
 
 // One CTA per (query head, sequence), one thread per head dim.
 __global__ void __launch_bounds__(kHeadDim) fp8kv_attn_combine_kernel(const AttnParams p) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the chunks' partials are complete
   const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
   const int len = seq_len_of(p, b);
   const size_t oi = (static_cast<size_t>(b) * p.num_q_heads + h) * kHeadDim + d;
@@ -609,6 +623,26 @@ __global__ void __launch_bounds__(kHeadDim) fp8kv_attn_combine_kernel(const Attn
     static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(y);
 }
 
+// Launch with programmatic stream serialisation (both attention kernels wait
+// for their predecessor with griddepcontrol.wait before touching memory).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Params>(args)...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <int G, bool kTma>
 cudaError_t launch_chunks_t(const AttnParams& p, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t stream) {
   const long long nch = (p.max_seq_len + p.chunk - 1) / p.chunk;
@@ -618,8 +652,7 @@ cudaError_t launch_chunks_t(const AttnParams& p, const CUtensorMap& mk, const CU
   // the attribute is per function and device; setting it again is harmless
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kAttnThreads, smem, stream>>>(p, mk, mv);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kAttnThreads), smem, stream, p, mk, mv);
 }
 
 template <int G>
@@ -657,8 +690,7 @@ cudaError_t launch_fp8kv_attention(const AttnParams& p, const CUtensorMap* tmap_
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  fp8kv_attn_combine_kernel<<<dim3(p.num_q_heads, p.batch), kHeadDim, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(fp8kv_attn_combine_kernel, dim3(p.num_q_heads, p.batch), dim3(kHeadDim), 0, stream, p);
 }
 
 }  // namespace w8a8
