@@ -264,7 +264,12 @@ W8A8_API w8a8_status w8a8_quant_scaled_mm(const void* x, int x_dtype, int64_t ld
  *                                <= 8);
  *            W8A8_REDUCE_AUTO    the cluster reduction when split_k <= 8,
  *                                else the global one.
- * Fields set to 0 (except swap_ab) mean "choose automatically". */
+ *  cta_pair  1: tiles of 256 token rows computed by a pair of CTAs on two SMs
+ *            with one tcgen05 MMA stream (cta_group::2): each CTA stages its
+ *            128 rows of A and half of the block_n columns of B (swap_ab 0,
+ *            split_k 1; block_n 128, 192, 224 or 256 for e4m3, 128 or 256
+ *            for int8); 0: one CTA per 128-row tile.
+ * Fields set to 0 (except swap_ab and cta_pair) mean "choose automatically". */
 #define W8A8_REDUCE_AUTO 0
 #define W8A8_REDUCE_GLOBAL 1
 #define W8A8_REDUCE_CLUSTER 2
@@ -276,6 +281,7 @@ typedef struct {
   int stages;
   int ctas_per_sm;
   int reduce;
+  int cta_pair;
 } w8a8_mm_config;
 
 /* The configuration w8a8_scaled_mm() picks for this problem (host only). */

@@ -56,7 +56,7 @@ EXPORTS = (
 class MmConfig(ctypes.Structure):
     _fields_ = [("swap_ab", ctypes.c_int), ("block_n", ctypes.c_int),
                 ("split_k", ctypes.c_int), ("stages", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
-                ("reduce", ctypes.c_int)]
+                ("reduce", ctypes.c_int), ("cta_pair", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -168,7 +168,8 @@ def _cfg(config) -> MmConfig | None:
         return config
     return MmConfig(int(config.get("swap_ab", 0)), int(config.get("block_n", 0)),
                     int(config.get("split_k", 0)), int(config.get("stages", 0)),
-                    int(config.get("ctas_per_sm", 0)), int(config.get("reduce", 0)))
+                    int(config.get("ctas_per_sm", 0)), int(config.get("reduce", 0)),
+                    int(config.get("cta_pair", 0)))
 
 
 def pick_config(M: int, N: int, K: int, q_dtype: int = E4M3) -> dict:

@@ -127,6 +127,7 @@ w8a8_status make_operand_map(CUtensorMap* map, const void* base, bool f16, long 
 constexpr int kSmemTwoPerSm = 113 * 1024;   // budget that lets two CTAs share an SM
 constexpr int kInt8ChunkK = 1024;           // exact fp32 accumulation bound: 1024 * 128 * 128 = 2^24
 constexpr long long kFusedRowsMaxBytes = 32768;  // one-kernel quant_scaled_mm: rows staged in shared memory
+constexpr long long kPairMinM = 1024;            // e4m3 tokens from which CTA-pair tiles are used
 
 bool valid_block_n(int bn, int q_dtype, int swap_ab) {
   if (bn == 16 || bn == 32 || bn == 64 || bn == 128) return true;
@@ -218,17 +219,50 @@ void auto_config(long long M, long long N, long long K, int q_dtype, int sms, w8
   // 256 x 4 slices against 30.1 us for 64 x 2; in the decode step it also
   // beat all 256 tokens in one swap-AB tile, 28.2 against 31.4 us)
   if (!c->swap_ab && q_dtype == W8A8_E4M3 && M <= 256 && K >= 8192) c->block_n = 256;
-  const long long tiles = c->swap_ab ? ceil_div(N, 128) * ceil_div(M, c->block_n)
-                                     : ceil_div(M, 128) * ceil_div(N, c->block_n);
-  c->split_k = one_wave_split(tiles, kb, static_cast<long long>(sms) * resident_per_sm(c->block_n, q_dtype));
   c->stages = 0;
   c->ctas_per_sm = 0;
   c->reduce = W8A8_REDUCE_AUTO;
+  c->cta_pair = 0;
+  // Large-M e4m3: 256 x block_n tiles on CTA pairs (each SM stages half of
+  // B).  Measured at M = 4096 on the Llama-3-8B projections: 2438 / 2368 /
+  // 3094 / 2751 TFLOP/s (QKV / O / gate-up / down) against 2326 / 2227 /
+  // 2837 / 2599 on one-CTA tiles.  block_n from the same wave-balance model
+  // over the pairs (sms / 2 of them).  int8 stays on one-CTA tiles: its
+  // chunk drains stall both CTAs of a pair (942-979 against 949-1003).
+  if (!c->swap_ab && q_dtype == W8A8_E4M3 && M >= kPairMinM) {
+    const int cands[3] = {256, 224, 192};
+    const long long pairs = std::max(1, sms / 2);
+    double best = 1e30;
+    for (int i = 0; i < 3; ++i) {
+      const int bn = cands[i];
+      const long long units = ceil_div(M, 256) * ceil_div(N, bn);
+      const long long waves = (units + pairs - 1) / pairs;
+      const double t = static_cast<double>(waves) * bn * (1.0 + 0.03 * i) /
+                       static_cast<double>(std::min<long long>(N, ceil_div(N, bn) * bn));
+      if (t < best - 1e-12) {
+        best = t;
+        c->block_n = bn;
+      }
+    }
+    c->cta_pair = 1;
+    c->split_k = 1;
+    return;
+  }
+  const long long tiles = c->swap_ab ? ceil_div(N, 128) * ceil_div(M, c->block_n)
+                                     : ceil_div(M, 128) * ceil_div(N, c->block_n);
+  c->split_k = one_wave_split(tiles, kb, static_cast<long long>(sms) * resident_per_sm(c->block_n, q_dtype));
 }
 
 int auto_stages(int block_n, int q_dtype, int smem_optin) {
   const int budget = resident_per_sm(block_n, q_dtype) == 2 ? kSmemTwoPerSm : smem_optin;
   return std::max(2, std::min(8, max_stages_for(block_n, budget)));
+}
+
+// CTA-pair tiles: each CTA stages 128 rows of A and block_n / 2 of B per stage.
+int auto_pair_stages(int block_n, int smem_optin) {
+  int s = 8;
+  while (s > 2 && gemm_pair_smem_bytes(block_n, s) > smem_optin) --s;
+  return s;
 }
 
 struct Plan {
@@ -252,12 +286,14 @@ Plan make_plan(long long M, long long N, long long K, int q_dtype, const w8a8_mm
   p.kb = num_kb(K, q_dtype);
   const long long P = cfg.swap_ab ? N : M;
   const long long Q = cfg.swap_ab ? M : N;
-  p.tiles_p = static_cast<int>(ceil_div(P, 128));
+  p.tiles_p = static_cast<int>(ceil_div(P, cfg.cta_pair ? 256 : 128));
   p.tiles_q = static_cast<int>(ceil_div(Q, cfg.block_n));
   int sp = std::max(1, std::min(cfg.split_k, p.kb));
   p.kb_per_split = static_cast<int>(ceil_div(p.kb, sp));
   p.splits = static_cast<int>(ceil_div(p.kb, p.kb_per_split));  // every slice non-empty
-  p.stages = cfg.stages > 0 ? cfg.stages : auto_stages(cfg.block_n, q_dtype, smem_optin);
+  p.stages = cfg.stages > 0 ? cfg.stages
+                            : (cfg.cta_pair ? auto_pair_stages(cfg.block_n, smem_optin)
+                                            : auto_stages(cfg.block_n, q_dtype, smem_optin));
   p.cluster = p.splits > 1 && cfg.reduce != W8A8_REDUCE_GLOBAL && p.splits <= kMaxClusterSplit;
   const size_t tiles = static_cast<size_t>(p.tiles_p) * p.tiles_q;
   const bool need_ws = p.splits > 1 || q_dtype == W8A8_INT8;
@@ -291,11 +327,25 @@ w8a8_status validate_config(const w8a8_mm_config& c, int q_dtype, int smem_optin
   if (c.reduce < W8A8_REDUCE_AUTO || c.reduce > W8A8_REDUCE_CLUSTER)
     return fail(W8A8_ERR_UNSUPPORTED, "reduce must be W8A8_REDUCE_AUTO, _GLOBAL or _CLUSTER");
   const int st = c.stages > 0 ? c.stages : auto_stages(c.block_n, q_dtype, smem_optin);
-  if (gemm_smem_bytes(c.block_n, st) > smem_optin)
+  if (!c.cta_pair && gemm_smem_bytes(c.block_n, st) > smem_optin)
     return fail(W8A8_ERR_UNSUPPORTED, "stages=%d with block_n=%d needs %d bytes of shared memory (> %d)", st,
                 c.block_n, gemm_smem_bytes(c.block_n, st), smem_optin);
   if (c.reduce == W8A8_REDUCE_CLUSTER && c.split_k > kMaxClusterSplit)
     return fail(W8A8_ERR_UNSUPPORTED, "the cluster reduction takes split_k <= %d", kMaxClusterSplit);
+  if (c.cta_pair != 0 && c.cta_pair != 1) return fail(W8A8_ERR_UNSUPPORTED, "cta_pair must be 0 or 1");
+  if (c.cta_pair) {
+    if (c.swap_ab || c.split_k != 1)
+      return fail(W8A8_ERR_UNSUPPORTED, "CTA-pair tiles take swap_ab = 0 and split_k = 1");
+    const bool bn_ok = q_dtype == W8A8_INT8 ? (c.block_n == 128 || c.block_n == 256)
+                                            : (c.block_n == 128 || c.block_n == 192 || c.block_n == 224 ||
+                                               c.block_n == 256);
+    if (!bn_ok)
+      return fail(W8A8_ERR_UNSUPPORTED, "CTA-pair tiles take block_n 128, 192, 224 or 256 (int8: 128 or 256)");
+    const int ps = c.stages > 0 ? c.stages : auto_pair_stages(c.block_n, smem_optin);
+    if (gemm_pair_smem_bytes(c.block_n, ps) > smem_optin)
+      return fail(W8A8_ERR_UNSUPPORTED, "stages=%d with block_n=%d needs more shared memory than a CTA has", ps,
+                  c.block_n);
+  }
   return W8A8_OK;
 }
 
@@ -388,7 +438,7 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
     w8a8_mm_config a;
     auto_config(M, N, K, q_dtype, dev.sms, &a);
     if (cfg.block_n == 0) cfg.block_n = a.block_n;
-    if (cfg.split_k == 0) cfg.split_k = a.split_k;
+    if (cfg.split_k == 0) cfg.split_k = cfg.cta_pair ? 1 : a.split_k;
   } else {
     auto_config(M, N, K, q_dtype, dev.sms, &cfg);
   }
@@ -432,7 +482,9 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
   const long long p_ld = cfg.swap_ab ? ldb_b : lda_b;
   const long long q_ld = cfg.swap_ab ? lda_b : ldb_b;
   if ((st = make_operand_map(&tp, p_base, i8, p_rows, K, p_ld, 128)) != W8A8_OK) return st;
-  if (!fa && (st = make_operand_map(&tq, q_base, i8, q_rows, K, q_ld, cfg.block_n)) != W8A8_OK) return st;
+  if (!fa && (st = make_operand_map(&tq, q_base, i8, q_rows, K, q_ld, cfg.cta_pair ? cfg.block_n / 2 : cfg.block_n)) !=
+                 W8A8_OK)
+    return st;
 
   MmParams prm{};
   prm.M = static_cast<int>(M);
@@ -487,7 +539,10 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
     e = launch_fused_quant_gemm(tp, prm, cfg.block_n, out_kind, stages, stream);
   } else {
     prm.dsmem_reduce = dsmem_reduce_fits(plan, cfg.block_n, plan.stages);
-    e = i8 ? launch_int8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream)
+    if (cfg.cta_pair)
+      e = launch_gemm_pair(tp, tq, prm, cfg.block_n, i8, out_kind, plan.stages, stream);
+    else
+      e = i8 ? launch_int8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream)
            : launch_fp8_gemm(tp, tq, prm, cfg.block_n, cfg.swap_ab != 0, out_kind, plan.stages, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "scaled_mm kernel launch");
@@ -617,7 +672,7 @@ size_t w8a8_scaled_mm_config_workspace_size(int64_t M, int64_t N, int64_t K, int
     w8a8_mm_config a;
     w8a8_scaled_mm_pick_config(M, N, K, q_dtype, &a);
     if (c.block_n == 0) c.block_n = a.block_n;
-    if (c.split_k == 0) c.split_k = a.split_k;
+    if (c.split_k == 0) c.split_k = c.cta_pair ? 1 : a.split_k;
   }
   if (c.split_k < 1) c.split_k = 1;
   return make_plan(M, N, K, q_dtype, c, 227 * 1024).total;

@@ -64,6 +64,13 @@ cudaError_t launch_fp8_gemm(const CUtensorMap& tmap_p, const CUtensorMap& tmap_q
                             const MmParams& p, int block_n, bool swap, int out_kind,
                             int stages, cudaStream_t stream);
 
+// The same matmul on CTA pairs (gemm2sm.cu): 256 x block_n tiles, tokens on
+// the 128-row side of each CTA (no swap, no split-K).  tmap_a boxes 128 rows,
+// tmap_b block_n / 2 rows.
+cudaError_t launch_gemm_pair(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const MmParams& p, int block_n,
+                             bool int8, int out_kind, int stages, cudaStream_t stream);
+int gemm_pair_smem_bytes(int block_n, int stages);
+
 // int8 GEMM.  Operands are first widened to f16 planes (exact), then
 // multiplied with tcgen05 kind::f16 in K chunks small enough that the fp32
 // accumulator is exact; each chunk is drained into an int32 total.

@@ -117,8 +117,13 @@ def test_pick_config_regimes(M):
     assert c["split_k"] <= 8 and c["reduce"] == w8.REDUCE_AUTO   # splits fit one cluster
     if M >= 4096:
         assert c["split_k"] == 1 and c["block_n"] >= 128   # many tiles: no split, wide tile
+    # 256-row tiles on CTA pairs for large-M e4m3 only
+    assert c["cta_pair"] == (1 if M >= 1024 else 0)
+    if c["cta_pair"]:
+        assert c["block_n"] in (192, 224, 256) and c["swap_ab"] == 0
     c8 = w8.pick_config(M, 4096, 4096, w8.INT8)
     assert c8["block_n"] <= 128 or (c8["block_n"] in (160, 256) and not c8["swap_ab"])
+    assert c8["cta_pair"] == 0
 
 
 @pytest.mark.parametrize("kw,status", [

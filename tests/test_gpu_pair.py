@@ -1,0 +1,85 @@
+"""Scaled matmul on CTA pairs (tcgen05 cta_group::2, 256-row tiles) against
+the oracle on seeded inputs, on shapes with several pair tiles and ragged
+tails in M, N and K ("[Kernel] Add w8a8 CUTLASS kernels", feature list of
+cutlass_scaled_mm_dq).  fp8: |gpu - y| <= 2^-7 |y| + 1e-3 against the
+oracle's fp32 y; int8: the int32 accumulators and the fp16 outputs bit for
+bit.  The 128-column tiles come first: they use 256 TMEM columns per CTA."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_bits16_equal, assert_fp8_close, out_to_f32, bits_np
+from test_gpu_gemm import fp8_problem, int8_problem, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def pair(bn, stages=0):
+    return {"swap_ab": 0, "block_n": bn, "split_k": 1, "stages": stages, "cta_pair": 1}
+
+
+SHAPES = [(256, 256, 512), (300, 200, 1008), (1024, 768, 2048), (520, 1040, 4112)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_pair_fp8_block_n_128(M, N, K):
+    A, B, sa, sb = fp8_problem(M, N, K, seed=M + N + K)
+    out = run_gpu(A, B, sa, sb, oracle.E4M3, torch.bfloat16, config=pair(128))
+    ref = oracle.scaled_mm(A, B, sa, sb, oracle.E4M3, oracle.BF16)
+    assert_fp8_close(out_to_f32(bits_np(out), oracle.BF16), ref["y"], "pair 128")
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES[:3])
+def test_pair_int8_block_n_128(M, N, K):
+    K = (K + 15) // 16 * 16
+    A, B, sa, sb = int8_problem(M, N, K, seed=M * 3 + N)
+    acc = run_gpu(A, B, np.ones(M, np.float32), np.ones(N, np.float32), oracle.INT8, torch.int32,
+                  config=pair(128))
+    ref = oracle.scaled_mm(A, B, sa, sb, oracle.INT8, oracle.FP16)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), ref["iacc"])
+    out = run_gpu(A, B, sa, sb, oracle.INT8, torch.float16, config=pair(128))
+    assert_bits16_equal(bits_np(out), ref["out"], oracle.FP16, "pair int8 128")
+
+
+@pytest.mark.parametrize("bn", [256, 224, 192])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_pair_fp8_wide(bn, M, N, K):
+    A, B, sa, sb = fp8_problem(M, N, K, seed=M + N + K + bn)
+    out = run_gpu(A, B, sa, sb, oracle.E4M3, torch.bfloat16, config=pair(bn))
+    ref = oracle.scaled_mm(A, B, sa, sb, oracle.E4M3, oracle.BF16)
+    assert_fp8_close(out_to_f32(bits_np(out), oracle.BF16), ref["y"], f"pair {bn}")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 512), (300, 200, 2048), (1024, 768, 3072)])
+def test_pair_int8_block_n_256(M, N, K):
+    """Three 1024-K chunks at K = 3072: the exact chunked accumulation drains
+    into the int32 total between chunks on both CTAs of the pair."""
+    A, B, sa, sb = int8_problem(M, N, K, seed=M * 5 + N)
+    acc = run_gpu(A, B, np.ones(M, np.float32), np.ones(N, np.float32), oracle.INT8, torch.int32,
+                  config=pair(256))
+    ref = oracle.scaled_mm(A, B, sa, sb, oracle.INT8, oracle.FP16)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), ref["iacc"])
+
+
+def test_pair_per_tensor_scales_fp16_and_two_stages():
+    M, N, K = 512, 512, 1024
+    A, B, sa, sb = fp8_problem(M, N, K, seed=77, a_per_row=False, b_per_row=False)
+    out = run_gpu(A, B, sa, sb, oracle.E4M3, torch.float16, config=pair(256, stages=2))
+    ref = oracle.scaled_mm(A, B, sa, sb, oracle.E4M3, oracle.FP16)
+    assert_fp8_close(out_to_f32(bits_np(out), oracle.FP16), ref["y"], "pair per-tensor")
+
+
+def test_pair_rejects_split_and_swap():
+    import int8_w8a8_scaled_gb300 as w8
+    A, B, sa, sb = fp8_problem(256, 256, 512, seed=5)
+    for bad in ({"swap_ab": 1, "block_n": 128, "split_k": 1, "cta_pair": 1},
+                {"swap_ab": 0, "block_n": 128, "split_k": 2, "cta_pair": 1},
+                {"swap_ab": 0, "block_n": 64, "split_k": 1, "cta_pair": 1}):
+        with pytest.raises(w8.W8A8Error):
+            run_gpu(A, B, sa, sb, oracle.E4M3, torch.bfloat16, config=bad)
+
+
+def test_pair_no_device_timeouts():
+    import int8_w8a8_scaled_gb300 as w8
+    assert w8.device_status() == 0
