@@ -218,15 +218,16 @@ class DecodeWorkload:
         self.ws = w8.Workspace(ws_need, dev)
         torch.cuda.synchronize()
 
-    def flops(self):
-        return sum(2.0 * it["M"] * self.weights[it["name"]][2] * self.weights[it["name"]][3] for it in self.items)
+    def flops(self, items=None):
+        return sum(2.0 * it["M"] * self.weights[it["name"]][2] * self.weights[it["name"]][3]
+                   for it in (items if items is not None else self.items))
 
-    def gemm_bytes(self):
+    def gemm_bytes(self, items=None):
         # algorithmic bytes of the matmul kernels: 1-byte weights once, the
         # activations once (16-bit x where the kernel quantises them itself,
         # 1-byte codes otherwise), 16-bit output, fp32 scales
         tot = 0
-        for it in self.items:
+        for it in (items if items is not None else self.items):
             _, sw, N, K = self.weights[it["name"]]
             M = it["M"]
             tot += N * K + (2 if it["fused"] else 1) * M * K + 2 * M * N + 4 * (M + sw.numel())
@@ -245,10 +246,10 @@ class DecodeWorkload:
         wq, sw, _, _ = self.weights[it["name"]]
         self.w8.quant_scaled_mm(it["x"], wq, sw, it["out"], scale_a_out=it["sa"], workspace=self.ws)
 
-    def run_gemm(self):
+    def run_gemm(self, items=None):
         # the matmul kernels of a step (those that quantise their own
         # activations included); the others read codes quantised beforehand
-        for it in self.items:
+        for it in (items if items is not None else self.items):
             wq, sw, _, _ = self.weights[it["name"]]
             if it["fused"]:
                 self._fused(it)
@@ -792,6 +793,19 @@ def run_profile_case(name: str, launches: int):
         raise SystemExit("a kernel reported a pipeline timeout")
 
 
+def run_int8_routes():
+    """Compile and run probes/int8_routes.cu: mma.sync s8 and f16 throughput
+    with register operands (the int8 matmul's route choice; the tcgen05
+    kind::f16 route is the library's own int8 matmul, measured by the int8
+    configuration of this benchmark)."""
+    from int8_w8a8_scaled_gb300 import _build
+    src = os.path.join(ROOT, "int8_w8a8_scaled_gb300", "probes", "int8_routes.cu")
+    os.makedirs(_build.BUILD, exist_ok=True)
+    exe = os.path.join(_build.BUILD, "int8_routes")
+    subprocess.run([_build.nvcc(), *_build.ARCH, "-O3", src, "-o", exe], check=True)
+    return subprocess.run([exe]).returncode
+
+
 # ---------------------------------------------------------------- main paths
 
 def run_reference(args):
@@ -890,6 +904,26 @@ def run_e2e(wl, stream, dev, steps, warmup, barrier):
     return t, n, h2d, d2h
 
 
+def decode_gemms_by_m(wl, stream, steps, warmup, pk):
+    """The decode step's four matmuls at each token count M, timed as a graph
+    of their own: {M: [us, fraction of HBM, fraction of the roofline]}.  The
+    roofline time of a GEMM is the larger of its algorithmic bytes at the
+    measured HBM rate and its flops at the dense fp8 peak; at M = 256 the two
+    are within 10 % of each other (2·M flops per weight byte against a ridge
+    near 560), so HBM alone understates how close that regime is to its
+    bound."""
+    out = {}
+    hbm, fp8 = pk["hbm_gbs"] * 1e9, 2.0 * pk["bf16_tflops"] * 1e12
+    for M in DECODE_MS:
+        its = [it for it in wl.items if it["M"] == M]
+        g = graph_of(lambda its=its: wl.run_gemm(its), stream)
+        t, _ = time_graph(g, stream, steps, warmup)
+        roof = sum(max(wl.gemm_bytes([it]) / hbm, wl.flops([it]) / fp8) for it in its)
+        out[str(M)] = [r4(t * 1e6), r4(wl.gemm_bytes(its) / t / hbm), r4(roof / t)]
+        del g
+    return out
+
+
 def run_ours(args):
     import torch
     ws_n, rank, local = dist_env()
@@ -944,7 +978,8 @@ def run_ours(args):
         cfgs["attn_fp8kv"] = measure_kv_attention(dev, st, w, stream, pk)
         cfgs["quant_prefill"] = measure_quant_prefill(dev, st, w, stream, pk)
     cfgs["c2_detail"] = {"gemm_us": r4(t_gemm * 1e6), "quant_us": r4(t_quant * 1e6),
-                         "quant_gbs": r4(quant_gbs), "quant_frac": r4(quant_gbs / hbm)}
+                         "quant_gbs": r4(quant_gbs), "quant_frac": r4(quant_gbs / hbm),
+                         "by_m": decode_gemms_by_m(wl, stream, args.steps, args.warmup, pk)}
 
     cpu = None
     if rank == 0 and args.gpus == 1 and not args.no_cpu_baseline:
@@ -997,7 +1032,11 @@ def main():
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
                     help="run a few launches of one kernel on a small case (for ncu) and exit")
     ap.add_argument("--launches", type=int, default=5)
+    ap.add_argument("--int8-routes", action="store_true",
+                    help="time the warp-level MMA instructions an int8 matmul could use (the route choice) and exit")
     args = ap.parse_args()
+    if args.int8_routes:
+        return run_int8_routes()
     if args.profile_case:
         run_profile_case(args.profile_case, args.launches)
         return 0

@@ -267,8 +267,8 @@ W8A8_API w8a8_status w8a8_quant_scaled_mm(const void* x, int x_dtype, int64_t ld
  *  cta_pair  1: tiles of 256 token rows computed by a pair of CTAs on two SMs
  *            with one tcgen05 MMA stream (cta_group::2): each CTA stages its
  *            128 rows of A and half of the block_n columns of B (swap_ab 0,
- *            split_k 1; block_n 128, 192, 224 or 256 for e4m3, 128 or 256
- *            for int8); 0: one CTA per 128-row tile.
+ *            split_k 1; block_n 64, 96, 128, 192, 224 or 256 for e4m3, 128
+ *            or 256 for int8); 0: one CTA per 128-row tile.
  * Fields set to 0 (except swap_ab and cta_pair) mean "choose automatically". */
 #define W8A8_REDUCE_AUTO 0
 #define W8A8_REDUCE_GLOBAL 1
@@ -424,8 +424,10 @@ W8A8_API w8a8_status w8a8_scaled_mm_noalloc(const void* a_q, int64_t lda, const 
  * after the cluster barrier [10] and its share of the reduction [11]; in a
  * matmul that quantises its own activations, when the token maxima [12],
  * the token scales [13] and the first token stage [14] were ready; unused
- * words are left as they were.  Each launch overwrites the buffer.  NULL turns tracing off (the
- * default).  Not for production use: concurrent launches share the buffer. */
+ * words are left as they were.  Each launch overwrites the buffer.  Launches
+ * on CTA pairs (cta_pair = 1) write no stamps.  NULL turns tracing off (the
+ * default).  A diagnostic aid, not part of the hot path: concurrent launches
+ * share the buffer. */
 W8A8_API w8a8_status w8a8_debug_mm_trace(void* buf, size_t bytes);
 
 /* Reads and clears the library's device-side status word on the current

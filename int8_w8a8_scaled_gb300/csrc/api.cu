@@ -315,7 +315,7 @@ Plan make_plan(long long M, long long N, long long K, int q_dtype, const w8a8_mm
 
 w8a8_status validate_config(const w8a8_mm_config& c, int q_dtype, int smem_optin) {
   if (c.swap_ab != 0 && c.swap_ab != 1) return fail(W8A8_ERR_UNSUPPORTED, "swap_ab must be 0 or 1");
-  if (!valid_block_n(c.block_n, q_dtype, c.swap_ab))
+  if (!c.cta_pair && !valid_block_n(c.block_n, q_dtype, c.swap_ab))
     return fail(W8A8_ERR_UNSUPPORTED,
                 "block_n %d not supported (16, 32, 64, 128, 256; 160/192/224 for e4m3 without swap; 160/256 for int8 without swap)",
                 c.block_n);
@@ -337,10 +337,11 @@ w8a8_status validate_config(const w8a8_mm_config& c, int q_dtype, int smem_optin
     if (c.swap_ab || c.split_k != 1)
       return fail(W8A8_ERR_UNSUPPORTED, "CTA-pair tiles take swap_ab = 0 and split_k = 1");
     const bool bn_ok = q_dtype == W8A8_INT8 ? (c.block_n == 128 || c.block_n == 256)
-                                            : (c.block_n == 128 || c.block_n == 192 || c.block_n == 224 ||
-                                               c.block_n == 256);
+                                            : (c.block_n == 64 || c.block_n == 96 || c.block_n == 128 ||
+                                               c.block_n == 192 || c.block_n == 224 || c.block_n == 256);
     if (!bn_ok)
-      return fail(W8A8_ERR_UNSUPPORTED, "CTA-pair tiles take block_n 128, 192, 224 or 256 (int8: 128 or 256)");
+      return fail(W8A8_ERR_UNSUPPORTED,
+                  "CTA-pair tiles take block_n 64, 96, 128, 192, 224 or 256 (int8: 128 or 256)");
     const int ps = c.stages > 0 ? c.stages : auto_pair_stages(c.block_n, smem_optin);
     if (gemm_pair_smem_bytes(c.block_n, ps) > smem_optin)
       return fail(W8A8_ERR_UNSUPPORTED, "stages=%d with block_n=%d needs more shared memory than a CTA has", ps,

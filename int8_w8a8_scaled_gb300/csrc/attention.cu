@@ -45,12 +45,14 @@
 //    (movmatrix), which is exactly the B fragment of the output MMA.
 //
 // Work split: a CTA of 4 warps takes one (chunk, KV head, sequence); each
-// warp takes a quarter of the chunk's tokens, 16 at a time, and its lanes
-// stream their own 16-byte pieces of the next blocks into a per-warp
-// shared-memory ring with cp.async while the current block is used; the 4
-// warps' (m, l, o) are combined in shared memory at the end.  The KV heads of
-// a chunk are consecutive CTAs, so they read the same cache rows (each its
-// 128-byte slice) at about the same time.
+// warp takes a quarter of the chunk's tokens, 16 at a time, into a per-warp
+// shared-memory ring of 16-token blocks filled while the current block is
+// used: by two bulk-tensor copies per block (K and V rows, 128-byte swizzle)
+// when every 16-token block is contiguous in the cache (no block table, or
+// 16 dividing the block size), else by the lanes' own 16-byte cp.async
+// pieces.  The 4 warps' (m, l, o) are combined in shared memory at the end.
+// The KV heads of a chunk are consecutive CTAs, so they read the same cache
+// rows (each its 128-byte slice) at about the same time.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>

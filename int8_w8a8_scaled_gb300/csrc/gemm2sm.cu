@@ -384,6 +384,8 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tmap_a, const CUtensorMap& tmap_
     case 224: return launch_pair_out<224, false>(tmap_a, tmap_b, p, out_kind, stages, stream);
     case 192: return launch_pair_out<192, false>(tmap_a, tmap_b, p, out_kind, stages, stream);
     case 128: return launch_pair_out<128, false>(tmap_a, tmap_b, p, out_kind, stages, stream);
+    case 96: return launch_pair_out<96, false>(tmap_a, tmap_b, p, out_kind, stages, stream);
+    case 64: return launch_pair_out<64, false>(tmap_a, tmap_b, p, out_kind, stages, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -42,7 +42,7 @@ def test_pair_int8_block_n_128(M, N, K):
     assert_bits16_equal(bits_np(out), ref["out"], oracle.FP16, "pair int8 128")
 
 
-@pytest.mark.parametrize("bn", [256, 224, 192])
+@pytest.mark.parametrize("bn", [256, 224, 192, 96, 64])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_pair_fp8_wide(bn, M, N, K):
     A, B, sa, sb = fp8_problem(M, N, K, seed=M + N + K + bn)
@@ -75,7 +75,7 @@ def test_pair_rejects_split_and_swap():
     A, B, sa, sb = fp8_problem(256, 256, 512, seed=5)
     for bad in ({"swap_ab": 1, "block_n": 128, "split_k": 1, "cta_pair": 1},
                 {"swap_ab": 0, "block_n": 128, "split_k": 2, "cta_pair": 1},
-                {"swap_ab": 0, "block_n": 64, "split_k": 1, "cta_pair": 1}):
+                {"swap_ab": 0, "block_n": 80, "split_k": 1, "cta_pair": 1}):
         with pytest.raises(w8.W8A8Error):
             run_gpu(A, B, sa, sb, oracle.E4M3, torch.bfloat16, config=bad)
 
