@@ -28,7 +28,9 @@
 // f16 values (hi = f16(p * 2^15), lo = f16(p * 2^15 - hi)), so a weight
 // keeps ~22 significant bits: for G <= 4 the lo halves take the four
 // padding columns of the 8-column MMA (no extra MMA), for G = 8 a second
-// MMA adds them.
+// MMA adds them.  For G <= 4 the query rows are also duplicated into those
+// columns, so the score MMA already gives the lanes that carry the lo
+// halves their heads' scores.
 //
 // Register layout (lane = 4 g + t):
 //  - scores: A = K tile, rows g and g + 8 are tokens g and g + 8; thread t
@@ -107,10 +109,6 @@ __device__ __forceinline__ uint32_t cvt2(uint32_t two_codes) {
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
-__device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
-  return static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
-}
-
 // D += A . B for one m16n8k16 tile: f16 operands, fp32 accumulators.
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -137,11 +135,22 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
   return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
 }
 
-// f16 weight pair hi + lo of x (hi = RN(x), lo = RN(x - hi)); `want_lo`
-// picks which of the two a lane contributes.
-__device__ __forceinline__ __half weight_part(float x, bool want_lo) {
-  const __half hi = __float2half_rn(x);
-  return want_lo ? __float2half_rn(x - __half2float(hi)) : hi;
+// Two weights a, b as f16 pairs hi = (RN(a), RN(b)) and lo = (RN(a - hi.a),
+// RN(b - hi.b)), a in the low half; a - hi.a is exact in fp32.
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// 2^x by the hardware approximation (relative error about 2^-22; results
+// below 2^-126 flush to zero, a softmax weight that no sum can see).
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // The codes one lane holds for a block of 16 tokens: K rows g and g + 8
@@ -262,6 +271,12 @@ __device__ __forceinline__ void read_block_tma(const uint8_t* slot, const AttnPa
     x.k[r][1] = *reinterpret_cast<const uint4*>(kt + swz(row, 4 + t));
     x.kval[r] = blk_ok && ib + row < end;
   }
+  if (blk_ok && ib + 16 <= end) {  // warp-uniform: a whole block of tokens
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      x.v[r] = *reinterpret_cast<const uint4*>(vt + swz(2 * t + (r & 1) + 8 * (r >> 1), g));
+    return;
+  }
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int row = 2 * t + (r & 1) + 8 * (r >> 1);
@@ -296,13 +311,12 @@ __device__ __forceinline__ void attend_block(const KvBlock& x, const uint32_t (&
   float s[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) s[k] = (sp[0][k] + sp[1][k]) + (sp[2][k] + sp[3][k]);
-  // lanes t >= 2 mirror their partner's columns (heads); invalid tokens -inf
+  // (with packing, lanes t >= 2 hold duplicates of their partner's
+  // columns: the query rows are duplicated); invalid tokens -inf
   float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const float v = __shfl_xor_sync(0xffffffffu, s[k], 2);
-    float y = lo_lane ? v : s[k];
-    y = x.kval[k >> 1] ? y * cs : -INFINITY;
+    const float y = x.kval[k >> 1] ? s[k] * cs : -INFINITY;
     s[k] = y;
     mx[k & 1] = fmaxf(mx[k & 1], y);
   }
@@ -318,7 +332,7 @@ __device__ __forceinline__ void attend_block(const KvBlock& x, const uint32_t (&
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], off));
       m_new[c] = fmaxf(st.m[c], mx[c]);
-      alpha[c] = m_new[c] == -INFINITY ? 1.f : exp2f(st.m[c] - m_new[c]);
+      alpha[c] = m_new[c] == -INFINITY ? 1.f : ex2_fast(st.m[c] - m_new[c]);
       st.m[c] = m_new[c];
       st.l[c] *= alpha[c];
     }
@@ -334,19 +348,24 @@ __device__ __forceinline__ void attend_block(const KvBlock& x, const uint32_t (&
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const float mc = m_new[k & 1];
-    pw[k] = (mc == -INFINITY) ? 0.f : exp2f(s[k] - mc);
+    pw[k] = (mc == -INFINITY) ? 0.f : ex2_fast(s[k] - mc);
     st.l[k & 1] += pw[k];
   }
   // P^T fragments (tokens 2t.., column g) by transposing the accumulator layout
   uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
-  if (kPack) {
-    bh0 = movmatrix_t(pack_half2(weight_part(pw[0] * kPScale, lo_lane), weight_part(pw[1] * kPScale, lo_lane)));
-    bh1 = movmatrix_t(pack_half2(weight_part(pw[2] * kPScale, lo_lane), weight_part(pw[3] * kPScale, lo_lane)));
-  } else {
-    bh0 = movmatrix_t(pack_half2(weight_part(pw[0] * kPScale, false), weight_part(pw[1] * kPScale, false)));
-    bh1 = movmatrix_t(pack_half2(weight_part(pw[2] * kPScale, false), weight_part(pw[3] * kPScale, false)));
-    bl0 = movmatrix_t(pack_half2(weight_part(pw[0] * kPScale, true), weight_part(pw[1] * kPScale, true)));
-    bl1 = movmatrix_t(pack_half2(weight_part(pw[2] * kPScale, true), weight_part(pw[3] * kPScale, true)));
+  {
+    uint32_t h01, l01, h23, l23;
+    split_pair(pw[0] * kPScale, pw[1] * kPScale, h01, l01);
+    split_pair(pw[2] * kPScale, pw[3] * kPScale, h23, l23);
+    if (kPack) {
+      bh0 = movmatrix_t(lo_lane ? l01 : h01);
+      bh1 = movmatrix_t(lo_lane ? l23 : h23);
+    } else {
+      bh0 = movmatrix_t(h01);
+      bh1 = movmatrix_t(h23);
+      bl0 = movmatrix_t(l01);
+      bl1 = movmatrix_t(l23);
+    }
   }
   // O^T[dims 16g+2i, 16g+2i+1][columns] += V^T . P^T
 #pragma unroll
@@ -453,9 +472,12 @@ __global__ void __launch_bounds__(kAttnThreads, W8A8_ATTN_MIN_CTAS)
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
   if (lane == 0) s_qmax[warp] = qmax;
-  // padding heads' rows of the fragment are zero
-  for (int i = G * kHeadDim + threadIdx.x; i < 8 * kHeadDim; i += kAttnThreads)
-    qs[i / kHeadDim][i % kHeadDim] = __float2half_rn(0.f);
+  // padding heads' rows of the fragment are zero (with packing, rows 4..7
+  // repeat rows 0..3)
+  for (int i = threadIdx.x; i < 8 * kHeadDim; i += kAttnThreads) {
+    const int r = i / kHeadDim;
+    if ((kPack ? (r & 3) : r) >= G) qs[r][i % kHeadDim] = __float2half_rn(0.f);
+  }
   __syncthreads();
   qmax = s_qmax[0];
 #pragma unroll
@@ -471,7 +493,11 @@ __global__ void __launch_bounds__(kAttnThreads, W8A8_ATTN_MIN_CTAS)
     const int i = 4 * (threadIdx.x + u * kAttnThreads);
     if (i < G * kHeadDim) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) qs[(i + c) / kHeadDim][(i + c) % kHeadDim] = __float2half_rn(ldexpf(qv[u][c], e));
+      for (int c = 0; c < 4; ++c) {
+        const __half h = __float2half_rn(ldexpf(qv[u][c], e));
+        qs[(i + c) / kHeadDim][(i + c) % kHeadDim] = h;
+        if (kPack) qs[(i + c) / kHeadDim + 4][(i + c) % kHeadDim] = h;
+      }
     }
   }
   __syncthreads();
