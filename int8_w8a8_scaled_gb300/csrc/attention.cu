@@ -57,7 +57,6 @@
 // rows (each its 128-byte slice) at about the same time.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 #include <cstring>
 
@@ -103,10 +102,13 @@ __device__ __forceinline__ int seq_len_of(const AttnParams& p, int b) {
   return len < 0 ? 0 : (len > p.max_seq_len ? p.max_seq_len : len);
 }
 
-// two e4m3 codes (low byte first) -> f16x2 (exact), as a 32-bit register
-__device__ __forceinline__ uint32_t cvt2(uint32_t two_codes) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// four e4m3 codes (low byte first) -> two f16x2 registers (exact): codes 0, 1
+// into `lo`, codes 2, 3 into `hi`, each half of the word converted in place
+__device__ __forceinline__ void cvt4(uint32_t four_codes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four_codes));
 }
 
 // D += A . B for one m16n8k16 tile: f16 operands, fp32 accumulators.
@@ -306,7 +308,10 @@ __device__ __forceinline__ void attend_block(const KvBlock& x, const uint32_t (&
   for (int j = 0; j < 8; ++j) {
     const uint32_t w0r = word_of(x.k[0][j >> 2], j & 3);
     const uint32_t w1r = word_of(x.k[1][j >> 2], j & 3);
-    mma16816(sp[j & 3], cvt2(w0r), cvt2(w1r), cvt2(w0r >> 16), cvt2(w1r >> 16), qf[j][0], qf[j][1]);
+    uint32_t a0, a1, a2, a3;
+    cvt4(w0r, a0, a2);
+    cvt4(w1r, a1, a3);
+    mma16816(sp[j & 3], a0, a1, a2, a3, qf[j][0], qf[j][1]);
   }
   float s[4];
 #pragma unroll
@@ -373,7 +378,9 @@ __device__ __forceinline__ void attend_block(const KvBlock& x, const uint32_t (&
     const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
     const uint32_t p01 = __byte_perm(word_of(x.v[0], i >> 1), word_of(x.v[1], i >> 1), sel);
     const uint32_t p23 = __byte_perm(word_of(x.v[2], i >> 1), word_of(x.v[3], i >> 1), sel);
-    const uint32_t a0 = cvt2(p01), a1 = cvt2(p01 >> 16), a2 = cvt2(p23), a3 = cvt2(p23 >> 16);
+    uint32_t a0, a1, a2, a3;
+    cvt4(p01, a0, a1);
+    cvt4(p23, a2, a3);
     mma16816(st.o[i], a0, a1, a2, a3, bh0, bh1);
     if (!kPack) mma16816(st.o[i], a0, a1, a2, a3, bl0, bl1);
   }
