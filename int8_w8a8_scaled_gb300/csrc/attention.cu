@@ -81,6 +81,7 @@ constexpr int kAttnThreads = 32 * kWarps;
 #endif
 constexpr int kMaxChunk = W8A8_ATTN_MAX_CHUNK;
 constexpr int kPartStride = kHeadDim + 4;         // o[128], m, l, 2 pad (floats)
+constexpr int kOStride = kHeadDim + kHeadDim / 16;  // a warp's o per head in shared memory (padded)
 constexpr float kPScale = 32768.f;                // weights enter the output MMA as p * 2^15
 
 __device__ __forceinline__ float load_q(const void* q, int q_fp16, size_t i) {
@@ -102,13 +103,8 @@ __device__ __forceinline__ int seq_len_of(const AttnParams& p, int b) {
   return len < 0 ? 0 : (len > p.max_seq_len ? p.max_seq_len : len);
 }
 
-// four e4m3 codes (low byte first) -> two f16x2 registers (exact): codes 0, 1
-// into `lo`, codes 2, 3 into `hi`, each half of the word converted in place
 __device__ __forceinline__ void cvt4(uint32_t four_codes, uint32_t& lo, uint32_t& hi) {
-  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(four_codes));
+  e4m3x4_to_f16x2x2(four_codes, lo, hi);
 }
 
 // D += A . B for one m16n8k16 tile: f16 operands, fp32 accumulators.
@@ -411,7 +407,6 @@ __global__ void __launch_bounds__(kAttnThreads, W8A8_ATTN_MIN_CTAS)
   __shared__ __align__(16) __half qs[8][kHeadDim];   // q * 2^e in f16; zero rows for padding heads
   __shared__ float s_qmax[kWarps];
   __shared__ float s_m[kWarps][8], s_l[kWarps][8];
-  __shared__ float s_o[kWarps][G][kHeadDim];
   extern __shared__ __align__(128) uint8_t ring_raw[];  // [kWarps][kRing][kBlockBytes], 1024-byte aligned
   __shared__ uint64_t s_bar[kWarps][kRing];             // bulk-tensor path: one per ring slot
   uint8_t* ring_smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ring_raw) + 1023) &
@@ -567,6 +562,12 @@ __global__ void __launch_bounds__(kAttnThreads, W8A8_ATTN_MIN_CTAS)
     for (int j = consumed; j < issued; ++j) mbar_wait(smem_addr(&s_bar[warp][j % kRing]), (j / kRing) & 1);
   }
   if (!kTma) cp_async_wait<0>();
+  // every copy into this warp's ring has landed and been read: the ring now
+  // holds the warp's o per head, [G][128 + 8] floats (one pad word per 16
+  // dims keeps the 8 lanes of a store on different banks)
+  __syncwarp();
+  float* s_o_w = reinterpret_cast<float*>(ring);
+  static_assert(G * kOStride * 4 <= kRing * kBlockBytes, "o fits the warp's ring");
   float (&o)[8][4] = st.o;
   float (&m_run)[2] = st.m;
   float (&l_run)[2] = st.l;
@@ -594,8 +595,9 @@ __global__ void __launch_bounds__(kAttnThreads, W8A8_ATTN_MIN_CTAS)
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          s_o[warp][h][16 * g + 2 * i] = o[i][c];
-          s_o[warp][h][16 * g + 2 * i + 1] = o[i][2 + c];
+          const int d = 16 * g + 2 * i;
+          s_o_w[h * kOStride + d + g] = o[i][c];  // d + d / 16
+          s_o_w[h * kOStride + d + 1 + g] = o[i][2 + c];
         }
       }
     }
@@ -614,7 +616,9 @@ __global__ void __launch_bounds__(kAttnThreads, W8A8_ATTN_MIN_CTAS)
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
         const float f = exp2f(s_m[w][h] - M);
-        acc = fmaf(f, s_o[w][h][d], acc);
+        acc = fmaf(f, reinterpret_cast<const float*>(ring_smem + static_cast<size_t>(w) * kRing * kBlockBytes)
+                              [h * kOStride + d + d / 16],
+                   acc);
         l = fmaf(f, s_l[w][h], l);
       }
     }

@@ -420,6 +420,41 @@ __device__ __forceinline__ uint16_t out16(float y) {
   return __half_as_ushort(__float2half_rn(y));
 }
 
+// two outputs RN(a), RN(b) in one 32-bit word, a in the low half
+template <int YK>
+__device__ __forceinline__ uint32_t out16x2(float a, float b) {
+  if (YK == 0) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
+  const __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// 16 codes (one 16-byte word, first code in the low byte) -> decode(q) * s
+// rounded to 16 bits, two per output word.  e4m3 decodes four codes per
+// conversion (exactly, through f16); the products and roundings are those
+// of dec1 and out16 one by one.
+template <int QK, int YK>
+__device__ __forceinline__ void dequant16(const uint4& w, float s, uint32_t (&o)[8]) {
+  const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+  if (QK == 0) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t h01, h23;
+      e4m3x4_to_f16x2x2(words[j], h01, h23);
+      const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+      const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+      o[2 * j] = out16x2<YK>(f01.x * s, f01.y * s);
+      o[2 * j + 1] = out16x2<YK>(f23.x * s, f23.y * s);
+    }
+  } else {
+    const uint8_t* bb = reinterpret_cast<const uint8_t*>(&w);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = out16x2<YK>(dec1<QK>(bb[2 * j]) * s, dec1<QK>(bb[2 * j + 1]) * s);
+  }
+}
+
 template <int QK, int YK>
 __global__ void __launch_bounds__(256)
     dequant_flat_kernel(const uint8_t* __restrict__ q, long long n, const float* __restrict__ scale,
@@ -430,12 +465,8 @@ __global__ void __launch_bounds__(256)
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; v < n16; v += stride) {
     const uint4 w = __ldcs(reinterpret_cast<const uint4*>(q) + v);
-    const uint8_t* b = reinterpret_cast<const uint8_t*>(&w);
     uint32_t o[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      o[j] = static_cast<uint32_t>(out16<YK>(dec1<QK>(b[2 * j]) * s)) |
-             (static_cast<uint32_t>(out16<YK>(dec1<QK>(b[2 * j + 1]) * s)) << 16);
+    dequant16<QK, YK>(w, s, o);
     uint4* d = reinterpret_cast<uint4*>(y) + 2 * v;
     __stcs(d, make_uint4(o[0], o[1], o[2], o[3]));
     __stcs(d + 1, make_uint4(o[4], o[5], o[6], o[7]));
@@ -665,12 +696,8 @@ __global__ void __launch_bounds__(256)
       break;
     }
     const uint4 w = reinterpret_cast<const uint4*>(in_buf[b])[threadIdx.x];
-    const uint8_t* bb = reinterpret_cast<const uint8_t*>(&w);
     uint32_t o[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      o[j] = static_cast<uint32_t>(out16<YK>(dec1<QK>(bb[2 * j]) * s)) |
-             (static_cast<uint32_t>(out16<YK>(dec1<QK>(bb[2 * j + 1]) * s)) << 16);
+    dequant16<QK, YK>(w, s, o);
     uint4* d = reinterpret_cast<uint4*>(out_buf[b]) + 2 * threadIdx.x;
     d[0] = make_uint4(o[0], o[1], o[2], o[3]);
     d[1] = make_uint4(o[4], o[5], o[6], o[7]);

@@ -152,6 +152,17 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity)
 
 // Order this thread's generic-proxy writes to shared memory before later
 // async-proxy (tensor core) reads of them.
+// Four e4m3 codes (low byte first) -> two f16x2 registers, exactly (every
+// e4m3 value is an f16 value): codes 0, 1 into `lo`, codes 2, 3 into `hi`.
+// Each 16-bit half of the word is converted in place, with no shift or mask
+// to extract it.  Codes 0x7F / 0xFF give NaN.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_codes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four_codes));
+}
+
 __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
