@@ -152,12 +152,16 @@ __device__ __forceinline__ float ex2_fast(float x) {
 }
 
 // The codes one lane holds for a block of 16 tokens: K rows g and g + 8
-// (bytes 16t and 64 + 16t), V rows 2t, 2t + 1, 2t + 8, 2t + 9 (bytes 16g),
-// and whether K rows g, g + 8 are tokens of the sequence.
+// (bytes 16t and 64 + 16t) and whether they are tokens of the sequence;
+// V rows 2t, 2t + 1, 2t + 8, 2t + 9 (bytes 16g) are read from the ring slot
+// only once the score MMAs have taken K (fewer registers live at once):
+// `vsrc` is the slot, `vlim` the number of its leading rows that hold tokens
+// (rows past it read as zero codes).
 struct KvBlock {
   uint4 k[2][2];
-  uint4 v[4];
   bool kval[2];
+  const uint8_t* vsrc;
+  int vlim;
 };
 
 // Ring of blocks in flight per warp (shared memory, filled by cp.async).  A
@@ -217,11 +221,12 @@ __device__ __forceinline__ void read_block(const uint8_t* slot_ptr, int lane, ui
   x.k[0][1] = c[1 * 32];
   x.k[1][0] = c[2 * 32];
   x.k[1][1] = c[3 * 32];
-#pragma unroll
-  for (int r = 0; r < 4; ++r) x.v[r] = c[(4 + r) * 32];
   x.kval[0] = (kv & 1u) != 0u;
   x.kval[1] = (kv & 2u) != 0u;
+  x.vsrc = slot_ptr;
+  x.vlim = 16;  // the copies zero-filled every V chunk that is not a token
 }
+
 
 // ---- the bulk-tensor path: per 16-token block two TMA copies (the K and the
 // V rows of this KV head, 16 x 128 bytes each, 128-byte swizzled) into the
@@ -269,17 +274,28 @@ __device__ __forceinline__ void read_block_tma(const uint8_t* slot, const AttnPa
     x.k[r][1] = *reinterpret_cast<const uint4*>(kt + swz(row, 4 + t));
     x.kval[r] = blk_ok && ib + row < end;
   }
-  if (blk_ok && ib + 16 <= end) {  // warp-uniform: a whole block of tokens
+  x.vsrc = slot;
+  x.vlim = blk_ok ? min(16, end - ib) : 0;
+  (void)vt;
+}
+
+// The lane's V chunks of a block (see KvBlock), from a per-lane ring slot
+// (kTma false: chunk r of lane L at (4 + r) * 32 + L) or a swizzled bulk-copy
+// slot (rows 2t, 2t+1, 2t+8, 2t+9, chunk g).
+template <bool kTma>
+__device__ __forceinline__ void read_v(const KvBlock& x, int lane, int g, int t, uint4 (&v)[4]) {
+  if (!kTma) {
+    const uint4* c = reinterpret_cast<const uint4*>(x.vsrc) + lane;
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
-      x.v[r] = *reinterpret_cast<const uint4*>(vt + swz(2 * t + (r & 1) + 8 * (r >> 1), g));
+    for (int r = 0; r < 4; ++r) v[r] = c[(4 + r) * 32];
     return;
   }
+  const uint8_t* vt = x.vsrc + kBlockBytes / 2;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int row = 2 * t + (r & 1) + 8 * (r >> 1);
-    const uint4 v = *reinterpret_cast<const uint4*>(vt + swz(row, g));
-    x.v[r] = (blk_ok && ib + row < end) ? v : make_uint4(0u, 0u, 0u, 0u);
+    v[r] = *reinterpret_cast<const uint4*>(vt + swz(row, g));
+    if (x.vlim < 16 && row >= x.vlim) v[r] = make_uint4(0u, 0u, 0u, 0u);  // warp-uniform test first
   }
 }
 
@@ -291,9 +307,9 @@ struct SoftmaxState {
 };
 
 // Scores, online softmax and output update for one block of 16 tokens.
-template <bool kPack>
+template <bool kPack, bool kTma>
 __device__ __forceinline__ void attend_block(const KvBlock& x, const uint32_t (&qf)[8][2], float cs, bool lo_lane,
-                                             SoftmaxState& st) {
+                                             int lane, int g, int t, SoftmaxState& st) {
   // scores S^T[token g / g+8][column 2t / 2t+1]: four independent
   // accumulator chains of two k-blocks each (a single chain of eight MMAs
   // would make the block wait for eight MMA latencies), summed after
@@ -309,6 +325,9 @@ __device__ __forceinline__ void attend_block(const KvBlock& x, const uint32_t (&
     cvt4(w1r, a1, a3);
     mma16816(sp[j & 3], a0, a1, a2, a3, qf[j][0], qf[j][1]);
   }
+  // V's codes, now that the score MMAs hold K
+  uint4 v[4];
+  read_v<kTma>(x, lane, g, t, v);
   float s[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) s[k] = (sp[0][k] + sp[1][k]) + (sp[2][k] + sp[3][k]);
@@ -372,8 +391,8 @@ __device__ __forceinline__ void attend_block(const KvBlock& x, const uint32_t (&
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
-    const uint32_t p01 = __byte_perm(word_of(x.v[0], i >> 1), word_of(x.v[1], i >> 1), sel);
-    const uint32_t p23 = __byte_perm(word_of(x.v[2], i >> 1), word_of(x.v[3], i >> 1), sel);
+    const uint32_t p01 = __byte_perm(word_of(v[0], i >> 1), word_of(v[1], i >> 1), sel);
+    const uint32_t p23 = __byte_perm(word_of(v[2], i >> 1), word_of(v[3], i >> 1), sel);
     uint32_t a0, a1, a2, a3;
     cvt4(p01, a0, a1);
     cvt4(p23, a2, a3);
@@ -554,7 +573,7 @@ __global__ void __launch_bounds__(kAttnThreads, W8A8_ATTN_MIN_CTAS)
       cp_async_wait<kRing - 1>();  // block i's group has landed
       read_block(ring + si * kBlockBytes, lane, (kvbits >> (2 * si)) & 3u, x);
     }
-    attend_block<kPack>(x, qf, cs, lo_lane, st);
+    attend_block<kPack, kTma>(x, qf, cs, lo_lane, lane, g, t, st);
   }
   if (kTma && !ok && lane == 0) {
     // a wait gave up (flagged in the device status): let the copies still in

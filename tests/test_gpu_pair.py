@@ -51,10 +51,12 @@ def test_pair_fp8_wide(bn, M, N, K):
     assert_fp8_close(out_to_f32(bits_np(out), oracle.BF16), ref["y"], f"pair {bn}")
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 256, 512), (300, 200, 2048), (1024, 768, 3072)])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 512), (300, 200, 2048), (1024, 768, 3072), (200, 512, 1040),
+                                   (520, 1040, 4112)])
 def test_pair_int8_block_n_256(M, N, K):
     """Three 1024-K chunks at K = 3072: the exact chunked accumulation drains
-    into the int32 total between chunks on both CTAs of the pair."""
+    into the int32 total between chunks on both CTAs of the pair.  K = 1040
+    and 4112 end in a partial 64-deep f16 block."""
     A, B, sa, sb = int8_problem(M, N, K, seed=M * 5 + N)
     acc = run_gpu(A, B, np.ones(M, np.float32), np.ones(N, np.float32), oracle.INT8, torch.int32,
                   config=pair(256))
