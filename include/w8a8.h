@@ -358,7 +358,11 @@ W8A8_API w8a8_status w8a8_requant_shards(const void* q, int q_dtype, int64_t col
  *   seq_lens      int32 [batch], clamped to [0, max_seq_len]
  *   k_scale, v_scale  fp32 [1]
  * head_dim must be 128 and G one of 1, 2, 4, 8.  The workspace holds the
- * per-chunk partial results (w8a8_fp8_kv_attention_workspace_size).  No
+ * per-chunk partial results (w8a8_fp8_kv_attention_workspace_size).  Its
+ * size is an upper bound on purpose: it assumes chunks of 64 tokens, the
+ * smallest the kernel picks, so one size serves every call with the same
+ * batch, heads and max_seq_len whatever the GPU (the kernel takes chunks of
+ * up to 512 tokens, and then uses an eighth of it).  No
  * allocation, no synchronisation; graph-capturable.  Errors: INVALID_ARG
  * (null pointer, sizes, head_dim, G), MISALIGNED (cache base not 16-byte
  * aligned), WORKSPACE (too small), CUDA (launch).  The workspace size is
