@@ -599,6 +599,12 @@ __device__ __forceinline__ void reduce_rows_dsmem_any(const MmParams& prm, const
 // Narrow tiles run two CTAs per SM (the dispatch sizes their shared memory
 // for that); cap their registers so that two fit (<= 168 per thread).
 __host__ __device__ constexpr int min_ctas_for(int bn, bool) { return bn <= 64 ? 2 : 1; }
+// int8 with one chunk accumulator (256 columns: the MMAs wait while a chunk
+// drains into the int32 total) adds four drain-helper warps (6..9), one per
+// TMEM lane quarter: each intermediate drain is split between the epilogue
+// warp and the helper of a quarter, half of the 16-column groups each.
+__host__ __device__ constexpr bool drain_helpers(int bn, bool int8) { return int8 && acc_bufs(bn, int8) == 1; }
+__host__ __device__ constexpr int threads_for(int bn, bool int8) { return drain_helpers(bn, int8) ? 320 : 192; }
 
 template <int BN, bool SWAP, bool INT8, typename OutT>
 __device__ __forceinline__ void reduce_rows_any(const MmParams& prm, const Unit& un, const uint32_t* tile0,
@@ -617,7 +623,7 @@ __device__ __forceinline__ void reduce_rows_any(const MmParams& prm, const Unit&
 }
 
 template <int BN, bool SWAP, bool INT8, typename OutT, bool FQ = false>
-__global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
+__global__ void __launch_bounds__(threads_for(BN, INT8), min_ctas_for(BN, INT8))
     w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_p,
                      const __grid_constant__ CUtensorMap tmap_q, const MmParams prm, int stages,
                      int group) {
@@ -708,8 +714,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
     mbar_init(drain_bar, 1);
     mbar_init(ufull_bar(0), 1);
     mbar_init(ufull_bar(1), 1);
-    mbar_init(uempty_bar(0), kEpiThreads);
-    mbar_init(uempty_bar(1), kEpiThreads);
+    // the epilogue threads (and the drain helpers) release an accumulator
+    mbar_init(uempty_bar(0), drain_helpers(BN, INT8) ? 2 * kEpiThreads : kEpiThreads);
+    mbar_init(uempty_bar(1), drain_helpers(BN, INT8) ? 2 * kEpiThreads : kEpiThreads);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -801,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // TMEM lane == tile row on the P side
@@ -888,8 +895,12 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
           // of a batch are in flight together (one wait per batch), so the
           // drain of a 1024-K chunk stays shorter than the next chunk's MMAs
           constexpr int kBatch = drain_batch(kGroups, min_ctas_for(BN, INT8) == 2 ? 2 : 4);  // register budget
+          // with drain helpers an intermediate drain covers the first half
+          // of the groups here (the helpers take the rest); the last chunk
+          // is drained and stored here in full
+          const int g_end = (drain_helpers(BN, INT8) && !last) ? kGroups / 2 : kGroups;
 #pragma unroll 1
-          for (int g0 = 0; g0 < kGroups; g0 += kBatch) {
+          for (int g0 = 0; g0 < g_end; g0 += kBatch) {
             uint32_t r[kBatch][16], t[kBatch][16];
 #pragma unroll
             for (int bb = 0; bb < kBatch; ++bb) {
@@ -966,6 +977,54 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
         }
       }
     }
+  } else if constexpr (drain_helpers(BN, INT8)) {
+    // ------------------------------------------------------ drain helpers
+    // Same units and chunks as the epilogue warps; every intermediate drain
+    // adds the second half of the chunk's columns into the int32 total.  On
+    // the last chunk they only release the accumulator (the epilogue warps
+    // read the whole total and store).
+    const int quarter = warp & 3;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    constexpr int kBufs = acc_bufs(BN, INT8);
+    constexpr int kBatch = drain_batch(kGroups, 4);
+    uint32_t u = 0;
+    bool ok = true;
+    for (int w = w_first; w < units && ok; w += w_step) {
+      const Unit un = unit_of(w, prm, group, BN);
+      const int chunk = prm.kchunk_kb;
+      const int nch = (un.nkb + chunk - 1) / chunk;
+      for (int c = 0; c < nch; ++c, ++u) {
+        const int b = static_cast<int>(u % kBufs);
+        if (!mbar_wait(ufull_bar(b), (u / kBufs) & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (c < nch - 1) {
+          const uint32_t acc_addr = lane_base + static_cast<uint32_t>(b * BN);
+          const uint32_t tot_addr = lane_base + static_cast<uint32_t>(kBufs * BN);
+#pragma unroll 1
+          for (int g0 = kGroups / 2; g0 < kGroups; g0 += kBatch) {
+            uint32_t r[kBatch][16], t[kBatch][16];
+#pragma unroll
+            for (int bb = 0; bb < kBatch; ++bb) {
+              tmem_ld16(acc_addr + (g0 + bb) * 16, r[bb]);
+              if (c > 0) tmem_ld16(tot_addr + (g0 + bb) * 16, t[bb]);
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int bb = 0; bb < kBatch; ++bb) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int prev = (c > 0) ? static_cast<int>(t[bb][j]) : 0;
+                t[bb][j] = static_cast<uint32_t>(prev + __float2int_rn(__uint_as_float(r[bb][j])));
+              }
+              tmem_st16(tot_addr + (g0 + bb) * 16, t[bb]);
+            }
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(uempty_bar(b));
+      }
+    }
   }
 
   if (warp == 1 && lane == 0) trace_stamp(prm, T_MMA_ISSUED);
@@ -979,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BN, INT8))
     // waits for another after this point.
     cluster_sync();
     if (threadIdx.x == 2 * 32) trace_stamp(prm, T_SYNCED);
-    if (warp >= 2) {
+    if (warp >= 2 && warp < 6) {
       const int et = threadIdx.x - 2 * 32;
       const Unit un = unit_of(w_first, prm, group, BN);
       const int S = prm.splits;
@@ -1051,8 +1110,9 @@ cudaError_t launch_one(const CUtensorMap& tp, const CUtensorMap& tq, const MmPar
   const int per_cta_smem = smem + fixed;
   const int regs_per_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
   int occ = smem_sm / per_cta_smem;
-  occ = min(occ, 65536 / (regs_per_warp * (kThreads / 32)));
-  occ = min(occ, 2048 / kThreads);
+  constexpr int kCtaThreads = threads_for(BN, INT8);
+  occ = min(occ, 65536 / (regs_per_warp * (kCtaThreads / 32)));
+  occ = min(occ, 2048 / kCtaThreads);
   occ = max(1, min(occ, 512 / tmem_cols_for(BN, INT8)));
   if (p.max_ctas_per_sm > 0) occ = min(occ, p.max_ctas_per_sm);
   const int units = p.tiles_p * p.tiles_q * p.splits;
@@ -1074,7 +1134,7 @@ cudaError_t launch_one(const CUtensorMap& tp, const CUtensorMap& tq, const MmPar
   const int group = SWAP ? 1 : static_cast<int>(g_tiles);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kCtaThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
