@@ -37,7 +37,11 @@ namespace w8a8 {
 
 namespace {
 
-constexpr int kPairThreads = 192;
+// int8 with one chunk accumulator per CTA (256 columns) adds four
+// drain-helper warps (6..9), one per TMEM lane quarter, that take half of
+// each intermediate drain (as in the one-CTA kernel)
+__host__ __device__ constexpr bool pair_drain_helpers(int bn, bool int8) { return int8 && acc_bufs(bn, int8) == 1; }
+__host__ __device__ constexpr int pair_threads(int bn, bool int8) { return pair_drain_helpers(bn, int8) ? 320 : 192; }
 
 // --- pair forms of the tcgen05 / TMA instructions (cta_group::2)
 
@@ -92,7 +96,7 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
 constexpr int kPairTileP = 2 * kTileP;  // 256 rows of A per pair tile
 
 template <int BN, bool INT8, typename OutT>
-__global__ void __launch_bounds__(kPairThreads, 1)
+__global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
     w8a8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                           const MmParams prm, int stages, int group) {
   constexpr int kHalfN = BN / 2;                        // B rows (output columns) per CTA
@@ -140,8 +144,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
     mbar_init(ufull_bar(0), 1);
     mbar_init(ufull_bar(1), 1);
-    mbar_init(uempty_bar(0), 2 * kEpiThreads);  // both CTAs' epilogue threads (leader's copy)
-    mbar_init(uempty_bar(1), 2 * kEpiThreads);
+    // both CTAs' epilogue threads (and drain helpers) release an accumulator
+    // (the leader's copy)
+    constexpr uint32_t kReleasers = (pair_drain_helpers(BN, INT8) ? 4 : 2) * kEpiThreads;
+    mbar_init(uempty_bar(0), kReleasers);
+    mbar_init(uempty_bar(1), kReleasers);
     mbar_init(drain_bar, 1);
     fence_barrier_init();
   }
@@ -225,7 +232,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
@@ -255,8 +262,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const uint32_t tot_addr = lane_base + static_cast<uint32_t>(kBufs * BN);
         if (INT8) {
           constexpr int kBatch = drain_batch(kGroups, 4);
+          // with drain helpers an intermediate drain covers the first half
+          // of the groups here; the last chunk is drained and stored here
+          const int g_end = (pair_drain_helpers(BN, INT8) && !last) ? kGroups / 2 : kGroups;
 #pragma unroll 1
-          for (int g0 = 0; g0 < kGroups; g0 += kBatch) {
+          for (int g0 = 0; g0 < g_end; g0 += kBatch) {
             uint32_t r[kBatch][16], t[kBatch][16];
 #pragma unroll
             for (int bb = 0; bb < kBatch; ++bb) {
@@ -300,6 +310,50 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         mbar_arrive_remote(uempty0 + static_cast<uint32_t>(b) * 8u);
       }
     }
+  } else if constexpr (pair_drain_helpers(BN, INT8)) {
+    // ------------------------------------------------------ drain helpers
+    // The epilogue's chunk sequence; each intermediate drain adds the second
+    // half of the columns into the int32 total, the last chunk only releases.
+    const int quarter = warp & 3;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    constexpr int kBatch = drain_batch(kGroups, 4);
+    uint32_t c_all = 0;
+    bool ok = true;
+    for (int u = pair; u < units && ok; u += npairs) {
+      const int chunk = prm.kchunk_kb;
+      const int nch = (prm.num_kb + chunk - 1) / chunk;
+      for (int c = 0; c < nch; ++c, ++c_all) {
+        const int b = static_cast<int>(c_all % kBufs);
+        if (!mbar_wait(ufull_bar(b), (c_all / kBufs) & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (c < nch - 1) {
+          const uint32_t acc_addr = lane_base + static_cast<uint32_t>(b * BN);
+          const uint32_t tot_addr = lane_base + static_cast<uint32_t>(kBufs * BN);
+#pragma unroll 1
+          for (int g0 = kGroups / 2; g0 < kGroups; g0 += kBatch) {
+            uint32_t r[kBatch][16], t[kBatch][16];
+#pragma unroll
+            for (int bb = 0; bb < kBatch; ++bb) {
+              tmem_ld16(acc_addr + (g0 + bb) * 16, r[bb]);
+              if (c > 0) tmem_ld16(tot_addr + (g0 + bb) * 16, t[bb]);
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int bb = 0; bb < kBatch; ++bb) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int prev = (c > 0) ? static_cast<int>(t[bb][j]) : 0;
+                t[bb][j] = static_cast<uint32_t>(prev + __float2int_rn(__uint_as_float(r[bb][j])));
+              }
+              tmem_st16(tot_addr + (g0 + bb) * 16, t[bb]);
+            }
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive_remote(uempty0 + static_cast<uint32_t>(b) * 8u);
+      }
+    }
   }
 
   tc_fence_before();
@@ -330,7 +384,7 @@ cudaError_t launch_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, const Mm
   if (g_tiles < 1) g_tiles = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * npairs);
-  cfg.blockDim = dim3(kPairThreads);
+  cfg.blockDim = dim3(pair_threads(BN, INT8));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
