@@ -742,6 +742,12 @@ __global__ void __launch_bounds__(threads_for(BN, INT8), min_ctas_for(BN, INT8))
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
+      // The token tiles are reused by every weight tile (of a
+      // rasterisation group) while the weights stream past once: keep the
+      // former in L2 ahead of the latter.  Tokens are the P side without
+      // swap, the Q side with it.
+      const uint64_t pol_p = SWAP ? policy_evict_first() : policy_evict_last();
+      const uint64_t pol_q = SWAP ? policy_evict_last() : policy_evict_first();
       for (int w = w_first; w < units && ok; w += w_step) {
         const Unit un = unit_of(w, prm, group, BN);
         for (int i = 0; i < un.nkb; ++i, ++it) {
@@ -750,8 +756,8 @@ __global__ void __launch_bounds__(threads_for(BN, INT8), min_ctas_for(BN, INT8))
           if (!mbar_wait(empty_bar(s), ph ^ 1)) { ok = false; break; }
           mbar_arrive_expect_tx(full_bar(s), FQ ? kPBytes : kStageBytes);
           const int kx = (un.kb_begin + i) * kKbElems;
-          tma_load_2d(smem_addr(sp + s * kPBytes), &tmap_p, full_bar(s), kx, un.p0);
-          if (!FQ) tma_load_2d(smem_addr(sq + s * kQBytes), &tmap_q, full_bar(s), kx, un.q0);
+          tma_load_2d_hint(smem_addr(sp + s * kPBytes), &tmap_p, full_bar(s), kx, un.p0, pol_p);
+          if (!FQ) tma_load_2d_hint(smem_addr(sq + s * kQBytes), &tmap_q, full_bar(s), kx, un.q0, pol_q);
         }
       }
       if (!ok) {
