@@ -83,13 +83,14 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
 }
 
 // 2-D tiled load into this CTA's shared memory, completing on an mbarrier of
-// either CTA of the pair (a shared::cluster address).
+// either CTA of the pair (a shared::cluster address), with an L2 cache
+// policy.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int32_t x,
-                                                 int32_t y) {
+                                                 int32_t y, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
 
@@ -172,6 +173,10 @@ __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
+      // token slabs are reused across the weight tiles of a group: kept in
+      // L2 ahead of the weights, which stream past once
+      const uint64_t pol_a = policy_evict_last();
+      const uint64_t pol_b = policy_evict_first();
       for (int u = pair; u < units && ok; u += npairs) {
         int tp, tq;
         tile_coords(u, prm.tiles_p, prm.tiles_q, group, tp, tq);
@@ -184,8 +189,8 @@ __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
           if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * kStageBytes);
           const uint32_t fb = full0 + static_cast<uint32_t>(s) * 8u;
           const int kx = i * kKbElems;
-          tma_load_2d_pair(smem_addr(sa + s * kPBytes), &tmap_a, fb, kx, a_row);
-          tma_load_2d_pair(smem_addr(sb + s * kQBytes), &tmap_b, fb, kx, b_row);
+          tma_load_2d_pair(smem_addr(sa + s * kPBytes), &tmap_a, fb, kx, a_row, pol_a);
+          tma_load_2d_pair(smem_addr(sb + s * kQBytes), &tmap_b, fb, kx, b_row, pol_b);
         }
       }
       if (!ok && leader) {
