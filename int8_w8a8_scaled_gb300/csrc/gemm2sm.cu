@@ -162,6 +162,17 @@ __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Request the first weight blocks of this CTA's first tile into L2 before
+  // waiting on the preceding kernel (a prefetch only reads coherent global
+  // memory, whatever that kernel writes), so the weight stream starts while
+  // it finishes.
+  if (threadIdx.x == 0 && pair < units) {
+    int tp, tq;
+    tile_coords(pair, prm.tiles_p, prm.tiles_q, group, tp, tq);
+    const int b_row = tq * BN + static_cast<int>(rank) * kHalfN;
+    const int n_pf = min(prm.num_kb, prm.prefetch_kb);
+    for (int i = 0; i < n_pf; ++i) tma_prefetch_l2_2d(&tmap_b, i * kKbElems, b_row);
+  }
   griddep_launch();
   griddep_wait();
 
