@@ -253,8 +253,11 @@ __device__ __forceinline__ void tma_issue_block(const AttnParams& p, const CUten
     return;
   }
   mbar_arrive_expect_tx(bar, kBlockBytes);
-  tma_load_2d(dst, mk, bar, kvh * kHeadDim, static_cast<int32_t>(row));
-  tma_load_2d(dst + kBlockBytes / 2, mv, bar, kvh * kHeadDim, static_cast<int32_t>(row));
+  // the cache is read once per call: ahead of it in L2 go the queries and
+  // the partial results
+  const uint64_t pol = policy_evict_first();
+  tma_load_2d_hint(dst, mk, bar, kvh * kHeadDim, static_cast<int32_t>(row), pol);
+  tma_load_2d_hint(dst + kBlockBytes / 2, mv, bar, kvh * kHeadDim, static_cast<int32_t>(row), pol);
 }
 
 __device__ __forceinline__ uint32_t swz(int r, int c) { return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4)); }
