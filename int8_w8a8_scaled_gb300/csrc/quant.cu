@@ -511,7 +511,10 @@ struct QzRing {
     if (c >= nchunks) return false;
     const int slot = i % kQzStages;
     mbar_arrive_expect_tx(smem_addr(&bar[slot]), elems(c) * 2);
-    bulk_load(smem_addr(buf[slot]), x + phys(c) * kQzChunk, elems(c) * 2, smem_addr(&bar[slot]));
+    // the absmax pass keeps what it reads in L2 for the convert pass, which
+    // walks the tensor back to front and reads it for the last time
+    bulk_load_hint(smem_addr(buf[slot]), x + phys(c) * kQzChunk, elems(c) * 2, smem_addr(&bar[slot]),
+                   reverse ? policy_evict_first() : policy_evict_last());
     return true;
   }
   // thread 0, after a failed wait at chunk i: let the loads still in flight
@@ -670,7 +673,9 @@ __global__ void __launch_bounds__(256)
     const long long c0 = blockIdx.x;
     if (c0 < nchunks) {
       mbar_arrive_expect_tx(smem_addr(&bar[0]), chunk_bytes(c0));
-      bulk_load(smem_addr(in_buf[0]), q + c0 * kDqChunk, chunk_bytes(c0), smem_addr(&bar[0]));
+      // codes are read once: behind everything else in L2
+      bulk_load_hint(smem_addr(in_buf[0]), q + c0 * kDqChunk, chunk_bytes(c0), smem_addr(&bar[0]),
+                     policy_evict_first());
     }
   }
   __syncthreads();
@@ -684,7 +689,8 @@ __global__ void __launch_bounds__(256)
       next_issued = next < nchunks;
       if (next_issued) {  // in_buf[b ^ 1] was consumed last iteration
         mbar_arrive_expect_tx(smem_addr(&bar[b ^ 1]), chunk_bytes(next));
-        bulk_load(smem_addr(in_buf[b ^ 1]), q + next * kDqChunk, chunk_bytes(next), smem_addr(&bar[b ^ 1]));
+        bulk_load_hint(smem_addr(in_buf[b ^ 1]), q + next * kDqChunk, chunk_bytes(next), smem_addr(&bar[b ^ 1]),
+                       policy_evict_first());
       }
       bulk_wait_read<1>();  // the store two chunks back has read out_buf[b]
     }
