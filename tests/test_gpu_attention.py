@@ -267,3 +267,29 @@ def test_argument_errors():
     kc64 = torch.zeros(2, 16, 4, 64, dtype=torch.uint8, device=dev)
     with pytest.raises(w8.W8A8Error):    # head_dim 64
         w8.fp8_kv_decode_attention(q64, kc64, kc64, lens, sc, sc, torch.empty_like(q64))
+
+
+def test_workspace_shared_across_shapes():
+    """One workspace serves calls of any shape in turn (it holds only each
+    call's own partial results): every call gives the bits of a call with a
+    fresh workspace."""
+    torch.manual_seed(0)
+    shapes = [(4, 32, 8, 1000), (2, 8, 2, 3000), (6, 16, 4, 700), (4, 32, 8, 1000)]
+    ws = w8.Workspace(max(w8.attention_workspace_size(B, Hq, T) for B, Hq, _, T in shapes))
+    for i, (B, Hq, Hkv, T) in enumerate(shapes):
+        g = torch.Generator(device="cuda")
+        g.manual_seed(100 + i)
+        kc = torch.randint(0, 126, (B, T, Hkv, 128), generator=g, device="cuda", dtype=torch.uint8)
+        vc = torch.randint(0, 126, (B, T, Hkv, 128), generator=g, device="cuda", dtype=torch.uint8)
+        q = torch.randn(B, Hq, 128, generator=g, device="cuda").to(torch.bfloat16)
+        lens = torch.randint(1, T + 1, (B,), generator=g, device="cuda", dtype=torch.int32)
+        sc = torch.full((1,), 0.05, device="cuda")
+        out = torch.empty(B, Hq, 128, dtype=torch.bfloat16, device="cuda")
+        ref = torch.empty_like(out)
+        w8.fp8_kv_decode_attention(q, kc, vc, lens, sc, sc, out, workspace=ws)
+        w8.fp8_kv_decode_attention(q, kc, vc, lens, sc, sc, ref,
+                                   workspace=w8.Workspace(w8.attention_workspace_size(B, Hq, T)))
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), (B, Hq, Hkv, T)
+    assert w8.device_status() == 0
+
