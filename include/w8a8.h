@@ -266,9 +266,14 @@ W8A8_API w8a8_status w8a8_quant_scaled_mm(const void* x, int x_dtype, int64_t ld
  *                                else the global one.
  *  cta_pair  1: tiles of 256 token rows computed by a pair of CTAs on two SMs
  *            with one tcgen05 MMA stream (cta_group::2): each CTA stages its
- *            128 rows of A and half of the block_n columns of B (swap_ab 0,
- *            split_k 1; block_n 64, 96, 128, 192, 224 or 256 for e4m3, 128
- *            or 256 for int8); 0: one CTA per 128-row tile.
+ *            128 rows of A and half of the block_n columns of B (swap_ab 0;
+ *            block_n 64, 96, 128, 192, 224 or 256 for e4m3, 128 or 256 for
+ *            int8); 0: one CTA per 128-row tile.  With pairs split_k is 1,
+ *            or 2 (e4m3): when the tiles leave a last round that keeps at
+ *            most half of the pairs (one per two SMs) busy, each tile of
+ *            that round is computed as two K halves on two pairs, whose fp32
+ *            partial tiles go through the workspace and are summed in half
+ *            order (deterministic) by the second to finish.
  * Fields set to 0 (except swap_ab and cta_pair) mean "choose automatically". */
 #define W8A8_REDUCE_AUTO 0
 #define W8A8_REDUCE_GLOBAL 1
@@ -393,10 +398,12 @@ W8A8_API w8a8_status w8a8_fp8_kv_decode_attention(
  * loads the library holds it until the process exits.  Nothing is allocated
  * or freed by the call, not even through a library routine.
  *
- *  - Problems whose scratch need (w8a8_scaled_mm_workspace_size) exceeds the
- *    array are rejected with W8A8_ERR_WORKSPACE and a message; in practice
- *    this covers e4m3 at every size (large M needs no scratch) and int8 only
- *    where its widened operand planes fit.
+ *  - It runs the configuration w8a8_scaled_mm_pick_config() gives, except
+ *    that CTA-pair tiles whose last-round K halves (split_k 2) need more
+ *    scratch than the array holds run whole (split_k 1).  Problems whose
+ *    scratch need still exceeds the array are rejected with
+ *    W8A8_ERR_WORKSPACE and a message; in practice this covers e4m3 at
+ *    every size and int8 only where its widened operand planes fit.
  *  - The array is shared by every call on a device and keeps the previous
  *    call's contents.  A call that uses split-K arrival counters clears
  *    them first (an asynchronous memset of those counters on `stream`);

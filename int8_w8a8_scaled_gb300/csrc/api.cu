@@ -124,6 +124,32 @@ w8a8_status make_operand_map(CUtensorMap* map, const void* base, bool f16, long 
 
 // ------------------------------------------------------------------ GEMM configuration
 
+// SM count of the current device; without a usable device (host-only size
+// queries) a GB300's 152.
+int sms_or_default() {
+  int sms = 152;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
+    else cudaGetLastError();
+  } else {
+    cudaGetLastError();
+  }
+  return sms;
+}
+
+// CTA-pair tiles with split_k 2: the tiles of the last, partial round of
+// pairs are split into two K halves when that round would otherwise keep at
+// most half of the pairs busy -- the halves then fill at most all of them and
+// the round takes about half as long (e4m3; at least two K blocks).
+int pair_tail_tiles(long long tiles, int kb, int sms, int split_k, int q_dtype) {
+  if (split_k != 2 || q_dtype != W8A8_E4M3 || kb < 2) return 0;
+  const long long pairs = pair_grid_pairs(tiles, sms);
+  const long long rem = tiles % pairs;
+  return (rem > 0 && 2 * rem <= pairs) ? static_cast<int>(rem) : 0;
+}
+
 constexpr int kSmemTwoPerSm = 113 * 1024;   // budget that lets two CTAs share an SM
 constexpr int kInt8ChunkK = 1024;           // exact fp32 accumulation bound: 1024 * 128 * 128 = 2^24
 constexpr long long kFusedRowsMaxBytes = 32768;  // one-kernel quant_scaled_mm: rows staged in shared memory
@@ -226,26 +252,38 @@ void auto_config(long long M, long long N, long long K, int q_dtype, int sms, w8
   // Large-M e4m3: 256 x block_n tiles on CTA pairs (each SM stages half of
   // B).  Measured at M = 4096 on the Llama-3-8B projections: 2438 / 2368 /
   // 3094 / 2751 TFLOP/s (QKV / O / gate-up / down) against 2326 / 2227 /
-  // 2837 / 2599 on one-CTA tiles.  block_n from the same wave-balance model
-  // over the pairs (sms / 2 of them).  int8 stays on one-CTA tiles: its
-  // chunk drains stall both CTAs of a pair (942-979 against 949-1003).
+  // 2837 / 2599 on one-CTA tiles.  int8 stays on one-CTA tiles: its chunk
+  // drains stall both CTAs of a pair (942-979 against 949-1003).
+  // block_n: a round of pair tiles takes the same time at 192-256 columns
+  // (its stages are bound by the operand round trip, not by the MMA width:
+  // 256 and 224 columns measured 84.6 / 84.4 us for QKV, 58.0 / 58.0 O,
+  // 174.8 / 174.4 down, all in six, four and four rounds), so the model
+  // counts rounds; a last round that keeps at most half of the pairs busy
+  // runs as K halves (split_k 2) and costs half a round plus the exchange
+  // of the halves, measured at about 8 us, 20 K blocks' worth (so only long
+  // K gains: the down projection 166.6 against 174.4-176.5 us; QKV and O
+  // at K = 4096 measured even, 84.7 / 59.8 against 84.8 / 59.6).
   if (!c->swap_ab && q_dtype == W8A8_E4M3 && M >= kPairMinM) {
     const int cands[3] = {256, 224, 192};
-    const long long pairs = std::max(1, sms / 2);
     double best = 1e30;
     for (int i = 0; i < 3; ++i) {
       const int bn = cands[i];
-      const long long units = ceil_div(M, 256) * ceil_div(N, bn);
-      const long long waves = (units + pairs - 1) / pairs;
-      const double t = static_cast<double>(waves) * bn * (1.0 + 0.03 * i) /
-                       static_cast<double>(std::min<long long>(N, ceil_div(N, bn) * bn));
-      if (t < best - 1e-12) {
+      const long long tiles = ceil_div(M, 256) * ceil_div(N, bn);
+      const long long pairs = pair_grid_pairs(tiles, sms);
+      const long long full = tiles / pairs;
+      const long long rem = tiles % pairs;
+      const bool halves = pair_tail_tiles(tiles, kb, sms, 2, q_dtype) > 0 && 0.5 + 20.0 / kb < 1.0;
+      // equal rounds: the narrower tile (less padding work, measured 84.8 /
+      // 59.6 us at 224 against 85.7 / 59.9 at 256 for QKV / O)
+      const double t =
+          static_cast<double>(full) + (rem == 0 ? 0.0 : halves ? 0.5 + 20.0 / kb : 1.0) + 1e-3 * bn / 256;
+      if (t < best - 1e-9) {
         best = t;
         c->block_n = bn;
+        c->split_k = halves ? 2 : 1;
       }
     }
     c->cta_pair = 1;
-    c->split_k = 1;
     return;
   }
   const long long tiles = c->swap_ab ? ceil_div(N, 128) * ceil_div(M, c->block_n)
@@ -268,7 +306,8 @@ int auto_pair_stages(int block_n, int smem_optin) {
 struct Plan {
   w8a8_mm_config cfg;
   int kb, kb_per_split, splits, tiles_p, tiles_q, stages;
-  bool cluster;  // split slices reduce through distributed shared memory
+  bool cluster;    // split slices reduce through distributed shared memory
+  int tail_tiles;  // CTA-pair tiles of the last round run as two K halves
   size_t off_counters, off_partial, off_a16, off_b16, total;
 };
 
@@ -280,7 +319,8 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // workspace stays valid across calls of any shape and configuration (scratch
 // data -- split-K partials, int8 f16 planes -- always lives after the region).
 
-Plan make_plan(long long M, long long N, long long K, int q_dtype, const w8a8_mm_config& cfg, int smem_optin) {
+Plan make_plan(long long M, long long N, long long K, int q_dtype, const w8a8_mm_config& cfg, int smem_optin,
+               int sms) {
   Plan p{};
   p.cfg = cfg;
   p.kb = num_kb(K, q_dtype);
@@ -288,7 +328,8 @@ Plan make_plan(long long M, long long N, long long K, int q_dtype, const w8a8_mm
   const long long Q = cfg.swap_ab ? M : N;
   p.tiles_p = static_cast<int>(ceil_div(P, cfg.cta_pair ? 256 : 128));
   p.tiles_q = static_cast<int>(ceil_div(Q, cfg.block_n));
-  int sp = std::max(1, std::min(cfg.split_k, p.kb));
+  // CTA pairs take split_k only as the last round's K halves
+  int sp = cfg.cta_pair ? 1 : std::max(1, std::min(cfg.split_k, p.kb));
   p.kb_per_split = static_cast<int>(ceil_div(p.kb, sp));
   p.splits = static_cast<int>(ceil_div(p.kb, p.kb_per_split));  // every slice non-empty
   p.stages = cfg.stages > 0 ? cfg.stages
@@ -296,12 +337,18 @@ Plan make_plan(long long M, long long N, long long K, int q_dtype, const w8a8_mm
                                             : auto_stages(cfg.block_n, q_dtype, smem_optin));
   p.cluster = p.splits > 1 && cfg.reduce != W8A8_REDUCE_GLOBAL && p.splits <= kMaxClusterSplit;
   const size_t tiles = static_cast<size_t>(p.tiles_p) * p.tiles_q;
-  const bool need_ws = p.splits > 1 || q_dtype == W8A8_INT8;
+  p.tail_tiles = cfg.cta_pair ? pair_tail_tiles(static_cast<long long>(tiles), p.kb, sms, cfg.split_k, q_dtype) : 0;
+  const bool need_ws = p.splits > 1 || p.tail_tiles > 0 || q_dtype == W8A8_INT8;
   size_t off = need_ws ? kCounterRegion : 0;
   p.off_counters = 0;
   if (p.splits > 1) {
     p.off_partial = off;
     off = align256(off + tiles * p.splits * 128 * cfg.block_n * sizeof(float));
+  }
+  if (p.tail_tiles > 0) {
+    // [tail][half][rank] partial tiles of 128 x block_n fp32
+    p.off_partial = off;
+    off = align256(off + static_cast<size_t>(p.tail_tiles) * 4 * 128 * cfg.block_n * sizeof(float));
   }
   if (q_dtype == W8A8_INT8) {
     p.off_a16 = off;
@@ -334,8 +381,9 @@ w8a8_status validate_config(const w8a8_mm_config& c, int q_dtype, int smem_optin
     return fail(W8A8_ERR_UNSUPPORTED, "the cluster reduction takes split_k <= %d", kMaxClusterSplit);
   if (c.cta_pair != 0 && c.cta_pair != 1) return fail(W8A8_ERR_UNSUPPORTED, "cta_pair must be 0 or 1");
   if (c.cta_pair) {
-    if (c.swap_ab || c.split_k != 1)
-      return fail(W8A8_ERR_UNSUPPORTED, "CTA-pair tiles take swap_ab = 0 and split_k = 1");
+    if (c.swap_ab || c.split_k < 1 || c.split_k > (q_dtype == W8A8_E4M3 ? 2 : 1))
+      return fail(W8A8_ERR_UNSUPPORTED,
+                  "CTA-pair tiles take swap_ab = 0 and split_k = 1 (e4m3: or 2, the last round's tiles in K halves)");
     const bool bn_ok = q_dtype == W8A8_INT8 ? (c.block_n == 128 || c.block_n == 256)
                                             : (c.block_n == 64 || c.block_n == 96 || c.block_n == 128 ||
                                                c.block_n == 192 || c.block_n == 224 || c.block_n == 256);
@@ -439,14 +487,15 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
     w8a8_mm_config a;
     auto_config(M, N, K, q_dtype, dev.sms, &a);
     if (cfg.block_n == 0) cfg.block_n = a.block_n;
-    if (cfg.split_k == 0) cfg.split_k = cfg.cta_pair ? 1 : a.split_k;
+    if (cfg.split_k == 0)
+      cfg.split_k = cfg.cta_pair ? (a.cta_pair && a.block_n == cfg.block_n ? a.split_k : 1) : a.split_k;
   } else {
     auto_config(M, N, K, q_dtype, dev.sms, &cfg);
   }
   if ((st = validate_config(cfg, q_dtype, dev.smem_optin)) != W8A8_OK) return st;
   if (fa && !fused_quant_ok(cfg, M, K, q_dtype))
     return fail(W8A8_ERR_UNSUPPORTED, "this configuration cannot quantise the activations inside the matmul");
-  const Plan plan = make_plan(M, N, K, q_dtype, cfg, dev.smem_optin);
+  const Plan plan = make_plan(M, N, K, q_dtype, cfg, dev.smem_optin, dev.sms);
   if (plan.splits > 1 && !plan.cluster && static_cast<size_t>(plan.tiles_p) * plan.tiles_q > kCounterSlots)
     return fail(W8A8_ERR_UNSUPPORTED, "split_k > 1 supports at most %zu output tiles (got %d)", kCounterSlots,
                 plan.tiles_p * plan.tiles_q);
@@ -509,6 +558,12 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
   prm.counters = plan.splits > 1 && !plan.cluster ? reinterpret_cast<unsigned*>(wsb + plan.off_counters) : nullptr;
   prm.kchunk_kb = kInt8ChunkK / 64;
   prm.num_sms = dev.sms;
+  if (plan.tail_tiles > 0) {
+    prm.tail_tiles = plan.tail_tiles;
+    prm.tail_kb_half = plan.kb / 2;
+    prm.partial = reinterpret_cast<float*>(wsb + plan.off_partial);
+    prm.counters = reinterpret_cast<unsigned*>(wsb + plan.off_counters);
+  }
   prm.pdl = 1;
   // up to 256 KB of each CTA's first weight slice (16 KB per K block of 128
   // weight rows)
@@ -554,12 +609,11 @@ w8a8_status run_mm(const void* a_q, long long lda, const void* b_q, long long ld
 
 void w8a8::set_last_error(const char* msg) { t_last_error = msg ? msg : ""; }
 
-size_t w8a8::mm_counter_bytes(long long M, long long N, long long K, int q_dtype) {
+size_t w8a8::mm_counter_bytes(long long M, long long N, long long K, int q_dtype, const w8a8_mm_config& cfg) {
   DeviceInfo dev;
   if (device_info(&dev) != W8A8_OK) return kCounterRegion;  // unknown: the whole region
-  w8a8_mm_config cfg;
-  auto_config(M, N, K, q_dtype, dev.sms, &cfg);
-  const Plan plan = make_plan(M, N, K, q_dtype, cfg, dev.smem_optin);
+  const Plan plan = make_plan(M, N, K, q_dtype, cfg, dev.smem_optin, dev.sms);
+  if (plan.tail_tiles > 0) return static_cast<size_t>(plan.tail_tiles) * 2 * sizeof(unsigned);
   if (plan.splits <= 1 || plan.cluster) return 0;
   return std::min(kCounterRegion, static_cast<size_t>(plan.tiles_p) * plan.tiles_q * sizeof(unsigned));
 }
@@ -653,15 +707,7 @@ w8a8_status w8a8_scaled_mm_pick_config(int64_t M, int64_t N, int64_t K, int q_dt
   if (!cfg) return fail(W8A8_ERR_INVALID_ARG, "cfg is null");
   if (M < 1 || N < 1 || K < 1) return fail(W8A8_ERR_INVALID_ARG, "M, N, K must be >= 1");
   if (q_dtype != W8A8_E4M3 && q_dtype != W8A8_INT8) return fail(W8A8_ERR_INVALID_ARG, "bad q_dtype");
-  int sms = 148;
-  int dev = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess) {
-    int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
-  } else {
-    cudaGetLastError();
-  }
-  auto_config(M, N, K, q_dtype, sms, cfg);
+  auto_config(M, N, K, q_dtype, sms_or_default(), cfg);
   return ok();
 }
 
@@ -673,10 +719,11 @@ size_t w8a8_scaled_mm_config_workspace_size(int64_t M, int64_t N, int64_t K, int
     w8a8_mm_config a;
     w8a8_scaled_mm_pick_config(M, N, K, q_dtype, &a);
     if (c.block_n == 0) c.block_n = a.block_n;
-    if (c.split_k == 0) c.split_k = c.cta_pair ? 1 : a.split_k;
+    if (c.split_k == 0)
+      c.split_k = c.cta_pair ? (a.cta_pair && a.block_n == c.block_n ? a.split_k : 1) : a.split_k;
   }
   if (c.split_k < 1) c.split_k = 1;
-  return make_plan(M, N, K, q_dtype, c, 227 * 1024).total;
+  return make_plan(M, N, K, q_dtype, c, 227 * 1024, sms_or_default()).total;
 }
 
 size_t w8a8_scaled_mm_workspace_size(int64_t M, int64_t N, int64_t K, int q_dtype) {

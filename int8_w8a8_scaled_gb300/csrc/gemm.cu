@@ -99,37 +99,6 @@ __device__ __forceinline__ void store4(const MmParams& prm, int p, int q, int nv
   }
 }
 
-// store4 with the scales already in registers: s_p for P row p, s_q[j] for
-// Q column q + j.  The product order stays (acc * scale_a) * scale_b.
-template <bool SWAP, typename OutT, typename V>
-__device__ __forceinline__ void store4s(const MmParams& prm, int p, int q, int nvalid, const V (&v)[4], float s_p,
-                                        const float (&s_q)[4]) {
-  OutT* out = reinterpret_cast<OutT*>(prm.out);
-  if (p >= (SWAP ? prm.N : prm.M)) return;
-  if (!SWAP && nvalid >= 4 && prm.out_vec_ok) {
-    // four consecutive outputs of one row in one store (q is a multiple of
-    // 4 and the rows are 16-byte aligned)
-    alignas(16) OutT o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) o[j] = OutConv<OutT>::conv(v[j], s_p, s_q[j]);
-    OutT* dst = out + static_cast<long long>(p) * prm.ldc + q;
-    if (sizeof(OutT) == 2)
-      *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(o);
-    else
-      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
-    return;
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if (j < nvalid) {
-      if (!SWAP)
-        out[static_cast<long long>(p) * prm.ldc + q + j] = OutConv<OutT>::conv(v[j], s_p, s_q[j]);
-      else
-        out[static_cast<long long>(q + j) * prm.ldc + p] = OutConv<OutT>::conv(v[j], s_q[j], s_p);
-    }
-  }
-}
-
 // One work unit is a (K slice, output tile) pair; the persistent CTAs walk
 // the units round-robin.  Units are numbered slice-major so that the slices
 // of a tile are spread over different CTAs.

@@ -26,6 +26,13 @@
 // Every wait is bounded (as in gemm.cu); a CTA whose wait gave up still meets
 // its peer at the final cluster barrier, after the copies and MMAs it may
 // have in flight have landed.
+//
+// The pairs walk the tiles round-robin, so a tile count just above a multiple
+// of the pair count leaves a last round in which few pairs work for a whole
+// tile's time.  With MmParams::tail_tiles > 0 (e4m3) the tiles of that round
+// run as two K halves on two pairs each: every CTA writes its fp32 half to
+// the workspace and the second half to arrive sums the two, half 0 first,
+// and stores them -- the round then lasts about half as long.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -96,6 +103,51 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
 
 constexpr int kPairTileP = 2 * kTileP;  // 256 rows of A per pair tile
 
+// Named barrier of the epilogue warps that also reduces a predicate: true
+// when it holds in every epilogue thread.
+__device__ __forceinline__ bool epi_bar_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(kEpiThreads)
+      : "memory");
+  return r != 0;
+}
+
+// One work item of a pair: a whole tile, or one K half of a tile of the
+// last round (prm.tail_tiles > 0).  Items [0, tiles - tail) are whole tiles
+// in rasterised order; items [tiles - tail, tiles + tail) are the halves of
+// the last `tail` tiles -- tail tile j = (item - first) % tail, half =
+// (item - first) / tail -- so a tile's two halves run on two pairs in the
+// same (last) round.
+struct PairItem {
+  int tile;      // linear tile id (tile_coords)
+  int kb0, kb1;  // K blocks [kb0, kb1)
+  int tail;      // index among the split tiles, -1 for a whole tile
+  int half;      // 0: K blocks [0, tail_kb_half), 1: the rest
+};
+
+__device__ __forceinline__ PairItem pair_item(int w, const MmParams& prm, int tiles) {
+  PairItem it;
+  const int first = tiles - prm.tail_tiles;
+  if (w < first) {
+    it.tile = w;
+    it.kb0 = 0;
+    it.kb1 = prm.num_kb;
+    it.tail = -1;
+    it.half = 0;
+    return it;
+  }
+  it.tail = (w - first) % prm.tail_tiles;
+  it.half = (w - first) / prm.tail_tiles;
+  it.tile = first + it.tail;
+  it.kb0 = it.half ? prm.tail_kb_half : 0;
+  it.kb1 = it.half ? prm.num_kb : prm.tail_kb_half;
+  return it;
+}
+
 template <int BN, bool INT8, typename OutT>
 __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
     w8a8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -121,6 +173,7 @@ __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 5);
   __shared__ float s_scale_p[kTileP];
   __shared__ float s_scale_q[BN];
+  __shared__ bool s_tail_last;
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -128,7 +181,8 @@ __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
   const bool leader = rank == 0;
   const int pair = static_cast<int>(cluster_id_x());
   const int npairs = static_cast<int>(gridDim.x / 2);
-  const int units = prm.tiles_p * prm.tiles_q;  // pair tiles: 256 rows x BN columns
+  const int tiles = prm.tiles_p * prm.tiles_q;  // pair tiles: 256 rows x BN columns
+  const int items = tiles + prm.tail_tiles;      // work items (whole tiles and K halves)
 
   auto full_bar = [&](int s) { return smem_addr(bars + s); };
   auto empty_bar = [&](int s) { return smem_addr(bars + stages + s); };
@@ -166,12 +220,13 @@ __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
   // waiting on the preceding kernel (a prefetch only reads coherent global
   // memory, whatever that kernel writes), so the weight stream starts while
   // it finishes.
-  if (threadIdx.x == 0 && pair < units) {
+  if (threadIdx.x == 0 && pair < items) {
+    const PairItem pi = pair_item(pair, prm, tiles);
     int tp, tq;
-    tile_coords(pair, prm.tiles_p, prm.tiles_q, group, tp, tq);
+    tile_coords(pi.tile, prm.tiles_p, prm.tiles_q, group, tp, tq);
     const int b_row = tq * BN + static_cast<int>(rank) * kHalfN;
-    const int n_pf = min(prm.num_kb, prm.prefetch_kb);
-    for (int i = 0; i < n_pf; ++i) tma_prefetch_l2_2d(&tmap_b, i * kKbElems, b_row);
+    const int kb_pf = min(pi.kb1, pi.kb0 + prm.prefetch_kb);
+    for (int i = pi.kb0; i < kb_pf; ++i) tma_prefetch_l2_2d(&tmap_b, i * kKbElems, b_row);
   }
   griddep_launch();
   griddep_wait();
@@ -188,12 +243,13 @@ __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
       // L2 ahead of the weights, which stream past once
       const uint64_t pol_a = policy_evict_last();
       const uint64_t pol_b = policy_evict_first();
-      for (int u = pair; u < units && ok; u += npairs) {
+      for (int w = pair; w < items && ok; w += npairs) {
+        const PairItem pi = pair_item(w, prm, tiles);
         int tp, tq;
-        tile_coords(u, prm.tiles_p, prm.tiles_q, group, tp, tq);
+        tile_coords(pi.tile, prm.tiles_p, prm.tiles_q, group, tp, tq);
         const int a_row = tp * kPairTileP + static_cast<int>(rank) * kTileP;
         const int b_row = tq * BN + static_cast<int>(rank) * kHalfN;
-        for (int i = 0; i < prm.num_kb; ++i, ++it) {
+        for (int i = pi.kb0; i < pi.kb1; ++i, ++it) {
           const int s = static_cast<int>(it % stages);
           const uint32_t ph = (it / stages) & 1;
           if (!mbar_wait(empty_bar(s), ph ^ 1)) { ok = false; break; }
@@ -215,9 +271,11 @@ __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
     if (leader && lane == 0) {
       uint32_t it = 0, c_all = 0;
       bool ok = true;
-      for (int u = pair; u < units && ok; u += npairs) {
-        const int chunk = INT8 ? prm.kchunk_kb : prm.num_kb;
-        const int nch = (prm.num_kb + chunk - 1) / chunk;
+      for (int w = pair; w < items && ok; w += npairs) {
+        const PairItem pi = pair_item(w, prm, tiles);
+        const int nkb = pi.kb1 - pi.kb0;
+        const int chunk = INT8 ? prm.kchunk_kb : nkb;
+        const int nch = (nkb + chunk - 1) / chunk;
         for (int c = 0; c < nch && ok; ++c, ++c_all) {
           const int b = static_cast<int>(c_all % kBufs);
           if (c_all >= static_cast<uint32_t>(kBufs)) {
@@ -226,8 +284,9 @@ __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
             tc_fence_after();
           }
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-          const int i_end = min(prm.num_kb, (c + 1) * chunk);
-          for (int i = c * chunk; i < i_end; ++i, ++it) {
+          const int i_begin = pi.kb0 + c * chunk;
+          const int i_end = min(pi.kb1, i_begin + chunk);
+          for (int i = i_begin; i < i_end; ++i, ++it) {
             const int s = static_cast<int>(it % stages);
             if (!mbar_wait(full_bar(s), (it / stages) & 1)) { ok = false; break; }
             tc_fence_after();
@@ -235,7 +294,7 @@ __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
             const uint64_t db = smem_desc_sw128(smem_addr(sb + s * kQBytes));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_pair<INT8>(d_tmem, da + 2 * kk, db + 2 * kk, kIdesc, (i == c * chunk && kk == 0) ? 0u : 1u);
+              mma_pair<INT8>(d_tmem, da + 2 * kk, db + 2 * kk, kIdesc, (i == i_begin && kk == 0) ? 0u : 1u);
             mma_commit_pair(empty_bar(s));
           }
           mma_commit_pair(ufull_bar(b));
@@ -256,13 +315,21 @@ __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     uint32_t c_all = 0;
     bool ok = true;
-    for (int u = pair; u < units && ok; u += npairs) {
+    for (int w = pair; w < items && ok; w += npairs) {
+      const PairItem pi = pair_item(w, prm, tiles);
       int tp, tq;
-      tile_coords(u, prm.tiles_p, prm.tiles_q, group, tp, tq);
+      tile_coords(pi.tile, prm.tiles_p, prm.tiles_q, group, tp, tq);
       const int p0 = tp * kPairTileP + static_cast<int>(rank) * kTileP;  // this CTA's 128 rows
       const int q0 = tq * BN;
-      const int chunk = INT8 ? prm.kchunk_kb : prm.num_kb;
-      const int nch = (prm.num_kb + chunk - 1) / chunk;
+      const int chunk = INT8 ? prm.kchunk_kb : (pi.kb1 - pi.kb0);
+      const int nch = (pi.kb1 - pi.kb0 + chunk - 1) / chunk;
+      // this CTA's fp32 half of a split tile, 128 rows x BN columns as
+      // float4s (row, c4) at c4 * 128 + row: a warp's 32 rows of one float4
+      // column are 512 contiguous bytes, written and read whole
+      float* const part = pi.tail < 0 ? nullptr
+                                      : prm.partial + static_cast<size_t>((pi.tail * 2 + pi.half) * 2 + rank) *
+                                                          (kTileP * BN);
+      uint32_t tail_acc = 0;  // TMEM address of the half's accumulator (kept for the sum)
       epi_bar_sync();
       s_scale_p[et] = prm.a_per_row ? __ldg(prm.scale_a + min(p0 + et, prm.M - 1)) : __ldg(prm.scale_a);
       for (int i = et; i < BN; i += kEpiThreads)
@@ -276,7 +343,7 @@ __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
         const bool last = (c == nch - 1);
         const uint32_t acc_addr = lane_base + static_cast<uint32_t>(b * BN);
         const uint32_t tot_addr = lane_base + static_cast<uint32_t>(kBufs * BN);
-        if (INT8) {
+        if constexpr (INT8) {
           constexpr int kBatch = drain_batch(kGroups, 4);
           // with drain helpers an intermediate drain covers the first half
           // of the groups here; the last chunk is drained and stored here
@@ -308,6 +375,19 @@ __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
               }
             }
           }
+        } else if (part) {
+          // a K half: the raw fp32 accumulator goes to the workspace
+          uint4* dst = reinterpret_cast<uint4*>(part) + row;
+          tail_acc = acc_addr;
+#pragma unroll 1
+          for (int g = 0; g < kGroups; ++g) {
+            uint32_t r[16];
+            tmem_ld16(acc_addr + g * 16, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[(g * 4 + j) * kTileP] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+          }
         } else {
 #pragma unroll 1
           for (int g = 0; g < kGroups; ++g) {
@@ -321,9 +401,69 @@ __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
           }
         }
         if (INT8 && !last) tmem_st_wait();
-        tc_fence_before();
-        // release the accumulator to the leader's MMA issuer
-        mbar_arrive_remote(uempty0 + static_cast<uint32_t>(b) * 8u);
+        // release the accumulator to the leader's MMA issuer; a K half keeps
+        // it for the sum below (a pair's K half is its last item: nothing
+        // waits for this accumulator any more)
+        if (!part) {
+          tc_fence_before();
+          mbar_arrive_remote(uempty0 + static_cast<uint32_t>(b) * 8u);
+        }
+      }
+      if constexpr (!INT8) {
+        // every epilogue thread takes the same path through the barriers
+        // below, even if one of them gave up on a wait
+        if (part) ok = epi_bar_all(ok);
+        if (ok && part) {
+          // The second of the tile's two halves (for this CTA's 128 rows) to
+          // arrive adds the other half's partial to its own accumulator, in
+          // half order from zero -- (0 + half 0) + half 1 -- so the bits do
+          // not depend on which pair finished first, and stores the rows as
+          // the whole-tile epilogue does.  The other half's loads of a batch
+          // are all requested before any is used.
+          __threadfence();
+          epi_bar_sync();
+          if (et == 0) s_tail_last = atomicAdd(prm.counters + pi.tail * 2 + rank, 1u) == 1u;
+          epi_bar_sync();
+          if (s_tail_last) {
+            __threadfence();
+            const uint4* other = reinterpret_cast<const uint4*>(
+                                     prm.partial + static_cast<size_t>((pi.tail * 2 + (pi.half ^ 1)) * 2 + rank) *
+                                                       (kTileP * BN)) +
+                                 row;
+            constexpr int kB = drain_batch(kGroups, 4);
+#pragma unroll 1
+            for (int g0 = 0; g0 < kGroups; g0 += kB) {
+              uint4 x[kB][4];
+              uint32_t r[kB][16];
+#pragma unroll
+              for (int bb = 0; bb < kB; ++bb)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) x[bb][j] = __ldcg(other + ((g0 + bb) * 4 + j) * kTileP);
+#pragma unroll
+              for (int bb = 0; bb < kB; ++bb) tmem_ld16(tail_acc + (g0 + bb) * 16, r[bb]);
+              tmem_ld_wait();
+#pragma unroll
+              for (int bb = 0; bb < kB; ++bb) {
+                float v[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const float o[4] = {__uint_as_float(x[bb][j].x), __uint_as_float(x[bb][j].y),
+                                      __uint_as_float(x[bb][j].z), __uint_as_float(x[bb][j].w)};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const float mine = __uint_as_float(r[bb][4 * j + e]);
+                    const float h0 = pi.half == 0 ? mine : o[e];
+                    const float h1 = pi.half == 0 ? o[e] : mine;
+                    v[4 * j + e] = (0.f + h0) + h1;
+                  }
+                }
+                const int g = g0 + bb;
+                store16<false, OutT>(prm, p0 + row, q0 + g * 16, g * 16, v, s_lane, s_scale_q);
+              }
+            }
+            if (et == 0) prm.counters[pi.tail * 2 + rank] = 0u;
+          }
+        }
       }
     }
   } else if constexpr (pair_drain_helpers(BN, INT8)) {
@@ -335,9 +475,9 @@ __global__ void __launch_bounds__(pair_threads(BN, INT8), 1)
     constexpr int kBatch = drain_batch(kGroups, 4);
     uint32_t c_all = 0;
     bool ok = true;
-    for (int u = pair; u < units && ok; u += npairs) {
+    for (int w = pair; w < items && ok; w += npairs) {
       const int chunk = prm.kchunk_kb;
-      const int nch = (prm.num_kb + chunk - 1) / chunk;
+      const int nch = (prm.num_kb + chunk - 1) / chunk;  // int8 items are whole tiles
       for (int c = 0; c < nch; ++c, ++c_all) {
         const int b = static_cast<int>(c_all % kBufs);
         if (!mbar_wait(ufull_bar(b), (c_all / kBufs) & 1)) { ok = false; break; }
@@ -391,8 +531,7 @@ cudaError_t launch_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, const Mm
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
-  const int units = p.tiles_p * p.tiles_q;
-  const int npairs = max(1, min(units, p.num_sms / 2));
+  const int npairs = pair_grid_pairs(static_cast<long long>(p.tiles_p) * p.tiles_q, p.num_sms);
   // rasterisation: groups of 256-row token slabs that fit in 48 MB of L2
   const long long slab = static_cast<long long>(kPairTileP) * p.K * (INT8 ? 2 : 1);
   long long g_tiles = (48LL << 20) / slab;

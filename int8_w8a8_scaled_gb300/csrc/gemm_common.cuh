@@ -124,6 +124,39 @@ __device__ __forceinline__ void store16(const MmParams& prm, int lane_idx, int c
   }
 }
 
+// Store of four reduced accumulators at P row p and Q columns q..q+3 (the
+// first `nvalid` inside the problem), with the scales in registers: s_p for
+// P row p, s_q[j] for Q column q + j.  The product order stays
+// (acc * scale_a) * scale_b.
+template <bool SWAP, typename OutT, typename V>
+__device__ __forceinline__ void store4s(const MmParams& prm, int p, int q, int nvalid, const V (&v)[4], float s_p,
+                                        const float (&s_q)[4]) {
+  OutT* out = reinterpret_cast<OutT*>(prm.out);
+  if (p >= (SWAP ? prm.N : prm.M)) return;
+  if (!SWAP && nvalid >= 4 && prm.out_vec_ok) {
+    // four consecutive outputs of one row in one store (q is a multiple of
+    // 4 and the rows are 16-byte aligned)
+    alignas(16) OutT o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = OutConv<OutT>::conv(v[j], s_p, s_q[j]);
+    OutT* dst = out + static_cast<long long>(p) * prm.ldc + q;
+    if (sizeof(OutT) == 2)
+      *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(o);
+    else
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (j < nvalid) {
+      if (!SWAP)
+        out[static_cast<long long>(p) * prm.ldc + q + j] = OutConv<OutT>::conv(v[j], s_p, s_q[j]);
+      else
+        out[static_cast<long long>(q + j) * prm.ldc + p] = OutConv<OutT>::conv(v[j], s_q[j], s_p);
+    }
+  }
+}
+
 __device__ __forceinline__ void epi_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
 }

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/w8a8.h"
+
 namespace w8a8 {
 
 // Parameters of one scaled-matmul launch.  "P" is the operand on the
@@ -38,6 +40,14 @@ struct MmParams {
   int num_sms;           // persistent grid = min(units, num_sms * resident CTAs per SM)
   int pdl;               // launch with programmatic stream serialisation
   int prefetch_kb;       // weight K blocks of the first unit prefetched into L2 early
+  // CTA-pair tiles only: the last, partial round of pair tiles, when it
+  // would leave at least half of the pairs idle, is run as two K halves per
+  // tile ([0, tail_kb_half) and [tail_kb_half, num_kb)) on two pairs; each
+  // CTA writes its fp32 half into `partial` ([tail][half][rank][128 *
+  // block_n]) and the last of the tile's two halves to arrive on
+  // counters[tail * 2 + rank] sums them in half order
+  int tail_tiles;        // 0: every tile whole
+  int tail_kb_half;
   int max_ctas_per_sm;   // 0: as many as fit; else cap the persistent grid per SM
   // fused activation quantiser (swap-AB e4m3 decode, one token tile): the
   // kernel quantises x itself (scale_a is then unused)
@@ -64,9 +74,15 @@ cudaError_t launch_fp8_gemm(const CUtensorMap& tmap_p, const CUtensorMap& tmap_q
                             const MmParams& p, int block_n, bool swap, int out_kind,
                             int stages, cudaStream_t stream);
 
+// Pairs in the persistent CTA-pair grid: one per two SMs, at most one per
+// tile.
+inline int pair_grid_pairs(long long tiles, int num_sms) {
+  const long long p = tiles < num_sms / 2 ? tiles : num_sms / 2;
+  return p < 1 ? 1 : static_cast<int>(p);
+}
 // The same matmul on CTA pairs (gemm2sm.cu): 256 x block_n tiles, tokens on
-// the 128-row side of each CTA (no swap, no split-K).  tmap_a boxes 128 rows,
-// tmap_b block_n / 2 rows.
+// the 128-row side of each CTA (no swap; split-K only as the last round's K
+// halves, p.tail_tiles).  tmap_a boxes 128 rows, tmap_b block_n / 2 rows.
 cudaError_t launch_gemm_pair(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const MmParams& p, int block_n,
                              bool int8, int out_kind, int stages, cudaStream_t stream);
 int gemm_pair_smem_bytes(int block_n, int stages);
@@ -165,10 +181,10 @@ void set_last_error(const char* msg);
 constexpr size_t kCounterSlots = 16384;
 constexpr size_t kCounterRegion = kCounterSlots * sizeof(unsigned);
 
-// Bytes at the head of the workspace whose counters the automatic
-// configuration of this matmul uses (0 when it uses none), on the current
-// device.
-size_t mm_counter_bytes(long long M, long long N, long long K, int q_dtype);
+// Bytes at the head of the workspace whose counters this matmul uses under
+// `cfg` (complete: no automatic fields) on the current device, 0 when it
+// uses none.
+size_t mm_counter_bytes(long long M, long long N, long long K, int q_dtype, const w8a8_mm_config& cfg);
 
 // Row shards of a merged weight: cumulative row ends.
 constexpr int kMaxShards = 16;

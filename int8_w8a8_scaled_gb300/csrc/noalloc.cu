@@ -104,7 +104,19 @@ w8a8_status w8a8_scaled_mm_noalloc(const void* a_q, int64_t lda, const void* b_q
     return w8a8_scaled_mm(a_q, lda, b_q, ldb, scale_a, a_gran, scale_b, b_gran, out, ldc, M, N, K, q_dtype,
                           out_dtype, nullptr, 0, stream);
   }
-  const size_t need = w8a8_scaled_mm_workspace_size(M, N, K, q_dtype);
+  w8a8_mm_config cfg;
+  if (w8a8_scaled_mm_pick_config(M, N, K, q_dtype, &cfg) != W8A8_OK) {
+    // an invalid q_dtype: the regular entry point produces the message
+    return w8a8_scaled_mm(a_q, lda, b_q, ldb, scale_a, a_gran, scale_b, b_gran, out, ldc, M, N, K, q_dtype,
+                          out_dtype, nullptr, 0, stream);
+  }
+  size_t need = w8a8_scaled_mm_config_workspace_size(M, N, K, q_dtype, &cfg);
+  if (need > kScratchBytes && cfg.cta_pair && cfg.split_k > 1) {
+    // K halves of the last round's CTA-pair tiles only shorten that round;
+    // where their partial tiles do not fit the array, the tiles run whole
+    cfg.split_k = 1;
+    need = w8a8_scaled_mm_config_workspace_size(M, N, K, q_dtype, &cfg);
+  }
   if (need > kScratchBytes) {
     w8a8::set_last_error("scaled_mm_noalloc: this problem needs more scratch than the library's fixed array");
     return W8A8_ERR_WORKSPACE;
@@ -116,14 +128,15 @@ w8a8_status w8a8_scaled_mm_noalloc(const void* a_q, int64_t lda, const void* b_q
   // counters this problem uses must start at zero: a successful call leaves
   // them zero, but a call whose kernel gave up on a wait may not, so they
   // are cleared (only they, and only when the plan uses them).
-  const size_t ctr = need > 0 ? w8a8::mm_counter_bytes(M, N, K, q_dtype) : 0;
+  const size_t ctr = need > 0 ? w8a8::mm_counter_bytes(M, N, K, q_dtype, cfg) : 0;
   if (ctr > 0 && cudaMemsetAsync(scratch, 0, ctr, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
     w8a8::set_last_error("scaled_mm_noalloc: clearing the split-K counters failed");
     return W8A8_ERR_CUDA;
   }
-  return w8a8_scaled_mm(a_q, lda, b_q, ldb, scale_a, a_gran, scale_b, b_gran, out, ldc, M, N, K, q_dtype, out_dtype,
-                        need > 0 ? scratch : nullptr, need > 0 ? kScratchBytes : 0, stream);
+  return w8a8_scaled_mm_with_config(a_q, lda, b_q, ldb, scale_a, a_gran, scale_b, b_gran, out, ldc, M, N, K, q_dtype,
+                                    out_dtype, need > 0 ? scratch : nullptr, need > 0 ? kScratchBytes : 0, &cfg,
+                                    stream);
 }
 
 }  // extern "C"

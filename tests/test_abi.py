@@ -92,8 +92,27 @@ def test_workspace_sizes():
     assert w8.quant_workspace_size(10, 10, per_token=False, dynamic=True) == 16
     assert w8.quant_workspace_size(10, 10, per_token=True, dynamic=True) == 0
     assert w8.quant_workspace_size(10, 10, per_token=False, dynamic=False) == 0
-    # no split, fp8: no workspace
+    # no split, fp8: no workspace (gate-up at M=4096: 1792 pair tiles over 76
+    # pairs, a last round of 44 tiles, more than half: the tiles run whole)
+    assert w8.pick_config(4096, 28672, 4096, w8.E4M3)["split_k"] == 1
+    assert w8.mm_workspace_size(4096, 28672, 4096, w8.E4M3) == 0
+    # CTA pairs whose last round keeps at most half of the pairs busy run its
+    # tiles as K halves where K is long enough to pay for the exchange (the
+    # down projection, K = 14336): 256 tiles of 256 x 256 over 76 pairs leave
+    # 28; two halves x two CTAs x 128 x 256 fp32 each, after the counter region
+    c = w8.pick_config(4096, 4096, 14336, w8.E4M3)
+    assert (c["cta_pair"], c["block_n"], c["split_k"]) == (1, 256, 2)
+    assert w8.mm_workspace_size(4096, 4096, 14336, w8.E4M3) == 65536 + 28 * 4 * 128 * 256 * 4
+    # the same tiles whole: no workspace
+    whole = dict(c, split_k=1)
+    assert w8.mm_workspace_size(4096, 4096, 14336, w8.E4M3, whole) == 0
+    # at K = 4096 the halves do not pay: whole tiles, no workspace
+    assert w8.pick_config(4096, 4096, 4096, w8.E4M3)["split_k"] == 1
     assert w8.mm_workspace_size(4096, 4096, 4096, w8.E4M3) == 0
+    # int8 pairs take no K halves: only the f16 operand planes
+    i8 = {"swap_ab": 0, "block_n": 256, "split_k": 2, "cta_pair": 1}
+    assert w8.mm_workspace_size(4096, 4096, 4096, w8.INT8, i8) == w8.mm_workspace_size(4096, 4096, 4096, w8.INT8,
+                                                                                       dict(i8, split_k=1))
     # int8 widens both operands to f16 planes
     assert w8.mm_workspace_size(512, 256, 1024, w8.INT8) >= (512 + 256) * 1024 * 2
     # split-K through the workspace: partials + counters
@@ -116,11 +135,11 @@ def test_pick_config_regimes(M):
     assert c["split_k"] >= 1
     assert c["split_k"] <= 8 and c["reduce"] == w8.REDUCE_AUTO   # splits fit one cluster
     if M >= 4096:
-        assert c["split_k"] == 1 and c["block_n"] >= 128   # many tiles: no split, wide tile
+        assert c["block_n"] >= 128   # many tiles: wide tile, no split-K (K halves of the last round only)
     # 256-row tiles on CTA pairs for large-M e4m3 only
     assert c["cta_pair"] == (1 if M >= 1024 else 0)
     if c["cta_pair"]:
-        assert c["block_n"] in (192, 224, 256) and c["swap_ab"] == 0
+        assert c["block_n"] in (192, 224, 256) and c["swap_ab"] == 0 and c["split_k"] in (1, 2)
     c8 = w8.pick_config(M, 4096, 4096, w8.INT8)
     assert c8["block_n"] <= 128 or (c8["block_n"] in (160, 256) and not c8["swap_ab"])
     assert c8["cta_pair"] == 0
