@@ -706,6 +706,7 @@ PROFILE_CASES = {
     "decode_gemm": "fp8 decode GEMM, M=16 x gate-up [28672 x 4096] (117 MB of weights)",
     "m256_gemm": "fp8 decode GEMM, M=256 x down [4096 x 14336] (59 MB of weights)",
     "prefill_gemm": "fp8 prefill GEMM, M=4096 x gate-up [28672 x 4096]",
+    "prefill_down": "fp8 prefill GEMM, M=4096 x down [4096 x 14336] (CTA pairs, last round in K halves)",
     "int8_gemm": "int8 GEMM, M=8192 x QKV-70B [10240 x 8192]",
     "quant_tokens": "per-token dynamic e4m3 quantiser, [4096 x 14336] bf16",
     "quant_kv": "per-tensor dynamic e4m3 quantiser (absmax + convert), KV [524288 x 128] bf16",
@@ -741,9 +742,10 @@ def run_profile_case(name: str, launches: int):
         print(json.dumps({"case": name, "configs": {f"M{it['M']}_{it['name']}": w8.pick_config(
             it["M"], wl.weights[it["name"]][2], wl.weights[it["name"]][3], w8.E4M3) for it in wl.items}}))
         return
-    if name.endswith("_gemm"):
+    if name.endswith("_gemm") or name == "prefill_down":
         M, N, K, qd = {"decode_gemm": (16, 28672, 4096, w8.E4M3), "prefill_gemm": (4096, 28672, 4096, w8.E4M3),
-                       "int8_gemm": (8192, 10240, 8192, w8.INT8), "m256_gemm": (256, 4096, 14336, w8.E4M3)}[name]
+                       "prefill_down": (4096, 4096, 14336, w8.E4M3), "int8_gemm": (8192, 10240, 8192, w8.INT8),
+                       "m256_gemm": (256, 4096, 14336, w8.E4M3)}[name]
         qt = torch.float8_e4m3fn if qd == w8.E4M3 else torch.int8
         a, sa = quantised((M, K), 1, qt, True, False)
         b, sb = quantised((N, K), 2, qt, True, True)
