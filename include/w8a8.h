@@ -174,11 +174,11 @@ W8A8_API w8a8_status w8a8_scaled_dequant(const void* q, int q_dtype, int64_t row
  *  q_dtype  W8A8_E4M3 (fp32 accumulation) or W8A8_INT8 (exact int32).
  *  workspace, workspace_bytes
  *           device scratch of at least w8a8_scaled_mm_workspace_size() bytes
- *           (0 for e4m3 without split-K), 256-byte aligned.  Its first 64 KiB
- *           hold split-K arrival counters that must be zero-filled before
- *           the first use; every call leaves them zero again and writes its
- *           other scratch (split-K partials, int8 f16 planes) only after
- *           them, so one zero-filled buffer serves any sequence of
+ *           (0 for e4m3 without split-K or K halves), 256-byte aligned.  Its
+ *           first 64 KiB hold split-K arrival counters that must be
+ *           zero-filled before the first use; every call leaves them zero
+ *           again and writes its other scratch (split-K partials, the K
+ *           halves of CTA-pair tiles, int8 f16 planes) only after them, so one zero-filled buffer serves any sequence of
  *           scaled_mm calls of any shape on one stream.  Use it for nothing
  *           else, and give calls that may overlap on the GPU separate
  *           workspaces.
