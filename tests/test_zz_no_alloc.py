@@ -91,6 +91,43 @@ def test_noalloc_matches_the_oracle():
     assert np.all(np.abs(got - y) <= 2.0 ** -7 * np.abs(y) + 1e-3)
 
 
+def test_noalloc_runs_pair_tiles_whole_when_their_k_halves_do_not_fit():
+    """The prefill down projection (M=4096, N=4096, K=14336): the automatic
+    configuration runs the last round of CTA-pair tiles as K halves, whose
+    partials (about 15 MB) exceed the fixed array, so the allocation-free
+    entry point runs those tiles whole.  Its output is then the bits of the
+    same configuration with split_k 1 through a caller workspace, and within
+    the fp8 tolerance of the oracle on sampled outputs."""
+    import int8_w8a8_scaled_gb300 as w8
+    import oracle
+    M, N, K = 4096, 4096, 14336
+    lib = _lib.load()
+    auto = w8.pick_config(M, N, K, w8.E4M3)
+    if not (auto["cta_pair"] and auto["split_k"] == 2):
+        pytest.skip("this GPU's automatic configuration takes no K halves here")
+    assert lib.w8a8_scaled_mm_workspace_size(M, N, K, E4M3) > lib.w8a8_scaled_mm_noalloc_max_scratch()
+    a, b, sa, sb = _problem(M, N, K, seed=77)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = lib.w8a8_scaled_mm_noalloc(_p(a), K, _p(b), K, _p(sa), PER_ROW, _p(sb), PER_ROW, _p(out), N, M, N, K,
+                                    E4M3, BF16, stream)
+    assert st == 0, lib.w8a8_last_error()
+    whole = dict(auto, split_k=1)
+    assert w8.mm_workspace_size(M, N, K, w8.E4M3, whole) == 0
+    ref = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    w8.scaled_mm(a.view(torch.float8_e4m3fn), b.view(torch.float8_e4m3fn), sa, sb, ref, config=whole)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    rng = np.random.default_rng(5)
+    im = rng.integers(0, M, 2048)
+    jn = rng.integers(0, N, 2048)
+    A, B = a.cpu().numpy(), b.cpu().numpy()
+    y = oracle.scaled_mm_sample(A, B, sa.cpu().numpy(), sb.cpu().numpy(), oracle.E4M3, oracle.BF16, im, jn)["y"]
+    got = out.float().cpu().numpy()[im, jn].astype(np.float64)
+    y = y.astype(np.float64)
+    assert np.all(np.abs(got - y) <= 2.0 ** -7 * np.abs(y) + 1e-3)
+
+
 def test_noalloc_rejects_problems_beyond_its_array():
     lib = _lib.load()
     a, b, sa, sb = _problem(16, 64, 64, seed=1)
