@@ -127,6 +127,26 @@ def test_workspace_sizes():
     assert w8.mm_workspace_size(1, 4096, 4096, w8.E4M3, cfg) >= 32 * 16 * 128 * 16 * 4
 
 
+@pytest.mark.parametrize("M,N,K,bn,tail", [
+    (4096, 4096, 14336, 256, 28),   # 256 tiles over 76 pairs: a last round of 28 <= 38
+    (1280, 4096, 1040, 256, 4),     # 80 tiles: 4 left
+    (1536, 4864, 256, 256, 38),     # 114 tiles: 38 left, exactly half of the pairs
+    (1536, 5120, 256, 256, 0),      # 120 tiles: 44 left, more than half: whole tiles
+    (4096, 4864, 4096, 256, 0),     # 304 tiles: four full rounds
+    (1280, 4096, 128, 256, 0),      # one K block: nothing to halve
+    (1024, 4096, 4096, 256, 0),     # 64 tiles: fewer tiles than pairs, one round
+    (4096, 4096, 14336, 224, 0),    # 304 tiles of 224 columns: four full rounds
+])
+def test_pair_k_halves_workspace(M, N, K, bn, tail):
+    """Host rule of the CTA-pair K halves (split_k 2) on a 152-SM GB300 (76
+    pairs): the tiles of a last round that keeps at most half of the pairs
+    busy are split, and each needs two halves x two CTAs x 128 x block_n
+    fp32 after the 64 KiB counter region; otherwise no workspace."""
+    cfg = {"swap_ab": 0, "block_n": bn, "split_k": 2, "cta_pair": 1}
+    want = 65536 + tail * 4 * 128 * bn * 4 if tail else 0
+    assert w8.mm_workspace_size(M, N, K, w8.E4M3, cfg) == want
+
+
 @pytest.mark.parametrize("M", [1, 16, 64, 256, 4096])
 def test_pick_config_regimes(M):
     c = w8.pick_config(M, 4096, 4096, w8.E4M3)
